@@ -1,0 +1,502 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Nothing here calls the CUDA path.  Each test ties the oracle to something
+other than itself: hand-derived closed forms (tests/golden), brute force
+over all subsets on tiny inputs, library routines in special cases the
+method reduces to, and invariants of the definition.  The mutation tests at
+the end plant plausible mistakes in the oracle and check that some pin fails.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import moe_oracle as om
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------- golden ---
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+def _golden_route_cases(golden_dir):
+    return _load(golden_dir, "route_cases.json")["cases"]
+
+
+def test_route_golden(golden_dir):
+    for c in _golden_route_cases(golden_dir):
+        logits = np.array([[math.log(q) for q in c["logits_ln"]]], dtype=np.float32)
+        w, ids, _ = oracle.route(logits, c["top_k"], c["method"], c["renormalize"],
+                                 c["k_group"], c["group_count"], c["group_select_mode"],
+                                 c["scale"])
+        assert ids[0].tolist() == c["ids"], c["name"]
+        np.testing.assert_allclose(w[0], c["weights"], rtol=0, atol=2e-7, err_msg=c["name"])
+
+
+def test_align_golden(golden_dir):
+    for c in _load(golden_dir, "align_cases.json")["cases"]:
+        a = oracle.align(np.array(c["topk_ids"], dtype=np.int32), c["E"], c["block_m"])
+        for key in ("expert_num_tokens", "expert_offsets", "sorted_token_ids",
+                    "block_expert_ids"):
+            assert a[key].tolist() == c[key], (c["name"], key)
+
+
+# ------------------------------------------------------------ brute force ---
+
+def _brute_route(l_row, top_k, method, renormalize, k_group, G, mode, scale,
+                 group_tol=0.0):
+    """Enumerate every group subset and every expert subset.  The best set is
+    the one with the largest score sum; among equal sums the lexicographically
+    smallest sorted id list wins.  Sums are taken over the sorted values so
+    equal multisets give bit-equal sums.  With group_tol > 0 every group subset
+    whose total is within group_tol of the best is also answered (a list of
+    (weights, ids) is returned): mode 1 has exact mathematical ties such as
+    sigmoid(a) + sigmoid(-a) = 1 that floating point breaks either way."""
+    E = len(l_row)
+    if method == "softmax":
+        ex = [math.exp(v - max(l_row)) for v in l_row]
+        tot = math.fsum(ex)
+        p = [v / tot for v in ex]
+    else:
+        p = [1.0 / (1.0 + math.exp(-v)) for v in l_row]
+    gs = E // G
+    if G > 1:
+        gscore = []
+        for g in range(G):
+            members = list(range(g * gs, (g + 1) * gs))
+            if mode == 0:
+                gscore.append(max(p[e] for e in members))
+            else:
+                gscore.append(max(sum(sorted((p[a], p[b])))
+                                  for a, b in itertools.combinations(members, 2)))
+        best = None
+        subs = list(itertools.combinations(range(G), k_group))
+        for gsub in subs:
+            key = (-sum(sorted(gscore[g] for g in gsub)), gsub)
+            if best is None or key < best:
+                best = key
+        if group_tol > 0:
+            return [_brute_route_in(p, [e for g in gsub for e in range(g * gs, (g + 1) * gs)],
+                                    top_k, method, renormalize, scale)
+                    for gsub in subs
+                    if -sum(sorted(gscore[g] for g in gsub)) - best[0] <= group_tol]
+        allowed = [e for g in best[1] for e in range(g * gs, (g + 1) * gs)]
+    else:
+        allowed = list(range(E))
+    if group_tol > 0:
+        return [_brute_route_in(p, allowed, top_k, method, renormalize, scale)]
+    return _brute_route_in(p, allowed, top_k, method, renormalize, scale)
+
+
+def _brute_route_in(p, allowed, top_k, method, renormalize, scale):
+    best = None
+    for sub in itertools.combinations(sorted(allowed), top_k):
+        key = (-sum(sorted(p[e] for e in sub)), sub)
+        if best is None or key < best:
+            best = key
+    chosen = sorted(best[1], key=lambda e: (-p[e], e))
+    w = [p[e] for e in chosen]
+    if method == "sigmoid" or renormalize:
+        s = math.fsum(w)
+        w = [v / s for v in w]
+    return [scale * v for v in w], chosen
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_route_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    n_cases = 0
+    for E, G in ((4, 1), (6, 1), (6, 2), (6, 3), (8, 2), (8, 4)):
+        for method in ("softmax", "sigmoid"):
+            for mode in ((0, 1) if G > 1 else (0,)):
+                if mode == 1 and E // G < 2:
+                    continue
+                for k_group in range(1, G + 1):
+                    kmax = min(3, k_group * (E // G))
+                    for top_k in range(1, kmax + 1):
+                        # small integer logits -> many exact ties
+                        l = rng.integers(-2, 3, size=(4, E)).astype(np.float32)
+                        for renorm in (False, True):
+                            scale = 1.0 if renorm else 2.5
+                            w, ids, _ = oracle.route(l, top_k, method, renorm, k_group, G,
+                                                     mode, scale)
+                            for t in range(l.shape[0]):
+                                row = [float(v) for v in l[t]]
+                                bw, bids = _brute_route(row, top_k, method, renorm, k_group,
+                                                        G, mode, scale)
+                                if ids[t].tolist() != bids and mode == 1:
+                                    # only a group-score tie within rounding may differ
+                                    alts = _brute_route(row, top_k, method, renorm, k_group,
+                                                        G, mode, scale, group_tol=1e-12)
+                                    match = [a for a in alts if a[1] == ids[t].tolist()]
+                                    assert match, (E, G, method, mode, top_k, l[t])
+                                    bw, bids = match[0]
+                                assert ids[t].tolist() == bids, (E, G, method, mode, top_k, l[t])
+                                np.testing.assert_allclose(w[t], bw, rtol=1e-12, atol=1e-14)
+                                n_cases += 1
+    assert n_cases > 200
+
+
+def test_route_matches_printed_routing_function():
+    """Without groups, softmax routing is the page's printed custom routing
+    function: softmax over experts, torch.topk, then divide by the sum of the
+    selected weights when renormalize is set.  Continuous logits -> no ties."""
+    g = torch.Generator().manual_seed(7)
+    for E, k in ((8, 2), (16, 4), (128, 8), (256, 8)):
+        logits = torch.randn(64, E, generator=g, dtype=torch.float64)
+        for renorm in (False, True):
+            vals, idx = logits.softmax(dim=-1).topk(k, dim=-1)
+            if renorm:
+                vals = vals / vals.sum(dim=-1, keepdim=True)
+            w, ids, _ = oracle.route(logits.numpy(), k, "softmax", renorm)
+            assert (ids == idx.numpy()).all()
+            np.testing.assert_allclose(w, vals.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_route_sigmoid_grouped_matches_library_path():
+    """Grouped sigmoid routing assembled from library routines (torch.sigmoid,
+    torch.topk over groups, masking, torch.topk over experts) on continuous
+    logits, mode 1 = sum of torch.topk(2) inside each group."""
+    g = torch.Generator().manual_seed(11)
+    E, G, kg, k = 256, 8, 4, 8
+    logits = torch.randn(128, E, generator=g, dtype=torch.float64)
+    p = torch.sigmoid(logits)
+    gscore = p.view(128, G, E // G).topk(2, dim=-1).values.sum(-1)
+    gidx = gscore.topk(kg, dim=-1).indices
+    gmask = torch.zeros(128, G, dtype=torch.bool).scatter_(1, gidx, True)
+    pm = p.masked_fill(~gmask.repeat_interleave(E // G, dim=1), -1.0)
+    vals, idx = pm.topk(k, dim=-1)
+    vals = vals / vals.sum(-1, keepdim=True) * 2.5
+    w, ids, _ = oracle.route(logits.numpy(), k, "sigmoid", False, kg, G, 1, 2.5)
+    assert (ids == idx.numpy()).all()
+    np.testing.assert_allclose(w, vals.numpy(), rtol=1e-12)
+
+
+# ------------------------------------------------------------------ align ---
+
+@pytest.mark.parametrize("seed", range(4))
+def test_align_invariants(seed):
+    rng = np.random.default_rng(seed)
+    for M, k, E, bm in ((1, 1, 1, 1), (37, 2, 8, 16), (200, 8, 32, 128), (64, 3, 5, 7)):
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+        if seed % 2:
+            ids[: M // 2] = ids[0]       # skew: many items on the same experts
+        a = oracle.align(ids, E, bm)
+        R = M * k
+        flat = ids.reshape(-1)
+        c = a["expert_num_tokens"]
+        off = a["expert_offsets"]
+        st = a["sorted_token_ids"]
+        assert c.sum() == R
+        for e in range(E):
+            assert off[e + 1] - off[e] == -(-c[e] // bm) * bm
+            seg = st[off[e]:off[e + 1]]
+            real = seg[seg < R]
+            assert real.tolist() == np.flatnonzero(flat == e).tolist()   # ascending, exact set
+            assert (seg[c[e]:] == R).all() and (seg[:c[e]] < R).all()
+        assert sorted(st[st < R].tolist()) == list(range(R))              # permutation
+        assert len(a["block_expert_ids"]) == off[E] // bm
+        for b, e in enumerate(a["block_expert_ids"]):
+            assert off[e] <= b * bm < off[e + 1]
+        # dispatch then combine is the identity (index_select / index_copy)
+        x = rng.standard_normal((R, 3))
+        disp = x[np.where(st < R, st, 0)]
+        back = np.zeros_like(x)
+        back[st[st < R]] = disp[st < R]
+        assert np.array_equal(back, x)
+
+
+def test_align_rejects_bad_ids():
+    with pytest.raises(ValueError):
+        oracle.align(np.array([[0, 4]]), 4, 2)
+    with pytest.raises(ValueError):
+        oracle.align(np.array([[-1, 0]]), 4, 2)
+
+
+# -------------------------------------------------------------------- ffn ---
+
+def _closed_form_case():
+    """H=2, I=3, E=2 hand-built weights (see the expert formulas below)."""
+    H, I, E = 2, 3, 2
+    w13 = np.zeros((E, H, 2 * I))
+    b13 = np.zeros((E, 2 * I))
+    w2 = np.zeros((E, I, H))
+    b2 = np.zeros((E, H))
+    # expert 0: gate = [x0, x1, x0+x1] + [0, .5, 0]; up = [2 x0, -x1, 0] + [0, 0, 1]
+    w13[0, :, :I] = [[1, 0, 1], [0, 1, 1]]
+    w13[0, :, I:] = [[2, 0, 0], [0, -1, 0]]
+    b13[0] = [0, 0.5, 0, 0, 0, 1]
+    # y = [z0 + z2, z1 - z2] + [0.1, -0.2]
+    w2[0] = [[1, 0], [0, 1], [1, -1]]
+    b2[0] = [0.1, -0.2]
+    # expert 1: gate = [-x0, 2 x1, 0]; up = [x1, x0, x0 + x1]; y = [z1 + 2 z2, z0]
+    w13[1, :, :I] = [[-1, 0, 0], [0, 2, 0]]
+    w13[1, :, I:] = [[0, 1, 1], [1, 0, 1]]
+    w2[1] = [[0, 1], [1, 0], [2, 0]]
+    return w13, b13, w2, b2
+
+
+def _s(u):
+    return u / (1.0 + math.exp(-u))
+
+
+def _closed_form_expert(e, x0, x1):
+    if e == 0:
+        z0 = _s(x0) * (2 * x0)
+        z1 = _s(x1 + 0.5) * (-x1)
+        z2 = _s(x0 + x1) * 1.0
+        return np.array([z0 + z2 + 0.1, z1 - z2 - 0.2])
+    z0 = _s(-x0) * x1
+    z1 = _s(2 * x1) * x0
+    z2 = _s(0.0) * (x0 + x1)
+    return np.array([z1 + 2 * z2, z0])
+
+
+def test_ffn_closed_form():
+    w13, b13, w2, b2 = _closed_form_case()
+    x = np.array([[1.0, -2.0], [0.5, 3.0]])
+    ids = np.array([[1, 0], [0, 1]])
+    a = np.array([[0.7, 0.2], [0.25, 0.5]])      # deliberately not summing to 1
+    y = oracle.forward(x, a, ids, w13, w2, b13, b2)
+    expect = np.stack([
+        0.7 * _closed_form_expert(1, 1.0, -2.0) + 0.2 * _closed_form_expert(0, 1.0, -2.0),
+        0.25 * _closed_form_expert(0, 0.5, 3.0) + 0.5 * _closed_form_expert(1, 0.5, 3.0),
+    ])
+    np.testing.assert_allclose(y, expect, rtol=1e-14, atol=1e-14)
+    for t in range(2):
+        np.testing.assert_allclose(oracle.token_output(x[t], a[t], ids[t], w13, w2, b13, b2),
+                                   expect[t], rtol=1e-14, atol=1e-14)
+
+
+def _dense_swiglu_torch(x, w13, w2, b13, b2):
+    """Dense SwiGLU FFN through torch.nn.functional (fp64 CPU)."""
+    xt = torch.from_numpy(x)
+    I = w2.shape[0]
+    gate = torch.nn.functional.linear(xt, torch.from_numpy(w13[:, :I].T.copy()),
+                                      torch.from_numpy(b13[:I]))
+    up = torch.nn.functional.linear(xt, torch.from_numpy(w13[:, I:].T.copy()),
+                                    torch.from_numpy(b13[I:]))
+    z = torch.nn.functional.silu(gate) * up
+    return torch.nn.functional.linear(z, torch.from_numpy(w2.T.copy()),
+                                      torch.from_numpy(b2)).numpy()
+
+
+def _rand_layer(rng, E, H, I, bias=True):
+    w13 = rng.standard_normal((E, H, 2 * I)) * 0.2
+    w2 = rng.standard_normal((E, I, H)) * 0.2
+    b13 = rng.standard_normal((E, 2 * I)) * 0.1 if bias else np.zeros((E, 2 * I))
+    b2 = rng.standard_normal((E, H)) * 0.1 if bias else np.zeros((E, H))
+    return w13, w2, b13, b2
+
+
+def test_single_expert_is_dense_swiglu():
+    """E=1, k=1: softmax of one logit is 1 (renormalised), so the layer is the
+    dense SwiGLU FFN."""
+    rng = np.random.default_rng(3)
+    w13, w2, b13, b2 = _rand_layer(rng, 1, 24, 40)
+    x = rng.standard_normal((17, 24))
+    logits = rng.standard_normal((17, 1))
+    y, w, ids, _ = oracle.moe_layer(x, logits, w13, w2, 1, "softmax", True,
+                                    w13_bias=b13, w2_bias=b2)
+    assert (ids == 0).all() and np.allclose(w, 1.0)
+    np.testing.assert_allclose(y, _dense_swiglu_torch(x, w13[0], w2[0], b13[0], b2[0]),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_uniform_topk_all_is_mean_of_experts():
+    """All logits equal, top_k = E, softmax: weights 1/E, ids 0..E-1 by the tie
+    rule, so y = mean over experts of the dense expert outputs."""
+    rng = np.random.default_rng(4)
+    E, H, I, M = 5, 16, 20, 9
+    w13, w2, b13, b2 = _rand_layer(rng, E, H, I)
+    x = rng.standard_normal((M, H))
+    y, w, ids, _ = oracle.moe_layer(x, np.zeros((M, E)), w13, w2, E, "softmax", False,
+                                    w13_bias=b13, w2_bias=b2)
+    assert (ids == np.arange(E)).all()
+    np.testing.assert_allclose(w, 1.0 / E, rtol=1e-15)
+    mean = sum(_dense_swiglu_torch(x, w13[e], w2[e], b13[e], b2[e]) for e in range(E)) / E
+    np.testing.assert_allclose(y, mean, rtol=1e-12, atol=1e-12)
+
+
+def test_linearity_and_equivariance():
+    rng = np.random.default_rng(5)
+    E, H, I, M, k = 6, 12, 18, 11, 3
+    w13, w2, b13, b2 = _rand_layer(rng, E, H, I)
+    x = rng.standard_normal((M, H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)])
+    a = rng.random((M, k))
+    y = oracle.forward(x, a, ids, w13, w2, b13, b2)
+    # routing weights enter linearly (b2 is inside f_e, so it scales too)
+    np.testing.assert_allclose(oracle.forward(x, 3 * a, ids, w13, w2, b13, b2), 3 * y,
+                               rtol=1e-12, atol=1e-12)
+    # with b2 = 0: w2 -> c w2 scales y by c; applying the weight before W2
+    # (apply_router_weight_on_input) gives the same y
+    y0 = oracle.forward(x, a, ids, w13, w2, b13, None)
+    np.testing.assert_allclose(oracle.forward(x, a, ids, w13, 2.5 * w2, b13, None), 2.5 * y0,
+                               rtol=1e-12, atol=1e-12)
+    y_in = np.zeros_like(y0)
+    for t in range(M):
+        for j in range(k):
+            e = ids[t, j]
+            h = x[t] @ w13[e] + b13[e]
+            z = a[t, j] * (h[:I] / (1 + np.exp(-h[:I])) * h[I:])
+            y_in[t] += z @ w2[e]
+    np.testing.assert_allclose(y_in, y0, rtol=1e-12, atol=1e-12)
+    # token permutation equivariance
+    perm = rng.permutation(M)
+    np.testing.assert_allclose(oracle.forward(x[perm], a[perm], ids[perm], w13, w2, b13, b2),
+                               y[perm], rtol=1e-12, atol=1e-12)
+    # a repeated expert in two slots equals one slot with the summed weight
+    ids2 = ids.copy()
+    ids2[:, 1] = ids2[:, 0]
+    a2 = a.copy()
+    a1 = a.copy()
+    a1[:, 0] += a1[:, 1]
+    a1[:, 1] = 0.0
+    np.testing.assert_allclose(oracle.forward(x, a2, ids2, w13, w2, b13, b2),
+                               oracle.forward(x, a1, ids2, w13, w2, b13, b2),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_batched_matches_contiguous_items():
+    """Scatter real tokens (each routed to k distinct experts) into the batched
+    layout; row (e, i) must equal the contiguous path's weighted item output."""
+    rng = np.random.default_rng(6)
+    E, H, I, M, k, T = 5, 10, 14, 13, 2, 8
+    w13, w2, b13, b2 = _rand_layer(rng, E, H, I)
+    x = rng.standard_normal((M, H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)])
+    a = rng.random((M, k))
+    xb = np.full((E, T, H), np.nan)
+    rw = np.zeros((E, T))
+    cnt = np.zeros(E, dtype=np.int32)
+    where = {}
+    for t in range(M):
+        for j in range(k):
+            e = ids[t, j]
+            i = cnt[e]
+            assert i < T
+            xb[e, i] = x[t]
+            rw[e, i] = a[t, j]
+            where[(e, i)] = (t, j)
+            cnt[e] += 1
+    outs = oracle.forward_batched(xb, cnt, w13, w2, b13, b2, rw)
+    y = np.zeros((M, H))
+    for e in range(E):
+        assert outs[e].shape == (cnt[e], H) and np.isfinite(outs[e]).all()
+        for i in range(cnt[e]):
+            t, j = where[(e, i)]
+            one = np.zeros((1, k))
+            one[0, j] = a[t, j]
+            np.testing.assert_allclose(outs[e][i],
+                                       oracle.forward(x[t:t + 1], one, ids[t:t + 1], w13, w2,
+                                                      b13, b2)[0], rtol=1e-12, atol=1e-12)
+            y[t] += outs[e][i]
+    np.testing.assert_allclose(y, oracle.forward(x, a, ids, w13, w2, b13, b2),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_fp64_oracle_vs_fp32_evaluation():
+    """The fp64 oracle and an fp32 evaluation of the same routed items agree to
+    fp32 rounding on a tiny workload (guards against accidental precision loss
+    in the oracle)."""
+    from mixture_experts_ffn_softmax_gb300 import workloads as wl
+    spec = wl.SPECS["tiny"]
+    d = wl.make_moe_inputs(spec)
+    f = {k: wl.to_f64(v) for k, v in d.items()}
+    y, w, ids, _ = oracle.moe_layer(f["hidden"], f["router_logits"], f["w13"], f["w2"],
+                                    spec.top_k, spec.routing_method, spec.renormalize)
+    x32 = d["hidden"].float()
+    y32 = torch.zeros_like(x32)
+    for t in range(spec.M):
+        for j in range(spec.top_k):
+            e = int(ids[t, j])
+            h = x32[t] @ d["w13"][e].float()
+            z = torch.nn.functional.silu(h[:spec.I]) * h[spec.I:]
+            y32[t] += float(w[t, j]) * (z @ d["w2"][e].float())
+    rel = np.linalg.norm(y - y32.double().numpy()) / np.linalg.norm(y)
+    assert rel < 1e-5
+
+
+# -------------------------------------------------------------- mutations ---
+
+def _pins_fail(golden_dir):
+    """Run the cheap pins; return True if at least one fails."""
+    checks = [lambda: test_route_golden(golden_dir),
+              lambda: test_route_brute_force(0),
+              test_ffn_closed_form,
+              test_single_expert_is_dense_swiglu,
+              test_uniform_topk_all_is_mean_of_experts,
+              test_route_matches_printed_routing_function,
+              lambda: test_align_golden(golden_dir)]
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            return True
+    return False
+
+
+def _mut_gate_up_swapped(x_rows, w13_e, w2_e, b13_e=None, b2_e=None):
+    I = w2_e.shape[0]
+    h = np.asarray(x_rows, float) @ w13_e + (0 if b13_e is None else b13_e)
+    z = om.silu(h[:, I:]) * h[:, :I]
+    return z @ w2_e + (0 if b2_e is None else b2_e)
+
+
+def _mut_b2_dropped(x_rows, w13_e, w2_e, b13_e=None, b2_e=None):
+    return _ORIG_FFN(x_rows, w13_e, w2_e, b13_e, None)
+
+
+def _mut_silu_sign(u):
+    u = np.asarray(u, float)
+    return u / (1.0 + np.exp(u))
+
+
+def _mut_tie_high_id(logits, allowed, top_k):
+    l = np.where(allowed, np.asarray(logits, float), -np.inf)
+    E = l.shape[1]
+    order = np.argsort(-l[:, ::-1], axis=1, kind="stable")
+    return (E - 1 - order)[:, :top_k]
+
+
+def _mut_no_renorm(p, ids, method, renormalize, scale):
+    return np.take_along_axis(p, ids, axis=1) * scale
+
+
+def _mut_sort_unstable_align(topk_ids, E, block_m):
+    a = _orig_align(topk_ids, E, block_m)
+    st = a["sorted_token_ids"].copy()
+    off = a["expert_offsets"]
+    for e in range(E):
+        c = a["expert_num_tokens"][e]
+        st[off[e]:off[e] + c] = st[off[e]:off[e] + c][::-1]
+    a["sorted_token_ids"] = st
+    return a
+
+
+_orig_align = om.align
+_ORIG_FFN = om.expert_ffn
+
+
+@pytest.mark.parametrize("target,mutant", [
+    ("expert_ffn", _mut_gate_up_swapped),
+    ("expert_ffn", _mut_b2_dropped),
+    ("silu", _mut_silu_sign),
+    ("topk_select", _mut_tie_high_id),
+    ("route_weights", _mut_no_renorm),
+    ("align", _mut_sort_unstable_align),
+])
+def test_planted_mistakes_are_caught(monkeypatch, golden_dir, target, mutant):
+    monkeypatch.setattr(om, target, mutant)
+    monkeypatch.setattr(oracle, target, mutant, raising=False)
+    assert _pins_fail(golden_dir), f"no pin caught the planted mistake in {target}"
