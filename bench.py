@@ -1,0 +1,401 @@
+"""Benchmark of the fused MoE forward (route + align + permute + SwiGLU
+grouped GEMM + down-projection grouped GEMM + top-k weight-and-reduce).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mixtral_prefill]
+
+One step = one pass of the whole path over one batch of synthetic inputs of
+the named workload (default: the Mixtral-8x7B-shape layer, prefill M=4096;
+the same layer's M=16 decode is measured alongside and reported under
+"decode").  Weights and inputs are resident in HBM before timing; the
+weights (2.8 GB) exceed the 129 MB L2, so no flush is needed between steps.
+
+--impl reference times the CPU oracle (test infrastructure, fp64 numpy) on a
+bounded sample of the same workload on the host cores.
+
+Multi-GPU: every rank runs an independent replica on its own batch (the
+path shards by tokens with no collective); value = all ranks' tokens / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_ffn_softmax_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "fused-MoE fwd tokens/s and TFLOP/s (1×GB300), % of roofline"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------- distributed --
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    """Samples nvidia-smi clocks / throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads --
+def algorithmic(spec, ids_np):
+    """FLOPs = 6 R H I; bytes = touched expert weights + x + out + logits."""
+    touched = int(np.unique(ids_np).size)
+    wbytes = touched * 3 * spec.H * spec.I * 2
+    if spec.bias:
+        wbytes += touched * (2 * spec.I + spec.H) * 2
+    io = spec.M * spec.H * 2 * 2 + spec.M * spec.E * 4
+    return spec.flops(), wbytes + io, touched
+
+
+class OurStep:
+    def __init__(self, spec, device):
+        import mixture_experts_ffn_softmax_gb300 as pkg
+        self.pkg = pkg
+        self.spec = spec
+        self.d = wl.make_moe_inputs(spec, device=device)
+        M, E, k = spec.M, spec.E, spec.top_k
+        self.w = torch.empty(M, k, dtype=torch.float32, device=device)
+        self.ids = torch.empty(M, k, dtype=torch.int32, device=device)
+        self.ws = pkg.alloc_workspace(pkg.workspace_size(M, spec.H, spec.I, E, k), device)
+        self.out = torch.empty_like(self.d["hidden"])
+
+    def __call__(self, hidden=None, logits=None):
+        s, d, pkg = self.spec, self.d, self.pkg
+        pkg.moe_route(d["router_logits"] if logits is None else logits, s.top_k,
+                      s.routing_method, s.renormalize, s.k_group, s.group_count,
+                      s.group_select_mode, s.routed_scaling_factor, self.w, self.ids)
+        pkg.moe_forward(d["hidden"] if hidden is None else hidden, self.w, self.ids, d["w13"],
+                        d["w2"], d["w13_bias"], d["w2_bias"], self.ws, self.out)
+        return self.out
+
+
+def time_steps(step, K, W, world, ev_stream=None):
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(K):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_ours(args, world, rank, local):
+    import mixture_experts_ffn_softmax_gb300 as pkg
+    pk = peaks()
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    spec = wl.SPECS[args.workload]
+    step = OurStep(spec, device)
+    K, W = args.steps, args.warmup
+
+    # headline: device-resident inputs
+    clocks = ClockSampler(local)
+    n0 = pkg.launch_count()
+    clocks.start()
+    ms = time_steps(step, K, W, world)
+    ck = clocks.stop()
+    launches = pkg.launch_count() - n0
+    ms_step = max_over_ranks(ms / K, world)
+    ids_np = step.ids.cpu().numpy()
+    flops, nbytes, touched = algorithmic(spec, ids_np)
+    tok_s = spec.M * world / (ms_step / 1e3)
+    tflops = flops * world / (ms_step / 1e3) / 1e12
+
+    # per-kernel timing with events on the launching stream (second timed pass)
+    pkg.profiler_start()
+    for _ in range(K):
+        step()
+    prof = pkg.profiler_stop()
+    kern = {k: {"launches": v[0], "avg_us": 1e3 * v[1] / max(v[0], 1)} for k, v in prof.items()}
+
+    g1 = kern.get("gemm1_swiglu", {}).get("avg_us")
+    g2 = kern.get("gemm2_scatter", {}).get("avg_us")
+    step_roof_ms = 1e3 * max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+    if spec.M >= 1024:
+        # tensor-bound: GEMM1 carries 4 R H I of the 6 R H I FLOPs
+        f1 = 4.0 * spec.R * spec.H * spec.I
+        ach = f1 / (g1 * 1e-6) / 1e12
+        roof = {"kernel": "gemm1_swiglu", "bound": "tensor", "achieved": round(ach, 1),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+                "traffic": None, "peak_source": pk["source"] + " burst bf16"}
+    else:
+        b1 = touched * spec.H * 2 * spec.I * 2 + spec.M * spec.H * 2
+        ach = b1 / (g1 * 1e-6) / 1e9
+        roof = {"kernel": "gemm1_swiglu", "bound": "hbm", "achieved": round(ach, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                "traffic": None, "peak_source": pk["source"] + " copy"}
+
+    # end to end through the public API with host buffers
+    hx = step.d["hidden"].cpu().pin_memory()
+    hl = step.d["router_logits"].cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    dx = torch.empty_like(step.d["hidden"])
+    dl = torch.empty_like(step.d["router_logits"])
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        y = step(dx, dl)
+        hy.copy_(y, non_blocking=True)
+
+    ms_e2e = max_over_ranks(time_steps(e2e_step, K, W, world) / K, world)
+    e2e = {"value": round(spec.M * world / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
+           "d2h_bytes_per_step": hy.numel() * 2, "ms_per_step": round(ms_e2e, 4)}
+
+    line = {
+        "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{spec.name}: Mixtral-8x7B-shape MoE layer" if "mixtral" in spec.name
+                   else spec.name, "M": spec.M, "H": spec.H, "I": spec.I, "E": spec.E,
+                   "top_k": spec.top_k, "routing": spec.routing_method,
+                   "renormalize": spec.renormalize, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (weights 2.8 GB)"},
+        "tflops": round(tflops, 2),
+        "roofline_step": {"t_roof_ms": round(step_roof_ms, 4),
+                          "frac": round(step_roof_ms / ms_step, 4),
+                          "bound": "tensor" if flops / pk["bf16_tflops"] / 1e12 > nbytes / pk["hbm_gbs"] / 1e9 else "hbm"},
+        "roofline": roof,
+        "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
+        "gpu_launches": launches,
+        "clocks": ck,
+        "e2e": e2e,
+    }
+
+    # the decode shape of the same layer, reported alongside
+    if args.workload == "mixtral_prefill" and not args.no_decode:
+        dspec = wl.SPECS["mixtral_decode"]
+        dstep = OurStep(dspec, device)
+        dstep.d["w13"], dstep.d["w2"] = step.d["w13"], step.d["w2"]
+        Kd = max(K, 20)
+        dms = max_over_ranks(time_steps(dstep, Kd, max(W, 3), world) / Kd, world)
+        pkg.profiler_start()
+        for _ in range(Kd):
+            dstep()
+        dprof = pkg.profiler_stop()
+        dids = dstep.ids.cpu().numpy()
+        dfl, dby, dt = algorithmic(dspec, dids)
+        g1d = 1e3 * dprof["gemm1_swiglu"][1] / dprof["gemm1_swiglu"][0]
+        b1 = dt * dspec.H * 2 * dspec.I * 2 + dspec.M * dspec.H * 2
+        line["decode"] = {
+            "M": dspec.M, "ms_per_step": round(dms, 4),
+            "tokens_per_s": round(dspec.M * world / (dms / 1e3), 1),
+            "experts_touched": dt,
+            "hbm_roofline_frac": round((dby / (pk["hbm_gbs"] * 1e9)) / (dms / 1e3), 4),
+            "gemm1_hbm_gbs": round(b1 / (g1d * 1e-6) / 1e9, 1),
+            "kernels_us": {k: round(1e3 * v[1] / v[0], 2) for k, v in dprof.items()},
+        }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, step.d, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------- CPU oracle legs --
+def _oracle_sample(spec, d, n_tokens):
+    """Host fp64 copies of a token sample and the experts it touches."""
+    sel = np.arange(n_tokens)
+    x = wl.to_f64(d["hidden"][:n_tokens])
+    logits = wl.to_f64(d["router_logits"][:n_tokens])
+    return sel, x, logits
+
+
+def cpu_baseline(spec, d, budget_s=15.0, kind="oracle"):
+    """Times the CPU oracle (as it stands) on a bounded token sample."""
+    import oracle
+    n = min(spec.M, 256 if spec.H * spec.I >= 4096 * 4096 else 1024)
+    _, x, logits = _oracle_sample(spec, d, n)
+    w13 = wl.to_f64(d["w13"])
+    w2 = wl.to_f64(d["w2"])
+    b13 = wl.to_f64(d["w13_bias"]) if d.get("w13_bias") is not None else None
+    b2 = wl.to_f64(d["w2_bias"]) if d.get("w2_bias") is not None else None
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.moe_layer(x, logits, w13, w2, spec.top_k, spec.routing_method, spec.renormalize,
+                         spec.k_group, spec.group_count, spec.group_select_mode,
+                         spec.routed_scaling_factor, b13, b2)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s / 2 or reps >= 3:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": kind,
+            "sample": f"{n} of {spec.M} tokens of {spec.name}, full routing + {spec.top_k} "
+                      f"experts per token in fp64 numpy, {reps} rep(s), {dt:.2f} s each"}
+
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    spec = wl.SPECS[args.workload]
+    d = wl.make_moe_inputs(spec, device="cpu")
+    import oracle
+    n = min(spec.M, 128)
+    x = wl.to_f64(d["hidden"][:n])
+    logits = wl.to_f64(d["router_logits"][:n])
+    w13, w2 = wl.to_f64(d["w13"]), wl.to_f64(d["w2"])
+    b13 = wl.to_f64(d["w13_bias"]) if d["w13_bias"] is not None else None
+    b2 = wl.to_f64(d["w2_bias"]) if d["w2_bias"] is not None else None
+
+    def step():
+        oracle.moe_layer(x, logits, w13, w2, spec.top_k, spec.routing_method, spec.renormalize,
+                         spec.k_group, spec.group_count, spec.group_select_mode,
+                         spec.routed_scaling_factor, b13, b2)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    v = round(n / dt, 2)
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": spec.name, "M": spec.M, "H": spec.H, "I": spec.I,
+                       "E": spec.E, "top_k": spec.top_k, "parallelism": "cpu oracle"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"{n} of {spec.M} tokens per step (fp64 numpy oracle)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral_prefill", choices=sorted(wl.SPECS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

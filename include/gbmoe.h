@@ -1,0 +1,249 @@
+/*
+ * gbmoe.h -- C ABI of the single-GPU fused Mixture-of-Experts FFN forward
+ * (routing, top-k, expert-sorted permutation, SwiGLU grouped GEMMs, top-k
+ * weight-and-reduce) for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named *device* are device (HBM) pointers owned by the caller;
+ *    the library never allocates, frees or copies device memory on its own
+ *    and never synchronises the stream (except moe_read_error, which says
+ *    so).  All work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and is asynchronous.
+ *  - Tensors are dense, row-major, last dimension contiguous.  "bf16" data
+ *    is IEEE bfloat16 passed as `const void*` (2-byte elements); every bf16
+ *    or fp32 base pointer must be 16-byte aligned.
+ *  - Validation of sizes, enums and pointers happens on the host before any
+ *    launch and returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE_TOO_SMALL without touching the GPU.  Errors that only
+ *    the GPU can see (an expert id out of range, a pipeline wait that ran
+ *    out of time) are written to a device error word and read back with
+ *    moe_read_error; kernels never trap.
+ *  - M == 0 (or an empty batched layout) is a valid no-op returning MOE_OK.
+ *  - moe_last_error_detail() returns a short text for the last failing call
+ *    on the calling thread.
+ *
+ * Citations are to the source pages by title and section.
+ */
+#ifndef GBMOE_H
+#define GBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GBMOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define GBMOE_API __attribute__((visibility("default")))
+#else
+#define GBMOE_API
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+  MOE_ERR_BAD_EXPERT_ID = 4, /* device-detected: topk_ids / counts out of range */
+  MOE_ERR_TIMEOUT = 5,       /* device-detected: a bounded pipeline wait gave up */
+  MOE_ERR_CUDA = 6,          /* a CUDA runtime/driver call failed */
+  MOE_ERR_NO_DEVICE = 7      /* no usable sm_103 device */
+} moe_status_t;
+
+typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID = 1 } moe_routing_t;
+
+/* Where the top-k weight multiply and the k-sum happen ("vLLM
+ * FusedMoEModularKernel" page, TopKWeightAndReduce section).  SEPARATE:
+ * the down-projection epilogue applies bias and weight and writes one fp32
+ * row per routed item; a vectorised reduce kernel sums each token's k rows.
+ * AUTO picks SEPARATE.  EPILOGUE_ATOMIC is reserved (MOE_ERR_UNSUPPORTED). */
+typedef enum {
+  MOE_REDUCE_AUTO = 0,
+  MOE_REDUCE_EPILOGUE_ATOMIC = 1,
+  MOE_REDUCE_SEPARATE = 2
+} moe_reduce_t;
+
+/* GEMM row block: experts' item lists are padded to a multiple of this. */
+#define MOE_BLOCK_M 128
+
+/* ---------------------------------------------------------------- route --
+ * moe_route: router scores -> top-k experts and weights per token.
+ * Defines: "MindIE-SD Fused MoE" page, parameter table (routing_method,
+ * renormalize, k_group, group_count, group_select_mode,
+ * routed_scaling_factor) and routing section; "FlagGems fused_moe.py
+ * analysis", section 1.1 (p_t = softmax(s_t), S_t = TopK(p_t, k)).
+ *
+ *  router_logits  device fp32 [M, E]
+ *  routing_method MOE_ROUTE_SOFTMAX (softmax over E) or MOE_ROUTE_SIGMOID
+ *  renormalize    softmax only: divide the k selected weights by their sum.
+ *                 Sigmoid weights are always divided by their sum.
+ *  group_count    experts split into group_count equal contiguous groups
+ *                 (E % group_count == 0); 1 = no grouping
+ *  k_group        groups kept, 1 <= k_group <= group_count
+ *  group_select_mode 0: group score = max score in the group;
+ *                 1: sum of the group's two largest scores (needs >= 2
+ *                 experts per group)
+ *  top_k          1 <= top_k <= k_group * E / group_count, top_k <= 64
+ *  routed_scaling_factor  multiplies every output weight (after renormalising)
+ *  topk_weights   device fp32 [M, top_k] out
+ *  topk_ids       device int32 [M, top_k] out, by descending score, ties to
+ *                 the lower expert id (and groups' ties to the lower group)
+ * Limits: 1 <= E <= 1024.
+ */
+GBMOE_API moe_status_t moe_route(const float* router_logits, int64_t M, int32_t E, int32_t top_k,
+                       int32_t routing_method, int32_t renormalize, int32_t k_group,
+                       int32_t group_count, int32_t group_select_mode,
+                       float routed_scaling_factor, float* topk_weights, int32_t* topk_ids,
+                       moe_stream_t stream);
+
+/* ---------------------------------------------------------------- align --
+ * moe_align: expert-sorted, block-padded permutation of the routed items.
+ * Defines: "FlagGems fused_moe.py analysis", section moe_align_block_size
+ * (flatten (token, slot) items, sort by expert, pad each expert's count to
+ * BLOCK_SIZE_M; sorted_token_ids, per-block expert ids,
+ * num_tokens_post_padded).
+ *
+ *  topk_ids           device int32 [M, top_k]; item index r = t * top_k + j
+ *  block_m            padding block, 1 <= block_m <= 1024
+ *  sorted_token_ids   device int32 [moe_align_capacity(...)] out: expert e's
+ *                     items in ascending r at [expert_offsets[e],
+ *                     expert_offsets[e] + expert_num_tokens[e]), then the
+ *                     sentinel R = M * top_k up to expert_offsets[e + 1];
+ *                     entries past expert_offsets[E] are left untouched
+ *  expert_offsets     device int32 [E + 1] out: exclusive scan of the padded
+ *                     counts; expert_offsets[E] = num_tokens_post_padded
+ *  expert_num_tokens  device int32 [E] out
+ *  block_expert_ids   device int32 [moe_align_capacity(...) / block_m] out:
+ *                     expert of each block_m-row block, -1 past the last
+ *  scratch            device, moe_align_scratch_size(...) bytes, any content
+ *  error_word         device int32 or NULL: set to MOE_ERR_BAD_EXPERT_ID if
+ *                     an id is outside [0, E) (such items are dropped)
+ */
+GBMOE_API size_t moe_align_capacity(int64_t M, int32_t top_k, int32_t E, int32_t block_m);
+GBMOE_API size_t moe_align_scratch_size(int64_t M, int32_t top_k, int32_t E);
+GBMOE_API moe_status_t moe_align(const int32_t* topk_ids, int64_t M, int32_t top_k, int32_t E,
+                       int32_t block_m, int32_t* sorted_token_ids, int32_t* expert_offsets,
+                       int32_t* expert_num_tokens, int32_t* block_expert_ids, void* scratch,
+                       size_t scratch_bytes, int32_t* error_word, moe_stream_t stream);
+
+/* -------------------------------------------------------------- forward --
+ * moe_forward: y_t = sum_j topk_weights[t, j] * f_{topk_ids[t, j]}(x_t) with
+ * the SwiGLU expert f_e(x) = (SiLU(x W13_e[:, :I] + b13_e[:I]) *
+ * (x W13_e[:, I:] + b13_e[I:])) W2_e + b2_e.
+ * Defines: "FlagGems fused_moe.py analysis", sections 1.1 and 1.2
+ * (routed items h_r, z_r = phi(h_r), o_r, y_t = sum a(r) o_r), SiLU-and-mul
+ * activation; "MindIE-SD Fused MoE" page, function signature (w13 fused
+ * gate/up [E, H, 2I], w2 [E, I, H], w13_bias [E, 2I], w2_bias [E, H]);
+ * "vLLM FusedMoEModularKernel" page, apply() steps (permute, W1 matmul,
+ * activation + mul, W2 matmul, unpermute, top-k weight + reduce).
+ *
+ *  hidden        device bf16 [M, H]
+ *  topk_weights  device fp32 [M, top_k];  topk_ids device int32 [M, top_k]
+ *  w13           device bf16 [E, H, 2I]: columns [0, I) gate, [I, 2I) up
+ *  w2            device bf16 [E, I, H]
+ *  w13_bias      device bf16 [E, 2I] or NULL;  w2_bias device bf16 [E, H] or NULL
+ *  workspace     device, >= moe_workspace_size(...) bytes, 256-byte aligned;
+ *                contents on entry are ignored.  Its first 4 bytes hold the
+ *                call's device error word (see moe_workspace_error_word).
+ *  out           device bf16 [M, H]; may equal hidden (in-place)
+ * Limits: H % 8 == 0, I % 8 == 0 (16-byte row pitch), 1 <= E <= 1024,
+ * 1 <= top_k <= 64.
+ * Tokens are processed in chunks of at most MOE_CHUNK_TOKENS, so the
+ * workspace is bounded by the chunk, not by M.
+ */
+#define MOE_CHUNK_TOKENS 16384
+GBMOE_API moe_status_t moe_workspace_size(int64_t M, int32_t H, int32_t I, int32_t E, int32_t top_k,
+                                int32_t reduce_mode, size_t* bytes);
+GBMOE_API moe_status_t moe_forward(const void* hidden, const float* topk_weights,
+                         const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                         int32_t E, int32_t top_k, const void* w13, const void* w2,
+                         const void* w13_bias, const void* w2_bias, void* workspace,
+                         size_t workspace_bytes, int32_t reduce_mode, void* out,
+                         moe_stream_t stream);
+
+/* ------------------------------------------------------ forward_batched --
+ * moe_forward_batched: the Batched activation format.  Defines: "vLLM
+ * FusedMoEModularKernel" page, Introduction (activations (num_experts,
+ * max_tokens, K) with expert_num_tokens; not every row is valid; Batched
+ * differs from Contiguous only in the permute / unpermute).
+ *   out[e, i] = row_weight[e, i] * f_e(x[e, i])   for i < expert_num_tokens[e]
+ *
+ *  x                  device bf16 [E, T, H]; rows i >= expert_num_tokens[e]
+ *                     are never read (they may hold anything, NaN included)
+ *  expert_num_tokens  device int32 [E], each in [0, T]; a value outside sets
+ *                     MOE_ERR_BAD_EXPERT_ID in the error word and that
+ *                     expert is skipped
+ *  row_weight         device fp32 [E, T] or NULL (= 1)
+ *  out                device bf16 [E, T, H]; rows past the count are not written
+ * Limits as moe_forward; 1 <= T.
+ */
+GBMOE_API moe_status_t moe_batched_workspace_size(int32_t E, int32_t T, int32_t H, int32_t I,
+                                        size_t* bytes);
+GBMOE_API moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens, int32_t E,
+                                 int32_t T, int32_t H, int32_t I, const void* w13,
+                                 const void* w2, const void* w13_bias, const void* w2_bias,
+                                 const float* row_weight, void* workspace,
+                                 size_t workspace_bytes, void* out, moe_stream_t stream);
+
+/* --------------------------------------------------------------- errors --
+ * moe_workspace_error_word: device address of the error word inside a
+ * forward workspace (pure pointer arithmetic, no GPU access).
+ * moe_read_error: SYNCHRONISES `stream`, copies the device error word to
+ * the host and returns it as a status (MOE_OK if zero); if reset != 0 the
+ * word is cleared afterwards.
+ */
+GBMOE_API int32_t* moe_workspace_error_word(void* workspace);
+GBMOE_API moe_status_t moe_read_error(const int32_t* error_word, int32_t reset, moe_stream_t stream);
+
+/* moe_workspace_layout: byte offsets, inside a forward workspace sized for
+ * (M, H, I, E, top_k), of its regions -- for inspecting intermediate stages
+ * in tests.  offsets[0..8] = error word, expert_num_tokens [E],
+ * expert_offsets [E+1], block_expert_ids, sorted_token_ids [cap], align
+ * scratch, permuted rows bf16 [cap, H], z = SiLU(gate)*up bf16 [cap, I],
+ * weighted item outputs fp32 [M*top_k, H] (first token chunk); offsets[9] =
+ * cap (rows of the padded layout).  No GPU access.
+ */
+GBMOE_API moe_status_t moe_workspace_layout(int64_t M, int32_t H, int32_t I, int32_t E,
+                                            int32_t top_k, size_t offsets[10]);
+
+/* moe_selftest_wait_timeout: failure-detection self-test.  Launches one CTA
+ * that waits on an mbarrier nothing ever arrives at, with a wait limit of
+ * limit_us microseconds; the kernel must give up, write MOE_ERR_TIMEOUT to
+ * *error_word (device int32) and return.  Read it with moe_read_error.
+ */
+GBMOE_API moe_status_t moe_selftest_wait_timeout(int32_t* error_word, uint32_t limit_us,
+                                                 moe_stream_t stream);
+
+GBMOE_API const char* moe_status_string(moe_status_t status);
+GBMOE_API const char* moe_last_error_detail(void);
+GBMOE_API int32_t moe_abi_version(void);
+
+/* ------------------------------------------------------------- profiler --
+ * Per-kernel timing with CUDA events recorded on the launching stream
+ * around every kernel the library launches from the calling thread.
+ * moe_profiler_start enables it (and clears previous records);
+ * moe_profiler_stop synchronises on the recorded events, fills up to
+ * `capacity` entries (kernel name, launches, total milliseconds) and
+ * disables it.  Returns the number of distinct kernels in *n.
+ */
+typedef struct {
+  char name[48];
+  int64_t launches;
+  double total_ms;
+} moe_kernel_time_t;
+GBMOE_API moe_status_t moe_profiler_start(void);
+GBMOE_API moe_status_t moe_profiler_stop(moe_kernel_time_t* out, int32_t capacity, int32_t* n);
+/* Total kernel launches issued by the library on this thread since load. */
+GBMOE_API int64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBMOE_H */

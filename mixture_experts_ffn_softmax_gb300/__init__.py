@@ -1,0 +1,227 @@
+"""GB300-native fused Mixture-of-Experts FFN forward.
+
+Python binding of libgbmoe.so with the C ABI's names.  These functions only
+marshal arguments: every step of the path (routing, align, permute, the two
+grouped GEMMs, weight-and-reduce) runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.
+
+    w, ids = moe_route(logits, top_k, "softmax", renormalize=True)
+    y = moe_forward(hidden, w, ids, w13, w2)            # [M, H] bf16
+    y = fused_moe(hidden, logits, w13, w2, top_k, ...)  # route + forward
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_BAD_EXPERT_ID", 5: "MOE_ERR_TIMEOUT",
+          6: "MOE_ERR_CUDA", 7: "MOE_ERR_NO_DEVICE"}
+ROUTING = {"softmax": 0, "sigmoid": 1}
+REDUCE = {"auto": 0, "epilogue_atomic": 1, "separate": 2}
+BLOCK_M = 128
+CHUNK_TOKENS = 16384
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}"
+                         + (f" ({detail})" if detail else ""))
+
+
+def lib():
+    return _lib.load()
+
+
+def _check(st: int, where: str):
+    if st != MOE_OK:
+        d = lib().moe_last_error_detail()
+        raise MoEError(st, where, d.decode() if d else "")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def workspace_size(M: int, H: int, I: int, E: int, top_k: int, reduce: str = "auto") -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(M, H, I, E, top_k, REDUCE[reduce], ctypes.byref(n)),
+           "moe_workspace_size")
+    return n.value
+
+
+def batched_workspace_size(E: int, T: int, H: int, I: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_batched_workspace_size(E, T, H, I, ctypes.byref(n)),
+           "moe_batched_workspace_size")
+    return n.value
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks.
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_route(router_logits: torch.Tensor, top_k: int, routing_method: str = "softmax",
+              renormalize: bool = False, k_group: int = 1, group_count: int = 1,
+              group_select_mode: int = 0, routed_scaling_factor: float = 1.0,
+              topk_weights: Optional[torch.Tensor] = None,
+              topk_ids: Optional[torch.Tensor] = None, stream=None):
+    """router_logits fp32 [M, E] -> (topk_weights fp32 [M, k], topk_ids int32 [M, k])."""
+    assert router_logits.dtype == torch.float32 and router_logits.dim() == 2
+    M, E = router_logits.shape
+    dev = router_logits.device
+    if topk_weights is None:
+        topk_weights = torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    _check(lib().moe_route(_ptr(router_logits), M, E, top_k, ROUTING[routing_method],
+                           int(bool(renormalize)), k_group, group_count, group_select_mode,
+                           float(routed_scaling_factor), _ptr(topk_weights), _ptr(topk_ids),
+                           _stream(stream)), "moe_route")
+    return topk_weights, topk_ids
+
+
+def align_capacity(M: int, top_k: int, E: int, block_m: int = BLOCK_M) -> int:
+    return lib().moe_align_capacity(M, top_k, E, block_m)
+
+
+def moe_align(topk_ids: torch.Tensor, E: int, block_m: int = BLOCK_M,
+              error_word: Optional[torch.Tensor] = None, stream=None):
+    """topk_ids int32 [M, k] -> dict(sorted_token_ids, expert_offsets,
+    expert_num_tokens, block_expert_ids); sorted_token_ids is trimmed to
+    capacity (valid up to expert_offsets[E])."""
+    assert topk_ids.dtype == torch.int32 and topk_ids.dim() == 2
+    M, k = topk_ids.shape
+    dev = topk_ids.device
+    cap = align_capacity(M, k, E, block_m)
+    sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    blocks = torch.empty(max(cap // block_m, 1), dtype=torch.int32, device=dev)
+    scratch_n = lib().moe_align_scratch_size(M, k, E)
+    scratch = torch.empty(max(scratch_n, 4), dtype=torch.uint8, device=dev)
+    _check(lib().moe_align(_ptr(topk_ids), M, k, E, block_m, _ptr(sorted_ids), _ptr(offsets),
+                           _ptr(counts), _ptr(blocks), _ptr(scratch), scratch.numel(),
+                           _ptr(error_word), _stream(stream)), "moe_align")
+    return {"sorted_token_ids": sorted_ids[:cap], "expert_offsets": offsets,
+            "expert_num_tokens": counts, "block_expert_ids": blocks[:cap // block_m]}
+
+
+def moe_forward(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: torch.Tensor,
+                w13: torch.Tensor, w2: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
+                w2_bias: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, reduce: str = "auto", stream=None):
+    """y [M, H] bf16 = sum_j topk_weights[:, j] * SwiGLU-expert_{topk_ids[:, j]}(hidden)."""
+    M, H = hidden.shape
+    E, H2, I2 = w13.shape
+    I = I2 // 2
+    k = topk_ids.shape[1]
+    assert hidden.dtype == torch.bfloat16 and w13.dtype == torch.bfloat16
+    assert w2.dtype == torch.bfloat16 and tuple(w2.shape) == (E, I, H) and H2 == H
+    assert topk_ids.dtype == torch.int32 and topk_weights.dtype == torch.float32
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(M, H, I, E, k, reduce), hidden.device)
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(lib().moe_forward(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E, k,
+                             _ptr(w13), _ptr(w2), _ptr(w13_bias), _ptr(w2_bias),
+                             _ptr(workspace), workspace.numel(), REDUCE[reduce], _ptr(out),
+                             _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_forward_batched(x: torch.Tensor, expert_num_tokens: torch.Tensor, w13: torch.Tensor,
+                        w2: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
+                        w2_bias: Optional[torch.Tensor] = None,
+                        row_weight: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None, stream=None):
+    """Batched layout: x [E, T, H] bf16 with expert_num_tokens [E] int32 ->
+    out [E, T, H] bf16 (rows past the count are not written)."""
+    E, T, H = x.shape
+    I = w13.shape[2] // 2
+    assert expert_num_tokens.dtype == torch.int32
+    if workspace is None:
+        workspace = alloc_workspace(batched_workspace_size(E, T, H, I), x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    _check(lib().moe_forward_batched(_ptr(x), _ptr(expert_num_tokens), E, T, H, I, _ptr(w13),
+                                     _ptr(w2), _ptr(w13_bias), _ptr(w2_bias), _ptr(row_weight),
+                                     _ptr(workspace), workspace.numel(), _ptr(out),
+                                     _stream(stream)), "moe_forward_batched")
+    return out
+
+
+def fused_moe(hidden: torch.Tensor, router_logits: torch.Tensor, w13: torch.Tensor,
+              w2: torch.Tensor, top_k: int, w13_bias=None, w2_bias=None, k_group: int = 1,
+              group_count: int = 1, group_select_mode: int = 0, routing_method: str = "softmax",
+              renormalize: bool = False, routed_scaling_factor: float = 1.0, workspace=None,
+              out=None, stream=None):
+    """The whole layer: route, then forward (the MindIE-SD `fused_moe` shape)."""
+    w, ids = moe_route(router_logits, top_k, routing_method, renormalize, k_group, group_count,
+                       group_select_mode, routed_scaling_factor, stream=stream)
+    return moe_forward(hidden, w, ids, w13, w2, w13_bias, w2_bias, workspace, out, stream=stream)
+
+
+def workspace_error_word(workspace: torch.Tensor) -> int:
+    return lib().moe_workspace_error_word(_ptr(workspace))
+
+
+def read_error(error_word_ptr: int, reset: bool = True, stream=None) -> int:
+    """Synchronises the stream and returns the device error status (0 = ok)."""
+    return lib().moe_read_error(error_word_ptr, int(reset), _stream(stream))
+
+
+def workspace_layout(M: int, H: int, I: int, E: int, top_k: int) -> dict:
+    """Byte offsets of the forward workspace's regions (for inspecting
+    intermediate stages)."""
+    arr = (ctypes.c_size_t * 10)()
+    _check(lib().moe_workspace_layout(M, H, I, E, top_k, arr), "moe_workspace_layout")
+    names = ["error_word", "expert_num_tokens", "expert_offsets", "block_expert_ids",
+             "sorted_token_ids", "align_scratch", "a_perm", "z", "item_out", "cap"]
+    return dict(zip(names, list(arr)))
+
+
+def selftest_wait_timeout(error_word: torch.Tensor, limit_us: int = 20000, stream=None):
+    _check(lib().moe_selftest_wait_timeout(_ptr(error_word), limit_us, _stream(stream)),
+           "moe_selftest_wait_timeout")
+
+
+def launch_count() -> int:
+    return lib().moe_launch_count()
+
+
+def profiler_start():
+    _check(lib().moe_profiler_start(), "moe_profiler_start")
+
+
+def profiler_stop():
+    """Returns {kernel name: (launches, total_ms)} for launches since start."""
+    cap = 64
+    arr = (_lib.KernelTime * cap)()
+    n = ctypes.c_int32(0)
+    _check(lib().moe_profiler_stop(arr, cap, ctypes.byref(n)), "moe_profiler_stop")
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}
+
+
+__all__ = ["moe_route", "moe_align", "moe_forward", "moe_forward_batched", "fused_moe",
+           "workspace_size", "batched_workspace_size", "alloc_workspace", "align_capacity",
+           "workspace_error_word", "read_error", "launch_count", "workspace_layout",
+           "selftest_wait_timeout", "profiler_start",
+           "profiler_stop", "MoEError", "STATUS", "lib"]

@@ -1,0 +1,290 @@
+// Expert-sorted, block-padded permutation of the routed items.
+//
+// Follows "FlagGems fused_moe.py analysis", section moe_align_block_size:
+// flatten the (token, slot) items, sort them by expert, pad each expert's
+// count up to the GEMM block size, and emit sorted_token_ids, the expert of
+// every block and the padded total.  Items of one expert keep ascending item
+// order (a stable sort); padding slots hold the sentinel R.
+//
+// Three deterministic passes, no atomics in the ranking:
+//   1. chunk histogram  -- each warp counts the experts of one 256-item chunk
+//   2. scan             -- one CTA: per-expert prefix over chunks, padded
+//                          counts, exclusive scan over experts, block ids,
+//                          sentinel fill of the padding slots
+//   3. scatter          -- each warp re-walks its chunk in order and writes
+//                          every item at offsets[e] + chunk prefix + rank
+#include "common.cuh"
+
+namespace gbmoe {
+namespace {
+
+constexpr int kChunk = 256;        // items per warp chunk
+constexpr int kAlignWarps = 8;     // warps (= chunks) per CTA
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ bool valid_id(int e, int E) { return e >= 0 && e < E; }
+
+__global__ void __launch_bounds__(kAlignWarps * 32)
+    align_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int num_chunks,
+                      int32_t* __restrict__ chunk_counts, int32_t* error_word) {
+  extern __shared__ int32_t hist_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kAlignWarps + warp;
+  if (chunk >= num_chunks) return;
+  int32_t* cnt = hist_smem + warp * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const int64_t r0 = static_cast<int64_t>(chunk) * kChunk;
+  bool bad = false;
+  for (int it = 0; it < kChunk / 32; ++it) {
+    const int64_t r = r0 + it * 32 + lane;
+    int e = -1;
+    if (r < R) e = ids[r];
+    const bool ok = (r < R) && valid_id(e, E);
+    bad |= (r < R) && !ok;
+    const int key = ok ? e : -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(grp) - 1;
+    if (ok && lane == leader) cnt[e] += __popc(grp);
+    __syncwarp();
+  }
+  if (bad) record_error(error_word, MOE_ERR_BAD_EXPERT_ID);
+  // expert-major layout: chunk_counts[e * num_chunks + chunk]
+  for (int e = lane; e < E; e += 32)
+    chunk_counts[static_cast<int64_t>(e) * num_chunks + chunk] = cnt[e];
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+    align_scan_kernel(int E, int num_chunks, int block_m, int32_t sentinel, int64_t cap,
+                      int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ block_expert,
+                      int32_t* __restrict__ sorted) {
+  __shared__ int32_t s_count[1024];
+  __shared__ int32_t s_off[1025];
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // (a) per expert: exclusive prefix over chunks (in place) and the total.
+  for (int e = warp; e < E; e += kScanThreads / 32) {
+    int32_t* col = chunk_counts + static_cast<int64_t>(e) * num_chunks;
+    const int per = ceil_div(num_chunks, 32);
+    const int c0 = lane * per, c1 = min(num_chunks, c0 + per);
+    int32_t part = 0;
+    for (int c = c0; c < c1; ++c) part += col[c];
+    int32_t incl = part;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int32_t run = incl - part;
+    for (int c = c0; c < c1; ++c) {
+      const int32_t v = col[c];
+      col[c] = run;
+      run += v;
+    }
+    const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) s_count[e] = total;
+  }
+  __syncthreads();
+
+  // (b) padded counts -> exclusive scan over experts (E <= 1024).
+  int32_t padded = 0;
+  if (tid < E) padded = ceil_div(s_count[tid], block_m) * block_m;
+  int32_t incl = padded;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = s_warp[lane];
+    int32_t wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += v;
+    }
+    s_warp[lane] = wi - w;
+  }
+  __syncthreads();
+  const int32_t excl = s_warp[warp] + incl - padded;
+  if (tid < E) {
+    s_off[tid] = excl;
+    counts[tid] = s_count[tid];
+    offsets[tid] = excl;
+  }
+  if (tid == E - 1) {
+    s_off[E] = excl + padded;
+    offsets[E] = excl + padded;
+  }
+  __syncthreads();
+
+  // (c) expert id of every block, -1 past the last block.
+  const int64_t nblk_cap = cap / block_m;
+  const int32_t nblk = s_off[E] / block_m;
+  for (int64_t b = tid; b < nblk_cap; b += kScanThreads) {
+    int32_t e = -1;
+    if (b < nblk) {
+      int lo = 0, hi = E - 1;  // largest e with s_off[e] <= b * block_m
+      const int32_t pos = static_cast<int32_t>(b) * block_m;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      e = lo;
+    }
+    block_expert[b] = e;
+  }
+  // (d) sentinel in every padding slot.
+  for (int e = warp; e < E; e += kScanThreads / 32)
+    for (int32_t pos = s_off[e] + s_count[e] + lane; pos < s_off[e + 1]; pos += 32)
+      sorted[pos] = sentinel;
+}
+
+__global__ void __launch_bounds__(kAlignWarps * 32)
+    align_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int num_chunks,
+                         const int32_t* __restrict__ chunk_prefix,
+                         const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted) {
+  extern __shared__ int32_t run_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kAlignWarps + warp;
+  if (chunk >= num_chunks) return;
+  int32_t* run = run_smem + warp * E;
+  for (int e = lane; e < E; e += 32)
+    run[e] = offsets[e] + chunk_prefix[static_cast<int64_t>(e) * num_chunks + chunk];
+  __syncwarp();
+  const int64_t r0 = static_cast<int64_t>(chunk) * kChunk;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int it = 0; it < kChunk / 32; ++it) {
+    const int64_t r = r0 + it * 32 + lane;
+    int e = -1;
+    if (r < R) e = ids[r];
+    const bool ok = (r < R) && valid_id(e, E);
+    const int key = ok ? e : -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    if (ok) sorted[run[e] + __popc(grp & lt_mask)] = static_cast<int32_t>(r);
+    __syncwarp();
+    if (ok && lane == __ffs(grp) - 1) run[e] += __popc(grp);
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+    batched_plan_kernel(const int32_t* __restrict__ counts_in, int E, int T, int block_m,
+                        int32_t sentinel, int64_t cap, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted,
+                        int32_t* error_word) {
+  __shared__ int32_t s_count[1024];
+  __shared__ int32_t s_off[1025];
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int32_t c = 0;
+  if (tid < E) {
+    c = counts_in[tid];
+    if (c < 0 || c > T) {
+      record_error(error_word, MOE_ERR_BAD_EXPERT_ID);
+      c = 0;
+    }
+    s_count[tid] = c;
+  }
+  const int32_t padded = (tid < E) ? ceil_div(c, block_m) * block_m : 0;
+  int32_t incl = padded;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = s_warp[lane];
+    int32_t wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += v;
+    }
+    s_warp[lane] = wi - w;
+  }
+  __syncthreads();
+  const int32_t excl = s_warp[warp] + incl - padded;
+  if (tid < E) {
+    s_off[tid] = excl;
+    offsets[tid] = excl;
+  }
+  if (tid == E - 1) {
+    s_off[E] = excl + padded;
+    offsets[E] = excl + padded;
+  }
+  __syncthreads();
+  const int64_t nblk_cap = cap / block_m;
+  const int32_t nblk = s_off[E] / block_m;
+  for (int64_t b = tid; b < nblk_cap; b += kScanThreads) {
+    int32_t e = -1;
+    if (b < nblk) {
+      int lo = 0, hi = E - 1;
+      const int32_t pos = static_cast<int32_t>(b) * block_m;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      e = lo;
+    }
+    block_expert[b] = e;
+  }
+  for (int e = warp; e < E; e += kScanThreads / 32) {
+    const int32_t base = s_off[e], cnt = s_count[e], end = s_off[e + 1];
+    for (int32_t i = lane; base + i < end; i += 32)
+      sorted[base + i] = (i < cnt) ? e * T + i : sentinel;
+  }
+}
+
+}  // namespace
+
+size_t align_scratch_bytes(int64_t R, int32_t E) {
+  const int64_t chunks = ceil_div<int64_t>(R, kChunk);
+  return static_cast<size_t>(chunks) * static_cast<size_t>(E) * sizeof(int32_t);
+}
+
+moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
+  const int num_chunks = static_cast<int>(ceil_div<int64_t>(a.R, kChunk));
+  const size_t smem = static_cast<size_t>(kAlignWarps) * a.E * sizeof(int32_t);
+  const unsigned grid = static_cast<unsigned>(ceil_div(num_chunks, kAlignWarps));
+  if (num_chunks > 0) {
+    prof_before("align_hist", s);
+    align_hist_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
+                                                           a.chunk_counts, a.error_word);
+    prof_after("align_hist", s);
+    if (moe_status_t st = check_launch("align_hist")) return st;
+  }
+  prof_before("align_scan", s);
+  align_scan_kernel<<<1, kScanThreads, 0, s>>>(a.E, num_chunks, a.block_m,
+                                               static_cast<int32_t>(a.R), a.cap,
+                                               a.chunk_counts, a.counts, a.offsets,
+                                               a.block_expert, a.sorted);
+  prof_after("align_scan", s);
+  if (moe_status_t st = check_launch("align_scan")) return st;
+  if (num_chunks > 0) {
+    prof_before("align_scatter", s);
+    align_scatter_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
+                                                              a.chunk_counts, a.offsets,
+                                                              a.sorted);
+    prof_after("align_scatter", s);
+    if (moe_status_t st = check_launch("align_scatter")) return st;
+  }
+  return MOE_OK;
+}
+
+moe_status_t launch_batched_plan(const BatchedPlanArgs& a, cudaStream_t s) {
+  prof_before("batched_plan", s);
+  batched_plan_kernel<<<1, kScanThreads, 0, s>>>(a.counts_in, a.E, a.T, a.block_m, a.sentinel,
+                                                 a.cap, a.offsets, a.block_expert, a.sorted,
+                                                 a.error_word);
+  prof_after("batched_plan", s);
+  return check_launch("batched_plan");
+}
+
+}  // namespace gbmoe

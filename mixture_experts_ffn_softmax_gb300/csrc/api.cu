@@ -1,0 +1,563 @@
+// C-ABI entry points: host-side validation, workspace layout, the token
+// chunk loop, launch bookkeeping and the event-based kernel profiler.
+//
+// The forward follows the "vLLM FusedMoEModularKernel" page's apply() step
+// list (permute, W1 matmul, activation + mul, W2 matmul, unpermute, top-k
+// weight + reduce) and workspace_shapes() idea (intermediates live in one
+// caller-allocated workspace), and the "FlagGems fused_moe.py analysis"
+// chunk loop (tokens processed CHUNK_SIZE = 16 * 1024 at a time to bound
+// the intermediate caches) and its input validation list.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace gbmoe {
+
+// ------------------------------------------------------------- errors ---
+namespace {
+thread_local char g_detail[512] = "";
+thread_local int64_t g_launches = 0;
+
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+thread_local bool g_prof = false;
+thread_local std::vector<ProfRec> g_recs;
+thread_local std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t take_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+moe_status_t set_error(moe_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+moe_status_t check_launch(const char* name) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "launch of %s failed: %s", name, cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+void prof_before(const char* name, cudaStream_t s) {
+  ++g_launches;
+  if (!g_prof) return;
+  cudaEvent_t a = take_event();
+  cudaEventRecord(a, s);
+  g_recs.push_back({name, a, nullptr});
+}
+
+void prof_after(const char* /*name*/, cudaStream_t s) {
+  if (!g_prof || g_recs.empty()) return;
+  cudaEvent_t b = take_event();
+  cudaEventRecord(b, s);
+  g_recs.back().b = b;
+}
+
+namespace {
+
+// ------------------------------------------------------------- device ---
+moe_status_t check_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(MOE_ERR_NO_DEVICE, "no CUDA device");
+  }
+  static int cached_dev = -1, cached_ok = 0, cached_sms = 0;
+  if (dev != cached_dev) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaGetLastError();
+    cached_dev = dev;
+    cached_ok = (major == 10 && minor == 3);
+    cached_sms = sms;
+    if (!cached_ok)
+      return set_error(MOE_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
+                       dev, major, minor);
+  }
+  if (!cached_ok) return set_error(MOE_ERR_NO_DEVICE, "device is not sm_103");
+  if (num_sms) *num_sms = cached_sms;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr size_t kRegionAlign = 1024;
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int64_t align_cap(int64_t R, int32_t E, int32_t block_m) {
+  const int64_t busy = R < E ? R : E;  // experts that can be non-empty
+  const int64_t cap = R + busy * (block_m - 1);
+  return round_up(static_cast<size_t>(cap), static_cast<size_t>(block_m));
+}
+
+// Workspace of one forward chunk (Rc routed items).
+struct FwdLayout {
+  int64_t cap = 0;
+  size_t err = 0, counts = 0, offsets = 0, block_expert = 0, sorted = 0, scratch = 0,
+         a_perm = 0, z = 0, o = 0, total = 0;
+};
+
+FwdLayout fwd_layout(int64_t Mc, int32_t H, int32_t I, int32_t E, int32_t k) {
+  FwdLayout L;
+  const int64_t Rc = Mc * k;
+  L.cap = align_cap(Rc, E, MOE_BLOCK_M);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, kRegionAlign);
+    return at;
+  };
+  L.err = take(256);
+  L.counts = take(sizeof(int32_t) * E);
+  L.offsets = take(sizeof(int32_t) * (E + 1));
+  L.block_expert = take(sizeof(int32_t) * (L.cap / MOE_BLOCK_M));
+  L.sorted = take(sizeof(int32_t) * L.cap);
+  L.scratch = take(align_scratch_bytes(Rc, E));
+  L.a_perm = take(sizeof(bf16) * L.cap * H);
+  L.z = take(sizeof(bf16) * L.cap * I);
+  L.o = take(sizeof(float) * Rc * H);
+  L.total = off;
+  return L;
+}
+
+struct BatLayout {
+  int64_t cap = 0;
+  size_t err = 0, offsets = 0, block_expert = 0, sorted = 0, a_perm = 0, z = 0, total = 0;
+};
+
+BatLayout bat_layout(int32_t E, int32_t T, int32_t H, int32_t I) {
+  BatLayout L;
+  L.cap = static_cast<int64_t>(E) * T + static_cast<int64_t>(E) * (MOE_BLOCK_M - 1);
+  L.cap = round_up(static_cast<size_t>(L.cap), MOE_BLOCK_M);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, kRegionAlign);
+    return at;
+  };
+  L.err = take(256);
+  L.offsets = take(sizeof(int32_t) * (E + 1));
+  L.block_expert = take(sizeof(int32_t) * (L.cap / MOE_BLOCK_M));
+  L.sorted = take(sizeof(int32_t) * L.cap);
+  L.a_perm = take(sizeof(bf16) * L.cap * H);
+  L.z = take(sizeof(bf16) * L.cap * I);
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+
+moe_status_t validate_ffn_dims(int32_t H, int32_t I, int32_t E) {
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_INVALID_ARG, "E=%d outside [1, 1024]", E);
+  if (H < 8 || H % 8 != 0) return set_error(MOE_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", H);
+  if (I < 8 || I % 8 != 0) return set_error(MOE_ERR_INVALID_ARG, "I=%d must be a positive multiple of 8", I);
+  if (static_cast<int64_t>(H) > (1 << 24) || static_cast<int64_t>(I) > (1 << 24))
+    return set_error(MOE_ERR_INVALID_ARG, "H or I too large");
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace gbmoe
+
+using namespace gbmoe;
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return GBMOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_BAD_EXPERT_ID: return "MOE_ERR_BAD_EXPERT_ID";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_NO_DEVICE: return "MOE_ERR_NO_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_error_detail(void) { return g_detail; }
+
+int64_t moe_launch_count(void) { return g_launches; }
+
+// ---------------------------------------------------------------- route --
+moe_status_t moe_route(const float* router_logits, int64_t M, int32_t E, int32_t top_k,
+                       int32_t routing_method, int32_t renormalize, int32_t k_group,
+                       int32_t group_count, int32_t group_select_mode,
+                       float routed_scaling_factor, float* topk_weights, int32_t* topk_ids,
+                       moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M=%lld < 0", (long long)M);
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_INVALID_ARG, "E=%d outside [1, 1024]", E);
+  if (routing_method != MOE_ROUTE_SOFTMAX && routing_method != MOE_ROUTE_SIGMOID)
+    return set_error(MOE_ERR_INVALID_ARG, "routing_method=%d", routing_method);
+  if (group_count < 1 || E % group_count != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "E=%d not divisible by group_count=%d", E, group_count);
+  if (k_group < 1 || k_group > group_count)
+    return set_error(MOE_ERR_INVALID_ARG, "k_group=%d outside [1, group_count=%d]", k_group,
+                     group_count);
+  if (group_select_mode != 0 && group_select_mode != 1)
+    return set_error(MOE_ERR_INVALID_ARG, "group_select_mode=%d", group_select_mode);
+  if (group_count > 1 && group_select_mode == 1 && E / group_count < 2)
+    return set_error(MOE_ERR_INVALID_ARG, "group_select_mode=1 needs >= 2 experts per group");
+  const int32_t reachable = (group_count > 1) ? k_group * (E / group_count) : E;
+  if (top_k < 1 || top_k > 64 || top_k > reachable)
+    return set_error(MOE_ERR_INVALID_ARG, "top_k=%d outside [1, min(64, %d)]", top_k, reachable);
+  if (!(routed_scaling_factor == routed_scaling_factor) ||
+      routed_scaling_factor > 3.0e38f || routed_scaling_factor < -3.0e38f)
+    return set_error(MOE_ERR_INVALID_ARG, "routed_scaling_factor is not finite");
+  if (M == 0) return MOE_OK;
+  if (!router_logits || !topk_weights || !topk_ids)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (moe_status_t st = check_device(nullptr)) return st;
+  RouteArgs a{router_logits, M, E, top_k, routing_method, renormalize ? 1 : 0, k_group,
+              group_count, group_select_mode, routed_scaling_factor, topk_weights, topk_ids};
+  return launch_route(a, stream);
+}
+
+// ---------------------------------------------------------------- align --
+size_t moe_align_capacity(int64_t M, int32_t top_k, int32_t E, int32_t block_m) {
+  if (M < 0 || top_k < 1 || E < 1 || block_m < 1) return 0;
+  return static_cast<size_t>(align_cap(M * top_k, E, block_m));
+}
+
+size_t moe_align_scratch_size(int64_t M, int32_t top_k, int32_t E) {
+  if (M < 0 || top_k < 1 || E < 1) return 0;
+  return align_scratch_bytes(M * top_k, E);
+}
+
+moe_status_t moe_align(const int32_t* topk_ids, int64_t M, int32_t top_k, int32_t E,
+                       int32_t block_m, int32_t* sorted_token_ids, int32_t* expert_offsets,
+                       int32_t* expert_num_tokens, int32_t* block_expert_ids, void* scratch,
+                       size_t scratch_bytes, int32_t* error_word, moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M < 0");
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_INVALID_ARG, "E=%d outside [1, 1024]", E);
+  if (top_k < 1 || top_k > 1024) return set_error(MOE_ERR_INVALID_ARG, "top_k=%d", top_k);
+  if (block_m < 1 || block_m > 1024)
+    return set_error(MOE_ERR_INVALID_ARG, "block_m=%d outside [1, 1024]", block_m);
+  const int64_t R = M * top_k;
+  if (align_cap(R, E, block_m) >= (int64_t(1) << 31))
+    return set_error(MOE_ERR_INVALID_ARG, "too many routed items for int32 indices");
+  if (!expert_offsets || !expert_num_tokens || !block_expert_ids || !sorted_token_ids)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (R > 0 && !topk_ids) return set_error(MOE_ERR_INVALID_ARG, "null topk_ids");
+  const size_t need = align_scratch_bytes(R, E);
+  if (need > 0 && (scratch == nullptr || scratch_bytes < need))
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL, "align scratch needs %zu bytes", need);
+  if (moe_status_t st = check_device(nullptr)) return st;
+  AlignArgs a{topk_ids, R, E, block_m, sorted_token_ids, expert_offsets, expert_num_tokens,
+              block_expert_ids, static_cast<int32_t*>(scratch), align_cap(R, E, block_m),
+              error_word};
+  return launch_align(a, stream);
+}
+
+// -------------------------------------------------------------- forward --
+moe_status_t moe_workspace_size(int64_t M, int32_t H, int32_t I, int32_t E, int32_t top_k,
+                                int32_t reduce_mode, size_t* bytes) {
+  g_detail[0] = 0;
+  if (!bytes) return set_error(MOE_ERR_INVALID_ARG, "null bytes");
+  if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M < 0");
+  if (moe_status_t st = validate_ffn_dims(H, I, E)) return st;
+  if (top_k < 1 || top_k > 64) return set_error(MOE_ERR_INVALID_ARG, "top_k=%d outside [1, 64]", top_k);
+  if (reduce_mode != MOE_REDUCE_AUTO && reduce_mode != MOE_REDUCE_SEPARATE) {
+    if (reduce_mode == MOE_REDUCE_EPILOGUE_ATOMIC)
+      return set_error(MOE_ERR_UNSUPPORTED, "MOE_REDUCE_EPILOGUE_ATOMIC is not built");
+    return set_error(MOE_ERR_INVALID_ARG, "reduce_mode=%d", reduce_mode);
+  }
+  const int64_t Mc = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
+  *bytes = fwd_layout(Mc, H, I, E, top_k).total;
+  return MOE_OK;
+}
+
+int32_t* moe_workspace_error_word(void* workspace) { return static_cast<int32_t*>(workspace); }
+
+moe_status_t moe_forward(const void* hidden, const float* topk_weights,
+                         const int32_t* topk_ids, int64_t M, int32_t H, int32_t I, int32_t E,
+                         int32_t top_k, const void* w13, const void* w2, const void* w13_bias,
+                         const void* w2_bias, void* workspace, size_t workspace_bytes,
+                         int32_t reduce_mode, void* out, moe_stream_t stream) {
+  size_t need = 0;
+  if (moe_status_t st = moe_workspace_size(M, H, I, E, top_k, reduce_mode, &need)) return st;
+  if (M == 0) return MOE_OK;
+  if (!hidden || !topk_weights || !topk_ids || !w13 || !w2 || !workspace || !out)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) ||
+      !aligned16(topk_weights) || (w13_bias && !aligned16(w13_bias)) ||
+      (w2_bias && !aligned16(w2_bias)))
+    return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < need)
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", need,
+                     workspace_bytes);
+  int sms = 0;
+  if (moe_status_t st = check_device(&sms)) return st;
+  cudaStream_t s = stream;
+
+  const int64_t Mc_max = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
+  const FwdLayout L = fwd_layout(Mc_max, H, I, E, top_k);
+  int32_t* err = at<int32_t>(workspace, L.err);
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
+
+  const bf16* x = static_cast<const bf16*>(hidden);
+  bf16* y = static_cast<bf16*>(out);
+  for (int64_t c0 = 0; c0 < M; c0 += Mc_max) {
+    const int64_t Mc = (M - c0) < Mc_max ? (M - c0) : Mc_max;
+    const int64_t Rc = Mc * top_k;
+    const int64_t cap = align_cap(Rc, E, MOE_BLOCK_M);
+    int32_t* sorted = at<int32_t>(workspace, L.sorted);
+    int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    AlignArgs al{topk_ids + c0 * top_k, Rc, E, MOE_BLOCK_M, sorted, offsets,
+                 at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.block_expert),
+                 at<int32_t>(workspace, L.scratch), cap, err};
+    if (moe_status_t st = launch_align(al, s)) return st;
+
+    bf16* a_perm = at<bf16>(workspace, L.a_perm);
+    GatherArgs ga{x + c0 * H, sorted, offsets, E, top_k, static_cast<int32_t>(Rc), H, cap,
+                  a_perm};
+    if (moe_status_t st = launch_gather(ga, s)) return st;
+
+    bf16* z = at<bf16>(workspace, L.z);
+    GroupedGemmArgs g1{};
+    g1.a = a_perm;
+    g1.w = static_cast<const bf16*>(w13);
+    g1.bias = static_cast<const bf16*>(w13_bias);
+    g1.cap = cap;
+    g1.E = E;
+    g1.N = I;
+    g1.K = H;
+    g1.offsets = offsets;
+    g1.out = z;
+    g1.error_word = err;
+    g1.num_sms = sms;
+    if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
+
+    float* o = at<float>(workspace, L.o);
+    GroupedGemmArgs g2{};
+    g2.a = z;
+    g2.w = static_cast<const bf16*>(w2);
+    g2.bias = static_cast<const bf16*>(w2_bias);
+    g2.cap = cap;
+    g2.E = E;
+    g2.N = H;
+    g2.K = I;
+    g2.offsets = offsets;
+    g2.out = o;
+    g2.row_index = sorted;
+    g2.row_weight = topk_weights + c0 * top_k;
+    g2.sentinel = static_cast<int32_t>(Rc);
+    g2.error_word = err;
+    g2.num_sms = sms;
+    if (moe_status_t st = launch_gemm2_scatter_f32(g2, s)) return st;
+
+    if (moe_status_t st = launch_reduce(o, Mc, top_k, H, y + c0 * H, s)) return st;
+  }
+  return MOE_OK;
+}
+
+// ------------------------------------------------------ forward_batched --
+moe_status_t moe_batched_workspace_size(int32_t E, int32_t T, int32_t H, int32_t I,
+                                        size_t* bytes) {
+  g_detail[0] = 0;
+  if (!bytes) return set_error(MOE_ERR_INVALID_ARG, "null bytes");
+  if (moe_status_t st = validate_ffn_dims(H, I, E)) return st;
+  if (T < 1) return set_error(MOE_ERR_INVALID_ARG, "T=%d < 1", T);
+  if (static_cast<int64_t>(E) * T + static_cast<int64_t>(E) * MOE_BLOCK_M >= (int64_t(1) << 31))
+    return set_error(MOE_ERR_INVALID_ARG, "E*T too large for int32 row indices");
+  *bytes = bat_layout(E, T, H, I).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens, int32_t E,
+                                 int32_t T, int32_t H, int32_t I, const void* w13,
+                                 const void* w2, const void* w13_bias, const void* w2_bias,
+                                 const float* row_weight, void* workspace,
+                                 size_t workspace_bytes, void* out, moe_stream_t stream) {
+  size_t need = 0;
+  if (moe_status_t st = moe_batched_workspace_size(E, T, H, I, &need)) return st;
+  if (!x || !expert_num_tokens || !w13 || !w2 || !workspace || !out)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) ||
+      (w13_bias && !aligned16(w13_bias)) || (w2_bias && !aligned16(w2_bias)))
+    return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < need)
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", need,
+                     workspace_bytes);
+  int sms = 0;
+  if (moe_status_t st = check_device(&sms)) return st;
+  cudaStream_t s = stream;
+  const BatLayout L = bat_layout(E, T, H, I);
+  int32_t* err = at<int32_t>(workspace, L.err);
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
+  const int32_t sentinel = E * T;
+  int32_t* sorted = at<int32_t>(workspace, L.sorted);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  BatchedPlanArgs bp{expert_num_tokens, E, T, MOE_BLOCK_M, sorted, offsets,
+                     at<int32_t>(workspace, L.block_expert), L.cap, sentinel, err};
+  if (moe_status_t st = launch_batched_plan(bp, s)) return st;
+
+  bf16* a_perm = at<bf16>(workspace, L.a_perm);
+  GatherArgs ga{static_cast<const bf16*>(x), sorted, offsets, E, 1, sentinel, H, L.cap, a_perm};
+  if (moe_status_t st = launch_gather(ga, s)) return st;
+
+  bf16* z = at<bf16>(workspace, L.z);
+  GroupedGemmArgs g1{};
+  g1.a = a_perm;
+  g1.w = static_cast<const bf16*>(w13);
+  g1.bias = static_cast<const bf16*>(w13_bias);
+  g1.cap = L.cap;
+  g1.E = E;
+  g1.N = I;
+  g1.K = H;
+  g1.offsets = offsets;
+  g1.out = z;
+  g1.error_word = err;
+  g1.num_sms = sms;
+  if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
+
+  GroupedGemmArgs g2{};
+  g2.a = z;
+  g2.w = static_cast<const bf16*>(w2);
+  g2.bias = static_cast<const bf16*>(w2_bias);
+  g2.cap = L.cap;
+  g2.E = E;
+  g2.N = H;
+  g2.K = I;
+  g2.offsets = offsets;
+  g2.out = out;
+  g2.row_index = sorted;
+  g2.row_weight = row_weight;
+  g2.sentinel = sentinel;
+  g2.error_word = err;
+  g2.num_sms = sms;
+  return launch_gemm2_rows_bf16(g2, s);
+}
+
+moe_status_t moe_workspace_layout(int64_t M, int32_t H, int32_t I, int32_t E, int32_t top_k,
+                                  size_t offsets[10]) {
+  size_t need = 0;
+  if (!offsets) return set_error(MOE_ERR_INVALID_ARG, "null offsets");
+  if (moe_status_t st = moe_workspace_size(M, H, I, E, top_k, MOE_REDUCE_AUTO, &need)) return st;
+  const int64_t Mc = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
+  const FwdLayout L = fwd_layout(Mc, H, I, E, top_k);
+  const size_t v[10] = {L.err, L.counts, L.offsets, L.block_expert, L.sorted, L.scratch,
+                        L.a_perm, L.z, L.o, static_cast<size_t>(L.cap)};
+  for (int i = 0; i < 10; ++i) offsets[i] = v[i];
+  return MOE_OK;
+}
+
+moe_status_t moe_selftest_wait_timeout(int32_t* error_word, uint32_t limit_us,
+                                       moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (!error_word) return set_error(MOE_ERR_INVALID_ARG, "null error word");
+  if (limit_us == 0 || limit_us > 1000000u)
+    return set_error(MOE_ERR_INVALID_ARG, "limit_us must be in [1, 1e6]");
+  if (moe_status_t st = check_device(nullptr)) return st;
+  return launch_wait_timeout_probe(error_word, limit_us, stream);
+}
+
+// --------------------------------------------------------------- errors --
+moe_status_t moe_read_error(const int32_t* error_word, int32_t reset, moe_stream_t stream) {
+  if (!error_word) return set_error(MOE_ERR_INVALID_ARG, "null error word");
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, error_word, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "reading the error word: %s",
+                     cudaGetErrorString(cudaGetLastError()));
+  if (reset && host != 0) {
+    if (cudaMemsetAsync(const_cast<int32_t*>(error_word), 0, sizeof(int32_t), stream) !=
+        cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "clearing the error word");
+  }
+  return static_cast<moe_status_t>(host);
+}
+
+// ------------------------------------------------------------- profiler --
+moe_status_t moe_profiler_start(void) {
+  for (auto& r : g_recs) {
+    if (r.a) g_pool.push_back(r.a);
+    if (r.b) g_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  g_prof = true;
+  return MOE_OK;
+}
+
+moe_status_t moe_profiler_stop(moe_kernel_time_t* out, int32_t capacity, int32_t* n) {
+  g_prof = false;
+  struct Agg {
+    std::string name;
+    int64_t launches;
+    double ms;
+  };
+  std::vector<Agg> agg;
+  moe_status_t st = MOE_OK;
+  for (auto& r : g_recs) {
+    if (!r.a || !r.b) continue;
+    if (cudaEventSynchronize(r.b) != cudaSuccess) {
+      st = set_error(MOE_ERR_CUDA, "cudaEventSynchronize: %s",
+                     cudaGetErrorString(cudaGetLastError()));
+      break;
+    }
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    bool found = false;
+    for (auto& a : agg)
+      if (a.name == r.name) {
+        a.launches++;
+        a.ms += ms;
+        found = true;
+      }
+    if (!found) agg.push_back({r.name, 1, ms});
+  }
+  for (auto& r : g_recs) {
+    if (r.a) g_pool.push_back(r.a);
+    if (r.b) g_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  if (n) *n = static_cast<int32_t>(agg.size());
+  if (out) {
+    for (int32_t i = 0; i < capacity && i < static_cast<int32_t>(agg.size()); ++i) {
+      std::memset(out[i].name, 0, sizeof(out[i].name));
+      std::strncpy(out[i].name, agg[i].name.c_str(), sizeof(out[i].name) - 1);
+      out[i].launches = agg[i].launches;
+      out[i].total_ms = agg[i].ms;
+    }
+  }
+  return st;
+}
+
+}  // extern "C"

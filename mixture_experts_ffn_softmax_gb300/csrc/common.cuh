@@ -1,0 +1,118 @@
+// Shared declarations of the gbmoe CUDA library (kernels + host launchers).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/gbmoe.h"
+
+namespace gbmoe {
+
+using bf16 = __nv_bfloat16;
+
+// A bounded wait gives up after this long; the kernel then records
+// MOE_ERR_TIMEOUT in the error word and returns instead of hanging.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ void record_error(int32_t* error_word, int32_t code) {
+  if (error_word != nullptr) atomicCAS(error_word, 0, code);
+}
+
+template <typename T>
+__host__ __device__ constexpr T ceil_div(T a, T b) {
+  return (a + b - 1) / b;
+}
+
+// ---- host-side launch bookkeeping (api.cu) ----
+// Every kernel launch goes through these so the profiler can bracket it with
+// CUDA events on the launching stream and count launches.
+void prof_before(const char* name, cudaStream_t s);
+void prof_after(const char* name, cudaStream_t s);
+moe_status_t set_error(moe_status_t st, const char* fmt, ...);
+moe_status_t check_launch(const char* name);
+
+// ---- launchers (one per .cu file) ----
+struct RouteArgs {
+  const float* logits;
+  int64_t M;
+  int32_t E, top_k, method, renormalize, k_group, group_count, group_select_mode;
+  float scale;
+  float* weights;
+  int32_t* ids;
+};
+moe_status_t launch_route(const RouteArgs& a, cudaStream_t s);
+
+struct AlignArgs {
+  const int32_t* ids;   // [R] expert id per item
+  int64_t R;            // items
+  int32_t E, block_m;
+  int32_t* sorted;      // [cap]
+  int32_t* offsets;     // [E+1]
+  int32_t* counts;      // [E]
+  int32_t* block_expert;  // [cap / block_m]
+  int32_t* chunk_counts;  // scratch [num_chunks * E]
+  int64_t cap;
+  int32_t* error_word;
+};
+size_t align_scratch_bytes(int64_t R, int32_t E);
+moe_status_t launch_align(const AlignArgs& a, cudaStream_t s);
+
+// Batched layout plan: per expert e, rows e*T + i (i < count_e) in order,
+// padded with the sentinel to a multiple of block_m.
+struct BatchedPlanArgs {
+  const int32_t* counts_in;  // [E]
+  int32_t E, T, block_m;
+  int32_t* sorted;     // [cap]
+  int32_t* offsets;    // [E+1]
+  int32_t* block_expert;
+  int64_t cap;
+  int32_t sentinel;
+  int32_t* error_word;
+};
+moe_status_t launch_batched_plan(const BatchedPlanArgs& a, cudaStream_t s);
+
+// A_perm[p, :] = src[index[p] / div, :] for p < offsets[E] (zero row when
+// index[p] >= sentinel).
+struct GatherArgs {
+  const bf16* src;
+  const int32_t* index;
+  const int32_t* offsets;  // [E+1]; offsets[E] = number of rows to produce
+  int32_t E;
+  int32_t div;
+  int32_t sentinel;
+  int32_t H;
+  int64_t cap;
+  bf16* dst;
+};
+moe_status_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+// y[t, :] = bf16( sum_j o[t*k + j, :] )
+moe_status_t launch_reduce(const float* o, int64_t M, int32_t k, int32_t H, bf16* y,
+                           cudaStream_t s);
+
+// Grouped GEMMs (gemm.cu).
+struct GroupedGemmArgs {
+  // operands
+  const bf16* a;          // [cap, K] expert-sorted rows
+  const bf16* w;          // GEMM1: w13 [E, K=H, 2N]; GEMM2: w2 [E, K=I, N=H]
+  const bf16* bias;       // GEMM1: [E, 2N]; GEMM2: [E, N]; or null
+  int64_t cap;            // rows of a
+  int32_t E, N, K;        // GEMM1: N = I (per half); GEMM2: N = H
+  const int32_t* offsets;  // [E+1] padded expert offsets
+  // epilogue
+  void* out;              // GEMM1: z bf16 [cap, N]; GEMM2: fp32 [*, N] or bf16 [*, N]
+  const int32_t* row_index;  // GEMM2: destination row per sorted position
+  const float* row_weight;   // GEMM2: weight per destination row, or null (=1)
+  int32_t sentinel;          // GEMM2: row_index >= sentinel -> not stored
+  int32_t* error_word;
+  int32_t num_sms;
+};
+moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s);
+moe_status_t launch_gemm2_scatter_f32(const GroupedGemmArgs& a, cudaStream_t s);
+moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s);
+
+}  // namespace gbmoe

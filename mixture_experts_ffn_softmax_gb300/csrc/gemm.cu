@@ -1,0 +1,511 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA through a 4-stage mbarrier pipeline.
+//
+// "FlagGems fused_moe.py analysis", section 1.3 / fused_moe_kernel: over the
+// expert-sorted, block-padded items, C[r, n] = sum_k A[t(r), k] B[e(r), n, k];
+// one program handles one block of rows of one expert and one block of output
+// columns; the expert of a row block comes from the align output.  Weights
+// are stored as on the "MindIE-SD Fused MoE" page: w13 [E, H, 2I] and
+// w2 [E, I, H], i.e. N-contiguous, so B is fed to the MMA as an MN-major
+// operand straight from its storage layout.
+//
+// Kernel shape (persistent, one CTA per SM, 192 threads):
+//   warp 0  lane 0 : TMA producer (A tile 128x64, B tile 64x256 per stage)
+//   warp 1         : TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=256,
+//                    K=16) and commits stage / accumulator barriers
+//   warps 2..5     : epilogue, one TMEM lane quadrant each (tcgen05.ld)
+// The 512 TMEM columns hold two 128x256 fp32 accumulators so the epilogue of
+// tile i overlaps the MMAs of tile i+1.
+//
+// Tiles are enumerated expert by expert, column block by column block, with
+// the row blocks of one expert innermost, so CTAs running at the same time
+// share the same weight columns in L2.  The tile count is read on the device
+// from the padded expert offsets: no host synchronisation.
+//
+// Epilogues:
+//   SwiGLU     : GEMM1.  Columns [0,128) of the accumulator are the gate
+//                block, [128,256) the matching up block; writes
+//                z = SiLU(gate + b_gate) * (up + b_up) as bf16.
+//   ScatterF32 : GEMM2, contiguous layout.  o = (acc + b2) * w(row) as fp32
+//                into row row_index[p] (the routed item) of the item buffer.
+//   RowsBF16   : GEMM2, batched layout.  Same, written as bf16 into the
+//                output row row_index[p] = e * T + i.
+// Every mbarrier wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT,
+// all roles stop, in-flight copies are given time to land, TMEM is freed.
+#include <algorithm>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace gbmoe {
+namespace {
+
+constexpr int BM = MOE_BLOCK_M;  // 128 rows per tile (MMA M)
+constexpr int BK = 64;           // K per stage: one 128-byte swizzle row of bf16
+constexpr int MMA_N = 256;       // accumulator columns per tile
+constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
+constexpr int STAGES = 4;
+constexpr int NTHREADS = 192;
+constexpr int A_STAGE_BYTES = BM * BK * 2;                 // 16 KB
+constexpr int B_CHUNK_BYTES = BK * 64 * 2;                 // 8 KB: 64 k-rows x 64 n
+constexpr int B_CHUNKS = MMA_N / 64;                       // 4
+constexpr int B_STAGE_BYTES = B_CHUNKS * B_CHUNK_BYTES;    // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // 48 KB
+constexpr int TMEM_COLS = 2 * MMA_N;                       // 512
+constexpr int MAX_E = 1024;
+constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES +
+                              (MAX_E + 1) * sizeof(int32_t);
+
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
+
+enum class Epi { SwiGLU = 0, ScatterF32 = 1, RowsBF16 = 2 };
+
+struct Ctl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint32_t tmem_base;
+  int32_t abort;
+};
+
+struct KParams {
+  const bf16* bias;
+  void* out;
+  const int32_t* offsets;
+  const int32_t* row_index;
+  const float* row_weight;
+  int32_t* error_word;
+  int32_t E, N, K, NB, sentinel;
+};
+
+// Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
+// when another role of the CTA has aborted, or after limit_ns, in which case
+// it records MOE_ERR_TIMEOUT and raises the CTA's abort flag.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* abort,
+                                             int32_t* err, uint64_t limit_ns = kWaitLimitNs) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int32_t*>(abort)) return false;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      *reinterpret_cast<volatile int32_t*>(abort) = 1;
+      record_error(err, MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// One CTA waits on a barrier that nothing arrives at; the bounded wait must
+// end it with MOE_ERR_TIMEOUT.
+__global__ void wait_timeout_probe_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) bounded_wait(&bar, 0, &abort_flag, err, limit_ns);
+}
+
+struct Tile {
+  int e, row0, nb;
+};
+
+// Tile t -> (expert, first padded row, column block).  Row blocks of one
+// expert are innermost.  s_off holds the padded expert offsets.
+__device__ __forceinline__ Tile map_tile(int t, const int32_t* s_off, int E, int NB) {
+  int lo = 0, hi = E - 1;  // largest e with (s_off[e] / BM) * NB <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((s_off[mid] / BM) * NB <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int mblocks = (s_off[e + 1] - s_off[e]) / BM;
+  const int local = t - (s_off[e] / BM) * NB;
+  Tile tl;
+  tl.e = e;
+  tl.nb = local / mblocks;
+  tl.row0 = s_off[e] + (local % mblocks) * BM;
+  return tl;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Loads 8 bf16 bias values as floats (zeros if bias == null or past n_lim).
+__device__ __forceinline__ void load_bias8(const bf16* bias, int64_t off, bool ok, float* f) {
+  if (bias != nullptr && ok) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(bias + off));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(h[i]);
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = 0.f;
+  }
+}
+
+template <Epi EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const KParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Ctl ctl;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // 1024-byte aligned tile area (128-byte swizzle atoms), then offsets.
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  int32_t* s_off = reinterpret_cast<int32_t*>(tiles + STAGES * STAGE_BYTES);
+
+  for (int i = threadIdx.x; i <= P.E; i += NTHREADS) s_off[i] = P.offsets[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&ctl.full[s], 1);
+      ptx::mbar_init(&ctl.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&ctl.tmem_full[a], 1);
+      ptx::mbar_init(&ctl.tmem_empty[a], 4 * 32);
+    }
+    ctl.abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl.tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+
+  const int total_tiles = (s_off[P.E] / BM) * P.NB;
+  const int KB = ceil_div(P.K, BK);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const Tile tl = map_tile(t, s_off, P.E, P.NB);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = tiles + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          ptx::mbar_arrive_expect_tx(&ctl.full[stage], STAGE_BYTES);
+          ptx::tma_load_2d(sa, &tmA, &ctl.full[stage], kb * BK, tl.row0);
+          if constexpr (EPI == Epi::SwiGLU) {
+            // gate columns [nb*128, +128) then the same columns of the up half
+#pragma unroll
+            for (int c = 0; c < B_CHUNKS; ++c)
+              ptx::tma_load_4d(sb + c * B_CHUNK_BYTES, &tmB, &ctl.full[stage],
+                               tl.nb * (MMA_N / 2) + (c & 1) * 64, c >> 1, kb * BK, tl.e);
+          } else {
+#pragma unroll
+            for (int c = 0; c < B_CHUNKS; ++c)
+              ptx::tma_load_3d(sb + c * B_CHUNK_BYTES, &tmB, &ctl.full[stage],
+                               tl.nb * MMA_N + c * 64, kb * BK, tl.e);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        if (!bounded_wait(&ctl.tmem_empty[acc], acc_phase ^ 1u, &ctl.abort, P.error_word)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!bounded_wait(&ctl.full[stage], phase, &ctl.abort, P.error_word)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < BK / UMMA_K; ++ks) {
+            // A (K-major): advance 16 bf16 = 32 bytes along the swizzled row.
+            const uint64_t adesc = ptx::smem_desc_sw128(sa + ks * 32, 16, 1024);
+            // B (MN-major): advance 16 k-rows = 2048 bytes; 64-column chunks
+            // are B_CHUNK_BYTES apart, 8-row k groups 1024 bytes apart.
+            const uint64_t bdesc = ptx::smem_desc_sw128(sb + ks * 2048, B_CHUNK_BYTES, 1024);
+            ptx::mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | ks) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&ctl.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&ctl.tmem_full[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const Tile tl = map_tile(t, s_off, P.E, P.NB);
+      const bool got = bounded_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, P.error_word);
+      if (!__all_sync(0xffffffffu, got)) break;
+      ptx::tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * MMA_N);
+      const int64_t p = tl.row0 + row;
+
+      if constexpr (EPI == Epi::SwiGLU) {
+        bf16* z = reinterpret_cast<bf16*>(P.out);
+        const int N = P.N;
+        const int64_t bias_row = static_cast<int64_t>(tl.e) * 2 * N;
+#pragma unroll 1
+        for (int c = 0; c < MMA_N / 2; c += 32) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld_32cols(taddr + c, g);
+          ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c, u);
+          ptx::tmem_ld_wait();
+          const int n0 = tl.nb * (MMA_N / 2) + c;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int n = n0 + v * 8;
+            const bool in = n < N;
+            float bg[8], bu[8];
+            load_bias8(P.bias, bias_row + n, in, bg);
+            load_bias8(P.bias, bias_row + N + n, in, bu);
+            uint4 pk;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float g0 = __uint_as_float(g[v * 8 + 2 * i]) + bg[2 * i];
+              const float g1 = __uint_as_float(g[v * 8 + 2 * i + 1]) + bg[2 * i + 1];
+              const float u0 = __uint_as_float(u[v * 8 + 2 * i]) + bu[2 * i];
+              const float u1 = __uint_as_float(u[v * 8 + 2 * i + 1]) + bu[2 * i + 1];
+              w[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+            }
+            if (in) *reinterpret_cast<uint4*>(z + p * N + n) = pk;
+          }
+        }
+      } else {
+        const int N = P.N;
+        const int32_t dst = P.row_index[p];
+        const bool store = dst >= 0 && dst < P.sentinel;
+        const float wgt = (store && P.row_weight != nullptr) ? P.row_weight[dst] : 1.0f;
+        const int64_t bias_row = static_cast<int64_t>(tl.e) * N;
+#pragma unroll 1
+        for (int c = 0; c < MMA_N; c += 32) {
+          uint32_t a[32];
+          ptx::tmem_ld_32cols(taddr + c, a);
+          ptx::tmem_ld_wait();
+          const int n0 = tl.nb * MMA_N + c;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int n = n0 + v * 8;
+            const bool in = n < N;
+            float b[8];
+            load_bias8(P.bias, bias_row + n, in, b);
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = (__uint_as_float(a[v * 8 + i]) + b[i]) * wgt;
+            if (store && in) {
+              if constexpr (EPI == Epi::ScatterF32) {
+                float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(P.out) +
+                                                      static_cast<int64_t>(dst) * N + n);
+                d[0] = make_float4(o[0], o[1], o[2], o[3]);
+                d[1] = make_float4(o[4], o[5], o[6], o[7]);
+              } else {
+                uint4 pk;
+                pk.x = pack_bf16x2(o[0], o[1]);
+                pk.y = pack_bf16x2(o[2], o[3]);
+                pk.z = pack_bf16x2(o[4], o[5]);
+                pk.w = pack_bf16x2(o[6], o[7]);
+                *reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(P.out) +
+                                          static_cast<int64_t>(dst) * N + n) = pk;
+              }
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ctl.tmem_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*reinterpret_cast<volatile int32_t*>(&ctl.abort)) {
+    // Give TMA copies and MMAs still in flight time to land before the
+    // shared memory and TMEM of this CTA are released.
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+    __syncthreads();
+  }
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle.  dims/strides innermost first;
+// strides are in bytes for dims 1..rank-1.
+moe_status_t make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd,
+                        gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", r);
+  return MOE_OK;
+}
+
+template <Epi EPI>
+moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                       cudaGetErrorString(cudaGetLastError()));
+    attr_done = true;
+  }
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.cap)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (moe_status_t st = make_map(&tmA, a.a, 2, dims, strides, box)) return st;
+  }
+  int NB;
+  if constexpr (EPI == Epi::SwiGLU) {
+    // w13 [E, K, 2, N] viewed 4-D: (n, half, k, e)
+    const uint64_t dims[4] = {static_cast<uint64_t>(a.N), 2, static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.E)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(a.N) * 2,
+                                 static_cast<uint64_t>(a.N) * 4,
+                                 static_cast<uint64_t>(a.N) * 4 * a.K};
+    const uint32_t box[4] = {64, 1, BK, 1};
+    if (moe_status_t st = make_map(&tmB, a.w, 4, dims, strides, box)) return st;
+    NB = ceil_div(a.N, MMA_N / 2);
+  } else {
+    // w2 [E, K, N] viewed 3-D: (n, k, e)
+    const uint64_t dims[3] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(a.N) * 2,
+                                 static_cast<uint64_t>(a.N) * 2 * a.K};
+    const uint32_t box[3] = {64, BK, 1};
+    if (moe_status_t st = make_map(&tmB, a.w, 3, dims, strides, box)) return st;
+    NB = ceil_div(a.N, MMA_N);
+  }
+  KParams P;
+  P.bias = a.bias;
+  P.out = a.out;
+  P.offsets = a.offsets;
+  P.row_index = a.row_index;
+  P.row_weight = a.row_weight;
+  P.error_word = a.error_word;
+  P.E = a.E;
+  P.N = a.N;
+  P.K = a.K;
+  P.NB = NB;
+  P.sentinel = a.sentinel;
+  const int64_t max_tiles = (a.cap / BM) * NB;
+  if (max_tiles <= 0) return MOE_OK;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_tiles, a.num_sms));
+  prof_before(name, s);
+  grouped_gemm_kernel<EPI><<<grid, NTHREADS, SMEM_BYTES, s>>>(tmA, tmB, P);
+  prof_after(name, s);
+  return check_launch(name);
+}
+
+}  // namespace
+
+moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s) {
+  prof_before("wait_timeout_probe", s);
+  wait_timeout_probe_kernel<<<1, 32, 0, s>>>(err, static_cast<uint64_t>(limit_us) * 1000ull);
+  prof_after("wait_timeout_probe", s);
+  return check_launch("wait_timeout_probe");
+}
+
+moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::SwiGLU>(a, "gemm1_swiglu", s);
+}
+moe_status_t launch_gemm2_scatter_f32(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::ScatterF32>(a, "gemm2_scatter", s);
+}
+moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::RowsBF16>(a, "gemm2_rows_bf16", s);
+}
+
+}  // namespace gbmoe

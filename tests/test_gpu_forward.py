@@ -1,0 +1,211 @@
+"""GPU parity of moe_forward / fused_moe against the oracle.
+
+Small workloads (every routing structure, ragged H/I/M, biases) are compared
+element by element; the full-size workloads run in the same launch
+configuration the benchmark times and are compared on sampled tokens that the
+oracle computes one by one.  Outputs: relative L2 <= 1e-2 and
+max abs <= 5e-2 * RMS of the oracle output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mixture_experts_ffn_softmax_gb300 as pkg
+from mixture_experts_ffn_softmax_gb300 import workloads as wl
+
+from helpers import LazyF64, check_out, check_route, f64, route_args
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_route(spec, logits):
+    a = route_args(spec)
+    return oracle.route(f64(logits), a["top_k"], a["method"], a["renormalize"], a["k_group"],
+                        a["group_count"], a["group_select_mode"], a["routed_scaling_factor"])
+
+
+@pytest.mark.parametrize("name", sorted(wl.SMALL_SPECS))
+def test_forward_small_workloads(name):
+    spec = wl.SMALL_SPECS[name]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    w, ids, _ = _oracle_route(spec, d["router_logits"])
+    tw = torch.from_numpy(w.astype(np.float32)).cuda()
+    tids = torch.from_numpy(ids).cuda()
+    y = pkg.moe_forward(d["hidden"], tw, tids, d["w13"], d["w2"], d["w13_bias"], d["w2_bias"])
+    torch.cuda.synchronize()
+    ref = oracle.forward(f64(d["hidden"]), w.astype(np.float32).astype(np.float64), ids,
+                         f64(d["w13"]), f64(d["w2"]), f64(d["w13_bias"]), f64(d["w2_bias"]))
+    check_out(f64(y), ref, name)
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek_small", "qwen_small", "ragged_small"])
+def test_fused_layer_small_workloads(name):
+    """route + forward through the GPU path vs oracle.moe_layer."""
+    spec = wl.SMALL_SPECS[name]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    a = route_args(spec)
+    y = pkg.fused_moe(d["hidden"], d["router_logits"], d["w13"], d["w2"], spec.top_k,
+                      d["w13_bias"], d["w2_bias"], spec.k_group, spec.group_count,
+                      spec.group_select_mode, spec.routing_method, spec.renormalize,
+                      spec.routed_scaling_factor)
+    gw, gids = pkg.moe_route(d["router_logits"], spec.top_k, a["method"], a["renormalize"],
+                             a["k_group"], a["group_count"], a["group_select_mode"],
+                             a["routed_scaling_factor"])
+    torch.cuda.synchronize()
+    check_route(d["router_logits"].cpu().numpy(), gw.cpu().numpy(), gids.cpu().numpy(), a)
+    ref, _, _, _ = oracle.moe_layer(f64(d["hidden"]), f64(d["router_logits"]), f64(d["w13"]),
+                                    f64(d["w2"]), spec.top_k, spec.routing_method,
+                                    spec.renormalize, spec.k_group, spec.group_count,
+                                    spec.group_select_mode, spec.routed_scaling_factor,
+                                    f64(d["w13_bias"]), f64(d["w2_bias"]))
+    check_out(f64(y), ref, name)
+
+
+def test_intermediate_stages_tiny():
+    """The permuted rows are bit-exact copies of the routed tokens; z matches
+    SiLU(gate) * up of the oracle within bf16 rounding."""
+    spec = wl.SMALL_SPECS["mixtral_small"]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    w, ids, _ = _oracle_route(spec, d["router_logits"])
+    tw = torch.from_numpy(w.astype(np.float32)).cuda()
+    tids = torch.from_numpy(ids).cuda()
+    M, H, I, E, k = spec.M, spec.H, spec.I, spec.E, spec.top_k
+    ws = pkg.alloc_workspace(pkg.workspace_size(M, H, I, E, k))
+    pkg.moe_forward(d["hidden"], tw, tids, d["w13"], d["w2"], workspace=ws)
+    torch.cuda.synchronize()
+    lay = pkg.workspace_layout(M, H, I, E, k)
+    al = oracle.align(ids, E, pkg.BLOCK_M)
+    n = al["num_tokens_post_padded"]
+    b = ws.cpu()
+
+    def view(off, count, dtype):
+        nbytes = count * torch.tensor([], dtype=dtype).element_size()
+        return b[off:off + nbytes].view(dtype)
+
+    st = view(lay["sorted_token_ids"], n, torch.int32).numpy()
+    assert st.tolist() == al["sorted_token_ids"].tolist()
+    a_perm = view(lay["a_perm"], n * H, torch.bfloat16).view(n, H)
+    x = d["hidden"].cpu()
+    valid = st < M * k
+    assert torch.equal(a_perm[torch.from_numpy(valid)], x[torch.from_numpy(st[valid] // k)])
+    assert (a_perm[torch.from_numpy(~valid)] == 0).all()
+    z = view(lay["z"], n * I, torch.bfloat16).view(n, I).double().numpy()
+    xf, w13 = f64(d["hidden"]), f64(d["w13"])
+    zref = np.zeros((n, I))
+    for p in np.flatnonzero(valid):
+        e = ids.reshape(-1)[st[p]]
+        h = xf[st[p] // k] @ w13[e]
+        zref[p] = oracle.silu(h[:I]) * h[I:]
+    check_out(z[valid], zref[valid], "z")
+
+
+def test_forward_in_place_and_reuse():
+    spec = wl.SMALL_SPECS["ragged_small"]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    w, ids, _ = _oracle_route(spec, d["router_logits"])
+    tw = torch.from_numpy(w.astype(np.float32)).cuda()
+    tids = torch.from_numpy(ids).cuda()
+    ws = pkg.alloc_workspace(pkg.workspace_size(spec.M, spec.H, spec.I, spec.E, spec.top_k))
+    ws.fill_(0xFF)  # workspace contents on entry must not matter
+    y1 = pkg.moe_forward(d["hidden"], tw, tids, d["w13"], d["w2"], d["w13_bias"],
+                         d["w2_bias"], workspace=ws)
+    x = d["hidden"].clone()
+    y2 = pkg.moe_forward(x, tw, tids, d["w13"], d["w2"], d["w13_bias"], d["w2_bias"],
+                         workspace=ws, out=x)                     # in place
+    torch.cuda.synchronize()
+    assert y2.data_ptr() == x.data_ptr()
+    assert torch.equal(y1, y2)
+    assert pkg.read_error(pkg.workspace_error_word(ws)) == 0
+
+
+@pytest.mark.parametrize("case", [
+    dict(M=1, H=64, I=64, E=1, k=1),
+    dict(M=5, H=136, I=72, E=3, k=3),      # top_k = E
+    dict(M=300, H=256, I=320, E=16, k=1),
+    dict(M=129, H=512, I=256, E=4, k=2, one_expert=True),
+    dict(M=40, H=64, I=128, E=8, k=4, dup=True),
+    dict(M=20000, H=64, I=64, E=4, k=2),   # crosses the 16384-token chunk
+])
+def test_forward_edge_cases(case):
+    g = torch.Generator(device="cuda").manual_seed(5)
+    M, H, I, E, k = case["M"], case["H"], case["I"], case["E"], case["k"]
+    x = torch.randn(M, H, generator=g, device="cuda").bfloat16()
+    w13 = (torch.randn(E, H, 2 * I, generator=g, device="cuda") * 0.05).bfloat16()
+    w2 = (torch.randn(E, I, H, generator=g, device="cuda") * 0.05).bfloat16()
+    rng = np.random.default_rng(M)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+    if case.get("one_expert"):
+        ids[:, 0] = 2
+        ids[:, 1] = np.where(ids[:, 1] == 2, 0, ids[:, 1])
+    if case.get("dup"):
+        ids[:, 1] = ids[:, 0]
+    wts = rng.random((M, k)).astype(np.float32)
+    y = pkg.moe_forward(x, torch.from_numpy(wts).cuda(), torch.from_numpy(ids).cuda(), w13, w2)
+    torch.cuda.synchronize()
+    if M > 4096:   # oracle on a sample of tokens (both chunks)
+        sel = np.r_[0:64, 16380:16400, M - 64:M]
+        ref = oracle.forward(f64(x)[sel], wts[sel], ids[sel], f64(w13), f64(w2))
+        check_out(f64(y)[sel], ref, str(case))
+    else:
+        ref = oracle.forward(f64(x), wts, ids, f64(w13), f64(w2))
+        check_out(f64(y), ref, str(case))
+
+
+def test_forward_uniform_topk_is_mean():
+    """All logits equal and top_k = E through the GPU path: the output is the
+    mean of the dense expert outputs."""
+    g = torch.Generator(device="cuda").manual_seed(9)
+    M, H, I, E = 70, 128, 192, 4
+    x = torch.randn(M, H, generator=g, device="cuda").bfloat16()
+    w13 = (torch.randn(E, H, 2 * I, generator=g, device="cuda") * 0.05).bfloat16()
+    w2 = (torch.randn(E, I, H, generator=g, device="cuda") * 0.05).bfloat16()
+    y = pkg.fused_moe(x, torch.zeros(M, E, device="cuda"), w13, w2, E, renormalize=False)
+    torch.cuda.synchronize()
+    xf, a, b = f64(x), f64(w13), f64(w2)
+    mean = sum(oracle.expert_ffn(xf, a[e], b[e]) for e in range(E)) / E
+    check_out(f64(y), mean, "uniform top-k")
+
+
+def test_forward_bad_ids_report_error():
+    g = torch.Generator(device="cuda").manual_seed(2)
+    M, H, I, E, k = 16, 64, 64, 4, 2
+    x = torch.randn(M, H, generator=g, device="cuda").bfloat16()
+    w13 = torch.randn(E, H, 2 * I, generator=g, device="cuda").bfloat16()
+    w2 = torch.randn(E, I, H, generator=g, device="cuda").bfloat16()
+    ids = torch.zeros(M, k, dtype=torch.int32, device="cuda")
+    ids[3, 1] = 7
+    ws = pkg.alloc_workspace(pkg.workspace_size(M, H, I, E, k))
+    pkg.moe_forward(x, torch.ones(M, k, device="cuda"), ids, w13, w2, workspace=ws)
+    assert pkg.read_error(pkg.workspace_error_word(ws)) == 4   # MOE_ERR_BAD_EXPERT_ID
+
+
+FULL = ["mixtral_prefill", "mixtral_decode", "deepseek_m64", "deepseek_m8192", "qwen_skew"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_forward_full_size_sampled(name):
+    """Full-size layer in the benchmark's launch configuration; sampled tokens
+    checked against the oracle one by one."""
+    spec = wl.SPECS[name]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    a = route_args(spec)
+    ws = pkg.alloc_workspace(pkg.workspace_size(spec.M, spec.H, spec.I, spec.E, spec.top_k))
+    gw, gids = pkg.moe_route(d["router_logits"], spec.top_k, a["method"], a["renormalize"],
+                             a["k_group"], a["group_count"], a["group_select_mode"],
+                             a["routed_scaling_factor"])
+    y = pkg.moe_forward(d["hidden"], gw, gids, d["w13"], d["w2"], d["w13_bias"], d["w2_bias"],
+                        workspace=ws)
+    torch.cuda.synchronize()
+    assert pkg.read_error(pkg.workspace_error_word(ws)) == 0
+    gw_np, gids_np = gw.cpu().numpy(), gids.cpu().numpy()
+    check_route(d["router_logits"].cpu().numpy(), gw_np, gids_np, a)
+    rng = np.random.default_rng(0)
+    n = min(spec.M, 12 if spec.E > 64 else 24)
+    sel = np.sort(rng.choice(spec.M, size=n, replace=False))
+    xs = f64(d["hidden"][torch.from_numpy(sel).cuda()])
+    ref = oracle.forward(xs, gw_np[sel].astype(np.float64), gids_np[sel], LazyF64(d["w13"]),
+                         LazyF64(d["w2"]),
+                         None if d["w13_bias"] is None else LazyF64(d["w13_bias"]),
+                         None if d["w2_bias"] is None else LazyF64(d["w2_bias"]))
+    check_out(f64(y)[sel], ref, name)
+    assert np.isfinite(f64(y)).all()
