@@ -98,7 +98,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -199,11 +199,13 @@ def run_ours(args, world, rank, local):
 
     # headline: device-resident inputs
     clocks = ClockSampler(local)
-    n0 = pkg.launch_count()
     clocks.start()
+    time.sleep(0.3)                       # sampler up before the timed region
+    n0 = pkg.launch_count()
     ms = time_steps(step, K, W, world)
+    launches_total = pkg.launch_count() - n0
     ck = clocks.stop()
-    launches = pkg.launch_count() - n0
+    launches = launches_total * K // (K + W)   # launches inside the timed region
     ms_step = max_over_ranks(ms / K, world)
     ids_np = step.ids.cpu().numpy()
     flops, nbytes, touched = algorithmic(spec, ids_np)
@@ -378,8 +380,8 @@ def run_reference(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixtral_prefill", choices=sorted(wl.SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -13,7 +13,7 @@ from helpers import LazyF64, check_out, f64
 
 pytestmark = pytest.mark.gpu
 
-SENTINEL = -1234.0   # exactly representable in bf16
+SENTINEL = -1536.0   # exactly representable in bf16 (1.5 * 2^10)
 
 
 def _run(d):
