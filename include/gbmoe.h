@@ -132,6 +132,33 @@ GBMOE_API moe_status_t moe_align(const int32_t* topk_ids, int64_t M, int32_t top
                        int32_t* expert_num_tokens, int32_t* block_expert_ids, void* scratch,
                        size_t scratch_bytes, int32_t* error_word, moe_stream_t stream);
 
+/* moe_align_static_scratch: moe_align for callers that cannot allocate
+ * device memory -- code that runs inside another framework's operator or a
+ * plugin with no handle to that framework's allocator, or a latency-critical
+ * loop where a cudaMalloc (which can synchronise the device) is not allowed.
+ * The pages have no counterpart to this entry point: it is a deployment aid.
+ *
+ * Same arguments, outputs and errors as moe_align, minus `scratch`: the
+ * per-chunk count table lives in a library-owned static device array of
+ * MOE_ALIGN_STATIC_SCRATCH_INTS int32 (1 MiB), allocated when the library is
+ * loaded on a GPU and held by every GPU that loads it until the process
+ * exits.  Sizes with ceil(M * top_k / 256) * E > MOE_ALIGN_STATIC_SCRATCH_INTS
+ * are rejected with MOE_ERR_WORKSPACE_TOO_SMALL.  The entry point calls no
+ * allocating routine.  The first call on each device looks up the array's
+ * device address (set-up); make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents (every
+ * entry a call reads is written earlier in that same call, so nothing has to
+ * start at zero); calls that overlap on the GPU, on any streams, race on it.
+ */
+#define MOE_ALIGN_STATIC_SCRATCH_INTS (1 << 18)
+GBMOE_API moe_status_t moe_align_static_scratch(const int32_t* topk_ids, int64_t M,
+                                                int32_t top_k, int32_t E, int32_t block_m,
+                                                int32_t* sorted_token_ids,
+                                                int32_t* expert_offsets,
+                                                int32_t* expert_num_tokens,
+                                                int32_t* block_expert_ids,
+                                                int32_t* error_word, moe_stream_t stream);
+
 /* -------------------------------------------------------------- forward --
  * moe_forward: y_t = sum_j topk_weights[t, j] * f_{topk_ids[t, j]}(x_t) with
  * the SwiGLU expert f_e(x) = (SiLU(x W13_e[:, :I] + b13_e[:I]) *

@@ -29,6 +29,8 @@ SIGNATURES = {
     "moe_align_scratch_size": (c_sz, [c_i64, c_i32, c_i32]),
     "moe_align": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,
                           c_vp, c_vp]),
+    "moe_align_static_scratch": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp,
+                                         c_vp, c_vp, c_vp]),
     "moe_workspace_size": (c_i32, [c_i64, c_i32, c_i32, c_i32, c_i32, c_i32,
                                    ctypes.POINTER(c_sz)]),
     "moe_forward": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,

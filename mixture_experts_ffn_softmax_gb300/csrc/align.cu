@@ -13,6 +13,8 @@
 //                          sentinel fill of the padding slots
 //   3. scatter          -- each warp re-walks its chunk in order and writes
 //                          every item at offsets[e] + chunk prefix + rank
+#include <mutex>
+
 #include "common.cuh"
 
 namespace gbmoe {
@@ -285,6 +287,54 @@ moe_status_t launch_batched_plan(const BatchedPlanArgs& a, cudaStream_t s) {
                                                  a.error_word);
   prof_after("batched_plan", s);
   return check_launch("batched_plan");
+}
+
+// ------------------------------------------------- static scratch variant --
+// moe_align without a caller-provided scratch buffer: the per-chunk count
+// table lives in this file-scope device array.  In host code the symbol is
+// only a host-side stand-in, so its device address is looked up once per
+// device with cudaGetSymbolAddress and that address is what the kernels get.
+namespace {
+
+static __device__ __align__(256) int32_t g_align_static_scratch[MOE_ALIGN_STATIC_SCRATCH_INTS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+int32_t* g_static_scratch_ptr[kMaxDevices] = {};
+
+moe_status_t static_scratch_for_current_device(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return set_error(MOE_ERR_NO_DEVICE, "no usable current device for the static scratch");
+  }
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (g_static_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_align_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return set_error(MOE_ERR_CUDA, "cudaGetSymbolAddress(static align scratch): %s",
+                       cudaGetErrorString(e));
+    }
+    g_static_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_static_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t launch_align_static_scratch(AlignArgs a, cudaStream_t s) {
+  const size_t need = align_scratch_bytes(a.R, a.E);
+  if (need > sizeof(int32_t) * static_cast<size_t>(MOE_ALIGN_STATIC_SCRATCH_INTS))
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL,
+                     "static align scratch holds %d ints; ceil(R/256)*E needs %zu",
+                     MOE_ALIGN_STATIC_SCRATCH_INTS, need / sizeof(int32_t));
+  int32_t* p = nullptr;
+  if (moe_status_t st = static_scratch_for_current_device(&p)) return st;
+  a.chunk_counts = p;
+  return launch_align(a, s);
 }
 
 }  // namespace gbmoe

@@ -279,6 +279,33 @@ moe_status_t moe_align(const int32_t* topk_ids, int64_t M, int32_t top_k, int32_
   return launch_align(a, stream);
 }
 
+moe_status_t moe_align_static_scratch(const int32_t* topk_ids, int64_t M, int32_t top_k,
+                                      int32_t E, int32_t block_m, int32_t* sorted_token_ids,
+                                      int32_t* expert_offsets, int32_t* expert_num_tokens,
+                                      int32_t* block_expert_ids, int32_t* error_word,
+                                      moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M < 0");
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_INVALID_ARG, "E=%d outside [1, 1024]", E);
+  if (top_k < 1 || top_k > 1024) return set_error(MOE_ERR_INVALID_ARG, "top_k=%d", top_k);
+  if (block_m < 1 || block_m > 1024)
+    return set_error(MOE_ERR_INVALID_ARG, "block_m=%d outside [1, 1024]", block_m);
+  const int64_t R = M * top_k;
+  if (align_cap(R, E, block_m) >= (int64_t(1) << 31))
+    return set_error(MOE_ERR_INVALID_ARG, "too many routed items for int32 indices");
+  if (!expert_offsets || !expert_num_tokens || !block_expert_ids || !sorted_token_ids)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (R > 0 && !topk_ids) return set_error(MOE_ERR_INVALID_ARG, "null topk_ids");
+  if (align_scratch_bytes(R, E) > sizeof(int32_t) * size_t(MOE_ALIGN_STATIC_SCRATCH_INTS))
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL,
+                     "ceil(M*top_k/256)*E exceeds the static scratch of %d ints",
+                     MOE_ALIGN_STATIC_SCRATCH_INTS);
+  if (moe_status_t st = check_device(nullptr)) return st;
+  AlignArgs a{topk_ids, R, E, block_m, sorted_token_ids, expert_offsets, expert_num_tokens,
+              block_expert_ids, nullptr, align_cap(R, E, block_m), error_word};
+  return launch_align_static_scratch(a, stream);
+}
+
 // -------------------------------------------------------------- forward --
 moe_status_t moe_workspace_size(int64_t M, int32_t H, int32_t I, int32_t E, int32_t top_k,
                                 int32_t reduce_mode, size_t* bytes) {

@@ -59,6 +59,8 @@ struct AlignArgs {
 };
 size_t align_scratch_bytes(int64_t R, int32_t E);
 moe_status_t launch_align(const AlignArgs& a, cudaStream_t s);
+// Same, with the chunk table in the library's static device array.
+moe_status_t launch_align_static_scratch(AlignArgs a, cudaStream_t s);
 
 // Batched layout plan: per expert e, rows e*T + i (i < count_e) in order,
 // padded with the sentinel to a multiple of block_m.
