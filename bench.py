@@ -167,6 +167,8 @@ def algorithmic(spec, ids_np):
 
 
 class OurStep:
+    reduce = "auto"
+
     def __init__(self, spec, device):
         import mixture_experts_ffn_softmax_gb300 as pkg
         self.pkg = pkg
@@ -184,7 +186,8 @@ class OurStep:
                       s.routing_method, s.renormalize, s.k_group, s.group_count,
                       s.group_select_mode, s.routed_scaling_factor, self.w, self.ids)
         pkg.moe_forward(d["hidden"] if hidden is None else hidden, self.w, self.ids, d["w13"],
-                        d["w2"], d["w13_bias"], d["w2_bias"], self.ws, self.out)
+                        d["w2"], d["w13_bias"], d["w2_bias"], self.ws, self.out,
+                        reduce=self.reduce)
         return self.out
 
 
@@ -408,8 +411,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--reduce", default="auto", choices=["auto", "separate", "epilogue_atomic"],
+                    help="TopKWeightAndReduce choice (default: the library's AUTO rule)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    OurStep.reduce = args.reduce
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank, local)

@@ -58,11 +58,16 @@ typedef enum {
 
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID = 1 } moe_routing_t;
 
-/* Where the top-k weight multiply and the k-sum happen ("vLLM
- * FusedMoEModularKernel" page, TopKWeightAndReduce section).  SEPARATE:
- * the down-projection epilogue applies bias and weight and writes one fp32
- * row per routed item; a vectorised reduce kernel sums each token's k rows.
- * AUTO picks SEPARATE.  EPILOGUE_ATOMIC is reserved (MOE_ERR_UNSUPPORTED). */
+/* Where the top-k weight multiply and the k-sum happen ("Fused MoE Modular
+ * Kernel" page, TopKWeightAndReduce section).  Both choices apply bias and
+ * routing weight in the down-projection (GEMM2) epilogue.
+ * SEPARATE: the epilogue writes one fp32 row per routed item in expert-sorted
+ *   order (TMA tensor stores); a vectorised kernel sums each token's k rows
+ *   through the inverse permutation and casts to bf16.
+ * EPILOGUE_ATOMIC: the epilogue adds each weighted row into the token's fp32
+ *   accumulator row with vector atomics (resolved in L2); a cast kernel
+ *   writes bf16.
+ * AUTO: SEPARATE (faster on every measured workload). */
 typedef enum {
   MOE_REDUCE_AUTO = 0,
   MOE_REDUCE_EPILOGUE_ATOMIC = 1,
@@ -232,12 +237,15 @@ GBMOE_API moe_status_t moe_read_error(const int32_t* error_word, int32_t reset, 
  * (M, H, I, E, top_k), of its regions -- for inspecting intermediate stages
  * in tests.  offsets[0..8] = error word, expert_num_tokens [E],
  * expert_offsets [E+1], block_expert_ids, sorted_token_ids [cap], align
- * scratch, permuted rows bf16 [cap, H], z = SiLU(gate)*up bf16 [cap, I],
- * weighted item outputs fp32 [M*top_k, H] (first token chunk); offsets[9] =
- * cap (rows of the padded layout).  No GPU access.
+ * scratch, inverse permutation int32 [M*top_k] (sorted position of each
+ * routed item, -1 if dropped), permuted token rows bf16 [cap, H],
+ * z = SiLU(gate)*up bf16 [cap, I], fp32 item rows [cap, H] (sorted,
+ * SEPARATE) / token accumulator [M, H] (EPILOGUE_ATOMIC) -- all for the
+ * first token chunk; offsets[10] = cap (rows of the padded layout).
+ * No GPU access.
  */
 GBMOE_API moe_status_t moe_workspace_layout(int64_t M, int32_t H, int32_t I, int32_t E,
-                                            int32_t top_k, size_t offsets[10]);
+                                            int32_t top_k, size_t offsets[11]);
 
 /* moe_selftest_wait_timeout: failure-detection self-test.  Launches one CTA
  * that waits on an mbarrier nothing ever arrives at, with a wait limit of

@@ -191,10 +191,10 @@ def read_error(error_word_ptr: int, reset: bool = True, stream=None) -> int:
 def workspace_layout(M: int, H: int, I: int, E: int, top_k: int) -> dict:
     """Byte offsets of the forward workspace's regions (for inspecting
     intermediate stages)."""
-    arr = (ctypes.c_size_t * 10)()
+    arr = (ctypes.c_size_t * 11)()
     _check(lib().moe_workspace_layout(M, H, I, E, top_k, arr), "moe_workspace_layout")
     names = ["error_word", "expert_num_tokens", "expert_offsets", "block_expert_ids",
-             "sorted_token_ids", "align_scratch", "a_perm", "z", "item_out", "cap"]
+             "sorted_token_ids", "align_scratch", "inv", "a_perm", "z", "item_out", "cap"]
     return dict(zip(names, list(arr)))
 
 

@@ -6,13 +6,15 @@
 // every block and the padded total.  Items of one expert keep ascending item
 // order (a stable sort); padding slots hold the sentinel R.
 //
-// Three deterministic passes, no atomics in the ranking:
+// Deterministic passes, no atomics in the ranking:
 //   1. chunk histogram  -- each warp counts the experts of one 256-item chunk
-//   2. scan             -- one CTA: per-expert prefix over chunks, padded
-//                          counts, exclusive scan over experts, block ids,
-//                          sentinel fill of the padding slots
-//   3. scatter          -- each warp re-walks its chunk in order and writes
+//   2. column scan      -- one block per expert: prefix of its chunk counts
+//   3. offsets          -- one block: padded counts, exclusive scan over
+//                          experts, block ids, sentinel fill of the padding
+//   4. scatter          -- each warp re-walks its chunk in order and writes
 //                          every item at offsets[e] + chunk prefix + rank
+// Problems of at most 4096 items and 256 experts run all of it in a single
+// block (one launch instead of four).
 #include <mutex>
 
 #include "common.cuh"
@@ -56,41 +58,15 @@ __global__ void __launch_bounds__(kAlignWarps * 32)
     chunk_counts[static_cast<int64_t>(e) * num_chunks + chunk] = cnt[e];
 }
 
-__global__ void __launch_bounds__(kScanThreads)
-    align_scan_kernel(int E, int num_chunks, int block_m, int32_t sentinel, int64_t cap,
-                      int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts,
-                      int32_t* __restrict__ offsets, int32_t* __restrict__ block_expert,
-                      int32_t* __restrict__ sorted) {
-  __shared__ int32_t s_count[1024];
-  __shared__ int32_t s_off[1025];
-  __shared__ int32_t s_warp[32];
+// Block-wide (kScanThreads threads) end of an align plan, given the item
+// count of every expert in s_count: padded counts, exclusive scan over the
+// experts (expert_offsets), the expert of every block_m block (-1 past the
+// last), and the sentinel in every padding slot.  Leaves the offsets in s_off.
+__device__ void finish_plan(int E, int block_m, int32_t sentinel, int64_t cap,
+                            const int32_t* s_count, int32_t* s_off, int32_t* s_warp,
+                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                            int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // (a) per expert: exclusive prefix over chunks (in place) and the total.
-  for (int e = warp; e < E; e += kScanThreads / 32) {
-    int32_t* col = chunk_counts + static_cast<int64_t>(e) * num_chunks;
-    const int per = ceil_div(num_chunks, 32);
-    const int c0 = lane * per, c1 = min(num_chunks, c0 + per);
-    int32_t part = 0;
-    for (int c = c0; c < c1; ++c) part += col[c];
-    int32_t incl = part;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    int32_t run = incl - part;
-    for (int c = c0; c < c1; ++c) {
-      const int32_t v = col[c];
-      col[c] = run;
-      run += v;
-    }
-    const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
-    if (lane == 0) s_count[e] = total;
-  }
-  __syncthreads();
-
-  // (b) padded counts -> exclusive scan over experts (E <= 1024).
   int32_t padded = 0;
   if (tid < E) padded = ceil_div(s_count[tid], block_m) * block_m;
   int32_t incl = padded;
@@ -102,7 +78,7 @@ __global__ void __launch_bounds__(kScanThreads)
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int32_t w = s_warp[lane];
+    const int32_t w = s_warp[lane];
     int32_t wi = w;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -115,7 +91,7 @@ __global__ void __launch_bounds__(kScanThreads)
   const int32_t excl = s_warp[warp] + incl - padded;
   if (tid < E) {
     s_off[tid] = excl;
-    counts[tid] = s_count[tid];
+    if (counts != nullptr) counts[tid] = s_count[tid];
     offsets[tid] = excl;
   }
   if (tid == E - 1) {
@@ -123,8 +99,6 @@ __global__ void __launch_bounds__(kScanThreads)
     offsets[E] = excl + padded;
   }
   __syncthreads();
-
-  // (c) expert id of every block, -1 past the last block.
   const int64_t nblk_cap = cap / block_m;
   const int32_t nblk = s_off[E] / block_m;
   for (int64_t b = tid; b < nblk_cap; b += kScanThreads) {
@@ -140,16 +114,138 @@ __global__ void __launch_bounds__(kScanThreads)
     }
     block_expert[b] = e;
   }
-  // (d) sentinel in every padding slot.
   for (int e = warp; e < E; e += kScanThreads / 32)
     for (int32_t pos = s_off[e] + s_count[e] + lane; pos < s_off[e + 1]; pos += 32)
       sorted[pos] = sentinel;
 }
 
+// Per expert (one block each): exclusive prefix of its chunk counts over the
+// chunks, in place, and its total.
+constexpr int kColScanThreads = 256;
+__global__ void __launch_bounds__(kColScanThreads)
+    align_colscan_kernel(int num_chunks, int32_t* __restrict__ chunk_counts,
+                         int32_t* __restrict__ counts) {
+  __shared__ int32_t s_warp[kColScanThreads / 32];
+  __shared__ int32_t s_carry;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int32_t* col = chunk_counts + static_cast<int64_t>(blockIdx.x) * num_chunks;
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < num_chunks; base += kColScanThreads * 4) {
+    int32_t v[4], part = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = base + tid * 4 + i;
+      v[i] = c < num_chunks ? col[c] : 0;
+      part += v[i];
+    }
+    int32_t incl = part;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t x = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += x;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int32_t wbase = 0, total = 0;
+    for (int w = 0; w < kColScanThreads / 32; ++w) {
+      if (w < warp) wbase += s_warp[w];
+      total += s_warp[w];
+    }
+    int32_t run = s_carry + wbase + incl - part;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = base + tid * 4 + i;
+      if (c < num_chunks) col[c] = run;
+      run += v[i];
+    }
+    __syncthreads();
+    if (tid == 0) s_carry += total;
+    __syncthreads();
+  }
+  if (tid == 0) counts[blockIdx.x] = s_carry;
+}
+
+// Offsets, block ids and sentinels from the per-expert totals (one block).
+__global__ void __launch_bounds__(kScanThreads)
+    align_offsets_kernel(int E, int block_m, int32_t sentinel, int64_t cap,
+                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted) {
+  __shared__ int32_t s_count[1024];
+  __shared__ int32_t s_off[1025];
+  __shared__ int32_t s_warp[32];
+  if (threadIdx.x < E) s_count[threadIdx.x] = counts[threadIdx.x];
+  __syncthreads();
+  finish_plan(E, block_m, sentinel, cap, s_count, s_off, s_warp, nullptr, offsets, block_expert,
+              sorted);
+}
+
+// The whole align in one block for small problems (R <= kSmallItems,
+// E <= kSmallExperts): warp w owns a contiguous run of items; per-warp
+// histograms, a prefix over the warps, the plan, then the stable scatter.
+constexpr int kSmallItems = 4096;
+constexpr int kSmallExperts = 256;
+__global__ void __launch_bounds__(kScanThreads)
+    align_small_kernel(const int32_t* __restrict__ ids, int R, int E, int block_m, int64_t cap,
+                       int32_t* __restrict__ sorted, int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ counts, int32_t* __restrict__ block_expert,
+                       int32_t* __restrict__ inv, int32_t* error_word) {
+  __shared__ int32_t s_cnt[32 * kSmallExperts];
+  __shared__ int32_t s_count[kSmallExperts];
+  __shared__ int32_t s_off[kSmallExperts + 1];
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per = ceil_div(ceil_div(R, 32), 32) * 32;  // items per warp, multiple of 32
+  const int r0 = warp * per;
+  int32_t* cnt = s_cnt + warp * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  bool bad = false;
+  for (int it = 0; it < per; it += 32) {
+    const int r = r0 + it + lane;
+    const int e = r < R ? ids[r] : -1;
+    const bool ok = r < R && valid_id(e, E);
+    bad |= r < R && !ok;
+    const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
+    if (ok && lane == __ffs(grp) - 1) cnt[e] += __popc(grp);
+    __syncwarp();
+  }
+  if (bad) record_error(error_word, MOE_ERR_BAD_EXPERT_ID);
+  __syncthreads();
+  if (tid < E) {  // exclusive prefix of expert tid over the warps
+    int32_t run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int32_t v = s_cnt[w * E + tid];
+      s_cnt[w * E + tid] = run;
+      run += v;
+    }
+    s_count[tid] = run;
+  }
+  __syncthreads();
+  finish_plan(E, block_m, R, cap, s_count, s_off, s_warp, counts, offsets, block_expert, sorted);
+  __syncthreads();
+  for (int e = lane; e < E; e += 32) cnt[e] += s_off[e];
+  __syncwarp();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int it = 0; it < per; it += 32) {
+    const int r = r0 + it + lane;
+    const int e = r < R ? ids[r] : -1;
+    const bool ok = r < R && valid_id(e, E);
+    const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
+    const int32_t pos = ok ? cnt[e] + __popc(grp & lt_mask) : -1;
+    if (ok) sorted[pos] = r;
+    if (inv != nullptr && r < R) inv[r] = pos;
+    __syncwarp();
+    if (ok && lane == __ffs(grp) - 1) cnt[e] += __popc(grp);
+    __syncwarp();
+  }
+}
+
 __global__ void __launch_bounds__(kAlignWarps * 32)
     align_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int num_chunks,
                          const int32_t* __restrict__ chunk_prefix,
-                         const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted) {
+                         const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted,
+                         int32_t* __restrict__ inv) {
   extern __shared__ int32_t run_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kAlignWarps + warp;
@@ -167,7 +263,9 @@ __global__ void __launch_bounds__(kAlignWarps * 32)
     const bool ok = (r < R) && valid_id(e, E);
     const int key = ok ? e : -1;
     const unsigned grp = __match_any_sync(0xffffffffu, key);
-    if (ok) sorted[run[e] + __popc(grp & lt_mask)] = static_cast<int32_t>(r);
+    const int32_t pos = ok ? run[e] + __popc(grp & lt_mask) : -1;
+    if (ok) sorted[pos] = static_cast<int32_t>(r);
+    if (inv != nullptr && r < R) inv[r] = pos;
     __syncwarp();
     if (ok && lane == __ffs(grp) - 1) run[e] += __popc(grp);
     __syncwarp();
@@ -252,32 +350,38 @@ size_t align_scratch_bytes(int64_t R, int32_t E) {
 }
 
 moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
+  if (a.R <= kSmallItems && a.E <= kSmallExperts) {
+    prof_before("align_small", s);
+    align_small_kernel<<<1, kScanThreads, 0, s>>>(a.ids, static_cast<int>(a.R), a.E, a.block_m,
+                                                  a.cap, a.sorted, a.offsets, a.counts,
+                                                  a.block_expert, a.inv, a.error_word);
+    prof_after("align_small", s);
+    return check_launch("align_small");
+  }
   const int num_chunks = static_cast<int>(ceil_div<int64_t>(a.R, kChunk));
   const size_t smem = static_cast<size_t>(kAlignWarps) * a.E * sizeof(int32_t);
   const unsigned grid = static_cast<unsigned>(ceil_div(num_chunks, kAlignWarps));
-  if (num_chunks > 0) {
-    prof_before("align_hist", s);
-    align_hist_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
-                                                           a.chunk_counts, a.error_word);
-    prof_after("align_hist", s);
-    if (moe_status_t st = check_launch("align_hist")) return st;
-  }
-  prof_before("align_scan", s);
-  align_scan_kernel<<<1, kScanThreads, 0, s>>>(a.E, num_chunks, a.block_m,
-                                               static_cast<int32_t>(a.R), a.cap,
-                                               a.chunk_counts, a.counts, a.offsets,
-                                               a.block_expert, a.sorted);
-  prof_after("align_scan", s);
-  if (moe_status_t st = check_launch("align_scan")) return st;
-  if (num_chunks > 0) {
-    prof_before("align_scatter", s);
-    align_scatter_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
-                                                              a.chunk_counts, a.offsets,
-                                                              a.sorted);
-    prof_after("align_scatter", s);
-    if (moe_status_t st = check_launch("align_scatter")) return st;
-  }
-  return MOE_OK;
+  prof_before("align_hist", s);
+  align_hist_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
+                                                         a.chunk_counts, a.error_word);
+  prof_after("align_hist", s);
+  if (moe_status_t st = check_launch("align_hist")) return st;
+  prof_before("align_colscan", s);
+  align_colscan_kernel<<<a.E, kColScanThreads, 0, s>>>(num_chunks, a.chunk_counts, a.counts);
+  prof_after("align_colscan", s);
+  if (moe_status_t st = check_launch("align_colscan")) return st;
+  prof_before("align_offsets", s);
+  align_offsets_kernel<<<1, kScanThreads, 0, s>>>(a.E, a.block_m, static_cast<int32_t>(a.R),
+                                                  a.cap, a.counts, a.offsets, a.block_expert,
+                                                  a.sorted);
+  prof_after("align_offsets", s);
+  if (moe_status_t st = check_launch("align_offsets")) return st;
+  prof_before("align_scatter", s);
+  align_scatter_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
+                                                            a.chunk_counts, a.offsets, a.sorted,
+                                                            a.inv);
+  prof_after("align_scatter", s);
+  return check_launch("align_scatter");
 }
 
 moe_status_t launch_batched_plan(const BatchedPlanArgs& a, cudaStream_t s) {

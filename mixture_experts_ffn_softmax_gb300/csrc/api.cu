@@ -115,7 +115,7 @@ int64_t align_cap(int64_t R, int32_t E, int32_t block_m) {
 struct FwdLayout {
   int64_t cap = 0;
   size_t err = 0, counts = 0, offsets = 0, block_expert = 0, sorted = 0, scratch = 0,
-         a_perm = 0, z = 0, o = 0, total = 0;
+         a_perm = 0, z = 0, o = 0, inv = 0, total = 0;
 };
 
 FwdLayout fwd_layout(int64_t Mc, int32_t H, int32_t I, int32_t E, int32_t k) {
@@ -134,11 +134,23 @@ FwdLayout fwd_layout(int64_t Mc, int32_t H, int32_t I, int32_t E, int32_t k) {
   L.block_expert = take(sizeof(int32_t) * (L.cap / MOE_BLOCK_M));
   L.sorted = take(sizeof(int32_t) * L.cap);
   L.scratch = take(align_scratch_bytes(Rc, E));
+  L.inv = take(sizeof(int32_t) * Rc);
   L.a_perm = take(sizeof(bf16) * L.cap * H);
   L.z = take(sizeof(bf16) * L.cap * I);
-  L.o = take(sizeof(float) * Rc * H);
+  // fp32 rows: sorted item rows [cap, H] (separate reduce) or the token
+  // accumulator [Mc, H] (atomic reduce); cap >= Mc, so one region serves both.
+  L.o = take(sizeof(float) * L.cap * H);
   L.total = off;
   return L;
+}
+
+// TopKWeightAndReduce choice for MOE_REDUCE_AUTO.  Measured on GB300 for the
+// Mixtral (k=2), Qwen (k=8, 16K tokens) and DeepSeek (k=8, 8K tokens)
+// shapes, sorted fp32 rows + a separate reduce beat the epilogue atomics on
+// every one (the 16-byte atomics into scattered token rows are L2-bound), so
+// AUTO selects SEPARATE.
+int32_t pick_reduce(int64_t /*Mc*/, int32_t /*H*/, int32_t /*k*/, int32_t mode) {
+  return mode == MOE_REDUCE_AUTO ? MOE_REDUCE_SEPARATE : mode;
 }
 
 struct BatLayout {
@@ -314,11 +326,9 @@ moe_status_t moe_workspace_size(int64_t M, int32_t H, int32_t I, int32_t E, int3
   if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M < 0");
   if (moe_status_t st = validate_ffn_dims(H, I, E)) return st;
   if (top_k < 1 || top_k > 64) return set_error(MOE_ERR_INVALID_ARG, "top_k=%d outside [1, 64]", top_k);
-  if (reduce_mode != MOE_REDUCE_AUTO && reduce_mode != MOE_REDUCE_SEPARATE) {
-    if (reduce_mode == MOE_REDUCE_EPILOGUE_ATOMIC)
-      return set_error(MOE_ERR_UNSUPPORTED, "MOE_REDUCE_EPILOGUE_ATOMIC is not built");
+  if (reduce_mode != MOE_REDUCE_AUTO && reduce_mode != MOE_REDUCE_SEPARATE &&
+      reduce_mode != MOE_REDUCE_EPILOGUE_ATOMIC)
     return set_error(MOE_ERR_INVALID_ARG, "reduce_mode=%d", reduce_mode);
-  }
   const int64_t Mc = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
   *bytes = fwd_layout(Mc, H, I, E, top_k).total;
   return MOE_OK;
@@ -363,9 +373,10 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     const int64_t cap = align_cap(Rc, E, MOE_BLOCK_M);
     int32_t* sorted = at<int32_t>(workspace, L.sorted);
     int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    int32_t* inv = at<int32_t>(workspace, L.inv);
     AlignArgs al{topk_ids + c0 * top_k, Rc, E, MOE_BLOCK_M, sorted, offsets,
                  at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.block_expert),
-                 at<int32_t>(workspace, L.scratch), cap, err};
+                 at<int32_t>(workspace, L.scratch), cap, err, inv};
     if (moe_status_t st = launch_align(al, s)) return st;
 
     bf16* a_perm = at<bf16>(workspace, L.a_perm);
@@ -384,11 +395,17 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     g1.K = H;
     g1.offsets = offsets;
     g1.out = z;
+    g1.row_index = sorted;
+    g1.sentinel = static_cast<int32_t>(Rc);
     g1.error_word = err;
     g1.num_sms = sms;
     if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
 
     float* o = at<float>(workspace, L.o);
+    const int32_t mode = pick_reduce(Mc, H, top_k, reduce_mode);
+    if (mode == MOE_REDUCE_EPILOGUE_ATOMIC &&
+        cudaMemsetAsync(o, 0, sizeof(float) * Mc * H, s) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
     GroupedGemmArgs g2{};
     g2.a = z;
     g2.w = static_cast<const bf16*>(w2);
@@ -402,11 +419,16 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     g2.row_index = sorted;
     g2.row_weight = topk_weights + c0 * top_k;
     g2.sentinel = static_cast<int32_t>(Rc);
+    g2.div = top_k;
     g2.error_word = err;
     g2.num_sms = sms;
-    if (moe_status_t st = launch_gemm2_scatter_f32(g2, s)) return st;
-
-    if (moe_status_t st = launch_reduce(o, Mc, top_k, H, y + c0 * H, s)) return st;
+    if (mode == MOE_REDUCE_EPILOGUE_ATOMIC) {
+      if (moe_status_t st = launch_gemm2_atomic_f32(g2, s)) return st;
+      if (moe_status_t st = launch_cast_f32_bf16(o, Mc * H, y + c0 * H, s)) return st;
+    } else {
+      if (moe_status_t st = launch_gemm2_sorted_f32(g2, s)) return st;
+      if (moe_status_t st = launch_reduce_sorted(o, inv, Mc, top_k, H, y + c0 * H, s)) return st;
+    }
   }
   return MOE_OK;
 }
@@ -470,6 +492,8 @@ moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens
   g1.K = H;
   g1.offsets = offsets;
   g1.out = z;
+  g1.row_index = sorted;
+  g1.sentinel = sentinel;
   g1.error_word = err;
   g1.num_sms = sms;
   if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
@@ -493,15 +517,15 @@ moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens
 }
 
 moe_status_t moe_workspace_layout(int64_t M, int32_t H, int32_t I, int32_t E, int32_t top_k,
-                                  size_t offsets[10]) {
+                                  size_t offsets[11]) {
   size_t need = 0;
   if (!offsets) return set_error(MOE_ERR_INVALID_ARG, "null offsets");
   if (moe_status_t st = moe_workspace_size(M, H, I, E, top_k, MOE_REDUCE_AUTO, &need)) return st;
   const int64_t Mc = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
   const FwdLayout L = fwd_layout(Mc, H, I, E, top_k);
-  const size_t v[10] = {L.err, L.counts, L.offsets, L.block_expert, L.sorted, L.scratch,
-                        L.a_perm, L.z, L.o, static_cast<size_t>(L.cap)};
-  for (int i = 0; i < 10; ++i) offsets[i] = v[i];
+  const size_t v[11] = {L.err, L.counts, L.offsets, L.block_expert, L.sorted, L.scratch,
+                        L.inv, L.a_perm, L.z, L.o, static_cast<size_t>(L.cap)};
+  for (int i = 0; i < 11; ++i) offsets[i] = v[i];
   return MOE_OK;
 }
 

@@ -56,6 +56,7 @@ struct AlignArgs {
   int32_t* chunk_counts;  // scratch [num_chunks * E]
   int64_t cap;
   int32_t* error_word;
+  int32_t* inv = nullptr;  // optional [R]: sorted position of item r (-1 if dropped)
 };
 size_t align_scratch_bytes(int64_t R, int32_t E);
 moe_status_t launch_align(const AlignArgs& a, cudaStream_t s);
@@ -91,9 +92,11 @@ struct GatherArgs {
 };
 moe_status_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
-// y[t, :] = bf16( sum_j o[t*k + j, :] )
-moe_status_t launch_reduce(const float* o, int64_t M, int32_t k, int32_t H, bf16* y,
-                           cudaStream_t s);
+// y[t, :] = bf16( sum_j o_sorted[inv[t*k + j], :] ), skipping inv < 0.
+moe_status_t launch_reduce_sorted(const float* o_sorted, const int32_t* inv, int64_t M,
+                                  int32_t k, int32_t H, bf16* y, cudaStream_t s);
+// y = bf16(acc), acc fp32 [M, H].
+moe_status_t launch_cast_f32_bf16(const float* acc, int64_t n, bf16* y, cudaStream_t s);
 
 // Grouped GEMMs (gemm.cu).
 struct GroupedGemmArgs {
@@ -106,14 +109,20 @@ struct GroupedGemmArgs {
   const int32_t* offsets;  // [E+1] padded expert offsets
   // epilogue
   void* out;              // GEMM1: z bf16 [cap, N]; GEMM2: fp32 [*, N] or bf16 [*, N]
-  const int32_t* row_index;  // GEMM2: destination row per sorted position
-  const float* row_weight;   // GEMM2: weight per destination row, or null (=1)
-  int32_t sentinel;          // GEMM2: row_index >= sentinel -> not stored
+  const int32_t* row_index;  // GEMM2: routed item (or batched row) per sorted position
+  const float* row_weight;   // GEMM2: weight per item / row, or null (=1)
+  int32_t sentinel;          // GEMM2: row_index >= sentinel -> padding
+  int32_t div;               // GEMM2 atomic: token of item r is r / div
   int32_t* error_word;
   int32_t num_sms;
 };
 moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s);
-moe_status_t launch_gemm2_scatter_f32(const GroupedGemmArgs& a, cudaStream_t s);
+// GEMM2, contiguous layout, SEPARATE reduce: weighted fp32 rows in sorted
+// order, out = o_sorted [cap, N], written with TMA tensor stores.
+moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s);
+// GEMM2, contiguous layout, ATOMIC reduce: out = acc fp32 [M, N]; each
+// weighted row is added into row row_index[p] / div with vector fp32 atomics.
+moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s);
 

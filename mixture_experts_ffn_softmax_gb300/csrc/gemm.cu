@@ -26,10 +26,14 @@
 //   SwiGLU     : GEMM1.  Columns [0,128) of the accumulator are the gate
 //                block, [128,256) the matching up block; writes
 //                z = SiLU(gate + b_gate) * (up + b_up) as bf16.
-//   ScatterF32 : GEMM2, contiguous layout.  o = (acc + b2) * w(row) as fp32
-//                into row row_index[p] (the routed item) of the item buffer.
-//   RowsBF16   : GEMM2, batched layout.  Same, written as bf16 into the
-//                output row row_index[p] = e * T + i.
+//   SortedF32  : GEMM2, contiguous layout, separate reduce.  o = (acc + b2) *
+//                w(item) as fp32 rows in sorted order, staged through shared
+//                memory and written with TMA tensor stores (coalesced, async).
+//   AtomicF32  : GEMM2, contiguous layout, reduce in the epilogue.  The same
+//                weighted row is added into the token's fp32 accumulator row
+//                with 16-byte vector atomics (the k-sum happens in L2).
+//   RowsBF16   : GEMM2, batched layout.  Written as bf16 into the output row
+//                row_index[p] = e * T + i of valid rows only.
 // Every mbarrier wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT,
 // all roles stop, in-flight copies are given time to land, TMEM is freed.
 #include <algorithm>
@@ -53,12 +57,14 @@ constexpr int B_STAGE_BYTES = B_CHUNKS * B_CHUNK_BYTES;    // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // 48 KB
 constexpr int TMEM_COLS = 2 * MMA_N;                       // 512
 constexpr int MAX_E = 1024;
+constexpr int EPI_WARPS = 4;
+constexpr int STAGING_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 128 bytes
 constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES +
-                              (MAX_E + 1) * sizeof(int32_t);
+                              EPI_WARPS * STAGING_BYTES + (MAX_E + 1) * sizeof(int32_t);
 
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
 
-enum class Epi { SwiGLU = 0, ScatterF32 = 1, RowsBF16 = 2 };
+enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3 };
 
 struct Ctl {
   uint64_t full[STAGES];
@@ -76,7 +82,7 @@ struct KParams {
   const int32_t* row_index;
   const float* row_weight;
   int32_t* error_word;
-  int32_t E, N, K, NB, sentinel;
+  int32_t E, N, K, NB, sentinel, div;
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
@@ -160,7 +166,8 @@ __device__ __forceinline__ void load_bias8(const bf16* bias, int64_t off, bool o
 template <Epi EPI>
 __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const KParams P) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO, const KParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl ctl;
 
@@ -170,7 +177,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // 1024-byte aligned tile area (128-byte swizzle atoms), then offsets.
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  int32_t* s_off = reinterpret_cast<int32_t*>(tiles + STAGES * STAGE_BYTES);
+  uint8_t* staging = tiles + STAGES * STAGE_BYTES;  // 1024-byte aligned
+  int32_t* s_off = reinterpret_cast<int32_t*>(staging + EPI_WARPS * STAGING_BYTES);
 
   for (int i = threadIdx.x; i <= P.E; i += NTHREADS) s_off[i] = P.offsets[i];
   if (threadIdx.x == 0) {
@@ -188,6 +196,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    if constexpr (EPI == Epi::SortedF32) ptx::prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     ptx::tmem_alloc(&ctl.tmem_base, TMEM_COLS);
@@ -298,6 +307,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if constexpr (EPI == Epi::SwiGLU) {
         bf16* z = reinterpret_cast<bf16*>(P.out);
         const int N = P.N;
+        const int32_t entry = P.row_index[p];
+        const bool real = entry >= 0 && entry < P.sentinel;  // padding rows are not stored
         const int64_t bias_row = static_cast<int64_t>(tl.e) * 2 * N;
 #pragma unroll 1
         for (int c = 0; c < MMA_N / 2; c += 32) {
@@ -323,44 +334,71 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const float u1 = __uint_as_float(u[v * 8 + 2 * i + 1]) + bu[2 * i + 1];
               w[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
             }
-            if (in) *reinterpret_cast<uint4*>(z + p * N + n) = pk;
+            if (in && real) *reinterpret_cast<uint4*>(z + p * N + n) = pk;
           }
         }
       } else {
         const int N = P.N;
-        const int32_t dst = P.row_index[p];
-        const bool store = dst >= 0 && dst < P.sentinel;
-        const float wgt = (store && P.row_weight != nullptr) ? P.row_weight[dst] : 1.0f;
+        const int32_t entry = P.row_index[p];
+        const bool valid = entry >= 0 && entry < P.sentinel;
+        const float wgt = valid ? (P.row_weight != nullptr ? P.row_weight[entry] : 1.0f) : 0.0f;
         const int64_t bias_row = static_cast<int64_t>(tl.e) * N;
+        uint8_t* stage_buf = staging + (warp - 2) * STAGING_BYTES;
+        // a warp whose 32 rows are all padding has nothing to store
+        const bool any_real = __ballot_sync(0xffffffffu, valid) != 0u;
 #pragma unroll 1
         for (int c = 0; c < MMA_N; c += 32) {
+          const int n0 = tl.nb * MMA_N + c;
+          if (n0 >= N || !any_real) break;  // warp-uniform
           uint32_t a[32];
           ptx::tmem_ld_32cols(taddr + c, a);
           ptx::tmem_ld_wait();
-          const int n0 = tl.nb * MMA_N + c;
+          float o[32];
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const int n = n0 + v * 8;
-            const bool in = n < N;
             float b[8];
-            load_bias8(P.bias, bias_row + n, in, b);
-            float o[8];
+            load_bias8(P.bias, bias_row + n0 + v * 8, n0 + v * 8 < N, b);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = (__uint_as_float(a[v * 8 + i]) + b[i]) * wgt;
-            if (store && in) {
-              if constexpr (EPI == Epi::ScatterF32) {
-                float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(P.out) +
-                                                      static_cast<int64_t>(dst) * N + n);
-                d[0] = make_float4(o[0], o[1], o[2], o[3]);
-                d[1] = make_float4(o[4], o[5], o[6], o[7]);
-              } else {
-                uint4 pk;
-                pk.x = pack_bf16x2(o[0], o[1]);
-                pk.y = pack_bf16x2(o[2], o[3]);
-                pk.z = pack_bf16x2(o[4], o[5]);
-                pk.w = pack_bf16x2(o[6], o[7]);
-                *reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(P.out) +
-                                          static_cast<int64_t>(dst) * N + n) = pk;
+            for (int i = 0; i < 8; ++i) o[v * 8 + i] = (__uint_as_float(a[v * 8 + i]) + b[i]) * wgt;
+          }
+          if constexpr (EPI == Epi::SortedF32) {
+            // Stage the warp's 32x32 fp32 block in the 128-byte-swizzled layout
+            // the tensor map expects (row = lane, 16-byte chunk j stored at
+            // chunk j ^ (row & 7): conflict-free), then one TMA store.
+            if (lane == 0) ptx::bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(stage_buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&tmO, stage_buf, n0, tl.row0 + q * 32);
+              ptx::bulk_commit();
+            }
+          } else if constexpr (EPI == Epi::AtomicF32) {
+            if (valid) {
+              float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(P.out) +
+                                                    static_cast<int64_t>(entry / P.div) * N + n0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                if (n0 + v * 4 < N)
+                  atomicAdd(d + v, make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]));
+            }
+          } else {
+            if (valid) {
+              bf16* d = reinterpret_cast<bf16*>(P.out) + static_cast<int64_t>(entry) * N + n0;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                if (n0 + v * 8 < N) {
+                  uint4 pk;
+                  pk.x = pack_bf16x2(o[8 * v], o[8 * v + 1]);
+                  pk.y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
+                  pk.z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
+                  pk.w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
+                  *reinterpret_cast<uint4*>(d + v * 8) = pk;
+                }
               }
             }
           }
@@ -375,6 +413,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  if constexpr (EPI == Epi::SortedF32) {
+    if (warp >= 2 && lane == 0) ptx::bulk_wait0();  // TMA stores done before smem is released
+  }
   __syncthreads();
   if (*reinterpret_cast<volatile int32_t*>(&ctl.abort)) {
     // Give TMA copies and MMAs still in flight time to land before the
@@ -412,7 +453,8 @@ EncodeTiledFn get_encode_fn() {
 // bf16 tensor map with 128-byte swizzle.  dims/strides innermost first;
 // strides are in bytes for dims 1..rank-1.
 moe_status_t make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides, const uint32_t* box) {
+                      const uint64_t* strides, const uint32_t* box,
+                      CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t gd[5], gs[4];
@@ -423,7 +465,7 @@ moe_status_t make_map(CUtensorMap* m, const void* base, int rank, const uint64_t
     es[i] = 1;
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd,
+  const CUresult r = fn(m, dtype, rank, const_cast<void*>(base), gd,
                         gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", r);
@@ -468,6 +510,18 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     if (moe_status_t st = make_map(&tmB, a.w, 3, dims, strides, box)) return st;
     NB = ceil_div(a.N, MMA_N);
   }
+  CUtensorMap tmO;
+  if constexpr (EPI == Epi::SortedF32) {
+    // fp32 [cap, N] output, 32 x 32 boxes, 128-byte swizzle (matches staging)
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.cap)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 4};
+    const uint32_t box[2] = {32, 32};
+    if (moe_status_t st = make_map(&tmO, a.out, 2, dims, strides, box,
+                                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return st;
+  } else {
+    tmO = tmA;  // unused
+  }
   KParams P;
   P.bias = a.bias;
   P.out = a.out;
@@ -480,11 +534,12 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   P.K = a.K;
   P.NB = NB;
   P.sentinel = a.sentinel;
+  P.div = a.div > 0 ? a.div : 1;
   const int64_t max_tiles = (a.cap / BM) * NB;
   if (max_tiles <= 0) return MOE_OK;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_tiles, a.num_sms));
   prof_before(name, s);
-  grouped_gemm_kernel<EPI><<<grid, NTHREADS, SMEM_BYTES, s>>>(tmA, tmB, P);
+  grouped_gemm_kernel<EPI><<<grid, NTHREADS, SMEM_BYTES, s>>>(tmA, tmB, tmO, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -501,8 +556,11 @@ moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStre
 moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::SwiGLU>(a, "gemm1_swiglu", s);
 }
-moe_status_t launch_gemm2_scatter_f32(const GroupedGemmArgs& a, cudaStream_t s) {
-  return launch_gemm<Epi::ScatterF32>(a, "gemm2_scatter", s);
+moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::SortedF32>(a, "gemm2_sorted", s);
+}
+moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::AtomicF32>(a, "gemm2_atomic", s);
 }
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::RowsBF16>(a, "gemm2_rows_bf16", s);

@@ -13,7 +13,7 @@ from mixture_experts_ffn_softmax_gb300 import _lib
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gbmoe.h")
 
-OK, INVALID, UNSUPPORTED, WS_SMALL, NO_DEVICE = 0, 1, 2, 3, 7
+OK, INVALID, WS_SMALL, NO_DEVICE = 0, 1, 3, 7
 
 
 def declared_symbols():
@@ -80,7 +80,8 @@ def test_workspace_size_validation():
     assert lib.moe_workspace_size(16, 64, 60, 8, 2, 0, ctypes.byref(n)) == INVALID
     assert lib.moe_workspace_size(16, 64, 64, 0, 2, 0, ctypes.byref(n)) == INVALID
     assert lib.moe_workspace_size(16, 64, 64, 8, 65, 0, ctypes.byref(n)) == INVALID
-    assert lib.moe_workspace_size(16, 64, 64, 8, 2, 1, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.moe_workspace_size(16, 64, 64, 8, 2, 1, ctypes.byref(n)) == OK   # atomic reduce
+    assert lib.moe_workspace_size(16, 64, 64, 8, 2, 2, ctypes.byref(n)) == OK   # separate
     assert lib.moe_workspace_size(16, 64, 64, 8, 2, 7, ctypes.byref(n)) == INVALID
     assert lib.moe_workspace_size(-1, 64, 64, 8, 2, 0, ctypes.byref(n)) == INVALID
 
@@ -95,14 +96,16 @@ def test_workspace_is_bounded_by_the_token_chunk():
 def test_workspace_layout_regions_are_ordered_and_aligned():
     lay = pkg.workspace_layout(333, 512, 640, 8, 2)
     keys = ["error_word", "expert_num_tokens", "expert_offsets", "block_expert_ids",
-            "sorted_token_ids", "align_scratch", "a_perm", "z", "item_out"]
+            "sorted_token_ids", "align_scratch", "inv", "a_perm", "z", "item_out"]
     offs = [lay[k] for k in keys]
     assert offs == sorted(offs) and offs[0] == 0
     assert all(o % 1024 == 0 for o in offs)
     cap = lay["cap"]
     assert cap % 128 == 0 and cap >= 333 * 2
+    assert lay["item_out"] - lay["z"] >= cap * 640 * 2
+    assert lay["a_perm"] - lay["inv"] >= 333 * 2 * 4
     assert lay["z"] - lay["a_perm"] >= cap * 512 * 2
-    assert pkg.workspace_size(333, 512, 640, 8, 2) >= lay["item_out"] + 333 * 2 * 512 * 4
+    assert pkg.workspace_size(333, 512, 640, 8, 2) >= lay["item_out"] + cap * 512 * 4
 
 
 def test_forward_validation():
@@ -118,7 +121,7 @@ def test_forward_validation():
     assert fwd(M=0) == OK
     assert fwd(H=60) == INVALID
     assert fwd(ws=need - 1) == WS_SMALL
-    assert fwd(mode=1) == UNSUPPORTED
+    assert fwd(mode=3) == INVALID
     assert fwd(out=None) == INVALID
     assert fwd(wsp=ctypes.c_void_p((1 << 20) + 16)) == INVALID   # workspace alignment
     bad = ctypes.c_void_p(4096 + 8)                                # misaligned tensor

@@ -41,6 +41,6 @@ def test_profiler_counts_launches():
                     torch.zeros(M, k, dtype=torch.int32, device="cuda"), w13, w2)
     prof = pkg.profiler_stop()
     assert pkg.launch_count() - n0 == sum(v[0] for v in prof.values())
-    for name in ("align_hist", "align_scan", "align_scatter", "gather_rows", "gemm1_swiglu",
-                 "gemm2_scatter", "reduce_topk"):
+    for name in ("align_small", "gather_rows", "gemm1_swiglu",
+                 "gemm2_sorted", "reduce_sorted"):
         assert prof[name][0] == 1 and prof[name][1] > 0
