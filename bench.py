@@ -191,6 +191,88 @@ class OurStep:
         return self.out
 
 
+class BatchedStep:
+    """One pass of the batched-layout forward: (E, T, H) rows with
+    expert_num_tokens, per-row weights, invalid rows NaN."""
+
+    def __init__(self, spec, device):
+        import mixture_experts_ffn_softmax_gb300 as pkg
+        self.pkg = pkg
+        self.spec = spec
+        self.d = wl.make_batched_inputs(spec, device=device)
+        self.ws = pkg.alloc_workspace(pkg.batched_workspace_size(spec.E, spec.T, spec.H, spec.I),
+                                      device)
+        self.out = torch.empty_like(self.d["x"])
+        self.rows = int(self.d["expert_num_tokens"].sum().item())
+
+    def __call__(self, x=None):
+        d = self.d
+        return self.pkg.moe_forward_batched(d["x"] if x is None else x, d["expert_num_tokens"],
+                                            d["w13"], d["w2"], d["w13_bias"], d["w2_bias"],
+                                            d["row_weight"], self.ws, self.out)
+
+
+def run_batched(args, world, rank, local):
+    import mixture_experts_ffn_softmax_gb300 as pkg
+    pk = peaks()
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    spec = wl.BATCHED_SPECS[args.workload]
+    step = BatchedStep(spec, device)
+    K, W = args.steps, args.warmup
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    n0 = pkg.launch_count()
+    ms = time_steps(step, K, W, world)
+    launches = (pkg.launch_count() - n0) * K // (K + W)
+    ck = clocks.stop()
+    ms_step = max_over_ranks(ms / K, world)
+    R = step.rows
+    flops = 6.0 * R * spec.H * spec.I
+    touched = int((step.d["expert_num_tokens"] > 0).sum().item())
+    nbytes = touched * 3 * spec.H * spec.I * 2 + 2 * R * spec.H * 2
+    pkg.profiler_start()
+    for _ in range(K):
+        step()
+    prof = pkg.profiler_stop()
+    kern = {k: 1e3 * v[1] / max(v[0], 1) for k, v in prof.items()}
+    roof_ms = 1e3 * max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+    g1 = kern["gemm1_swiglu"]
+    b1 = touched * spec.H * 2 * spec.I * 2 + R * spec.H * 2
+    hx = step.d["x"].cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    dx = torch.empty_like(step.d["x"])
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        y = step(dx)
+        hy.copy_(y, non_blocking=True)
+
+    ms_e2e = max_over_ranks(time_steps(e2e_step, K, W, world) / K, world)
+    line = {
+        "metric": METRIC, "value": round(R * world / (ms_step / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{spec.name}: batched layout (E, max_tokens, H)", "E": spec.E,
+                   "T": spec.T, "H": spec.H, "I": spec.I, "valid_rows": R,
+                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2"},
+        "tflops": round(flops * world / (ms_step / 1e3) / 1e12, 2),
+        "roofline_step": {"t_roof_ms": round(roof_ms, 4), "frac": round(roof_ms / ms_step, 4)},
+        "roofline": {"kernel": "gemm1_swiglu", "bound": "hbm",
+                     "achieved": round(b1 / (g1 * 1e-6) / 1e9, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(b1 / (g1 * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                     "traffic": None, "peak_source": pk["source"] + " copy"},
+        "kernels_us": {k: round(v, 2) for k, v in kern.items()},
+        "gpu_launches": launches, "clocks": ck,
+        "e2e": {"value": round(R * world / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hy.numel() * 2},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def time_steps(step, K, W, world, ev_stream=None):
     for _ in range(W):
         step()
@@ -215,7 +297,7 @@ def run_ours(args, world, rank, local):
     pk = peaks()
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    spec = wl.SPECS[args.workload]
+    spec = {**wl.SPECS, **wl.PROFILE_SPECS}[args.workload]
     step = OurStep(spec, device)
     K, W = args.steps, args.warmup
 
@@ -407,7 +489,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="mixtral_prefill", choices=sorted(wl.SPECS))
+    ap.add_argument("--workload", default="mixtral_prefill",
+                    choices=sorted(wl.SPECS) + sorted(wl.PROFILE_SPECS) + sorted(wl.BATCHED_SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -419,6 +502,8 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank, local)
+    elif args.workload in wl.BATCHED_SPECS:
+        run_batched(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

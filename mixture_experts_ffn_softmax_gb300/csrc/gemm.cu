@@ -9,11 +9,12 @@
 // w2 [E, I, H], i.e. N-contiguous, so B is fed to the MMA as an MN-major
 // operand straight from its storage layout.
 //
-// Kernel shape (persistent, one CTA per SM, 192 threads):
+// Kernel shape (persistent, one CTA per SM, 320 threads):
 //   warp 0  lane 0 : TMA producer (A tile 128x64, B tile 64x256 per stage)
 //   warp 1         : TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=256,
 //                    K=16) and commits stage / accumulator barriers
-//   warps 2..5     : epilogue, one TMEM lane quadrant each (tcgen05.ld)
+//   warps 2..9     : epilogue, two warps per TMEM lane quadrant (tcgen05.ld),
+//                    each owning half of the tile's columns
 // The 512 TMEM columns hold two 128x256 fp32 accumulators so the epilogue of
 // tile i overlaps the MMAs of tile i+1.
 //
@@ -49,7 +50,8 @@ constexpr int BK = 64;           // K per stage: one 128-byte swizzle row of bf1
 constexpr int MMA_N = 256;       // accumulator columns per tile
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
 constexpr int STAGES = 4;
-constexpr int NTHREADS = 192;
+constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant
+constexpr int NTHREADS = 64 + EPI_WARPS * 32;  // producer + MMA + epilogue
 constexpr int A_STAGE_BYTES = BM * BK * 2;                 // 16 KB
 constexpr int B_CHUNK_BYTES = BK * 64 * 2;                 // 8 KB: 64 k-rows x 64 n
 constexpr int B_CHUNKS = MMA_N / 64;                       // 4
@@ -57,10 +59,9 @@ constexpr int B_STAGE_BYTES = B_CHUNKS * B_CHUNK_BYTES;    // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // 48 KB
 constexpr int TMEM_COLS = 2 * MMA_N;                       // 512
 constexpr int MAX_E = 1024;
-constexpr int EPI_WARPS = 4;
 constexpr int STAGING_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 128 bytes
 constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES +
-                              EPI_WARPS * STAGING_BYTES + (MAX_E + 1) * sizeof(int32_t);
+                              EPI_WARPS * STAGING_BYTES;
 
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
 
@@ -122,8 +123,10 @@ struct Tile {
 };
 
 // Tile t -> (expert, first padded row, column block).  Row blocks of one
-// expert are innermost.  s_off holds the padded expert offsets.
-__device__ __forceinline__ Tile map_tile(int t, const int32_t* s_off, int E, int NB) {
+// expert are innermost.  s_off holds the padded expert offsets (read through
+// L1: a binary search per tile).
+__device__ __forceinline__ Tile map_tile(int t, const int32_t* __restrict__ s_off, int E,
+                                         int NB) {
   int lo = 0, hi = E - 1;  // largest e with (s_off[e] / BM) * NB <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -178,9 +181,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* staging = tiles + STAGES * STAGE_BYTES;  // 1024-byte aligned
-  int32_t* s_off = reinterpret_cast<int32_t*>(staging + EPI_WARPS * STAGING_BYTES);
+  const int32_t* s_off = P.offsets;
 
-  for (int i = threadIdx.x; i <= P.E; i += NTHREADS) s_off[i] = P.offsets[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&ctl.full[s], 1);
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ctl.tmem_full[a], 1);
-      ptx::mbar_init(&ctl.tmem_empty[a], 4 * 32);
+      ptx::mbar_init(&ctl.tmem_empty[a], EPI_WARPS * 32);
     }
     ctl.abort = 0;
     ptx::fence_barrier_init();
@@ -291,7 +293,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue --
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;               // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;     // which half of the tile's columns it owns
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool real = entry >= 0 && entry < P.sentinel;  // padding rows are not stored
         const int64_t bias_row = static_cast<int64_t>(tl.e) * 2 * N;
 #pragma unroll 1
-        for (int c = 0; c < MMA_N / 2; c += 32) {
+        for (int c = half * (MMA_N / 4); c < (half + 1) * (MMA_N / 4); c += 32) {
           uint32_t g[32], u[32];
           ptx::tmem_ld_32cols(taddr + c, g);
           ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c, u);
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // a warp whose 32 rows are all padding has nothing to store
         const bool any_real = __ballot_sync(0xffffffffu, valid) != 0u;
 #pragma unroll 1
-        for (int c = 0; c < MMA_N; c += 32) {
+        for (int c = half * (MMA_N / 2); c < (half + 1) * (MMA_N / 2); c += 32) {
           const int n0 = tl.nb * MMA_N + c;
           if (n0 >= N || !any_real) break;  // warp-uniform
           uint32_t a[32];

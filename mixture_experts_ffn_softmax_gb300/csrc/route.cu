@@ -56,6 +56,32 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Order-preserving map of a float to an unsigned key (larger float ->
+// larger key); never 0 for a float, so 0 can mean "no candidate".
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = (f == 0.0f) ? 0u : __float_as_uint(f);  // -0 and +0 compare equal
+  const uint32_t k = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return k == 0u ? 1u : k;
+}
+
+// Best of a lane's slots: largest key, ties to the lower slot (= lower
+// expert id, since expert = slot * 32 + lane).
+template <int EPL>
+__device__ __forceinline__ void local_best(const uint32_t (&key)[EPL], const float (&p)[EPL],
+                                           uint32_t& bk, int& bi, float& bp) {
+  bk = key[0];
+  bi = 0;
+  bp = p[0];
+#pragma unroll
+  for (int i = 1; i < EPL; ++i) {
+    if (key[i] > bk) {
+      bk = key[i];
+      bi = i;
+      bp = p[i];
+    }
+  }
+}
+
 // EPL = experts per lane (expert e = i * 32 + lane).
 template <int EPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
@@ -158,31 +184,43 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 
   // ---- top-k by logit, ties to the lower expert id ----
+  // Each lane keeps its best remaining candidate; a round is one warp-wide
+  // max over order-preserving integer keys of the logits (REDUX), a ballot
+  // for ties, and -- only when two lanes tie -- a min over their expert ids.
+  uint32_t key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) key[i] = ((allowed >> i) & 1u) ? order_key(l[i]) : 0u;
+  uint32_t bk;
+  int bi;
+  float bp;
+  local_best<EPL>(key, p, bk, bi, bp);
   float wsum = 0.f;
   int my_id0 = 0, my_id1 = 0;
   float my_p0 = 0.f, my_p1 = 0.f;
   for (int j = 0; j < top_k; ++j) {
-    Cand c{-INFINITY, 0x7fffffff, 0.f};
-    bool have = false;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = i * 32 + lane;
-      if ((allowed >> i) & 1u) {
-        if (!have || better(l[i], e, c.key, c.idx)) {
-          c = Cand{l[i], e, p[i]};
-          have = true;
-        }
-      }
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
+    const unsigned holders = __ballot_sync(0xffffffffu, bk == mx);
+    int win_lane = __ffs(holders) - 1;
+    int win_e = __shfl_sync(0xffffffffu, bi * 32 + lane, win_lane);
+    if (__popc(holders) > 1) {  // equal logits in several lanes: lowest expert id wins
+      win_e = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, bk == mx ? static_cast<unsigned>(bi * 32 + lane) : 0xffffffffu));
+      win_lane = win_e & 31;
     }
-    c = warp_best(c);
-    if (c.idx < E && (c.idx & 31) == lane) allowed &= ~(1u << (c.idx >> 5));
-    wsum += c.val;
+    const float win_p = __shfl_sync(0xffffffffu, bp, win_lane);
+    if (lane == win_lane) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (i == bi) key[i] = 0u;
+      local_best<EPL>(key, p, bk, bi, bp);
+    }
+    wsum += win_p;
     if (j == lane) {
-      my_id0 = c.idx;
-      my_p0 = c.val;
+      my_id0 = win_e;
+      my_p0 = win_p;
     } else if (j == lane + 32) {
-      my_id1 = c.idx;
-      my_p1 = c.val;
+      my_id1 = win_e;
+      my_p1 = win_p;
     }
   }
   const bool norm = (method == MOE_ROUTE_SIGMOID) || renormalize;

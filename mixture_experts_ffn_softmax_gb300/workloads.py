@@ -120,6 +120,14 @@ SMALL_SPECS = {
                             routing_method="softmax", renormalize=True, bias=True),
 }
 
+# Copies sized for detailed profiler captures (a few GB on the device): the
+# DeepSeek-V3 expert shape and rows per expert (256) with 32 experts.
+PROFILE_SPECS = {
+    "deepseek_e32": MoESpec("deepseek_e32", M=1024, H=7168, I=2048, E=32, top_k=8,
+                            routing_method="sigmoid", k_group=4, group_count=8,
+                            group_select_mode=1, routed_scaling_factor=2.5),
+}
+
 SMALL_BATCHED_SPECS = {
     "batched_small": BatchedSpec("batched_small", E=6, T=160, H=256, I=320, top_k=4),
     "batched_bias_small": BatchedSpec("batched_bias_small", E=5, T=140, H=200, I=136,
@@ -241,6 +249,6 @@ def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-__all__ = ["MoESpec", "BatchedSpec", "SPECS", "BATCHED_SPECS", "SMALL_SPECS",
+__all__ = ["MoESpec", "BatchedSpec", "SPECS", "BATCHED_SPECS", "SMALL_SPECS", "PROFILE_SPECS",
            "SMALL_BATCHED_SPECS", "make_moe_inputs", "make_batched_inputs",
            "logit_bias", "to_f64", "ceil_div"]

@@ -88,6 +88,17 @@ def test_route_shapes_and_ties(case, ties):
     check_route(logits.numpy(), w, ids, a)
 
 
+def test_route_signed_zero_ties():
+    """-0.0 and +0.0 are equal logits: the lower expert id wins."""
+    logits = torch.tensor([[0.0, -0.0, -1.0, 0.0, -0.0, 0.5, -0.0, 0.0]]).repeat(3, 1)
+    logits[1] = torch.tensor([-0.0, 0.0, -0.0, -2.0, 0.0, -0.0, 0.0, -0.0])
+    a = dict(top_k=4, method="softmax", renormalize=True, k_group=1, group_count=1,
+             group_select_mode=0, routed_scaling_factor=1.0)
+    w, ids = _gpu_route(logits.cuda(), a)
+    check_route(logits.numpy(), w, ids, a)
+    assert ids[0].tolist() == [5, 0, 1, 3]
+
+
 def test_route_large_logits_and_empty():
     # sigmoid saturates in fp32 for large logits; selection is still exact
     logits = torch.tensor([[30.0, 40.0, 35.0, -50.0, 39.0, 41.0, 0.0, 20.0]]).repeat(9, 1)
