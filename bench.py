@@ -494,12 +494,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--tiles", default="auto", choices=["auto", "single", "pairs"],
+                    help="grouped-GEMM tile shape (default: the library's automatic choice)")
     ap.add_argument("--reduce", default="auto", choices=["auto", "separate", "epilogue_atomic"],
                     help="TopKWeightAndReduce choice (default: the library's AUTO rule)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     OurStep.reduce = args.reduce
     world, rank, local = dist_setup(args.gpus)
+    if args.impl == "ours" and args.tiles != "auto":
+        import mixture_experts_ffn_softmax_gb300 as pkg
+        pkg.set_gemm_tiles(args.tiles)
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     elif args.workload in wl.BATCHED_SPECS:

@@ -274,6 +274,13 @@ typedef struct {
 } moe_kernel_time_t;
 GBMOE_API moe_status_t moe_profiler_start(void);
 GBMOE_API moe_status_t moe_profiler_stop(moe_kernel_time_t* out, int32_t capacity, int32_t* n);
+/* Grouped-GEMM tile shape (process-wide tuning / testing knob):
+ * 0 = automatic (CTA pairs when the routed rows average at least four
+ * 128-row blocks per expert), 1 = single-CTA 128x256 tiles, 2 = CTA-pair
+ * 256x256 tiles (tcgen05 cta_group::2).  Results are the same up to fp32
+ * summation order.  Invalid values return MOE_ERR_INVALID_ARG. */
+GBMOE_API moe_status_t moe_set_gemm_tiles(int32_t mode);
+
 /* Total kernel launches issued by the library on this thread since load. */
 GBMOE_API int64_t moe_launch_count(void);
 

@@ -203,6 +203,13 @@ def selftest_wait_timeout(error_word: torch.Tensor, limit_us: int = 20000, strea
            "moe_selftest_wait_timeout")
 
 
+def set_gemm_tiles(mode: str = "auto"):
+    """Grouped-GEMM tile shape: "auto", "single" (one CTA per 128x256 tile)
+    or "pairs" (CTA pairs sharing a 256x256 tcgen05 cta_group::2 tile)."""
+    _check(lib().moe_set_gemm_tiles({"auto": 0, "single": 1, "pairs": 2}[mode]),
+           "moe_set_gemm_tiles")
+
+
 def launch_count() -> int:
     return lib().moe_launch_count()
 
@@ -223,5 +230,5 @@ def profiler_stop():
 __all__ = ["moe_route", "moe_align", "moe_forward", "moe_forward_batched", "fused_moe",
            "workspace_size", "batched_workspace_size", "alloc_workspace", "align_capacity",
            "workspace_error_word", "read_error", "launch_count", "workspace_layout",
-           "selftest_wait_timeout", "profiler_start",
+           "selftest_wait_timeout", "set_gemm_tiles", "profiler_start",
            "profiler_stop", "MoEError", "STATUS", "lib"]

@@ -7,6 +7,7 @@
 // caller-allocated workspace), and the "FlagGems fused_moe.py analysis"
 // chunk loop (tokens processed CHUNK_SIZE = 16 * 1024 at a time to bound
 // the intermediate caches) and its input validation list.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -41,6 +42,12 @@ cudaEvent_t take_event() {
   return e;
 }
 }  // namespace
+
+namespace {
+std::atomic<int> g_gemm_tile_mode{0};
+}  // namespace
+
+int gemm_tile_mode() { return g_gemm_tile_mode.load(std::memory_order_relaxed); }
 
 moe_status_t set_error(moe_status_t st, const char* fmt, ...) {
   va_list ap;
@@ -218,6 +225,12 @@ const char* moe_status_string(moe_status_t s) {
 const char* moe_last_error_detail(void) { return g_detail; }
 
 int64_t moe_launch_count(void) { return g_launches; }
+
+moe_status_t moe_set_gemm_tiles(int32_t mode) {
+  if (mode < 0 || mode > 2) return set_error(MOE_ERR_INVALID_ARG, "gemm tile mode %d", mode);
+  g_gemm_tile_mode.store(mode, std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 // ---------------------------------------------------------------- route --
 moe_status_t moe_route(const float* router_logits, int64_t M, int32_t E, int32_t top_k,
@@ -399,6 +412,7 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     g1.sentinel = static_cast<int32_t>(Rc);
     g1.error_word = err;
     g1.num_sms = sms;
+    g1.rows_hint = Rc;
     if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
 
     float* o = at<float>(workspace, L.o);
@@ -422,6 +436,7 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     g2.div = top_k;
     g2.error_word = err;
     g2.num_sms = sms;
+    g2.rows_hint = Rc;
     if (mode == MOE_REDUCE_EPILOGUE_ATOMIC) {
       if (moe_status_t st = launch_gemm2_atomic_f32(g2, s)) return st;
       if (moe_status_t st = launch_cast_f32_bf16(o, Mc * H, y + c0 * H, s)) return st;
@@ -496,6 +511,7 @@ moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens
   g1.sentinel = sentinel;
   g1.error_word = err;
   g1.num_sms = sms;
+  g1.rows_hint = static_cast<int64_t>(E) * T / 2;
   if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
 
   GroupedGemmArgs g2{};
@@ -513,6 +529,7 @@ moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens
   g2.sentinel = sentinel;
   g2.error_word = err;
   g2.num_sms = sms;
+  g2.rows_hint = static_cast<int64_t>(E) * T / 2;
   return launch_gemm2_rows_bf16(g2, s);
 }
 

@@ -34,6 +34,9 @@ void prof_after(const char* name, cudaStream_t s);
 moe_status_t set_error(moe_status_t st, const char* fmt, ...);
 moe_status_t check_launch(const char* name);
 
+// GEMM tile shape selection: 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles.
+int gemm_tile_mode();
+
 // ---- launchers (one per .cu file) ----
 struct RouteArgs {
   const float* logits;
@@ -115,6 +118,7 @@ struct GroupedGemmArgs {
   int32_t div;               // GEMM2 atomic: token of item r is r / div
   int32_t* error_word;
   int32_t num_sms;
+  int64_t rows_hint;         // routed rows (before padding), for the tile shape choice
 };
 moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s);
 // GEMM2, contiguous layout, SEPARATE reduce: weighted fp32 rows in sorted

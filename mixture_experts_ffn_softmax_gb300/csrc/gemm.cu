@@ -49,27 +49,39 @@ constexpr int BM = MOE_BLOCK_M;  // 128 rows per tile (MMA M)
 constexpr int BK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int MMA_N = 256;       // accumulator columns per tile
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
-constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant
 constexpr int NTHREADS = 64 + EPI_WARPS * 32;  // producer + MMA + epilogue
-constexpr int A_STAGE_BYTES = BM * BK * 2;                 // 16 KB
-constexpr int B_CHUNK_BYTES = BK * 64 * 2;                 // 8 KB: 64 k-rows x 64 n
-constexpr int B_CHUNKS = MMA_N / 64;                       // 4
-constexpr int B_STAGE_BYTES = B_CHUNKS * B_CHUNK_BYTES;    // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // 48 KB
-constexpr int TMEM_COLS = 2 * MMA_N;                       // 512
+constexpr int A_STAGE_BYTES = BM * BK * 2;     // 16 KB
+constexpr int B_CHUNK_BYTES = BK * 64 * 2;     // 8 KB: 64 k-rows x 64 n
+constexpr int B_CHUNKS = MMA_N / 64;           // 4 column chunks per tile
+constexpr int TMEM_COLS = 2 * MMA_N;           // 512: two accumulators
 constexpr int MAX_E = 1024;
-constexpr int STAGING_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 128 bytes
-constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES +
-                              EPI_WARPS * STAGING_BYTES;
+constexpr int STAGING_BYTES = 32 * 128;        // per epilogue warp: 32 rows x 128 bytes
 
-constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
+// CG = CTAs cooperating on one MMA tile.  CG = 1: a 128 x 256 tile per CTA,
+// 48 KB per pipeline stage.  CG = 2 (a CTA pair, tcgen05 cta_group::2): a
+// 256 x 256 tile per pair, each CTA staging its 128 rows of A and its 128
+// columns of B -- 32 KB per stage per CTA, a third less shared-memory fill
+// per MMA than CG = 1.
+template <int CG>
+struct Geo {
+  static constexpr int B_CHUNKS_CTA = B_CHUNKS / CG;
+  static constexpr int STAGE = A_STAGE_BYTES + B_CHUNKS_CTA * B_CHUNK_BYTES;
+  static constexpr int NSTAGES = CG == 1 ? 4 : 5;
+  static constexpr size_t PREFIX_BYTES = CG == 1 ? 0 : (MAX_E + 1) * sizeof(int32_t);
+  static constexpr size_t SMEM =
+      1024 /*alignment slack*/ + NSTAGES * STAGE + EPI_WARPS * STAGING_BYTES + PREFIX_BYTES;
+  static constexpr uint32_t IDESC =
+      ptx::idesc_bf16_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
+};
+static_assert(Geo<1>::SMEM <= 232448 && Geo<2>::SMEM <= 232448, "shared memory budget");
 
 enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3 };
 
+template <int NS>
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[NS];
+  uint64_t empty[NS];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint32_t tmem_base;
@@ -142,6 +154,35 @@ __device__ __forceinline__ Tile map_tile(int t, const int32_t* __restrict__ s_of
   return tl;
 }
 
+// CTA pairs: pair tile t -> (expert, column block, pair of row blocks).
+// s_pp[e] = sum over e' < e of ceil(row blocks of e' / 2).  CTA `rank` of
+// the pair takes row block 2 * pair + rank, which may not exist (odd count):
+// then it still feeds its half of the MMA (rows past the expert, never
+// stored) and skips the epilogue.
+struct PairTile {
+  int e, row0, nb;
+  bool mine;  // this CTA's row block belongs to the expert
+};
+__device__ __forceinline__ PairTile map_pair_tile(int t, const int32_t* s_pp,
+                                                  const int32_t* __restrict__ off, int E,
+                                                  int NB, int rank) {
+  int lo = 0, hi = E - 1;  // largest e with s_pp[e] * NB <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pp[mid] * NB <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int pairs = s_pp[e + 1] - s_pp[e];
+  const int local = t - s_pp[e] * NB;
+  const int mb = 2 * (local % pairs) + rank;
+  PairTile tl;
+  tl.e = e;
+  tl.nb = local / pairs;
+  tl.row0 = off[e] + mb * BM;
+  tl.mine = mb < (off[e + 1] - off[e]) / BM;
+  return tl;
+}
+
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -166,51 +207,96 @@ __device__ __forceinline__ void load_bias8(const bf16* bias, int64_t off, bool o
   }
 }
 
-template <Epi EPI>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmO, const KParams P) {
+template <Epi EPI, int CG>
+__device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                          const CUtensorMap* tmO, const KParams& P) {
+  using G = Geo<CG>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Ctl ctl;
+  __shared__ Ctl<G::NSTAGES> ctl;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
 
-  // 1024-byte aligned tile area (128-byte swizzle atoms), then offsets.
+  // 1024-byte aligned tile area (128-byte swizzle atoms), staging, prefix.
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* staging = tiles + STAGES * STAGE_BYTES;  // 1024-byte aligned
-  const int32_t* s_off = P.offsets;
+  uint8_t* staging = tiles + G::NSTAGES * G::STAGE;  // 1024-byte aligned
+  int32_t* s_pp = reinterpret_cast<int32_t*>(staging + EPI_WARPS * STAGING_BYTES);
+  const int32_t* off = P.offsets;
 
+  if constexpr (CG == 2) {
+    // prefix of ceil(row blocks / 2) over the experts: lane chunks + warp scan
+    if (warp == 0) {
+      const int per = ceil_div(P.E, 32);
+      const int e0 = lane * per, e1 = min(P.E, e0 + per);
+      int32_t part = 0;
+      for (int e = e0; e < e1; ++e) part += (((off[e + 1] - off[e]) / BM) + 1) >> 1;
+      int32_t incl = part;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int32_t run = incl - part;
+      for (int e = e0; e < e1; ++e) {
+        s_pp[e] = run;
+        run += (((off[e + 1] - off[e]) / BM) + 1) >> 1;
+      }
+      if (lane == 31) s_pp[P.E] = incl;
+    }
+  }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&ctl.full[s], 1);
-      ptx::mbar_init(&ctl.empty[s], 1);
+    for (int i = 0; i < G::NSTAGES; ++i) {
+      ptx::mbar_init(&ctl.full[i], 1);
+      ptx::mbar_init(&ctl.empty[i], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ctl.tmem_full[a], 1);
-      ptx::mbar_init(&ctl.tmem_empty[a], EPI_WARPS * 32);
+      ptx::mbar_init(&ctl.tmem_empty[a], CG * EPI_WARPS);
     }
     ctl.abort = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&tmA);
-    ptx::prefetch_tmap(&tmB);
-    if constexpr (EPI == Epi::SortedF32) ptx::prefetch_tmap(&tmO);
+    ptx::prefetch_tmap(tmA);
+    ptx::prefetch_tmap(tmB);
+    if constexpr (EPI == Epi::SortedF32) ptx::prefetch_tmap(tmO);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl.tmem_base, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (CG == 2) {
+      ptx::tmem_alloc_pair(&ctl.tmem_base, TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&ctl.tmem_base, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
 
-  const int total_tiles = (s_off[P.E] / BM) * P.NB;
+  const int total_tiles = (CG == 2) ? s_pp[P.E] * P.NB : (off[P.E] / BM) * P.NB;
+  const int unit = (CG == 2) ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = (CG == 2) ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int KB = ceil_div(P.K, BK);
+
+  auto tile_of = [&](int t, int& e, int& row0, int& nb, bool& mine) {
+    if constexpr (CG == 2) {
+      const PairTile pt = map_pair_tile(t, s_pp, off, P.E, P.NB, static_cast<int>(rank));
+      e = pt.e;
+      row0 = pt.row0;
+      nb = pt.nb;
+      mine = pt.mine;
+    } else {
+      const Tile tl = map_tile(t, off, P.E, P.NB);
+      e = tl.e;
+      row0 = tl.row0;
+      nb = tl.nb;
+      mine = true;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -218,30 +304,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const Tile tl = map_tile(t, s_off, P.E, P.NB);
+      for (int t = unit; t < total_tiles && ok; t += units) {
+        int e, row0, nb;
+        bool mine;
+        tile_of(t, e, row0, nb, mine);
         for (int kb = 0; kb < KB; ++kb) {
           if (!bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word)) {
             ok = false;
             break;
           }
-          uint8_t* sa = tiles + stage * STAGE_BYTES;
+          uint8_t* sa = tiles + stage * G::STAGE;
           uint8_t* sb = sa + A_STAGE_BYTES;
-          ptx::mbar_arrive_expect_tx(&ctl.full[stage], STAGE_BYTES);
-          ptx::tma_load_2d(sa, &tmA, &ctl.full[stage], kb * BK, tl.row0);
-          if constexpr (EPI == Epi::SwiGLU) {
-            // gate columns [nb*128, +128) then the same columns of the up half
+          if constexpr (CG == 1) {
+            ptx::mbar_arrive_expect_tx(&ctl.full[stage], G::STAGE);
+            ptx::tma_load_2d(sa, tmA, &ctl.full[stage], kb * BK, row0);
 #pragma unroll
-            for (int c = 0; c < B_CHUNKS; ++c)
-              ptx::tma_load_4d(sb + c * B_CHUNK_BYTES, &tmB, &ctl.full[stage],
-                               tl.nb * (MMA_N / 2) + (c & 1) * 64, c >> 1, kb * BK, tl.e);
+            for (int c = 0; c < B_CHUNKS; ++c) {
+              if constexpr (EPI == Epi::SwiGLU)  // gate cols [nb*128,+128), then the up half
+                ptx::tma_load_4d(sb + c * B_CHUNK_BYTES, tmB, &ctl.full[stage],
+                                 nb * (MMA_N / 2) + (c & 1) * 64, c >> 1, kb * BK, e);
+              else
+                ptx::tma_load_3d(sb + c * B_CHUNK_BYTES, tmB, &ctl.full[stage],
+                                 nb * MMA_N + c * 64, kb * BK, e);
+            }
           } else {
+            // both CTAs' copies complete on the even CTA's barrier, which
+            // expects the bytes of the whole pair
+            const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0);
+            if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * G::STAGE);
+            ptx::tma_load_2d_pair(sa, tmA, full0, kb * BK, row0);
 #pragma unroll
-            for (int c = 0; c < B_CHUNKS; ++c)
-              ptx::tma_load_3d(sb + c * B_CHUNK_BYTES, &tmB, &ctl.full[stage],
-                               tl.nb * MMA_N + c * 64, kb * BK, tl.e);
+            for (int c = 0; c < G::B_CHUNKS_CTA; ++c) {
+              const int gc = static_cast<int>(rank) * G::B_CHUNKS_CTA + c;  // chunk of the tile
+              if constexpr (EPI == Epi::SwiGLU)  // even CTA: gate columns, odd CTA: up columns
+                ptx::tma_load_4d_pair(sb + c * B_CHUNK_BYTES, tmB, full0,
+                                      nb * (MMA_N / 2) + (gc & 1) * 64, gc >> 1, kb * BK, e);
+              else
+                ptx::tma_load_3d_pair(sb + c * B_CHUNK_BYTES, tmB, full0, nb * MMA_N + gc * 64,
+                                      kb * BK, e);
+            }
           }
-          if (++stage == STAGES) {
+          if (++stage == G::NSTAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -250,13 +353,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    // (CG = 2: only the even CTA issues; its MMAs read both CTAs' tiles)
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < total_tiles && ok; t += units) {
         if (!bounded_wait(&ctl.tmem_empty[acc], acc_phase ^ 1u, &ctl.abort, P.error_word)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
@@ -266,7 +370,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t sa = ptx::smem_u32(tiles + stage * G::STAGE);
           const uint32_t sb = sa + A_STAGE_BYTES;
 #pragma unroll
           for (int ks = 0; ks < BK / UMMA_K; ++ks) {
@@ -275,16 +379,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // B (MN-major): advance 16 k-rows = 2048 bytes; 64-column chunks
             // are B_CHUNK_BYTES apart, 8-row k groups 1024 bytes apart.
             const uint64_t bdesc = ptx::smem_desc_sw128(sb + ks * 2048, B_CHUNK_BYTES, 1024);
-            ptx::mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | ks) != 0 ? 1u : 0u);
+            if constexpr (CG == 2)
+              ptx::mma_bf16_pair(d_tmem, adesc, bdesc, G::IDESC, (kb | ks) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16(d_tmem, adesc, bdesc, G::IDESC, (kb | ks) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(&ctl.empty[stage]);
-          if (++stage == STAGES) {
+          if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.empty[stage], 0x3);
+          else ptx::mma_commit(&ctl.empty[stage]);
+          if (++stage == G::NSTAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(&ctl.tmem_full[acc]);
+        if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.tmem_full[acc], 0x3);
+        else ptx::mma_commit(&ctl.tmem_full[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -298,28 +407,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const Tile tl = map_tile(t, s_off, P.E, P.NB);
+    for (int t = unit; t < total_tiles; t += units) {
+      int e, row0, nb;
+      bool mine;
+      tile_of(t, e, row0, nb, mine);
       const bool got = bounded_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, P.error_word);
       if (!__all_sync(0xffffffffu, got)) break;
       ptx::tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * MMA_N);
-      const int64_t p = tl.row0 + row;
+      const int64_t p = row0 + row;
 
-      if constexpr (EPI == Epi::SwiGLU) {
+      if (!mine) {
+        // this CTA's half of a pair tile has no rows of the expert
+      } else if constexpr (EPI == Epi::SwiGLU) {
         bf16* z = reinterpret_cast<bf16*>(P.out);
         const int N = P.N;
         const int32_t entry = P.row_index[p];
         const bool real = entry >= 0 && entry < P.sentinel;  // padding rows are not stored
-        const int64_t bias_row = static_cast<int64_t>(tl.e) * 2 * N;
+        const int64_t bias_row = static_cast<int64_t>(e) * 2 * N;
 #pragma unroll 1
         for (int c = half * (MMA_N / 4); c < (half + 1) * (MMA_N / 4); c += 32) {
           uint32_t g[32], u[32];
           ptx::tmem_ld_32cols(taddr + c, g);
           ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c, u);
           ptx::tmem_ld_wait();
-          const int n0 = tl.nb * (MMA_N / 2) + c;
+          const int n0 = nb * (MMA_N / 2) + c;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int n = n0 + v * 8;
@@ -345,13 +458,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int32_t entry = P.row_index[p];
         const bool valid = entry >= 0 && entry < P.sentinel;
         const float wgt = valid ? (P.row_weight != nullptr ? P.row_weight[entry] : 1.0f) : 0.0f;
-        const int64_t bias_row = static_cast<int64_t>(tl.e) * N;
+        const int64_t bias_row = static_cast<int64_t>(e) * N;
         uint8_t* stage_buf = staging + (warp - 2) * STAGING_BYTES;
         // a warp whose 32 rows are all padding has nothing to store
         const bool any_real = __ballot_sync(0xffffffffu, valid) != 0u;
 #pragma unroll 1
         for (int c = half * (MMA_N / 2); c < (half + 1) * (MMA_N / 2); c += 32) {
-          const int n0 = tl.nb * MMA_N + c;
+          const int n0 = nb * MMA_N + c;
           if (n0 >= N || !any_real) break;  // warp-uniform
           uint32_t a[32];
           ptx::tmem_ld_32cols(taddr + c, a);
@@ -377,7 +490,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              ptx::tma_store_2d(&tmO, stage_buf, n0, tl.row0 + q * 32);
+              ptx::tma_store_2d(tmO, stage_buf, n0, row0 + q * 32);
               ptx::bulk_commit();
             }
           } else if constexpr (EPI == Epi::AtomicF32) {
@@ -407,8 +520,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
+      // release the accumulator (the even CTA's MMA waits for both CTAs)
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&ctl.tmem_empty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2)
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ctl.tmem_empty[acc]), 0));
+        else
+          ptx::mbar_arrive(&ctl.tmem_empty[acc]);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -419,18 +539,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if constexpr (EPI == Epi::SortedF32) {
     if (warp >= 2 && lane == 0) ptx::bulk_wait0();  // TMA stores done before smem is released
   }
-  __syncthreads();
+  __syncwarp();  // lane-0-only roles rejoin their warp before the aligned barriers
+  if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
   if (*reinterpret_cast<volatile int32_t*>(&ctl.abort)) {
     // Give TMA copies and MMAs still in flight time to land before the
     // shared memory and TMEM of this CTA are released.
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
-    __syncthreads();
   }
+  if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (CG == 2) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else ptx::tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+template <Epi EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  gemm_body<EPI, 1>(&tmA, &tmB, &tmO, P);
+}
+
+template <Epi EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  gemm_body<EPI, 2>(&tmA, &tmB, &tmO, P);
 }
 
 // ------------------------------------------------------------------ host --
@@ -475,12 +613,27 @@ moe_status_t make_map(CUtensorMap* m, const void* base, int rank, const uint64_t
   return MOE_OK;
 }
 
+// CTA pairs (cta_group::2) pay off when the GEMM is tensor-bound and experts
+// have several 128-row blocks each.  Measured on GB300: pairs win for the
+// Mixtral- and Qwen-shape layers (~1000 rows per expert) and lose for the
+// HBM-bound DeepSeek-shape layer (256 rows per expert), so the automatic
+// choice asks for at least four row blocks per expert on average.
+bool use_pairs(const GroupedGemmArgs& a) {
+  const int mode = gemm_tile_mode();
+  if (mode == 1) return false;
+  if (mode == 2) return a.num_sms >= 2;
+  return a.rows_hint >= static_cast<int64_t>(4 * BM) * a.E && a.num_sms >= 2;
+}
+
 template <Epi EPI>
 moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+                             static_cast<int>(Geo<1>::SMEM)) != cudaSuccess ||
+        cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Geo<2>::SMEM)) != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
                        cudaGetErrorString(cudaGetLastError()));
     attr_done = true;
@@ -538,11 +691,36 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   P.NB = NB;
   P.sentinel = a.sentinel;
   P.div = a.div > 0 ? a.div : 1;
-  const int64_t max_tiles = (a.cap / BM) * NB;
-  if (max_tiles <= 0) return MOE_OK;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_tiles, a.num_sms));
+  const int64_t max_blocks = a.cap / BM;
+  if (max_blocks <= 0) return MOE_OK;
+  if (use_pairs(a)) {
+    // Persistent pairs: no more clusters than can be resident at once (the
+    // tiles are split statically among them).
+    static int resident = -1;
+    if (resident < 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (a.num_sms / 2));
+      cfg.blockDim = dim3(NTHREADS);
+      cfg.dynamicSmemBytes = Geo<2>::SMEM;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI>, &cfg) != cudaSuccess ||
+          n <= 0) {
+        cudaGetLastError();
+        n = a.num_sms / 2;
+      }
+      resident = std::min(n, a.num_sms / 2);
+    }
+    // at most blocks/2 + E/2 pair tiles per column block
+    const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
+    const unsigned clusters = static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
+    prof_before(name, s);
+    grouped_gemm_pair_kernel<EPI><<<2 * clusters, NTHREADS, Geo<2>::SMEM, s>>>(tmA, tmB, tmO, P);
+    prof_after(name, s);
+    return check_launch(name);
+  }
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
   prof_before(name, s);
-  grouped_gemm_kernel<EPI><<<grid, NTHREADS, SMEM_BYTES, s>>>(tmA, tmB, tmO, P);
+  grouped_gemm_kernel<EPI><<<grid, NTHREADS, Geo<1>::SMEM, s>>>(tmA, tmB, tmO, P);
   prof_after(name, s);
   return check_launch(name);
 }

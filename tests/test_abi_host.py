@@ -149,6 +149,14 @@ def test_align_capacity_and_validation():
     assert lib.moe_align(p, 4, 2, 8, 16, p, p, p, p, p, 0, None, None) == WS_SMALL
 
 
+def test_gemm_tile_mode_validation():
+    lib = pkg.lib()
+    assert lib.moe_set_gemm_tiles(3) == INVALID
+    assert lib.moe_set_gemm_tiles(-1) == INVALID
+    for m in (2, 1, 0):
+        assert lib.moe_set_gemm_tiles(m) == OK
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     _lib._lib_saved = _lib._lib
     try:

@@ -30,11 +30,16 @@ def _check_untouched(out, counts):
         assert (o[e, c:] == SENTINEL).all(), f"expert {e}: rows past the count were written"
 
 
+@pytest.mark.parametrize("tiles", ["single", "pairs"])
 @pytest.mark.parametrize("name", sorted(wl.SMALL_BATCHED_SPECS))
-def test_batched_small(name):
+def test_batched_small(name, tiles):
     spec = wl.SMALL_BATCHED_SPECS[name]
     d = wl.make_batched_inputs(spec, device="cuda")
-    out = _run(d)
+    pkg.set_gemm_tiles(tiles)
+    try:
+        out = _run(d)
+    finally:
+        pkg.set_gemm_tiles("auto")
     counts = d["expert_num_tokens"].cpu().numpy()
     ref = oracle.forward_batched(f64(d["x"]), counts, f64(d["w13"]), f64(d["w2"]),
                                  f64(d["w13_bias"]), f64(d["w2_bias"]), f64(d["row_weight"]))

@@ -24,10 +24,20 @@ def _oracle_route(spec, logits):
                         a["group_count"], a["group_select_mode"], a["routed_scaling_factor"])
 
 
+@pytest.fixture
+def tiles(request):
+    """Forces the grouped-GEMM tile shape for one test, then restores auto."""
+    pkg.set_gemm_tiles(request.param)
+    yield request.param
+    pkg.set_gemm_tiles("auto")
+
+
+@pytest.mark.parametrize("tiles", ["single", "pairs"], indirect=True)
 @pytest.mark.parametrize("reduce", ["separate", "epilogue_atomic"])
 @pytest.mark.parametrize("name", sorted(wl.SMALL_SPECS))
-def test_forward_small_workloads(name, reduce):
-    """Both TopKWeightAndReduce choices against the oracle."""
+def test_forward_small_workloads(name, reduce, tiles):
+    """Both TopKWeightAndReduce choices and both GEMM tile shapes (single CTA,
+    CTA pair) against the oracle."""
     spec = wl.SMALL_SPECS[name]
     d = wl.make_moe_inputs(spec, device="cuda")
     w, ids, _ = _oracle_route(spec, d["router_logits"])
@@ -124,6 +134,7 @@ def test_forward_in_place_and_reuse():
     assert pkg.read_error(pkg.workspace_error_word(ws)) == 0
 
 
+@pytest.mark.parametrize("tiles", ["auto", "pairs"], indirect=True)
 @pytest.mark.parametrize("reduce", ["auto", "separate", "epilogue_atomic"])
 @pytest.mark.parametrize("case", [
     dict(M=1, H=64, I=64, E=1, k=1),
@@ -133,7 +144,7 @@ def test_forward_in_place_and_reuse():
     dict(M=40, H=64, I=128, E=8, k=4, dup=True),
     dict(M=20000, H=64, I=64, E=4, k=2),   # crosses the 16384-token chunk
 ])
-def test_forward_edge_cases(case, reduce):
+def test_forward_edge_cases(case, reduce, tiles):
     g = torch.Generator(device="cuda").manual_seed(5)
     M, H, I, E, k = case["M"], case["H"], case["I"], case["E"], case["k"]
     x = torch.randn(M, H, generator=g, device="cuda").bfloat16()
@@ -197,6 +208,21 @@ def test_forward_bad_ids_report_error():
     ws = pkg.alloc_workspace(pkg.workspace_size(M, H, I, E, k))
     pkg.moe_forward(x, torch.ones(M, k, device="cuda"), ids, w13, w2, workspace=ws)
     assert pkg.read_error(pkg.workspace_error_word(ws)) == 4   # MOE_ERR_BAD_EXPERT_ID
+
+
+def test_tile_shapes_agree_full_size_mixtral():
+    """Single-CTA and CTA-pair GEMMs on the full Mixtral-shape prefill: same
+    result up to fp32 summation order."""
+    spec = wl.SPECS["mixtral_prefill"]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    w, ids = pkg.moe_route(d["router_logits"], spec.top_k, "softmax", True)
+    ys = []
+    for mode in ("single", "pairs"):
+        pkg.set_gemm_tiles(mode)
+        ys.append(pkg.moe_forward(d["hidden"], w, ids, d["w13"], d["w2"]))
+    pkg.set_gemm_tiles("auto")
+    torch.cuda.synchronize()
+    check_out(f64(ys[1]), f64(ys[0]), "pairs vs single")
 
 
 FULL = ["mixtral_prefill", "mixtral_decode", "deepseek_m64", "deepseek_m8192", "qwen_skew"]
