@@ -325,16 +325,20 @@ def run_ours(args, world, rank, local):
 
     g1 = kern.get("gemm1_swiglu", {}).get("avg_us")
     g2 = kern.get("gemm2_scatter", {}).get("avg_us")
-    step_roof_ms = 1e3 * max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+    step_roof_ms = 1e3 * max(flops / (pk["bf16_tflops_sustained"] * 1e12),
+                             nbytes / (pk["hbm_gbs"] * 1e9))
     if spec.M >= 1024:
         # tensor-bound: GEMM1 carries 4 R H I of the 6 R H I FLOPs
         f1 = 4.0 * spec.R * spec.H * spec.I
         ach = f1 / (g1 * 1e-6) / 1e12
+        # timed inside a long loop of steps (power cap engages): the sustained peak
+        peak = pk["bf16_tflops_sustained"]
         roof = {"kernel": "gemm1_swiglu", "bound": "tensor", "achieved": round(ach, 1),
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                 "traffic": measured_traffic("gemm1_swiglu", "mixtral_prefill")
                 if spec.name == "mixtral_prefill" else None,
-                "peak_source": pk["source"] + " burst bf16"}
+                "peak_source": pk["source"] + " sustained bf16 (kernel timed inside the step loop)",
+                "frac_of_burst_peak": round(ach / pk["bf16_tflops"], 4)}
     else:
         b1 = touched * spec.H * 2 * spec.I * 2 + spec.M * spec.H * 2
         ach = b1 / (g1 * 1e-6) / 1e9
@@ -372,7 +376,8 @@ def run_ours(args, world, rank, local):
         "tflops": round(tflops, 2),
         "roofline_step": {"t_roof_ms": round(step_roof_ms, 4),
                           "frac": round(step_roof_ms / ms_step, 4),
-                          "bound": "tensor" if flops / pk["bf16_tflops"] / 1e12 > nbytes / pk["hbm_gbs"] / 1e9 else "hbm"},
+                          "bound": "tensor" if flops / pk["bf16_tflops_sustained"] / 1e12 > nbytes / pk["hbm_gbs"] / 1e9 else "hbm",
+                          "peaks": "measured sustained bf16, measured copy GB/s"},
         "roofline": roof,
         "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
         "gpu_launches": launches,
