@@ -67,10 +67,22 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "scores", "group_mask", "topk_select", "route_weights", "route",
+    "router_logits", "scores", "group_mask", "topk_select", "route_weights", "route",
     "route_with_groups", "align", "silu", "expert_ffn", "forward",
     "token_output", "forward_batched", "moe_layer",
 ]
+
+
+# --------------------------------------------------------------------------
+# Router (FlagDoc fused_moe.py 分析, section 1.1: s_t = W_g^T x_t + b_g)
+# --------------------------------------------------------------------------
+
+def router_logits(x, w_gate, b_gate=None):
+    """s = x W_g + b_g with W_g stored [H, E] (d x E on the page) and b_g [E]."""
+    s = np.asarray(x, dtype=np.float64) @ np.asarray(w_gate, dtype=np.float64)
+    if b_gate is not None:
+        s = s + np.asarray(b_gate, dtype=np.float64)
+    return s
 
 
 # --------------------------------------------------------------------------
@@ -219,27 +231,42 @@ def silu(u):
         return u / (1.0 + np.exp(-u))
 
 
-def expert_ffn(x_rows, w13_e, w2_e, b13_e=None, b2_e=None):
+def expert_ffn(x_rows, w13_e, w2_e, b13_e=None, b2_e=None, z_scale=None):
     """f_e for a stack of rows: h = x W13_e + b13_e (2I wide), z = SiLU(h[:, :I])
-    * h[:, I:], o = z W2_e + b2_e.  Weights are stored [H, 2I] and [I, H]."""
+    * h[:, I:], o = z W2_e + b2_e.  Weights are stored [H, 2I] and [I, H].
+    z_scale (one scalar per row), if given, multiplies z before W2."""
     x_rows = np.asarray(x_rows, dtype=np.float64)
     I = w2_e.shape[0]
     h = x_rows @ w13_e
     if b13_e is not None:
         h = h + b13_e
     z = silu(h[:, :I]) * h[:, I:]
+    if z_scale is not None:
+        z = z * np.asarray(z_scale, dtype=np.float64)[:, None]
     o = z @ w2_e
     if b2_e is not None:
         o = o + b2_e
     return o
 
 
-def forward(x, topk_weights, topk_ids, w13, w2, w13_bias=None, w2_bias=None):
+def forward(x, topk_weights, topk_ids, w13, w2, w13_bias=None, w2_bias=None,
+            apply_router_weight_on_input=False, expert_map=None):
     """y_t = sum_j a(t, j) * f_{ids[t, j]}(x_t), evaluated expert by expert over
-    the routed items (t, j) that name that expert."""
+    the routed items (t, j) that name that expert.
+
+    apply_router_weight_on_input (FlagDoc section 1.2, the switch of the same
+    name): a(r) multiplies the input z_r of the second linear layer instead
+    of its output, o_r = W2^T (a z_r) + b2 and y_t = sum_r o_r.  By linearity
+    this equals the default when b2 = 0.
+
+    expert_map ("expert_map" of the FlagDoc kernel, expert parallelism):
+    global expert id -> index of that expert in the given (local) weights, or
+    -1 for an expert held elsewhere; items routed there contribute nothing."""
     x = np.asarray(x, dtype=np.float64)
     a = np.asarray(topk_weights, dtype=np.float64)
     ids = np.asarray(topk_ids)
+    if expert_map is not None:
+        ids = np.asarray(expert_map)[ids]
     M, H = x.shape
     E = w13.shape[0]
     y = np.zeros((M, H), dtype=np.float64)
@@ -247,10 +274,12 @@ def forward(x, topk_weights, topk_ids, w13, w2, w13_bias=None, w2_bias=None):
         t, j = np.nonzero(ids == e)
         if t.size == 0:
             continue
-        o = expert_ffn(x[t], w13[e], w2[e],
-                       None if w13_bias is None else w13_bias[e],
-                       None if w2_bias is None else w2_bias[e])
-        np.add.at(y, t, a[t, j][:, None] * o)
+        b13 = None if w13_bias is None else w13_bias[e]
+        b2 = None if w2_bias is None else w2_bias[e]
+        if apply_router_weight_on_input:
+            np.add.at(y, t, expert_ffn(x[t], w13[e], w2[e], b13, b2, z_scale=a[t, j]))
+        else:
+            np.add.at(y, t, a[t, j][:, None] * expert_ffn(x[t], w13[e], w2[e], b13, b2))
     return y
 
 

@@ -427,6 +427,77 @@ def test_fp64_oracle_vs_fp32_evaluation():
     assert rel < 1e-5
 
 
+def test_router_logits_closed_form_and_linearity():
+    """s = x W_g + b_g: with W_g picking coordinates the logits are the
+    coordinates themselves plus the bias; the map is linear in x."""
+    rng = np.random.default_rng(12)
+    H, E, M = 6, 4, 5
+    wg = np.zeros((H, E))
+    wg[2, 0] = wg[0, 1] = wg[5, 2] = 1.0
+    wg[1, 3], wg[4, 3] = 2.0, -1.0
+    bg = np.array([0.5, 0.0, -0.25, 1.0])
+    x = rng.standard_normal((M, H))
+    s = oracle.router_logits(x, wg, bg)
+    expect = np.stack([x[:, 2] + 0.5, x[:, 0], x[:, 5] - 0.25, 2 * x[:, 1] - x[:, 4] + 1.0], 1)
+    np.testing.assert_allclose(s, expect, rtol=0, atol=1e-15)
+    x2 = rng.standard_normal((M, H))
+    w = rng.standard_normal((H, E))
+    np.testing.assert_allclose(oracle.router_logits(x + 3 * x2, w),
+                               oracle.router_logits(x, w) + 3 * oracle.router_logits(x2, w),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_router_weight_on_input():
+    """FlagDoc section 1.2: multiplying the router weight into the second
+    layer's input equals multiplying its output when b2 = 0; with a bias the
+    difference is exactly sum_j (1 - a_j) b2[e_j]."""
+    rng = np.random.default_rng(13)
+    E, H, I, M, k = 5, 12, 16, 9, 2
+    w13, w2, b13, b2 = _rand_layer(rng, E, H, I)
+    x = rng.standard_normal((M, H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)])
+    a = rng.random((M, k))
+    np.testing.assert_allclose(
+        oracle.forward(x, a, ids, w13, w2, b13, None, apply_router_weight_on_input=True),
+        oracle.forward(x, a, ids, w13, w2, b13, None), rtol=1e-12, atol=1e-12)
+    d = (oracle.forward(x, a, ids, w13, w2, b13, b2, apply_router_weight_on_input=True)
+         - oracle.forward(x, a, ids, w13, w2, b13, b2))
+    expect = sum((1 - a[:, j])[:, None] * b2[ids[:, j]] for j in range(k))
+    np.testing.assert_allclose(d, expect, rtol=1e-10, atol=1e-12)
+    # closed-form layer: weight on input scales z, bias unscaled
+    w13c, b13c, w2c, b2c = _closed_form_case()
+    xc = np.array([[1.0, -2.0]])
+    y = oracle.forward(xc, np.array([[0.3]]), np.array([[0]]), w13c, w2c, b13c, b2c,
+                       apply_router_weight_on_input=True)
+    np.testing.assert_allclose(y[0], 0.3 * (_closed_form_expert(0, 1.0, -2.0) - b2c[0]) + b2c[0],
+                               rtol=1e-14, atol=1e-14)
+
+
+def test_expert_map_partition_sums_to_full_layer():
+    """Experts split across two holders (expert parallelism): each holder's
+    output counts only its experts' items; the two outputs sum to the layer."""
+    rng = np.random.default_rng(14)
+    E, H, I, M, k = 8, 10, 12, 11, 3
+    w13, w2, b13, b2 = _rand_layer(rng, E, H, I)
+    x = rng.standard_normal((M, H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)])
+    a = rng.random((M, k))
+    full = oracle.forward(x, a, ids, w13, w2, b13, b2)
+    owner = rng.permutation(E) % 2
+    parts = []
+    for r in (0, 1):
+        mine = np.flatnonzero(owner == r)
+        emap = np.full(E, -1)
+        emap[mine] = np.arange(mine.size)
+        parts.append(oracle.forward(x, a, ids, w13[mine], w2[mine], b13[mine], b2[mine],
+                                    expert_map=emap))
+    np.testing.assert_allclose(parts[0] + parts[1], full, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.forward(x, a, ids, w13, w2, b13, b2,
+                                              expert_map=np.arange(E)), full, rtol=0, atol=0)
+    assert not oracle.forward(x, a, ids, w13[:1], w2[:1], b13[:1], b2[:1],
+                              expert_map=np.full(E, -1)).any()
+
+
 # -------------------------------------------------------------- mutations ---
 
 def _pins_fail(golden_dir):
