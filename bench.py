@@ -409,10 +409,68 @@ def run_ours(args, world, rank, local):
             "kernels_us": {k: round(1e3 * v[1] / v[0], 2) for k, v in dprof.items()},
         }
 
+    if args.workload == "mixtral_prefill" and not args.no_next_rows:
+        line["next_rows"] = measure_next_rows(step, spec, K, W, world, pk)
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, step.d, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def measure_next_rows(step, spec, K, W, world, pk):
+    """The rows next to the hot path on the same layer: the router logits GEMM
+    (s = x W_g + b_g, W_g ~ N(0, 0.02)), the whole layer from the hidden
+    states, the router weight applied to the second layer's input, and one
+    expert-parallel holder of half the experts (expert_map)."""
+    import mixture_experts_ffn_softmax_gb300 as pkg
+    d = step.d
+    dev = d["hidden"].device
+    g = torch.Generator(device=dev).manual_seed(11)
+    wg = (torch.randn(spec.H, spec.E, generator=g, device=dev) * 0.02).bfloat16()
+    bg = (torch.randn(spec.E, generator=g, device=dev) * 0.02).bfloat16()
+    logits = torch.empty(spec.M, spec.E, device=dev)
+    out = {}
+
+    def router():
+        pkg.moe_router_logits(d["hidden"], wg, bg, logits)
+
+    ms = max_over_ranks(time_steps(router, K, W, world) / K, world)
+    rbytes = spec.M * spec.H * 2 + spec.H * spec.E * 2 + spec.M * spec.E * 4
+    out["router_logits"] = {"us": round(ms * 1e3, 2), "hbm_gbs": round(rbytes / (ms * 1e-3) / 1e9, 1),
+                            "hbm_frac": round(rbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+
+    def layer():
+        pkg.moe_router_logits(d["hidden"], wg, bg, logits)
+        step(logits=logits)
+
+    ms = max_over_ranks(time_steps(layer, K, W, world) / K, world)
+    out["layer_from_hidden"] = {"ms_per_step": round(ms, 4),
+                                "tokens_per_s": round(spec.M * world / (ms / 1e3), 1)}
+
+    def on_input():
+        pkg.moe_forward(d["hidden"], step.w, step.ids, d["w13"], d["w2"], d["w13_bias"],
+                        d["w2_bias"], step.ws, step.out, apply_router_weight_on_input=True)
+
+    ms = max_over_ranks(time_steps(on_input, K, W, world) / K, world)
+    out["router_weight_on_input"] = {"ms_per_step": round(ms, 4),
+                                     "tokens_per_s": round(spec.M * world / (ms / 1e3), 1)}
+
+    mine = torch.arange(0, spec.E, 2, device=dev)
+    emap = torch.full((spec.E,), -1, dtype=torch.int32, device=dev)
+    emap[mine] = torch.arange(mine.numel(), dtype=torch.int32, device=dev)
+    lw13, lw2 = d["w13"][mine].contiguous(), d["w2"][mine].contiguous()
+
+    def ep_half():
+        pkg.moe_forward(d["hidden"], step.w, step.ids, lw13, lw2, None, None, step.ws, step.out,
+                        expert_map=emap)
+
+    ms = max_over_ranks(time_steps(ep_half, K, W, world) / K, world)
+    local_items = int(torch.isin(step.ids, mine.to(torch.int32)).sum().item())
+    fl = 6.0 * local_items * spec.H * spec.I
+    out["expert_parallel_half"] = {"ms_per_step": round(ms, 4), "local_items": local_items,
+                                   "tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+    return out
 
 
 # ------------------------------------------------------- CPU oracle legs --
@@ -498,6 +556,7 @@ def main():
                     choices=sorted(wl.SPECS) + sorted(wl.PROFILE_SPECS) + sorted(wl.BATCHED_SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--tiles", default="auto", choices=["auto", "single", "pairs"],
                     help="grouped-GEMM tile shape (default: the library's automatic choice)")

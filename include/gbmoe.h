@@ -107,6 +107,31 @@ GBMOE_API moe_status_t moe_route(const float* router_logits, int64_t M, int32_t 
                        float routed_scaling_factor, float* topk_weights, int32_t* topk_ids,
                        moe_stream_t stream);
 
+/* moe_route_bf16: moe_route with bf16 router logits (the "MindIE-SD Fused
+ * MoE" page accepts bf16 router logits).  Each logit is widened exactly to
+ * fp32 first; everything else is as moe_route. */
+GBMOE_API moe_status_t moe_route_bf16(const void* router_logits, int64_t M, int32_t E,
+                                      int32_t top_k, int32_t routing_method, int32_t renormalize,
+                                      int32_t k_group, int32_t group_count,
+                                      int32_t group_select_mode, float routed_scaling_factor,
+                                      float* topk_weights, int32_t* topk_ids,
+                                      moe_stream_t stream);
+
+/* ---------------------------------------------------------- router GEMM --
+ * moe_router_logits: the router scores ahead of routing,
+ *   s_t = W_g^T x_t + b_g        ("fused_moe.py 分析" (FlagDoc), section 1.1)
+ * with fp32 accumulation: for few experts (E <= 32, H % 256 == 0, W_g up to
+ * 160 KB as fp32) a warp-per-token kernel with W_g in shared memory,
+ * otherwise the tensor-core grouped GEMM with one "expert".
+ *  hidden  device bf16 [M, H];  w_gate device bf16 [H, E] (W_g, d x E);
+ *  b_gate  device bf16 [E] or NULL;  logits device fp32 [M, E] out
+ * Limits: H % 8 == 0; E % 8 == 0 (16-byte weight rows; else
+ * MOE_ERR_UNSUPPORTED), 1 <= E <= 1024.
+ */
+GBMOE_API moe_status_t moe_router_logits(const void* hidden, const void* w_gate,
+                                         const void* b_gate, int64_t M, int32_t H, int32_t E,
+                                         float* logits, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- align --
  * moe_align: expert-sorted, block-padded permutation of the routed items.
  * Defines: "FlagGems fused_moe.py analysis", section moe_align_block_size
@@ -198,6 +223,34 @@ GBMOE_API moe_status_t moe_forward(const void* hidden, const float* topk_weights
                          const void* w13_bias, const void* w2_bias, void* workspace,
                          size_t workspace_bytes, int32_t reduce_mode, void* out,
                          moe_stream_t stream);
+
+/* moe_forward_opts: moe_forward with options.
+ *  reduce_mode   as moe_forward's (moe_reduce_t)
+ *  apply_router_weight_on_input  0: y_t = sum_r a(r) (W2^T z_r + b2);
+ *                1: the weight multiplies the second layer's input instead,
+ *                y_t = sum_r (W2^T (a(r) z_r) + b2) -- the switch of that name
+ *                in "fused_moe.py 分析" section 1.2; equal to 0 when b2 = 0.
+ *  expert_map    device int32 [num_global_experts] or NULL: topk_ids are then
+ *                global expert ids, mapped to the local expert index (into
+ *                w13 / w2 / biases, E of them) or -1 for experts held
+ *                elsewhere -- those items contribute nothing (expert-parallel
+ *                local compute; "fused_moe.py 分析", expert_map /
+ *                write_zeros_to_output).  A map entry outside [-1, E) or an id
+ *                outside [0, num_global_experts) sets MOE_ERR_BAD_EXPERT_ID.
+ */
+typedef struct {
+  int32_t reduce_mode;
+  int32_t apply_router_weight_on_input;
+  const int32_t* expert_map;
+  int32_t num_global_experts;
+} moe_forward_opts_t;
+GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
+                                        const int32_t* topk_ids, int64_t M, int32_t H,
+                                        int32_t I, int32_t E, int32_t top_k, const void* w13,
+                                        const void* w2, const void* w13_bias,
+                                        const void* w2_bias, void* workspace,
+                                        size_t workspace_bytes, const moe_forward_opts_t* opts,
+                                        void* out, moe_stream_t stream);
 
 /* ------------------------------------------------------ forward_batched --
  * moe_forward_batched: the Batched activation format.  Defines: "vLLM

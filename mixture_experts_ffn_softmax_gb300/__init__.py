@@ -82,19 +82,36 @@ def moe_route(router_logits: torch.Tensor, top_k: int, routing_method: str = "so
               group_select_mode: int = 0, routed_scaling_factor: float = 1.0,
               topk_weights: Optional[torch.Tensor] = None,
               topk_ids: Optional[torch.Tensor] = None, stream=None):
-    """router_logits fp32 [M, E] -> (topk_weights fp32 [M, k], topk_ids int32 [M, k])."""
-    assert router_logits.dtype == torch.float32 and router_logits.dim() == 2
+    """router_logits fp32 or bf16 [M, E] -> (topk_weights fp32 [M, k],
+    topk_ids int32 [M, k])."""
+    assert router_logits.dtype in (torch.float32, torch.bfloat16) and router_logits.dim() == 2
     M, E = router_logits.shape
     dev = router_logits.device
     if topk_weights is None:
         topk_weights = torch.empty(M, top_k, dtype=torch.float32, device=dev)
     if topk_ids is None:
         topk_ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
-    _check(lib().moe_route(_ptr(router_logits), M, E, top_k, ROUTING[routing_method],
-                           int(bool(renormalize)), k_group, group_count, group_select_mode,
-                           float(routed_scaling_factor), _ptr(topk_weights), _ptr(topk_ids),
-                           _stream(stream)), "moe_route")
+    fn = lib().moe_route if router_logits.dtype == torch.float32 else lib().moe_route_bf16
+    _check(fn(_ptr(router_logits), M, E, top_k, ROUTING[routing_method],
+              int(bool(renormalize)), k_group, group_count, group_select_mode,
+              float(routed_scaling_factor), _ptr(topk_weights), _ptr(topk_ids),
+              _stream(stream)), "moe_route")
     return topk_weights, topk_ids
+
+
+def moe_router_logits(hidden: torch.Tensor, w_gate: torch.Tensor,
+                      b_gate: Optional[torch.Tensor] = None,
+                      logits: Optional[torch.Tensor] = None, stream=None):
+    """s = hidden @ w_gate + b_gate on the tensor cores: hidden bf16 [M, H],
+    w_gate bf16 [H, E], b_gate bf16 [E] -> fp32 [M, E]."""
+    M, H = hidden.shape
+    E = w_gate.shape[1]
+    assert hidden.dtype == torch.bfloat16 and w_gate.dtype == torch.bfloat16
+    if logits is None:
+        logits = torch.empty(M, E, dtype=torch.float32, device=hidden.device)
+    _check(lib().moe_router_logits(_ptr(hidden), _ptr(w_gate), _ptr(b_gate), M, H, E,
+                                   _ptr(logits), _stream(stream)), "moe_router_logits")
+    return logits
 
 
 def align_capacity(M: int, top_k: int, E: int, block_m: int = BLOCK_M) -> int:
@@ -126,8 +143,15 @@ def moe_align(topk_ids: torch.Tensor, E: int, block_m: int = BLOCK_M,
 def moe_forward(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: torch.Tensor,
                 w13: torch.Tensor, w2: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
                 w2_bias: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                out: Optional[torch.Tensor] = None, reduce: str = "auto", stream=None):
-    """y [M, H] bf16 = sum_j topk_weights[:, j] * SwiGLU-expert_{topk_ids[:, j]}(hidden)."""
+                out: Optional[torch.Tensor] = None, reduce: str = "auto", stream=None,
+                apply_router_weight_on_input: bool = False,
+                expert_map: Optional[torch.Tensor] = None):
+    """y [M, H] bf16 = sum_j topk_weights[:, j] * SwiGLU-expert_{topk_ids[:, j]}(hidden).
+
+    apply_router_weight_on_input: the weight multiplies the second layer's
+    input instead of its output.  expert_map: int32 [num_global_experts]
+    mapping global ids in topk_ids to local experts (the E of w13) or -1
+    (held elsewhere; those items contribute nothing)."""
     M, H = hidden.shape
     E, H2, I2 = w13.shape
     I = I2 // 2
@@ -139,10 +163,20 @@ def moe_forward(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: torc
         workspace = alloc_workspace(workspace_size(M, H, I, E, k, reduce), hidden.device)
     if out is None:
         out = torch.empty_like(hidden)
-    _check(lib().moe_forward(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E, k,
-                             _ptr(w13), _ptr(w2), _ptr(w13_bias), _ptr(w2_bias),
-                             _ptr(workspace), workspace.numel(), REDUCE[reduce], _ptr(out),
-                             _stream(stream)), "moe_forward")
+    if not apply_router_weight_on_input and expert_map is None:
+        _check(lib().moe_forward(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E,
+                                 k, _ptr(w13), _ptr(w2), _ptr(w13_bias), _ptr(w2_bias),
+                                 _ptr(workspace), workspace.numel(), REDUCE[reduce], _ptr(out),
+                                 _stream(stream)), "moe_forward")
+        return out
+    if expert_map is not None:
+        assert expert_map.dtype == torch.int32 and expert_map.dim() == 1
+    opts = _lib.ForwardOpts(REDUCE[reduce], int(bool(apply_router_weight_on_input)),
+                            _ptr(expert_map), 0 if expert_map is None else expert_map.numel())
+    _check(lib().moe_forward_opts(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E,
+                                  k, _ptr(w13), _ptr(w2), _ptr(w13_bias), _ptr(w2_bias),
+                                  _ptr(workspace), workspace.numel(), ctypes.byref(opts),
+                                  _ptr(out), _stream(stream)), "moe_forward_opts")
     return out
 
 
@@ -177,6 +211,19 @@ def fused_moe(hidden: torch.Tensor, router_logits: torch.Tensor, w13: torch.Tens
     w, ids = moe_route(router_logits, top_k, routing_method, renormalize, k_group, group_count,
                        group_select_mode, routed_scaling_factor, stream=stream)
     return moe_forward(hidden, w, ids, w13, w2, w13_bias, w2_bias, workspace, out, stream=stream)
+
+
+def moe_layer(hidden: torch.Tensor, w_gate: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor,
+              top_k: int, b_gate=None, w13_bias=None, w2_bias=None, k_group: int = 1,
+              group_count: int = 1, group_select_mode: int = 0,
+              routing_method: str = "softmax", renormalize: bool = False,
+              routed_scaling_factor: float = 1.0, workspace=None, out=None, stream=None):
+    """The layer from the hidden states: router logits (x W_g + b_g), routing,
+    then the expert forward."""
+    logits = moe_router_logits(hidden, w_gate, b_gate, stream=stream)
+    return fused_moe(hidden, logits, w13, w2, top_k, w13_bias, w2_bias, k_group, group_count,
+                     group_select_mode, routing_method, renormalize, routed_scaling_factor,
+                     workspace, out, stream)
 
 
 def workspace_error_word(workspace: torch.Tensor) -> int:
@@ -227,7 +274,8 @@ def profiler_stop():
     return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}
 
 
-__all__ = ["moe_route", "moe_align", "moe_forward", "moe_forward_batched", "fused_moe",
+__all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
+           "moe_forward_batched", "fused_moe",
            "workspace_size", "batched_workspace_size", "alloc_workspace", "align_capacity",
            "workspace_error_word", "read_error", "launch_count", "workspace_layout",
            "selftest_wait_timeout", "set_gemm_tiles", "profiler_start",

@@ -12,6 +12,11 @@ c_i32, c_i64, c_f32, c_sz, c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_floa
 P_i32 = ctypes.POINTER(ctypes.c_int32)
 
 
+class ForwardOpts(ctypes.Structure):
+    _fields_ = [("reduce_mode", ctypes.c_int32), ("apply_router_weight_on_input", ctypes.c_int32),
+                ("expert_map", ctypes.c_void_p), ("num_global_experts", ctypes.c_int32)]
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
                 ("total_ms", ctypes.c_double)]
@@ -25,6 +30,12 @@ SIGNATURES = {
     "moe_launch_count": (c_i64, []),
     "moe_route": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_f32,
                           c_vp, c_vp, c_vp]),
+    "moe_route_bf16": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                               c_f32, c_vp, c_vp, c_vp]),
+    "moe_router_logits": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_vp, c_vp]),
+    "moe_forward_opts": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,
+                                 c_vp, c_vp, c_vp, c_sz, ctypes.POINTER(ForwardOpts), c_vp,
+                                 c_vp]),
     "moe_align_capacity": (c_sz, [c_i64, c_i32, c_i32, c_i32]),
     "moe_align_scratch_size": (c_sz, [c_i64, c_i32, c_i32]),
     "moe_align": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,

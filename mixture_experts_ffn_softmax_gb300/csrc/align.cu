@@ -26,11 +26,33 @@ constexpr int kChunk = 256;        // items per warp chunk
 constexpr int kAlignWarps = 8;     // warps (= chunks) per CTA
 constexpr int kScanThreads = 1024;
 
-__device__ __forceinline__ bool valid_id(int e, int E) { return e >= 0 && e < E; }
+// Expert of an item: the local expert id, or -1 if the item is not counted
+// here (expert held elsewhere per expert_map, or a bad id -- `bad` says which).
+__device__ __forceinline__ int local_expert(int e, int E, const int32_t* __restrict__ emap,
+                                            int E_global, bool& bad) {
+  if (emap != nullptr) {
+    if (e < 0 || e >= E_global) {
+      bad = true;
+      return -1;
+    }
+    e = __ldg(emap + e);
+    if (e >= E || e < -1) {
+      bad = true;
+      return -1;
+    }
+    return e;
+  }
+  if (e < 0 || e >= E) {
+    bad = true;
+    return -1;
+  }
+  return e;
+}
 
 __global__ void __launch_bounds__(kAlignWarps * 32)
     align_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int num_chunks,
-                      int32_t* __restrict__ chunk_counts, int32_t* error_word) {
+                      int32_t* __restrict__ chunk_counts, int32_t* error_word,
+                      const int32_t* __restrict__ emap, int E_global) {
   extern __shared__ int32_t hist_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kAlignWarps + warp;
@@ -43,9 +65,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32)
   for (int it = 0; it < kChunk / 32; ++it) {
     const int64_t r = r0 + it * 32 + lane;
     int e = -1;
-    if (r < R) e = ids[r];
-    const bool ok = (r < R) && valid_id(e, E);
-    bad |= (r < R) && !ok;
+    if (r < R) e = local_expert(ids[r], E, emap, E_global, bad);
+    const bool ok = e >= 0;
     const int key = ok ? e : -1;
     const unsigned grp = __match_any_sync(0xffffffffu, key);
     const int leader = __ffs(grp) - 1;
@@ -189,7 +210,8 @@ __global__ void __launch_bounds__(kScanThreads)
     align_small_kernel(const int32_t* __restrict__ ids, int R, int E, int block_m, int64_t cap,
                        int32_t* __restrict__ sorted, int32_t* __restrict__ offsets,
                        int32_t* __restrict__ counts, int32_t* __restrict__ block_expert,
-                       int32_t* __restrict__ inv, int32_t* error_word) {
+                       int32_t* __restrict__ inv, int32_t* error_word,
+                       const int32_t* __restrict__ emap, int E_global) {
   __shared__ int32_t s_cnt[32 * kSmallExperts];
   __shared__ int32_t s_count[kSmallExperts];
   __shared__ int32_t s_off[kSmallExperts + 1];
@@ -203,9 +225,8 @@ __global__ void __launch_bounds__(kScanThreads)
   bool bad = false;
   for (int it = 0; it < per; it += 32) {
     const int r = r0 + it + lane;
-    const int e = r < R ? ids[r] : -1;
-    const bool ok = r < R && valid_id(e, E);
-    bad |= r < R && !ok;
+    const int e = r < R ? local_expert(ids[r], E, emap, E_global, bad) : -1;
+    const bool ok = e >= 0;
     const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
     if (ok && lane == __ffs(grp) - 1) cnt[e] += __popc(grp);
     __syncwarp();
@@ -229,8 +250,9 @@ __global__ void __launch_bounds__(kScanThreads)
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int it = 0; it < per; it += 32) {
     const int r = r0 + it + lane;
-    const int e = r < R ? ids[r] : -1;
-    const bool ok = r < R && valid_id(e, E);
+    bool bad2 = false;
+    const int e = r < R ? local_expert(ids[r], E, emap, E_global, bad2) : -1;
+    const bool ok = e >= 0;
     const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
     const int32_t pos = ok ? cnt[e] + __popc(grp & lt_mask) : -1;
     if (ok) sorted[pos] = r;
@@ -245,7 +267,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32)
     align_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int num_chunks,
                          const int32_t* __restrict__ chunk_prefix,
                          const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted,
-                         int32_t* __restrict__ inv) {
+                         int32_t* __restrict__ inv, const int32_t* __restrict__ emap,
+                         int E_global) {
   extern __shared__ int32_t run_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kAlignWarps + warp;
@@ -259,8 +282,9 @@ __global__ void __launch_bounds__(kAlignWarps * 32)
   for (int it = 0; it < kChunk / 32; ++it) {
     const int64_t r = r0 + it * 32 + lane;
     int e = -1;
-    if (r < R) e = ids[r];
-    const bool ok = (r < R) && valid_id(e, E);
+    bool bad = false;
+    if (r < R) e = local_expert(ids[r], E, emap, E_global, bad);
+    const bool ok = e >= 0;
     const int key = ok ? e : -1;
     const unsigned grp = __match_any_sync(0xffffffffu, key);
     const int32_t pos = ok ? run[e] + __popc(grp & lt_mask) : -1;
@@ -354,7 +378,8 @@ moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
     prof_before("align_small", s);
     align_small_kernel<<<1, kScanThreads, 0, s>>>(a.ids, static_cast<int>(a.R), a.E, a.block_m,
                                                   a.cap, a.sorted, a.offsets, a.counts,
-                                                  a.block_expert, a.inv, a.error_word);
+                                                  a.block_expert, a.inv, a.error_word,
+                                                  a.expert_map, a.E_global);
     prof_after("align_small", s);
     return check_launch("align_small");
   }
@@ -363,7 +388,8 @@ moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>(ceil_div(num_chunks, kAlignWarps));
   prof_before("align_hist", s);
   align_hist_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
-                                                         a.chunk_counts, a.error_word);
+                                                         a.chunk_counts, a.error_word,
+                                                         a.expert_map, a.E_global);
   prof_after("align_hist", s);
   if (moe_status_t st = check_launch("align_hist")) return st;
   prof_before("align_colscan", s);
@@ -379,7 +405,7 @@ moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
   prof_before("align_scatter", s);
   align_scatter_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
                                                             a.chunk_counts, a.offsets, a.sorted,
-                                                            a.inv);
+                                                            a.inv, a.expert_map, a.E_global);
   prof_after("align_scatter", s);
   return check_launch("align_scatter");
 }

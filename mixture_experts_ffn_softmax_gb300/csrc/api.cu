@@ -233,11 +233,11 @@ moe_status_t moe_set_gemm_tiles(int32_t mode) {
 }
 
 // ---------------------------------------------------------------- route --
-moe_status_t moe_route(const float* router_logits, int64_t M, int32_t E, int32_t top_k,
-                       int32_t routing_method, int32_t renormalize, int32_t k_group,
-                       int32_t group_count, int32_t group_select_mode,
-                       float routed_scaling_factor, float* topk_weights, int32_t* topk_ids,
-                       moe_stream_t stream) {
+static moe_status_t route_impl(const void* router_logits, int32_t logits_bf16, int64_t M,
+                               int32_t E, int32_t top_k, int32_t routing_method,
+                               int32_t renormalize, int32_t k_group, int32_t group_count,
+                               int32_t group_select_mode, float routed_scaling_factor,
+                               float* topk_weights, int32_t* topk_ids, moe_stream_t stream) {
   g_detail[0] = 0;
   if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M=%lld < 0", (long long)M);
   if (E < 1 || E > 1024) return set_error(MOE_ERR_INVALID_ARG, "E=%d outside [1, 1024]", E);
@@ -263,8 +263,65 @@ moe_status_t moe_route(const float* router_logits, int64_t M, int32_t E, int32_t
     return set_error(MOE_ERR_INVALID_ARG, "null pointer");
   if (moe_status_t st = check_device(nullptr)) return st;
   RouteArgs a{router_logits, M, E, top_k, routing_method, renormalize ? 1 : 0, k_group,
-              group_count, group_select_mode, routed_scaling_factor, topk_weights, topk_ids};
+              group_count, group_select_mode, routed_scaling_factor, topk_weights, topk_ids,
+              logits_bf16};
   return launch_route(a, stream);
+}
+
+moe_status_t moe_route(const float* router_logits, int64_t M, int32_t E, int32_t top_k,
+                       int32_t routing_method, int32_t renormalize, int32_t k_group,
+                       int32_t group_count, int32_t group_select_mode,
+                       float routed_scaling_factor, float* topk_weights, int32_t* topk_ids,
+                       moe_stream_t stream) {
+  return route_impl(router_logits, 0, M, E, top_k, routing_method, renormalize, k_group,
+                    group_count, group_select_mode, routed_scaling_factor, topk_weights,
+                    topk_ids, stream);
+}
+
+moe_status_t moe_route_bf16(const void* router_logits, int64_t M, int32_t E, int32_t top_k,
+                            int32_t routing_method, int32_t renormalize, int32_t k_group,
+                            int32_t group_count, int32_t group_select_mode,
+                            float routed_scaling_factor, float* topk_weights,
+                            int32_t* topk_ids, moe_stream_t stream) {
+  return route_impl(router_logits, 1, M, E, top_k, routing_method, renormalize, k_group,
+                    group_count, group_select_mode, routed_scaling_factor, topk_weights,
+                    topk_ids, stream);
+}
+
+// ---------------------------------------------------------- router GEMM --
+moe_status_t moe_router_logits(const void* hidden, const void* w_gate, const void* b_gate,
+                               int64_t M, int32_t H, int32_t E, float* logits,
+                               moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M < 0");
+  if (H < 8 || H % 8 != 0) return set_error(MOE_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", H);
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_INVALID_ARG, "E=%d outside [1, 1024]", E);
+  if (E % 8 != 0)
+    return set_error(MOE_ERR_UNSUPPORTED, "E=%d: the router weight rows must be 16-byte multiples (E %% 8 == 0)", E);
+  if (M >= (int64_t(1) << 31)) return set_error(MOE_ERR_INVALID_ARG, "M too large");
+  if (M == 0) return MOE_OK;
+  if (!hidden || !w_gate || !logits) return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(hidden) || !aligned16(w_gate) || !aligned16(logits) ||
+      (b_gate && !aligned16(b_gate)))
+    return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  int sms = 0;
+  if (moe_status_t st = check_device(&sms)) return st;
+  if (router_small_fits(H, E))
+    return launch_router_small(static_cast<const bf16*>(hidden), static_cast<const bf16*>(w_gate),
+                               static_cast<const bf16*>(b_gate), M, H, E, logits, stream);
+  GroupedGemmArgs g{};
+  g.a = static_cast<const bf16*>(hidden);
+  g.w = static_cast<const bf16*>(w_gate);
+  g.bias = static_cast<const bf16*>(b_gate);
+  g.cap = M;
+  g.E = 1;
+  g.N = E;
+  g.K = H;
+  g.out = logits;
+  g.sentinel = static_cast<int32_t>(M);
+  g.num_sms = sms;
+  g.rows_hint = M;
+  return launch_dense_f32(g, stream);
 }
 
 // ---------------------------------------------------------------- align --
@@ -354,6 +411,27 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
                          int32_t top_k, const void* w13, const void* w2, const void* w13_bias,
                          const void* w2_bias, void* workspace, size_t workspace_bytes,
                          int32_t reduce_mode, void* out, moe_stream_t stream) {
+  moe_forward_opts_t o{};
+  o.reduce_mode = reduce_mode;
+  return moe_forward_opts(hidden, topk_weights, topk_ids, M, H, I, E, top_k, w13, w2, w13_bias,
+                          w2_bias, workspace, workspace_bytes, &o, out, stream);
+}
+
+moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
+                              const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                              int32_t E, int32_t top_k, const void* w13, const void* w2,
+                              const void* w13_bias, const void* w2_bias, void* workspace,
+                              size_t workspace_bytes, const moe_forward_opts_t* opts, void* out,
+                              moe_stream_t stream) {
+  if (!opts) return set_error(MOE_ERR_INVALID_ARG, "null opts");
+  const int32_t reduce_mode = opts->reduce_mode;
+  const bool weight_on_input = opts->apply_router_weight_on_input != 0;
+  if (opts->apply_router_weight_on_input != 0 && opts->apply_router_weight_on_input != 1)
+    return set_error(MOE_ERR_INVALID_ARG, "apply_router_weight_on_input must be 0 or 1");
+  if (opts->expert_map != nullptr &&
+      (opts->num_global_experts < 1 || opts->num_global_experts > (1 << 20)))
+    return set_error(MOE_ERR_INVALID_ARG, "num_global_experts=%d outside [1, 2^20]",
+                     opts->num_global_experts);
   size_t need = 0;
   if (moe_status_t st = moe_workspace_size(M, H, I, E, top_k, reduce_mode, &need)) return st;
   if (M == 0) return MOE_OK;
@@ -390,6 +468,8 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     AlignArgs al{topk_ids + c0 * top_k, Rc, E, MOE_BLOCK_M, sorted, offsets,
                  at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.block_expert),
                  at<int32_t>(workspace, L.scratch), cap, err, inv};
+    al.expert_map = opts->expert_map;
+    al.E_global = opts->num_global_experts;
     if (moe_status_t st = launch_align(al, s)) return st;
 
     bf16* a_perm = at<bf16>(workspace, L.a_perm);
@@ -410,6 +490,7 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     g1.out = z;
     g1.row_index = sorted;
     g1.sentinel = static_cast<int32_t>(Rc);
+    if (weight_on_input) g1.gemm1_row_weight = topk_weights + c0 * top_k;
     g1.error_word = err;
     g1.num_sms = sms;
     g1.rows_hint = Rc;
@@ -431,7 +512,7 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
     g2.offsets = offsets;
     g2.out = o;
     g2.row_index = sorted;
-    g2.row_weight = topk_weights + c0 * top_k;
+    g2.row_weight = weight_on_input ? nullptr : topk_weights + c0 * top_k;
     g2.sentinel = static_cast<int32_t>(Rc);
     g2.div = top_k;
     g2.error_word = err;

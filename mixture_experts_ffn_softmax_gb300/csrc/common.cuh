@@ -39,12 +39,13 @@ int gemm_tile_mode();
 
 // ---- launchers (one per .cu file) ----
 struct RouteArgs {
-  const float* logits;
+  const void* logits;  // fp32 or bf16 [M, E]
   int64_t M;
   int32_t E, top_k, method, renormalize, k_group, group_count, group_select_mode;
   float scale;
   float* weights;
   int32_t* ids;
+  int32_t logits_bf16 = 0;
 };
 moe_status_t launch_route(const RouteArgs& a, cudaStream_t s);
 
@@ -60,6 +61,11 @@ struct AlignArgs {
   int64_t cap;
   int32_t* error_word;
   int32_t* inv = nullptr;  // optional [R]: sorted position of item r (-1 if dropped)
+  // optional expert parallelism: ids are global ids in [0, E_global); an id
+  // maps to local expert expert_map[id] in [0, E), or -1 (held elsewhere:
+  // the item is skipped, not an error)
+  const int32_t* expert_map = nullptr;
+  int32_t E_global = 0;
 };
 size_t align_scratch_bytes(int64_t R, int32_t E);
 moe_status_t launch_align(const AlignArgs& a, cudaStream_t s);
@@ -119,7 +125,17 @@ struct GroupedGemmArgs {
   int32_t* error_word;
   int32_t num_sms;
   int64_t rows_hint;         // routed rows (before padding), for the tile shape choice
+  const float* gemm1_row_weight = nullptr;  // GEMM1: weight per routed item multiplied
+                                            // into z (router weight on the input)
 };
+// Dense GEMM with fp32 output: out [M, N] = a [M, K] @ w [K, N] + bias [N]
+// (the router logits), one "expert", single-CTA tiles.
+moe_status_t launch_dense_f32(const GroupedGemmArgs& a, cudaStream_t s);
+// Router logits for few experts (E <= 32, H % 256 == 0, W_g fits in shared
+// memory): SIMT, one warp per token, W_g staged in shared memory.
+bool router_small_fits(int H, int E);
+moe_status_t launch_router_small(const bf16* x, const bf16* wg, const bf16* bg, int64_t M,
+                                 int H, int E, float* s, cudaStream_t st);
 moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s);
 // GEMM2, contiguous layout, SEPARATE reduce: weighted fp32 rows in sorted
 // order, out = o_sorted [cap, N], written with TMA tensor stores.

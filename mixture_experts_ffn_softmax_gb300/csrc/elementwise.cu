@@ -133,3 +133,134 @@ moe_status_t launch_cast_f32_bf16(const float* acc, int64_t n, bf16* y, cudaStre
 }
 
 }  // namespace gbmoe
+
+namespace gbmoe {
+namespace {
+
+// Router logits for few experts: s[t, e] = sum_h x[t, h] W_g[h, e] + b_g[e]
+// ("fused_moe.py 分析" section 1.1), fp32 accumulate.  W_g [H, E] is staged
+// in shared memory (as fp32) once per block; one warp per token streams the
+// token's row (16-byte loads) -- x is read once, where a tensor-core tile
+// would have only M / 128 blocks of work.
+constexpr int kRouterWarps = 32;
+
+template <int EMAX>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_small_kernel(const bf16* __restrict__ x, const bf16* __restrict__ wg,
+                        const bf16* __restrict__ bg, int64_t M, int H, int E,
+                        float* __restrict__ s) {
+  extern __shared__ float4 router_smem[];
+  // W_g as fp32 [H][EMAX] (zero past E), 16 bytes of padding after every 8
+  // rows so that the 32 lanes, 8 rows apart, hit different banks.
+  float* sw = reinterpret_cast<float*>(router_smem);
+  constexpr int kRowPad = 4;  // floats per 8 rows
+  if (E == EMAX) {
+    // 16-byte loads: 8 bf16 weights at a time
+    for (int i = threadIdx.x; i < H * EMAX / 8; i += blockDim.x) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(wg) + i);
+      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+      const int h = (i * 8) / EMAX, e0 = (i * 8) % EMAX;
+      float* d = sw + h * EMAX + (h >> 3) * kRowPad + e0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(w2[j]);
+        d[2 * j] = f.x;
+        d[2 * j + 1] = f.y;
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < H * EMAX; i += blockDim.x) {
+      const int h = i / EMAX, e = i - h * EMAX;
+      sw[h * EMAX + (h >> 3) * kRowPad + e] =
+          e < E ? __bfloat162float(wg[static_cast<int64_t>(h) * E + e]) : 0.f;
+    }
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kRouterWarps + (threadIdx.x >> 5);
+  for (int64_t t = warp0; t < M; t += static_cast<int64_t>(gridDim.x) * kRouterWarps) {
+    float acc[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+    const bf16* row = x + t * H;
+    for (int hb = lane * 8; hb < H; hb += 4 * 256) {
+      uint4 xs[4];  // four 16-byte loads in flight before the math
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        xs[u] = (hb + u * 256 < H) ? __ldg(reinterpret_cast<const uint4*>(row + hb + u * 256))
+                                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+      const int h0 = hb + u * 256;
+      if (h0 >= H) break;
+      const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xs[u]);
+      const float* wrow = sw + h0 * EMAX + (h0 >> 3) * kRowPad;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 xf = __bfloat1622float2(xp[i]);
+        const float4* w0 = reinterpret_cast<const float4*>(wrow + (2 * i) * EMAX);
+        const float4* w1 = reinterpret_cast<const float4*>(wrow + (2 * i + 1) * EMAX);
+#pragma unroll
+        for (int q = 0; q < EMAX / 4; ++q) {
+          const float4 a = w0[q], b = w1[q];
+          acc[4 * q + 0] = fmaf(xf.x, a.x, fmaf(xf.y, b.x, acc[4 * q + 0]));
+          acc[4 * q + 1] = fmaf(xf.x, a.y, fmaf(xf.y, b.y, acc[4 * q + 1]));
+          acc[4 * q + 2] = fmaf(xf.x, a.z, fmaf(xf.y, b.z, acc[4 * q + 2]));
+          acc[4 * q + 3] = fmaf(xf.x, a.w, fmaf(xf.y, b.w, acc[4 * q + 3]));
+        }
+      }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      float v = acc[e];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc[e] = v;
+    }
+    if (lane < E && lane < EMAX) {
+      float v = 0.f;
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e)
+        if (e == lane) v = acc[e];
+      s[t * E + lane] = v + (bg != nullptr ? __bfloat162float(bg[lane]) : 0.f);
+    }
+  }
+}
+
+template <int EMAX>
+moe_status_t launch_router_small_t(const bf16* x, const bf16* wg, const bf16* bg, int64_t M,
+                                   int H, int E, float* s, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(H) * EMAX * sizeof(float) + (H / 8) * 16;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(router_small_kernel<EMAX>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
+        cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(router_small)");
+    attr = true;
+  }
+  const unsigned grid = static_cast<unsigned>(
+      std::min<int64_t>(ceil_div<int64_t>(M, kRouterWarps), device_sms()));
+  prof_before("router_small", st);
+  router_small_kernel<EMAX><<<grid, kRouterWarps * 32, smem, st>>>(x, wg, bg, M, H, E, s);
+  prof_after("router_small", st);
+  return check_launch("router_small");
+}
+
+}  // namespace
+
+bool router_small_fits(int H, int E) {
+  const int emax = E <= 8 ? 8 : (E <= 16 ? 16 : 32);
+  return E <= 32 && H % 256 == 0 &&
+         static_cast<size_t>(H) * emax * 4 + (H / 8) * 16 <= 160 * 1024;
+}
+
+moe_status_t launch_router_small(const bf16* x, const bf16* wg, const bf16* bg, int64_t M,
+                                 int H, int E, float* s, cudaStream_t st) {
+  if (E <= 8) return launch_router_small_t<8>(x, wg, bg, M, H, E, s, st);
+  if (E <= 16) return launch_router_small_t<16>(x, wg, bg, M, H, E, s, st);
+  return launch_router_small_t<32>(x, wg, bg, M, H, E, s, st);
+}
+
+}  // namespace gbmoe

@@ -35,6 +35,8 @@
 //                with 16-byte vector atomics (the k-sum happens in L2).
 //   RowsBF16   : GEMM2, batched layout.  Written as bf16 into the output row
 //                row_index[p] = e * T + i of valid rows only.
+//   DenseF32   : the router logits s = x W_g + b_g: one "expert", rows in
+//                token order, fp32 output [M, E].
 // Every mbarrier wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT,
 // all roles stop, in-flight copies are given time to land, TMEM is freed.
 #include <algorithm>
@@ -76,7 +78,7 @@ struct Geo {
 };
 static_assert(Geo<1>::SMEM <= 232448 && Geo<2>::SMEM <= 232448, "shared memory budget");
 
-enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3 };
+enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3, DenseF32 = 4 };
 
 template <int NS>
 struct Ctl {
@@ -96,6 +98,8 @@ struct KParams {
   const float* row_weight;
   int32_t* error_word;
   int32_t E, N, K, NB, sentinel, div;
+  int32_t dense_rows;             // > 0: one expert, rows [0, dense_rows), no offsets
+  const float* gemm1_row_weight;  // SwiGLU: per-item weight multiplied into z, or null
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
@@ -277,7 +281,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
 
-  const int total_tiles = (CG == 2) ? s_pp[P.E] * P.NB : (off[P.E] / BM) * P.NB;
+  const int dense_blocks = ceil_div(P.dense_rows, BM);
+  const int total_tiles = P.dense_rows > 0 ? dense_blocks * P.NB
+                          : (CG == 2)      ? s_pp[P.E] * P.NB
+                                           : (off[P.E] / BM) * P.NB;
   const int unit = (CG == 2) ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int units = (CG == 2) ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int KB = ceil_div(P.K, BK);
@@ -289,6 +296,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       row0 = pt.row0;
       nb = pt.nb;
       mine = pt.mine;
+    } else if (P.dense_rows > 0) {
+      e = 0;
+      nb = t / dense_blocks;
+      row0 = (t % dense_blocks) * BM;
+      mine = true;
     } else {
       const Tile tl = map_tile(t, off, P.E, P.NB);
       e = tl.e;
@@ -425,6 +437,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         const int N = P.N;
         const int32_t entry = P.row_index[p];
         const bool real = entry >= 0 && entry < P.sentinel;  // padding rows are not stored
+        // router weight applied to the second layer's input, if asked for
+        const float zw = (real && P.gemm1_row_weight != nullptr) ? P.gemm1_row_weight[entry] : 1.0f;
         const int64_t bias_row = static_cast<int64_t>(e) * 2 * N;
 #pragma unroll 1
         for (int c = half * (MMA_N / 4); c < (half + 1) * (MMA_N / 4); c += 32) {
@@ -448,14 +462,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
               const float g1 = __uint_as_float(g[v * 8 + 2 * i + 1]) + bg[2 * i + 1];
               const float u0 = __uint_as_float(u[v * 8 + 2 * i]) + bu[2 * i];
               const float u1 = __uint_as_float(u[v * 8 + 2 * i + 1]) + bu[2 * i + 1];
-              w[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+              w[i] = pack_bf16x2(silu_f(g0) * u0 * zw, silu_f(g1) * u1 * zw);
             }
             if (in && real) *reinterpret_cast<uint4*>(z + p * N + n) = pk;
           }
         }
       } else {
         const int N = P.N;
-        const int32_t entry = P.row_index[p];
+        const int32_t entry = (EPI == Epi::DenseF32) ? static_cast<int32_t>(p) : P.row_index[p];
         const bool valid = entry >= 0 && entry < P.sentinel;
         const float wgt = valid ? (P.row_weight != nullptr ? P.row_weight[entry] : 1.0f) : 0.0f;
         const int64_t bias_row = static_cast<int64_t>(e) * N;
@@ -501,6 +515,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
               for (int v = 0; v < 8; ++v)
                 if (n0 + v * 4 < N)
                   atomicAdd(d + v, make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]));
+            }
+          } else if constexpr (EPI == Epi::DenseF32) {
+            if (valid) {
+              float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(P.out) +
+                                                    static_cast<int64_t>(entry) * N + n0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                if (n0 + v * 4 < N)
+                  d[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
             }
           } else {
             if (valid) {
@@ -691,9 +714,12 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   P.NB = NB;
   P.sentinel = a.sentinel;
   P.div = a.div > 0 ? a.div : 1;
-  const int64_t max_blocks = a.cap / BM;
+  P.dense_rows = (EPI == Epi::DenseF32) ? static_cast<int32_t>(a.sentinel) : 0;
+  P.gemm1_row_weight = a.gemm1_row_weight;
+  // grouped operands are padded to whole 128-row blocks; the dense one is not
+  const int64_t max_blocks = (EPI == Epi::DenseF32) ? ceil_div<int64_t>(a.cap, BM) : a.cap / BM;
   if (max_blocks <= 0) return MOE_OK;
-  if (use_pairs(a)) {
+  if (EPI != Epi::DenseF32 && use_pairs(a)) {
     // Persistent pairs: no more clusters than can be resident at once (the
     // tiles are split statically among them).
     static int resident = -1;
@@ -742,6 +768,9 @@ moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s) {
 }
 moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::AtomicF32>(a, "gemm2_atomic", s);
+}
+moe_status_t launch_dense_f32(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::DenseF32>(a, "router_logits", s);
 }
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::RowsBF16>(a, "gemm2_rows_bf16", s);

@@ -82,10 +82,14 @@ __device__ __forceinline__ void local_best(const uint32_t (&key)[EPL], const flo
   }
 }
 
-// EPL = experts per lane (expert e = i * 32 + lane).
-template <int EPL>
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+
+// EPL = experts per lane (expert e = i * 32 + lane); T = fp32 or bf16 logits
+// (bf16 is widened exactly to fp32 before anything else).
+template <int EPL, typename T>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    route_kernel(const float* __restrict__ logits, int64_t M, int E, int top_k, int method,
+    route_kernel(const T* __restrict__ logits, int64_t M, int E, int top_k, int method,
                  int renormalize, int k_group, int group_count, int group_select_mode,
                  float scale, float* __restrict__ out_w, int32_t* __restrict__ out_ids) {
   extern __shared__ float route_smem[];
@@ -94,12 +98,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
   if (t >= M) return;
 
-  const float* row = logits + t * E;
+  const T* row = logits + t * E;
   float l[EPL], p[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = i * 32 + lane;
-    l[i] = (e < E) ? __ldg(row + e) : -FLT_MAX;
+    l[i] = (e < E) ? to_f32(row[e]) : -FLT_MAX;
   }
 
   // ---- scores ----
@@ -242,9 +246,14 @@ moe_status_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
   if (a.group_count > 1)
     smem = static_cast<size_t>(kWarpsPerBlock) * (2 * a.E + 2 * a.group_count) * sizeof(float);
   prof_before("route", s);
-  route_kernel<EPL><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, smem, s>>>(
-      a.logits, a.M, a.E, a.top_k, a.method, a.renormalize, a.k_group, a.group_count,
-      a.group_select_mode, a.scale, a.weights, a.ids);
+  if (a.logits_bf16)
+    route_kernel<EPL, bf16><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, smem, s>>>(
+        static_cast<const bf16*>(a.logits), a.M, a.E, a.top_k, a.method, a.renormalize,
+        a.k_group, a.group_count, a.group_select_mode, a.scale, a.weights, a.ids);
+  else
+    route_kernel<EPL, float><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, smem, s>>>(
+        static_cast<const float*>(a.logits), a.M, a.E, a.top_k, a.method, a.renormalize,
+        a.k_group, a.group_count, a.group_select_mode, a.scale, a.weights, a.ids);
   prof_after("route", s);
   return check_launch("route");
 }

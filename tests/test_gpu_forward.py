@@ -143,6 +143,8 @@ def test_forward_in_place_and_reuse():
     dict(M=129, H=512, I=256, E=4, k=2, one_expert=True),
     dict(M=40, H=64, I=128, E=8, k=4, dup=True),
     dict(M=20000, H=64, I=64, E=4, k=2),   # crosses the 16384-token chunk
+    dict(M=3, H=16, I=8, E=2, k=2),        # H, I below one 64-wide TMA box
+    dict(M=70, H=8, I=24, E=3, k=1),
 ])
 def test_forward_edge_cases(case, reduce, tiles):
     g = torch.Generator(device="cuda").manual_seed(5)
