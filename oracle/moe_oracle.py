@@ -67,6 +67,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
+    "e4m3_round", "quantize_rows_e4m3", "forward_fp8",
     "router_logits", "scores", "group_mask", "topk_select", "route_weights", "route",
     "route_with_groups", "align", "silu", "expert_ffn", "forward",
     "token_output", "forward_batched", "moe_layer",
@@ -324,4 +325,76 @@ def moe_layer(x, logits, w13, w2, top_k, method="softmax", renormalize=False,
     w, ids, margin = route(logits, top_k, method, renormalize, k_group, group_count,
                            group_select_mode, routed_scaling_factor)
     return forward(x, w, ids, w13, w2, w13_bias, w2_bias), w, ids, margin
+
+
+# --------------------------------------------------------------------------
+# FP8 W8A8 (FlagDoc fused_moe.py 分析, "FP8 W8A8" and "数据类型与量化辅助":
+# activations quantised to FP8 before each GEMM; the kernel multiplies the
+# FP8 dot product by the activation scale and the weight scale)
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v):
+    """Round float32 values to the nearest FP8 E4M3 value (1 sign, 4 exponent
+    bits with bias 7, 3 mantissa bits, no infinities, largest finite 448),
+    ties to even, saturating to +-448.  Returns the rounded values as fp64.
+    Normal binades [2^e, 2^(e+1)) for e in [-6, 8] have spacing 2^(e-3);
+    below 2^-6 the subnormal spacing is 2^-9."""
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)
+    step = np.exp2(e - 3)
+    q = np.round(a / step) * step        # numpy rounds half to even
+    q = np.minimum(q, E4M3_MAX)
+    return np.sign(v) * q
+
+
+def quantize_rows_e4m3(x):
+    """Dynamic per-row (per-token) FP8 quantisation: scale = max|row| / 448
+    (1 for an all-zero row), q = e4m3(x / scale); the division and the scale
+    are taken in fp32 (the decision that picks each code is made in the
+    precision of the kernel).  Returns (q as fp64 values, scale as fp64)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x32).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = e4m3_round(x32 / scale[:, None])
+    return q, scale.astype(np.float64)
+
+
+def forward_fp8(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2_scale,
+                w13_bias=None, w2_bias=None):
+    """The FP8 W8A8 layer.  Weights are FP8 values w_q with scales per expert
+    ([E]) or per output channel ([E, 2I] / [E, H]); each routed row is
+    quantised per row before GEMM1 (x) and before GEMM2 (z):
+        h = (q_x W13q) * s_x * s_w13 + b13,  z = SiLU(h_gate) * h_up,
+        o = (q_z W2q) * s_z * s_w2 + b2,     y_t = sum_j a(t, j) o.
+    Dot products of the FP8 values are exact in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.asarray(topk_weights, dtype=np.float64)
+    ids = np.asarray(topk_ids)
+    M, H = x.shape
+    E = w13_q.shape[0]
+    I = w2_q.shape[1]
+    y = np.zeros((M, H), dtype=np.float64)
+    qx, sx = quantize_rows_e4m3(x)
+    for e in range(E):
+        t, j = np.nonzero(ids == e)
+        if t.size == 0:
+            continue
+        s13 = np.asarray(w13_scale[e], dtype=np.float64)
+        s2 = np.asarray(w2_scale[e], dtype=np.float64)
+        h = (qx[t] @ np.asarray(w13_q[e], dtype=np.float64)) * sx[t][:, None] * s13
+        if w13_bias is not None:
+            h = h + w13_bias[e]
+        z = silu(h[:, :I]) * h[:, I:]
+        qz, sz = quantize_rows_e4m3(z)
+        o = (qz @ np.asarray(w2_q[e], dtype=np.float64)) * sz[:, None] * s2
+        if w2_bias is not None:
+            o = o + w2_bias[e]
+        np.add.at(y, t, a[t, j][:, None] * o)
+    return y
 

@@ -498,6 +498,104 @@ def test_expert_map_partition_sums_to_full_layer():
                               expert_map=np.full(E, -1)).any()
 
 
+def _e4m3_table():
+    """Every finite E4M3 value, decoded from its bit fields by the format's
+    definition (bias 7; exponent field 0 = subnormal; S.1111.111 = NaN)."""
+    vals = []
+    for code in range(256):
+        sgn = -1.0 if code & 0x80 else 1.0
+        ef, mf = (code >> 3) & 0xF, code & 0x7
+        if ef == 0xF and mf == 0x7:
+            continue
+        v = (mf / 8.0) * 2.0 ** -6 if ef == 0 else (1.0 + mf / 8.0) * 2.0 ** (ef - 7)
+        vals.append(sgn * v)
+    return np.array(sorted(set(vals)))
+
+
+def test_e4m3_rounding_against_the_format():
+    """Brute force over the code table: e4m3_round returns the nearest table
+    value (ties to the even mantissa), is the identity on the table, and
+    saturates at +-448; torch's float8_e4m3fn cast agrees inside the range."""
+    table = _e4m3_table()
+    assert table.size == 253 and table.max() == 448.0 and table[table > 0].min() == 2.0 ** -9
+    np.testing.assert_array_equal(oracle.e4m3_round(table), table)
+    rng = np.random.default_rng(21)
+    v = np.concatenate([rng.standard_normal(20000) * 10 ** rng.uniform(-4, 2.5, 20000),
+                        (table[:-1] + table[1:]) / 2])              # exact midpoints
+    v = v.astype(np.float32).astype(np.float64)
+    got = oracle.e4m3_round(v)
+    def mantissa_field(val):
+        a = abs(val)
+        if a < 2.0 ** -6:
+            return int(round(a / 2.0 ** -9))
+        e = np.floor(np.log2(a))
+        return int(round((a / 2.0 ** e - 1.0) * 8))
+
+    ties = 0
+    for x, g in zip(v[::3], got[::3]):
+        d = np.abs(table - min(max(x, -448.0), 448.0))
+        best = table[d == d.min()]
+        if best.size == 1:
+            assert g == best[0], x
+        else:  # a tie between two neighbours: the one with the even mantissa
+            assert g in best and mantissa_field(g) % 2 == 0, (x, best, g)
+            ties += 1
+    assert ties > 10
+    assert oracle.e4m3_round(np.array([1000.0, -1e6]))[0] == 448.0
+    assert oracle.e4m3_round(np.array([-1e6]))[0] == -448.0
+    inside = v[np.abs(v) <= 448.0]
+    ref = torch.from_numpy(inside.astype(np.float32)).to(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(oracle.e4m3_round(inside), ref)
+
+
+def test_quantize_rows_error_bound_and_scale():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((50, 300)) * rng.uniform(0.01, 10, (50, 1))
+    x[3] = 0.0
+    q, s = oracle.quantize_rows_e4m3(x)
+    assert s[3] == 1.0 and not q[3].any()
+    assert np.allclose(np.abs(q).max(axis=1)[np.arange(50) != 3], 448.0)
+    deq = q * s[:, None]
+    # relative half-step of a 3-bit mantissa, or half a subnormal step (times scale)
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * s[:, None]) * (1 + 1e-6)
+    assert (np.abs(deq - x) <= bound).all()
+
+
+def test_fp8_forward_reduces_to_exact_layer_on_representable_inputs():
+    """With every row's values in {0, +-1, +-2, +-4, +-8} and amax 8 (so
+    x / scale = 56 x lands on E4M3 values) and FP8 weights w_q with scale s,
+    the FP8 layer equals the layer with dequantised weights w_q * s and the
+    z quantisation written out by hand; per-expert scales broadcast like
+    per-channel ones."""
+    rng = np.random.default_rng(23)
+    E, H, I, M = 2, 16, 8, 7
+    x = rng.choice([0.0, 1.0, -1.0, 2.0, -2.0, 4.0, -4.0], size=(M, H))
+    x[:, 0] = 8.0                                     # row amax 8: x / scale = 56 x
+    table = _e4m3_table()
+    w13q = rng.choice(table[(np.abs(table) <= 4) & (np.abs(table) >= 0.25)], size=(E, H, 2 * I))
+    w2q = rng.choice(table[(np.abs(table) <= 4) & (np.abs(table) >= 0.25)], size=(E, I, H))
+    s13 = rng.uniform(0.01, 0.03, (E, 2 * I))
+    s2 = rng.uniform(0.01, 0.03, (E, H))
+    ids = np.stack([rng.permutation(E)[:1] for _ in range(M)])
+    a = rng.random((M, 1))
+    y8 = oracle.forward_fp8(x, a, ids, w13q, w2q, s13, s2)
+    # the same computation with the z quantisation made explicit
+    y = np.zeros((M, H))
+    for t in range(M):
+        e = ids[t, 0]
+        h = x[t] @ (w13q[e] * s13[e])
+        z = oracle.silu(h[:I]) * h[I:]
+        qz, sz = oracle.quantize_rows_e4m3(z[None, :])
+        y[t] = a[t, 0] * ((qz[0] * sz[0]) @ (w2q[e] * s2[e]))
+    # equal up to the fp32 rounding of the activation scale 8/448 (2^-24 relative)
+    np.testing.assert_allclose(y8, y, rtol=1e-6, atol=1e-12)
+    # and per-expert (tensor-wise) scales broadcast like per-channel ones
+    y8t = oracle.forward_fp8(x, a, ids, w13q, w2q, s13[:, :1] * np.ones((1, 2 * I)),
+                             s2[:, :1] * np.ones((1, H)))
+    y8e = oracle.forward_fp8(x, a, ids, w13q, w2q, s13[:, 0], s2[:, 0])
+    np.testing.assert_allclose(y8t, y8e, rtol=1e-12, atol=1e-14)
+
+
 # -------------------------------------------------------------- mutations ---
 
 def _pins_fail(golden_dir):
@@ -508,7 +606,10 @@ def _pins_fail(golden_dir):
               test_single_expert_is_dense_swiglu,
               test_uniform_topk_all_is_mean_of_experts,
               test_route_matches_printed_routing_function,
-              lambda: test_align_golden(golden_dir)]
+              lambda: test_align_golden(golden_dir),
+              test_e4m3_rounding_against_the_format,
+              test_quantize_rows_error_bound_and_scale,
+              test_fp8_forward_reduces_to_exact_layer_on_representable_inputs]
     for c in checks:
         try:
             c()
@@ -555,6 +656,22 @@ def _mut_sort_unstable_align(topk_ids, E, block_m):
     return a
 
 
+def _mut_e4m3_half_away(v):
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.clip(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6, 8)
+    step = np.exp2(e - 3)
+    return np.sign(v) * np.minimum(np.floor(a / step + 0.5) * step, 448.0)
+
+
+def _mut_quant_wrong_max(x):
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x32).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(240.0), np.float32(1.0)).astype(np.float32)
+    return om.e4m3_round(x32 / scale[:, None]), scale.astype(np.float64)
+
+
 _orig_align = om.align
 _ORIG_FFN = om.expert_ffn
 
@@ -566,6 +683,8 @@ _ORIG_FFN = om.expert_ffn
     ("topk_select", _mut_tie_high_id),
     ("route_weights", _mut_no_renorm),
     ("align", _mut_sort_unstable_align),
+    ("e4m3_round", _mut_e4m3_half_away),
+    ("quantize_rows_e4m3", _mut_quant_wrong_max),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, golden_dir, target, mutant):
     monkeypatch.setattr(om, target, mutant)
