@@ -252,6 +252,39 @@ GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_we
                                         size_t workspace_bytes, const moe_forward_opts_t* opts,
                                         void* out, moe_stream_t stream);
 
+/* ------------------------------------------------------------ FP8 W8A8 --
+ * moe_forward_fp8: the layer with FP8 (E4M3) weights and activations
+ * ("fused_moe.py 分析", "FP8 W8A8": the inputs of both GEMMs are quantised
+ * to FP8 before the GEMM, and each FP8 dot product is multiplied by the
+ * activation scale and the weight scale):
+ *   h = (q(x) W13q) s_x s_w13 + b13,  z = SiLU(h_gate) h_up,
+ *   o = (q(z) W2q) s_z s_w2 + b2,     y_t = sum_j a(t, j) o.
+ * Activations (each routed row of x, and of z) are quantised dynamically
+ * per row: scale = max|row| / 448, q = e4m3(row / scale), round to nearest
+ * even, saturating.  Weight scales are per expert ([E]) or per output
+ * channel ([E, 2I] and [E, H]).  Block-wise (128 x 128) weight scales are
+ * not offered.
+ *  w13, w2       device E4M3 bytes [E, H, 2I] and [E, I, H]
+ *  biases        bf16 as in moe_forward, or NULL
+ *  workspace     >= moe_workspace_size_fp8(...) bytes, 256-byte aligned
+ * Limits: as moe_forward, and H % 16 == 0, I % 16 == 0.
+ */
+typedef struct {
+  const void* w13;
+  const void* w2;
+  const float* w13_scale;
+  const float* w2_scale;
+  int32_t scale_per_channel; /* 0: scales [E]; 1: [E, 2I] and [E, H] */
+} moe_fp8_weights_t;
+GBMOE_API moe_status_t moe_workspace_size_fp8(int64_t M, int32_t H, int32_t I, int32_t E,
+                                              int32_t top_k, size_t* bytes);
+GBMOE_API moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
+                                       const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                                       int32_t E, int32_t top_k, const moe_fp8_weights_t* w,
+                                       const void* w13_bias, const void* w2_bias,
+                                       void* workspace, size_t workspace_bytes, void* out,
+                                       moe_stream_t stream);
+
 /* ------------------------------------------------------ forward_batched --
  * moe_forward_batched: the Batched activation format.  Defines: "vLLM
  * FusedMoEModularKernel" page, Introduction (activations (num_experts,

@@ -180,6 +180,40 @@ def moe_forward(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: torc
     return out
 
 
+def workspace_size_fp8(M: int, H: int, I: int, E: int, top_k: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size_fp8(M, H, I, E, top_k, ctypes.byref(n)),
+           "moe_workspace_size_fp8")
+    return n.value
+
+
+def moe_forward_fp8(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: torch.Tensor,
+                    w13_q: torch.Tensor, w2_q: torch.Tensor, w13_scale: torch.Tensor,
+                    w2_scale: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
+                    w2_bias: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None, stream=None):
+    """FP8 W8A8 layer: w13_q [E, H, 2I] / w2_q [E, I, H] E4M3 (torch.float8_e4m3fn
+    or uint8 bytes), scales fp32 per expert [E] or per output channel
+    ([E, 2I] / [E, H]); activations are quantised per row on the GPU."""
+    M, H = hidden.shape
+    E, _, I2 = w13_q.shape
+    I = I2 // 2
+    k = topk_ids.shape[1]
+    per_channel = int(w13_scale.dim() == 2)
+    assert w13_scale.dtype == torch.float32 and w2_scale.dtype == torch.float32
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size_fp8(M, H, I, E, k), hidden.device)
+    if out is None:
+        out = torch.empty_like(hidden)
+    wts = _lib.Fp8Weights(_ptr(w13_q), _ptr(w2_q), _ptr(w13_scale), _ptr(w2_scale), per_channel)
+    _check(lib().moe_forward_fp8(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E, k,
+                                 ctypes.byref(wts), _ptr(w13_bias), _ptr(w2_bias),
+                                 _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)),
+           "moe_forward_fp8")
+    return out
+
+
 def moe_forward_batched(x: torch.Tensor, expert_num_tokens: torch.Tensor, w13: torch.Tensor,
                         w2: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
                         w2_bias: Optional[torch.Tensor] = None,
@@ -275,7 +309,7 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
-           "moe_forward_batched", "fused_moe",
+           "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "fused_moe",
            "workspace_size", "batched_workspace_size", "alloc_workspace", "align_capacity",
            "workspace_error_word", "read_error", "launch_count", "workspace_layout",
            "selftest_wait_timeout", "set_gemm_tiles", "profiler_start",

@@ -17,6 +17,11 @@ class ForwardOpts(ctypes.Structure):
                 ("expert_map", ctypes.c_void_p), ("num_global_experts", ctypes.c_int32)]
 
 
+class Fp8Weights(ctypes.Structure):
+    _fields_ = [("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
+                ("w2_scale", ctypes.c_void_p), ("scale_per_channel", ctypes.c_int32)]
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
                 ("total_ms", ctypes.c_double)]
@@ -36,6 +41,9 @@ SIGNATURES = {
     "moe_forward_opts": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,
                                  c_vp, c_vp, c_vp, c_sz, ctypes.POINTER(ForwardOpts), c_vp,
                                  c_vp]),
+    "moe_workspace_size_fp8": (c_i32, [c_i64, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]),
+    "moe_forward_fp8": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32,
+                                ctypes.POINTER(Fp8Weights), c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_align_capacity": (c_sz, [c_i64, c_i32, c_i32, c_i32]),
     "moe_align_scratch_size": (c_sz, [c_i64, c_i32, c_i32]),
     "moe_align": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,

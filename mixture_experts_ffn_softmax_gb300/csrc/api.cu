@@ -529,6 +529,158 @@ moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
   return MOE_OK;
 }
 
+// ------------------------------------------------------------ FP8 W8A8 --
+namespace {
+struct Fp8Layout {
+  int64_t cap = 0;
+  size_t err = 0, counts = 0, offsets = 0, block_expert = 0, sorted = 0, scratch = 0, inv = 0,
+         a8 = 0, a_scale = 0, z = 0, z8 = 0, z_scale = 0, o = 0, total = 0;
+};
+
+Fp8Layout fp8_layout(int64_t Mc, int32_t H, int32_t I, int32_t E, int32_t k) {
+  Fp8Layout L;
+  const int64_t Rc = Mc * k;
+  L.cap = align_cap(Rc, E, MOE_BLOCK_M);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, kRegionAlign);
+    return at;
+  };
+  L.err = take(256);
+  L.counts = take(sizeof(int32_t) * E);
+  L.offsets = take(sizeof(int32_t) * (E + 1));
+  L.block_expert = take(sizeof(int32_t) * (L.cap / MOE_BLOCK_M));
+  L.sorted = take(sizeof(int32_t) * L.cap);
+  L.scratch = take(align_scratch_bytes(Rc, E));
+  L.inv = take(sizeof(int32_t) * Rc);
+  L.a8 = take(static_cast<size_t>(L.cap) * H);
+  L.a_scale = take(sizeof(float) * L.cap);
+  L.z = take(sizeof(bf16) * L.cap * I);
+  L.z8 = take(static_cast<size_t>(L.cap) * I);
+  L.z_scale = take(sizeof(float) * L.cap);
+  L.o = take(sizeof(float) * L.cap * H);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+moe_status_t moe_workspace_size_fp8(int64_t M, int32_t H, int32_t I, int32_t E, int32_t top_k,
+                                    size_t* bytes) {
+  g_detail[0] = 0;
+  if (!bytes) return set_error(MOE_ERR_INVALID_ARG, "null bytes");
+  if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M < 0");
+  if (moe_status_t st = validate_ffn_dims(H, I, E)) return st;
+  if (H % 16 != 0 || I % 16 != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "FP8 needs H and I multiples of 16 (16-byte rows)");
+  if (top_k < 1 || top_k > 64) return set_error(MOE_ERR_INVALID_ARG, "top_k=%d outside [1, 64]", top_k);
+  const int64_t Mc = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
+  *bytes = fp8_layout(Mc, H, I, E, top_k).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
+                             const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                             int32_t E, int32_t top_k, const moe_fp8_weights_t* w,
+                             const void* w13_bias, const void* w2_bias, void* workspace,
+                             size_t workspace_bytes, void* out, moe_stream_t stream) {
+  size_t need = 0;
+  if (moe_status_t st = moe_workspace_size_fp8(M, H, I, E, top_k, &need)) return st;
+  if (M == 0) return MOE_OK;
+  if (!w || !w->w13 || !w->w2 || !w->w13_scale || !w->w2_scale)
+    return set_error(MOE_ERR_INVALID_ARG, "null FP8 weights or scales");
+  if (w->scale_per_channel != 0 && w->scale_per_channel != 1)
+    return set_error(MOE_ERR_INVALID_ARG, "scale_per_channel must be 0 or 1");
+  if (!hidden || !topk_weights || !topk_ids || !workspace || !out)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(hidden) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(out) ||
+      !aligned16(w->w13_scale) || !aligned16(w->w2_scale) || (w13_bias && !aligned16(w13_bias)) ||
+      (w2_bias && !aligned16(w2_bias)))
+    return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < need)
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", need,
+                     workspace_bytes);
+  int sms = 0;
+  if (moe_status_t st = check_device(&sms)) return st;
+  cudaStream_t s = stream;
+  const int64_t Mc_max = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
+  const Fp8Layout L = fp8_layout(Mc_max, H, I, E, top_k);
+  int32_t* err = at<int32_t>(workspace, L.err);
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
+  const bf16* x = static_cast<const bf16*>(hidden);
+  bf16* y = static_cast<bf16*>(out);
+  for (int64_t c0 = 0; c0 < M; c0 += Mc_max) {
+    const int64_t Mc = (M - c0) < Mc_max ? (M - c0) : Mc_max;
+    const int64_t Rc = Mc * top_k;
+    const int64_t cap = align_cap(Rc, E, MOE_BLOCK_M);
+    int32_t* sorted = at<int32_t>(workspace, L.sorted);
+    int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    int32_t* inv = at<int32_t>(workspace, L.inv);
+    AlignArgs al{topk_ids + c0 * top_k, Rc, E, MOE_BLOCK_M, sorted, offsets,
+                 at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.block_expert),
+                 at<int32_t>(workspace, L.scratch), cap, err, inv};
+    if (moe_status_t st = launch_align(al, s)) return st;
+    // permute + quantise the token rows (E4M3, one scale per routed row)
+    uint8_t* a8 = at<uint8_t>(workspace, L.a8);
+    float* a_scale = at<float>(workspace, L.a_scale);
+    QuantRowsArgs qa{x + c0 * H, sorted, offsets, E, top_k, static_cast<int32_t>(Rc), H, cap, a8,
+                     a_scale};
+    if (moe_status_t st = launch_quant_rows_fp8(qa, s)) return st;
+    bf16* z = at<bf16>(workspace, L.z);
+    GroupedGemmArgs g1{};
+    g1.a = reinterpret_cast<const bf16*>(a8);
+    g1.w = static_cast<const bf16*>(w->w13);
+    g1.bias = static_cast<const bf16*>(w13_bias);
+    g1.cap = cap;
+    g1.E = E;
+    g1.N = I;
+    g1.K = H;
+    g1.offsets = offsets;
+    g1.out = z;
+    g1.row_index = sorted;
+    g1.sentinel = static_cast<int32_t>(Rc);
+    g1.error_word = err;
+    g1.num_sms = sms;
+    g1.rows_hint = Rc;
+    g1.a_scale = a_scale;
+    g1.w_scale = w->w13_scale;
+    g1.w_scale_per_channel = w->scale_per_channel;
+    if (moe_status_t st = launch_gemm1_swiglu_fp8(g1, s)) return st;
+    // quantise z per row for the second GEMM
+    uint8_t* z8 = at<uint8_t>(workspace, L.z8);
+    float* z_scale = at<float>(workspace, L.z_scale);
+    QuantRowsArgs qz{z, sorted, offsets, E, 0, static_cast<int32_t>(Rc), I, cap, z8, z_scale};
+    if (moe_status_t st = launch_quant_rows_fp8(qz, s)) return st;
+    float* o = at<float>(workspace, L.o);
+    GroupedGemmArgs g2{};
+    g2.a = reinterpret_cast<const bf16*>(z8);
+    g2.w = static_cast<const bf16*>(w->w2);
+    g2.bias = static_cast<const bf16*>(w2_bias);
+    g2.cap = cap;
+    g2.E = E;
+    g2.N = H;
+    g2.K = I;
+    g2.offsets = offsets;
+    g2.out = o;
+    g2.row_index = sorted;
+    g2.row_weight = topk_weights + c0 * top_k;
+    g2.sentinel = static_cast<int32_t>(Rc);
+    g2.div = top_k;
+    g2.error_word = err;
+    g2.num_sms = sms;
+    g2.rows_hint = Rc;
+    g2.a_scale = z_scale;
+    g2.w_scale = w->w2_scale;
+    g2.w_scale_per_channel = w->scale_per_channel;
+    if (moe_status_t st = launch_gemm2_sorted_fp8(g2, s)) return st;
+    if (moe_status_t st = launch_reduce_sorted(o, inv, Mc, top_k, H, y + c0 * H, s)) return st;
+  }
+  return MOE_OK;
+}
+
 // ------------------------------------------------------ forward_batched --
 moe_status_t moe_batched_workspace_size(int32_t E, int32_t T, int32_t H, int32_t I,
                                         size_t* bytes) {

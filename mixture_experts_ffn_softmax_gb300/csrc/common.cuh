@@ -101,6 +101,20 @@ struct GatherArgs {
 };
 moe_status_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
+// FP8 rows: for sorted position p < offsets[E] whose index[p] is a real
+// entry, row src[index[p] / div] (index == null: row p) is quantised with
+// its own scale = amax / 448: q8[p] = e4m3(row / scale), scale[p] = scale.
+struct QuantRowsArgs {
+  const bf16* src;
+  const int32_t* index;   // or null
+  const int32_t* offsets;
+  int32_t E, div, sentinel, H;
+  int64_t cap;
+  uint8_t* q8;
+  float* scale;
+};
+moe_status_t launch_quant_rows_fp8(const QuantRowsArgs& a, cudaStream_t s);
+
 // y[t, :] = bf16( sum_j o_sorted[inv[t*k + j], :] ), skipping inv < 0.
 moe_status_t launch_reduce_sorted(const float* o_sorted, const int32_t* inv, int64_t M,
                                   int32_t k, int32_t H, bf16* y, cudaStream_t s);
@@ -127,7 +141,13 @@ struct GroupedGemmArgs {
   int64_t rows_hint;         // routed rows (before padding), for the tile shape choice
   const float* gemm1_row_weight = nullptr;  // GEMM1: weight per routed item multiplied
                                             // into z (router weight on the input)
+  // FP8 operands (a and w are E4M3): acc * a_scale[sorted row] * weight scale
+  const float* a_scale = nullptr;
+  const float* w_scale = nullptr;       // [E, 2N] / [E, N] per channel, or [E]
+  int32_t w_scale_per_channel = 0;
 };
+moe_status_t launch_gemm1_swiglu_fp8(const GroupedGemmArgs& a, cudaStream_t s);
+moe_status_t launch_gemm2_sorted_fp8(const GroupedGemmArgs& a, cudaStream_t s);
 // Dense GEMM with fp32 output: out [M, N] = a [M, K] @ w [K, N] + bias [N]
 // (the router logits), one "expert", single-CTA tiles.
 moe_status_t launch_dense_f32(const GroupedGemmArgs& a, cudaStream_t s);

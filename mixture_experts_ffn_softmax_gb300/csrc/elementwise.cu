@@ -264,3 +264,78 @@ moe_status_t launch_router_small(const bf16* x, const bf16* wg, const bf16* bg, 
 }
 
 }  // namespace gbmoe
+
+#include <cuda_fp8.h>
+
+namespace gbmoe {
+namespace {
+
+constexpr int kQuantWarps = 8;
+
+// Dynamic per-row FP8 (E4M3) quantisation, one warp per row: scale =
+// amax / 448 (1 for an all-zero row), q = e4m3(x / scale) with round to
+// nearest even and saturation ("fused_moe.py 分析": activations are
+// quantised before each GEMM).  The division is IEEE fp32.
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quant_rows_fp8_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ index,
+                          const int32_t* __restrict__ offsets, int E, int div, int32_t sentinel,
+                          int H, int64_t cap, uint8_t* __restrict__ q8,
+                          float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = min(static_cast<int64_t>(offsets[E]), cap);
+  const int nvec = H / 8;
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
+  for (int64_t p = warp0; p < rows; p += nwarps) {
+    int64_t srow = p;
+    if (index != nullptr) {
+      const int32_t idx = index[p];
+      if (idx < 0 || idx >= sentinel) continue;  // padding row
+      if (div > 0) srow = idx / div;
+    }
+    const uint4* sv = reinterpret_cast<const uint4*>(src + srow * H);
+    float amax = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(sv + v);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    uint2* dq = reinterpret_cast<uint2*>(q8 + p * H);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(sv + v);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+      uint16_t b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        b[i] = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc)),
+                                        __NV_SATFINITE, __NV_E4M3);
+      }
+      dq[v] = make_uint2(static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16),
+                         static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16));
+    }
+    if (lane == 0) scale[p] = sc;
+  }
+}
+
+}  // namespace
+
+moe_status_t launch_quant_rows_fp8(const QuantRowsArgs& a, cudaStream_t s) {
+  if (a.cap <= 0) return MOE_OK;
+  const int64_t want = ceil_div<int64_t>(a.cap, kQuantWarps);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
+  prof_before("quant_rows_fp8", s);
+  quant_rows_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(a.src, a.index, a.offsets, a.E, a.div,
+                                                          a.sentinel, a.H, a.cap, a.q8, a.scale);
+  prof_after("quant_rows_fp8", s);
+  return check_launch("quant_rows_fp8");
+}
+
+}  // namespace gbmoe

@@ -48,14 +48,10 @@ namespace gbmoe {
 namespace {
 
 constexpr int BM = MOE_BLOCK_M;  // 128 rows per tile (MMA M)
-constexpr int BK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int MMA_N = 256;       // accumulator columns per tile
-constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
 constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant
 constexpr int NTHREADS = 64 + EPI_WARPS * 32;  // producer + MMA + epilogue
-constexpr int A_STAGE_BYTES = BM * BK * 2;     // 16 KB
-constexpr int B_CHUNK_BYTES = BK * 64 * 2;     // 8 KB: 64 k-rows x 64 n
-constexpr int B_CHUNKS = MMA_N / 64;           // 4 column chunks per tile
+constexpr int A_STAGE_BYTES = BM * 128;        // 16 KB: 128 rows x one 128-byte swizzle row
 constexpr int TMEM_COLS = 2 * MMA_N;           // 512: two accumulators
 constexpr int MAX_E = 1024;
 constexpr int STAGING_BYTES = 32 * 128;        // per epilogue warp: 32 rows x 128 bytes
@@ -65,18 +61,32 @@ constexpr int STAGING_BYTES = 32 * 128;        // per epilogue warp: 32 rows x 1
 // 256 x 256 tile per pair, each CTA staging its 128 rows of A and its 128
 // columns of B -- 32 KB per stage per CTA, a third less shared-memory fill
 // per MMA than CG = 1.
-template <int CG>
+// F8 = E4M3 operands (kind::f8f6f4, K = 32 per MMA) instead of bf16
+// (kind::f16, K = 16).  Either way a stage holds one 128-byte swizzle row of
+// K per A row: 64 bf16 or 128 E4M3; B is staged in chunks of one 128-byte
+// row of N (64 or 128 columns) by those K rows.
+template <int CG, bool F8 = false>
 struct Geo {
-  static constexpr int B_CHUNKS_CTA = B_CHUNKS / CG;
-  static constexpr int STAGE = A_STAGE_BYTES + B_CHUNKS_CTA * B_CHUNK_BYTES;
+  static constexpr int BKE = F8 ? 128 : 64;       // K elements per stage
+  static constexpr int CW = F8 ? 128 : 64;        // B columns per chunk
+  static constexpr int CHUNKS = MMA_N / CW;       // B chunks per tile
+  static constexpr int CHUNK_BYTES = BKE * 128;   // one chunk: BKE k-rows x 128 bytes
+  static constexpr int B_CHUNKS_CTA = CHUNKS / CG;
+  static constexpr int STAGE = A_STAGE_BYTES + B_CHUNKS_CTA * CHUNK_BYTES;
+  static constexpr int UMMA_K = F8 ? 32 : 16;     // K per tcgen05.mma
+  static constexpr int KSTEPS = BKE / UMMA_K;
+  static constexpr int B_KSTEP = UMMA_K * 128;    // bytes per MMA K step within a chunk
   static constexpr int NSTAGES = CG == 1 ? 4 : 5;
   static constexpr size_t PREFIX_BYTES = CG == 1 ? 0 : (MAX_E + 1) * sizeof(int32_t);
   static constexpr size_t SMEM =
       1024 /*alignment slack*/ + NSTAGES * STAGE + EPI_WARPS * STAGING_BYTES + PREFIX_BYTES;
   static constexpr uint32_t IDESC =
-      ptx::idesc_bf16_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
+      F8 ? ptx::idesc_e4m3_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true)
+         : ptx::idesc_bf16_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
 };
 static_assert(Geo<1>::SMEM <= 232448 && Geo<2>::SMEM <= 232448, "shared memory budget");
+static_assert(Geo<1, true>::SMEM <= 232448 && Geo<2, true>::SMEM <= 232448,
+              "shared memory budget");
 
 enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3, DenseF32 = 4 };
 
@@ -100,6 +110,11 @@ struct KParams {
   int32_t E, N, K, NB, sentinel, div;
   int32_t dense_rows;             // > 0: one expert, rows [0, dense_rows), no offsets
   const float* gemm1_row_weight;  // SwiGLU: per-item weight multiplied into z, or null
+  // FP8 dequantisation: acc * a_scale[row] * w_scale[e, col] (per channel,
+  // w_scale_ld columns per expert) or * w_scale[e] (per expert)
+  const float* a_scale;
+  const float* w_scale;
+  int32_t w_scale_per_channel, w_scale_ld;
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
@@ -194,6 +209,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 8 per-channel weight scales starting at column n of expert e (or the
+// expert's one scale 8 times); ones when there is no scale.
+__device__ __forceinline__ void load_wscale8(const KParams& P, int e, int n, bool ok, float* f) {
+  if (P.w_scale == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = 1.f;
+  } else if (!P.w_scale_per_channel) {
+    const float v = __ldg(P.w_scale + e);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = v;
+  } else if (ok) {
+    const float4* q = reinterpret_cast<const float4*>(P.w_scale +
+                                                      static_cast<int64_t>(e) * P.w_scale_ld + n);
+    const float4 a = __ldg(q), b = __ldg(q + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = 0.f;
+  }
+}
+
 // Loads 8 bf16 bias values as floats (zeros if bias == null or past n_lim).
 __device__ __forceinline__ void load_bias8(const bf16* bias, int64_t off, bool ok, float* f) {
   if (bias != nullptr && ok) {
@@ -211,10 +248,10 @@ __device__ __forceinline__ void load_bias8(const bf16* bias, int64_t off, bool o
   }
 }
 
-template <Epi EPI, int CG>
+template <Epi EPI, int CG, bool F8>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                           const CUtensorMap* tmO, const KParams& P) {
-  using G = Geo<CG>;
+  using G = Geo<CG, F8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl<G::NSTAGES> ctl;
 
@@ -287,7 +324,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
                                            : (off[P.E] / BM) * P.NB;
   const int unit = (CG == 2) ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int units = (CG == 2) ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  const int KB = ceil_div(P.K, BK);
+  const int KB = ceil_div(P.K, G::BKE);
 
   auto tile_of = [&](int t, int& e, int& row0, int& nb, bool& mine) {
     if constexpr (CG == 2) {
@@ -329,31 +366,33 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           uint8_t* sb = sa + A_STAGE_BYTES;
           if constexpr (CG == 1) {
             ptx::mbar_arrive_expect_tx(&ctl.full[stage], G::STAGE);
-            ptx::tma_load_2d(sa, tmA, &ctl.full[stage], kb * BK, row0);
+            ptx::tma_load_2d(sa, tmA, &ctl.full[stage], kb * G::BKE, row0);
 #pragma unroll
-            for (int c = 0; c < B_CHUNKS; ++c) {
+            for (int c = 0; c < G::CHUNKS; ++c) {
               if constexpr (EPI == Epi::SwiGLU)  // gate cols [nb*128,+128), then the up half
-                ptx::tma_load_4d(sb + c * B_CHUNK_BYTES, tmB, &ctl.full[stage],
-                                 nb * (MMA_N / 2) + (c & 1) * 64, c >> 1, kb * BK, e);
+                ptx::tma_load_4d(sb + c * G::CHUNK_BYTES, tmB, &ctl.full[stage],
+                                 nb * (MMA_N / 2) + (c % (G::CHUNKS / 2)) * G::CW,
+                                 c / (G::CHUNKS / 2), kb * G::BKE, e);
               else
-                ptx::tma_load_3d(sb + c * B_CHUNK_BYTES, tmB, &ctl.full[stage],
-                                 nb * MMA_N + c * 64, kb * BK, e);
+                ptx::tma_load_3d(sb + c * G::CHUNK_BYTES, tmB, &ctl.full[stage],
+                                 nb * MMA_N + c * G::CW, kb * G::BKE, e);
             }
           } else {
             // both CTAs' copies complete on the even CTA's barrier, which
             // expects the bytes of the whole pair
             const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0);
             if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * G::STAGE);
-            ptx::tma_load_2d_pair(sa, tmA, full0, kb * BK, row0);
+            ptx::tma_load_2d_pair(sa, tmA, full0, kb * G::BKE, row0);
 #pragma unroll
             for (int c = 0; c < G::B_CHUNKS_CTA; ++c) {
               const int gc = static_cast<int>(rank) * G::B_CHUNKS_CTA + c;  // chunk of the tile
               if constexpr (EPI == Epi::SwiGLU)  // even CTA: gate columns, odd CTA: up columns
-                ptx::tma_load_4d_pair(sb + c * B_CHUNK_BYTES, tmB, full0,
-                                      nb * (MMA_N / 2) + (gc & 1) * 64, gc >> 1, kb * BK, e);
+                ptx::tma_load_4d_pair(sb + c * G::CHUNK_BYTES, tmB, full0,
+                                      nb * (MMA_N / 2) + (gc % (G::CHUNKS / 2)) * G::CW,
+                                      gc / (G::CHUNKS / 2), kb * G::BKE, e);
               else
-                ptx::tma_load_3d_pair(sb + c * B_CHUNK_BYTES, tmB, full0, nb * MMA_N + gc * 64,
-                                      kb * BK, e);
+                ptx::tma_load_3d_pair(sb + c * G::CHUNK_BYTES, tmB, full0,
+                                      nb * MMA_N + gc * G::CW, kb * G::BKE, e);
             }
           }
           if (++stage == G::NSTAGES) {
@@ -385,16 +424,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           const uint32_t sa = ptx::smem_u32(tiles + stage * G::STAGE);
           const uint32_t sb = sa + A_STAGE_BYTES;
 #pragma unroll
-          for (int ks = 0; ks < BK / UMMA_K; ++ks) {
-            // A (K-major): advance 16 bf16 = 32 bytes along the swizzled row.
+          for (int ks = 0; ks < G::KSTEPS; ++ks) {
+            // A (K-major): advance UMMA_K elements = 32 bytes along the swizzled row.
             const uint64_t adesc = ptx::smem_desc_sw128(sa + ks * 32, 16, 1024);
-            // B (MN-major): advance 16 k-rows = 2048 bytes; 64-column chunks
-            // are B_CHUNK_BYTES apart, 8-row k groups 1024 bytes apart.
-            const uint64_t bdesc = ptx::smem_desc_sw128(sb + ks * 2048, B_CHUNK_BYTES, 1024);
-            if constexpr (CG == 2)
-              ptx::mma_bf16_pair(d_tmem, adesc, bdesc, G::IDESC, (kb | ks) != 0 ? 1u : 0u);
-            else
-              ptx::mma_bf16(d_tmem, adesc, bdesc, G::IDESC, (kb | ks) != 0 ? 1u : 0u);
+            // B (MN-major): advance UMMA_K k-rows; column chunks are
+            // CHUNK_BYTES apart, 8-row k groups 1024 bytes apart.
+            const uint64_t bdesc =
+                ptx::smem_desc_sw128(sb + ks * G::B_KSTEP, G::CHUNK_BYTES, 1024);
+            const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
+            if constexpr (CG == 2 && F8) ptx::mma_e4m3_pair(d_tmem, adesc, bdesc, G::IDESC, accum);
+            else if constexpr (CG == 2) ptx::mma_bf16_pair(d_tmem, adesc, bdesc, G::IDESC, accum);
+            else if constexpr (F8) ptx::mma_e4m3(d_tmem, adesc, bdesc, G::IDESC, accum);
+            else ptx::mma_bf16(d_tmem, adesc, bdesc, G::IDESC, accum);
           }
           if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.empty[stage], 0x3);
           else ptx::mma_commit(&ctl.empty[stage]);
@@ -447,21 +488,34 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c, u);
           ptx::tmem_ld_wait();
           const int n0 = nb * (MMA_N / 2) + c;
+          const float sa = F8 ? P.a_scale[p] : 1.0f;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int n = n0 + v * 8;
             const bool in = n < N;
-            float bg[8], bu[8];
+            float bg[8], bu[8], sg[8], su[8];
             load_bias8(P.bias, bias_row + n, in, bg);
             load_bias8(P.bias, bias_row + N + n, in, bu);
+            if constexpr (F8) {
+              load_wscale8(P, e, n, in, sg);
+              load_wscale8(P, e, N + n, in, su);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                sg[i] *= sa;
+                su[i] *= sa;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) sg[i] = su[i] = 1.f;
+            }
             uint4 pk;
             uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float g0 = __uint_as_float(g[v * 8 + 2 * i]) + bg[2 * i];
-              const float g1 = __uint_as_float(g[v * 8 + 2 * i + 1]) + bg[2 * i + 1];
-              const float u0 = __uint_as_float(u[v * 8 + 2 * i]) + bu[2 * i];
-              const float u1 = __uint_as_float(u[v * 8 + 2 * i + 1]) + bu[2 * i + 1];
+              const float g0 = __uint_as_float(g[v * 8 + 2 * i]) * sg[2 * i] + bg[2 * i];
+              const float g1 = __uint_as_float(g[v * 8 + 2 * i + 1]) * sg[2 * i + 1] + bg[2 * i + 1];
+              const float u0 = __uint_as_float(u[v * 8 + 2 * i]) * su[2 * i] + bu[2 * i];
+              const float u1 = __uint_as_float(u[v * 8 + 2 * i + 1]) * su[2 * i + 1] + bu[2 * i + 1];
               w[i] = pack_bf16x2(silu_f(g0) * u0 * zw, silu_f(g1) * u1 * zw);
             }
             if (in && real) *reinterpret_cast<uint4*>(z + p * N + n) = pk;
@@ -486,10 +540,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           float o[32];
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            float b[8];
+            float b[8], sc[8];
             load_bias8(P.bias, bias_row + n0 + v * 8, n0 + v * 8 < N, b);
+            if constexpr (F8) {
+              load_wscale8(P, e, n0 + v * 8, n0 + v * 8 < N, sc);
+              const float sa = P.a_scale[p];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[v * 8 + i] = (__uint_as_float(a[v * 8 + i]) + b[i]) * wgt;
+              for (int i = 0; i < 8; ++i) sc[i] *= sa;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) sc[i] = 1.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[v * 8 + i] = (__uint_as_float(a[v * 8 + i]) * sc[i] + b[i]) * wgt;
           }
           if constexpr (EPI == Epi::SortedF32) {
             // Stage the warp's 32x32 fp32 block in the 128-byte-swizzled layout
@@ -578,20 +642,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   }
 }
 
-template <Epi EPI>
+template <Epi EPI, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const KParams P) {
-  gemm_body<EPI, 1>(&tmA, &tmB, &tmO, P);
+  gemm_body<EPI, 1, F8>(&tmA, &tmB, &tmO, P);
 }
 
-template <Epi EPI>
+template <Epi EPI, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmO, const KParams P) {
-  gemm_body<EPI, 2>(&tmA, &tmB, &tmO, P);
+  gemm_body<EPI, 2, F8>(&tmA, &tmB, &tmO, P);
 }
 
 // ------------------------------------------------------------------ host --
@@ -648,15 +712,21 @@ bool use_pairs(const GroupedGemmArgs& a) {
   return a.rows_hint >= static_cast<int64_t>(4 * BM) * a.E && a.num_sms >= 2;
 }
 
-template <Epi EPI>
+template <Epi EPI, bool F8 = false>
 moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
+  using G1 = Geo<1, F8>;
+  using G2 = Geo<2, F8>;
+  const CUtensorMapDataType dt =
+      F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t eb = F8 ? 1 : 2;  // bytes per operand element
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Geo<1>::SMEM)) != cudaSuccess ||
-        cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>,
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<EPI, F8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Geo<2>::SMEM)) != cudaSuccess)
+                             static_cast<int>(G1::SMEM)) != cudaSuccess ||
+        cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI, F8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(G2::SMEM)) != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
                        cudaGetErrorString(cudaGetLastError()));
     attr_done = true;
@@ -664,29 +734,29 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   CUtensorMap tmA, tmB;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.cap)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
-    const uint32_t box[2] = {BK, BM};
-    if (moe_status_t st = make_map(&tmA, a.a, 2, dims, strides, box)) return st;
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * eb};
+    const uint32_t box[2] = {G1::BKE, BM};
+    if (moe_status_t st = make_map(&tmA, a.a, 2, dims, strides, box, dt)) return st;
   }
   int NB;
   if constexpr (EPI == Epi::SwiGLU) {
     // w13 [E, K, 2, N] viewed 4-D: (n, half, k, e)
     const uint64_t dims[4] = {static_cast<uint64_t>(a.N), 2, static_cast<uint64_t>(a.K),
                               static_cast<uint64_t>(a.E)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(a.N) * 2,
-                                 static_cast<uint64_t>(a.N) * 4,
-                                 static_cast<uint64_t>(a.N) * 4 * a.K};
-    const uint32_t box[4] = {64, 1, BK, 1};
-    if (moe_status_t st = make_map(&tmB, a.w, 4, dims, strides, box)) return st;
+    const uint64_t strides[3] = {static_cast<uint64_t>(a.N) * eb,
+                                 static_cast<uint64_t>(a.N) * 2 * eb,
+                                 static_cast<uint64_t>(a.N) * 2 * eb * a.K};
+    const uint32_t box[4] = {G1::CW, 1, G1::BKE, 1};
+    if (moe_status_t st = make_map(&tmB, a.w, 4, dims, strides, box, dt)) return st;
     NB = ceil_div(a.N, MMA_N / 2);
   } else {
     // w2 [E, K, N] viewed 3-D: (n, k, e)
     const uint64_t dims[3] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
                               static_cast<uint64_t>(a.E)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(a.N) * 2,
-                                 static_cast<uint64_t>(a.N) * 2 * a.K};
-    const uint32_t box[3] = {64, BK, 1};
-    if (moe_status_t st = make_map(&tmB, a.w, 3, dims, strides, box)) return st;
+    const uint64_t strides[2] = {static_cast<uint64_t>(a.N) * eb,
+                                 static_cast<uint64_t>(a.N) * eb * a.K};
+    const uint32_t box[3] = {G1::CW, G1::BKE, 1};
+    if (moe_status_t st = make_map(&tmB, a.w, 3, dims, strides, box, dt)) return st;
     NB = ceil_div(a.N, MMA_N);
   }
   CUtensorMap tmO;
@@ -716,6 +786,10 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   P.div = a.div > 0 ? a.div : 1;
   P.dense_rows = (EPI == Epi::DenseF32) ? static_cast<int32_t>(a.sentinel) : 0;
   P.gemm1_row_weight = a.gemm1_row_weight;
+  P.a_scale = a.a_scale;
+  P.w_scale = a.w_scale;
+  P.w_scale_per_channel = a.w_scale_per_channel;
+  P.w_scale_ld = (EPI == Epi::SwiGLU) ? 2 * a.N : a.N;
   // grouped operands are padded to whole 128-row blocks; the dense one is not
   const int64_t max_blocks = (EPI == Epi::DenseF32) ? ceil_div<int64_t>(a.cap, BM) : a.cap / BM;
   if (max_blocks <= 0) return MOE_OK;
@@ -727,9 +801,10 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * (a.num_sms / 2));
       cfg.blockDim = dim3(NTHREADS);
-      cfg.dynamicSmemBytes = Geo<2>::SMEM;
+      cfg.dynamicSmemBytes = G2::SMEM;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI>, &cfg) != cudaSuccess ||
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI, F8>, &cfg) !=
+              cudaSuccess ||
           n <= 0) {
         cudaGetLastError();
         n = a.num_sms / 2;
@@ -740,13 +815,13 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
     const unsigned clusters = static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
     prof_before(name, s);
-    grouped_gemm_pair_kernel<EPI><<<2 * clusters, NTHREADS, Geo<2>::SMEM, s>>>(tmA, tmB, tmO, P);
+    grouped_gemm_pair_kernel<EPI, F8><<<2 * clusters, NTHREADS, G2::SMEM, s>>>(tmA, tmB, tmO, P);
     prof_after(name, s);
     return check_launch(name);
   }
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
   prof_before(name, s);
-  grouped_gemm_kernel<EPI><<<grid, NTHREADS, Geo<1>::SMEM, s>>>(tmA, tmB, tmO, P);
+  grouped_gemm_kernel<EPI, F8><<<grid, NTHREADS, G1::SMEM, s>>>(tmA, tmB, tmO, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -768,6 +843,12 @@ moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s) {
 }
 moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::AtomicF32>(a, "gemm2_atomic", s);
+}
+moe_status_t launch_gemm1_swiglu_fp8(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::SwiGLU, true>(a, "gemm1_swiglu_fp8", s);
+}
+moe_status_t launch_gemm2_sorted_fp8(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::SortedF32, true>(a, "gemm2_sorted_fp8", s);
 }
 moe_status_t launch_dense_f32(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::DenseF32>(a, "router_logits", s);

@@ -202,6 +202,23 @@ def make_moe_inputs(spec: MoESpec, device="cpu", seed: int = 0, weights: bool = 
     return d
 
 
+def make_fp8_weights(spec: MoESpec, device="cpu", seed: int = 0, per_channel: bool = True):
+    """FP8 (E4M3) expert weights for the W8A8 layer: codes drawn as N(0, 1)
+    values cast to float8_e4m3fn, and scales ~ U(0.015, 0.025) per output
+    channel ([E, 2I] and [E, H]) or per expert ([E]) -- effective weights of
+    standard deviation ~0.02, like the bf16 workloads."""
+    device = torch.device(device)
+    E, H, I = spec.E, spec.H, spec.I
+    g = _gen(seed + 13, device)
+    w13 = _normal((E, H, 2 * I), 1.0, g, device, torch.float8_e4m3fn)
+    w2 = _normal((E, I, H), 1.0, g, device, torch.float8_e4m3fn)
+    gs = _gen(seed + 14, device)
+    shape13, shape2 = ((E, 2 * I), (E, H)) if per_channel else ((E,), (E,))
+    s13 = torch.rand(shape13, generator=gs, device=device) * 0.01 + 0.015
+    s2 = torch.rand(shape2, generator=gs, device=device) * 0.01 + 0.015
+    return {"w13_q": w13, "w2_q": w2, "w13_scale": s13, "w2_scale": s2}
+
+
 def make_batched_inputs(spec: BatchedSpec, device="cpu", seed: int = 0):
     """Returns a dict: x [E,T,H] bf16 (rows >= count are NaN), expert_num_tokens
     [E] int32 ~ U{0..T}, w13, w2, biases, row_weight [E,T] fp32 (one component
@@ -250,5 +267,5 @@ def ceil_div(a: int, b: int) -> int:
 
 
 __all__ = ["MoESpec", "BatchedSpec", "SPECS", "BATCHED_SPECS", "SMALL_SPECS", "PROFILE_SPECS",
-           "SMALL_BATCHED_SPECS", "make_moe_inputs", "make_batched_inputs",
+           "SMALL_BATCHED_SPECS", "make_moe_inputs", "make_batched_inputs", "make_fp8_weights",
            "logit_bias", "to_f64", "ceil_div"]

@@ -67,7 +67,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "e4m3_round", "quantize_rows_e4m3", "forward_fp8",
+    "e4m3_round", "quantize_rows_e4m3", "bf16_round", "forward_fp8",
     "router_logits", "scores", "group_mask", "topk_select", "route_weights", "route",
     "route_with_groups", "align", "silu", "expert_ffn", "forward",
     "token_output", "forward_batched", "moe_layer",
@@ -365,6 +365,13 @@ def quantize_rows_e4m3(x):
     return q, scale.astype(np.float64)
 
 
+def bf16_round(v):
+    """Round to bfloat16 (nearest, ties to even) via float32, as fp64."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32))
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
 def forward_fp8(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2_scale,
                 w13_bias=None, w2_bias=None):
     """The FP8 W8A8 layer.  Weights are FP8 values w_q with scales per expert
@@ -372,7 +379,11 @@ def forward_fp8(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2_scale,
     quantised per row before GEMM1 (x) and before GEMM2 (z):
         h = (q_x W13q) * s_x * s_w13 + b13,  z = SiLU(h_gate) * h_up,
         o = (q_z W2q) * s_z * s_w2 + b2,     y_t = sum_j a(t, j) o.
-    Dot products of the FP8 values are exact in fp64."""
+    The second quantisation reads z as held between the GEMMs, in the
+    compute dtype (bf16): on the FlagDoc page the activation output
+    (intermediate_cache2) is stored in compute_type and that is what
+    moe_kernel_quantize_input quantises for the w2 GEMM.  Dot products of the
+    FP8 values are exact in fp64."""
     x = np.asarray(x, dtype=np.float64)
     a = np.asarray(topk_weights, dtype=np.float64)
     ids = np.asarray(topk_ids)
@@ -391,7 +402,7 @@ def forward_fp8(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2_scale,
         if w13_bias is not None:
             h = h + w13_bias[e]
         z = silu(h[:, :I]) * h[:, I:]
-        qz, sz = quantize_rows_e4m3(z)
+        qz, sz = quantize_rows_e4m3(bf16_round(z))
         o = (qz @ np.asarray(w2_q[e], dtype=np.float64)) * sz[:, None] * s2
         if w2_bias is not None:
             o = o + w2_bias[e]

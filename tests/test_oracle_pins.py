@@ -585,7 +585,8 @@ def test_fp8_forward_reduces_to_exact_layer_on_representable_inputs():
         e = ids[t, 0]
         h = x[t] @ (w13q[e] * s13[e])
         z = oracle.silu(h[:I]) * h[I:]
-        qz, sz = oracle.quantize_rows_e4m3(z[None, :])
+        zb = torch.tensor(z, dtype=torch.float32).bfloat16().double().numpy()   # z held in bf16
+        qz, sz = oracle.quantize_rows_e4m3(zb[None, :])
         y[t] = a[t, 0] * ((qz[0] * sz[0]) @ (w2q[e] * s2[e]))
     # equal up to the fp32 rounding of the activation scale 8/448 (2^-24 relative)
     np.testing.assert_allclose(y8, y, rtol=1e-6, atol=1e-12)
