@@ -470,6 +470,37 @@ def measure_next_rows(step, spec, K, W, world, pk):
     fl = 6.0 * local_items * spec.H * spec.I
     out["expert_parallel_half"] = {"ms_per_step": round(ms, 4), "local_items": local_items,
                                    "tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+    del lw13, lw2
+
+    # FP8 W8A8: E4M3 weights with per-output-channel scales, activations
+    # quantised per row on the GPU; the fp8 tensor peak is the measured
+    # sustained bf16 peak x 2 (nominal dense fp8 : bf16 = 4.5 : 2.25)
+    q = wl.make_fp8_weights(spec, device=dev, per_channel=True)
+    ws8 = pkg.alloc_workspace(pkg.workspace_size_fp8(spec.M, spec.H, spec.I, spec.E,
+                                                     spec.top_k), dev)
+
+    def fp8():
+        pkg.moe_forward_fp8(d["hidden"], step.w, step.ids, q["w13_q"], q["w2_q"],
+                            q["w13_scale"], q["w2_scale"], None, None, ws8, step.out)
+
+    ms = max_over_ranks(time_steps(fp8, K, W, world) / K, world)
+    pkg.profiler_start()
+    for _ in range(K):
+        fp8()
+    prof = pkg.profiler_stop()
+    us = {k: 1e3 * v[1] / max(v[0], 1) for k, v in prof.items()}
+    f1 = 4.0 * spec.R * spec.H * spec.I
+    peak8 = 2.0 * pk["bf16_tflops_sustained"]
+    ach = f1 / (us["gemm1_swiglu_fp8"] * 1e-6) / 1e12
+    out["fp8_w8a8"] = {"ms_per_step": round(ms, 4),
+                       "tokens_per_s": round(spec.M * world / (ms / 1e3), 1),
+                       "tflops": round(spec.flops() / (ms / 1e3) / 1e12, 1),
+                       "kernels_us": {k: round(v, 2) for k, v in us.items()},
+                       "roofline": {"kernel": "gemm1_swiglu_fp8", "bound": "tensor",
+                                    "achieved": round(ach, 1), "peak": round(peak8, 1),
+                                    "unit": "TFLOP/s", "frac": round(ach / peak8, 4),
+                                    "peak_source": "measured sustained bf16 x 2 (nominal ratio)"}}
+    del q, ws8
     return out
 
 

@@ -259,9 +259,10 @@ GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_we
  * activation scale and the weight scale):
  *   h = (q(x) W13q) s_x s_w13 + b13,  z = SiLU(h_gate) h_up,
  *   o = (q(z) W2q) s_z s_w2 + b2,     y_t = sum_j a(t, j) o.
- * Activations (each routed row of x, and of z) are quantised dynamically
- * per row: scale = max|row| / 448, q = e4m3(row / scale), round to nearest
- * even, saturating.  Weight scales are per expert ([E]) or per output
+ * Activations (each routed row of x, and of z as held in bf16) are
+ * quantised dynamically per row: scale = fp32(max|row| / 448) (1 for an
+ * all-zero row), q = e4m3(fp32(row / scale)), round to nearest even,
+ * saturating; the quotient is the correctly rounded fp32 one.  Weight scales are per expert ([E]) or per output
  * channel ([E, 2I] and [E, H]).  Block-wise (128 x 128) weight scales are
  * not offered.
  *  w13, w2       device E4M3 bytes [E, H, 2I] and [E, I, H]
@@ -284,6 +285,19 @@ GBMOE_API moe_status_t moe_forward_fp8(const void* hidden, const float* topk_wei
                                        const void* w13_bias, const void* w2_bias,
                                        void* workspace, size_t workspace_bytes, void* out,
                                        moe_stream_t stream);
+
+/* moe_quant_rows_fp8: the per-row activation quantisation of the FP8 layer
+ * on its own ("fused_moe.py 分析", the quantisation of each GEMM's input):
+ * scale[m] = fp32(max_h |x[m, h]| / 448), 1 for an all-zero row;
+ * q8[m, h] = e4m3(fp32(x[m, h] / scale[m])) with round to nearest even and
+ * saturation to +-448.
+ *  x       device bf16 [M, H], row-major
+ *  q8      device E4M3 bytes [M, H] (caller-owned, written)
+ *  scale   device fp32 [M] (caller-owned, written)
+ * Limits: H % 16 == 0; x and q8 16-byte aligned.  M == 0 is a no-op.
+ */
+GBMOE_API moe_status_t moe_quant_rows_fp8(const void* x, int64_t M, int32_t H, void* q8,
+                                          float* scale, moe_stream_t stream);
 
 /* ------------------------------------------------------ forward_batched --
  * moe_forward_batched: the Batched activation format.  Defines: "vLLM

@@ -214,6 +214,20 @@ def moe_forward_fp8(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: 
     return out
 
 
+def moe_quant_rows_fp8(x: torch.Tensor, q8: Optional[torch.Tensor] = None,
+                       scale: Optional[torch.Tensor] = None, stream=None):
+    """Per-row E4M3 quantisation of x [M, H] bf16 -> (codes [M, H]
+    torch.float8_e4m3fn, scale [M] fp32): x ~ codes * scale[:, None]."""
+    M, H = x.shape
+    if q8 is None:
+        q8 = torch.empty(M, H, dtype=torch.float8_e4m3fn, device=x.device)
+    if scale is None:
+        scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib().moe_quant_rows_fp8(_ptr(x), M, H, _ptr(q8), _ptr(scale), _stream(stream)),
+           "moe_quant_rows_fp8")
+    return q8, scale
+
+
 def moe_forward_batched(x: torch.Tensor, expert_num_tokens: torch.Tensor, w13: torch.Tensor,
                         w2: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
                         w2_bias: Optional[torch.Tensor] = None,
@@ -309,7 +323,8 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
-           "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "fused_moe",
+           "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
+           "fused_moe",
            "workspace_size", "batched_workspace_size", "alloc_workspace", "align_capacity",
            "workspace_error_word", "read_error", "launch_count", "workspace_layout",
            "selftest_wait_timeout", "set_gemm_tiles", "profiler_start",

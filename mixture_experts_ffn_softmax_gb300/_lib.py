@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_workspace_size_fp8": (c_i32, [c_i64, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]),
     "moe_forward_fp8": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32,
                                 ctypes.POINTER(Fp8Weights), c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_quant_rows_fp8": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
     "moe_align_capacity": (c_sz, [c_i64, c_i32, c_i32, c_i32]),
     "moe_align_scratch_size": (c_sz, [c_i64, c_i32, c_i32]),
     "moe_align": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,

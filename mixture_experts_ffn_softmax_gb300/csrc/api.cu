@@ -623,12 +623,13 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
                  at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.block_expert),
                  at<int32_t>(workspace, L.scratch), cap, err, inv};
     if (moe_status_t st = launch_align(al, s)) return st;
-    // permute + quantise the token rows (E4M3, one scale per routed row)
+    // quantise each token row once (E4M3, one scale per row) into its k
+    // sorted rows; zero those rows' z amax for GEMM1's epilogue
     uint8_t* a8 = at<uint8_t>(workspace, L.a8);
     float* a_scale = at<float>(workspace, L.a_scale);
-    QuantRowsArgs qa{x + c0 * H, sorted, offsets, E, top_k, static_cast<int32_t>(Rc), H, cap, a8,
-                     a_scale};
-    if (moe_status_t st = launch_quant_rows_fp8(qa, s)) return st;
+    float* z_scale = at<float>(workspace, L.z_scale);
+    QuantTokensArgs qa{x + c0 * H, inv, Mc, top_k, H, a8, a_scale, z_scale};
+    if (moe_status_t st = launch_quant_tokens_fp8(qa, s)) return st;
     bf16* z = at<bf16>(workspace, L.z);
     GroupedGemmArgs g1{};
     g1.a = reinterpret_cast<const bf16*>(a8);
@@ -648,12 +649,12 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     g1.a_scale = a_scale;
     g1.w_scale = w->w13_scale;
     g1.w_scale_per_channel = w->scale_per_channel;
+    g1.row_amax = z_scale;
     if (moe_status_t st = launch_gemm1_swiglu_fp8(g1, s)) return st;
-    // quantise z per row for the second GEMM
+    // quantise z per row for the second GEMM (amax taken by GEMM1)
     uint8_t* z8 = at<uint8_t>(workspace, L.z8);
-    float* z_scale = at<float>(workspace, L.z_scale);
-    QuantRowsArgs qz{z, sorted, offsets, E, 0, static_cast<int32_t>(Rc), I, cap, z8, z_scale};
-    if (moe_status_t st = launch_quant_rows_fp8(qz, s)) return st;
+    QuantSortedArgs qz{z, sorted, offsets, E, static_cast<int32_t>(Rc), I, cap, z8, z_scale};
+    if (moe_status_t st = launch_quant_sorted_fp8(qz, s)) return st;
     float* o = at<float>(workspace, L.o);
     GroupedGemmArgs g2{};
     g2.a = reinterpret_cast<const bf16*>(z8);
@@ -679,6 +680,22 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     if (moe_status_t st = launch_reduce_sorted(o, inv, Mc, top_k, H, y + c0 * H, s)) return st;
   }
   return MOE_OK;
+}
+
+moe_status_t moe_quant_rows_fp8(const void* x, int64_t M, int32_t H, void* q8, float* scale,
+                                moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M < 0");
+  if (H <= 0 || H % 16 != 0) return set_error(MOE_ERR_INVALID_ARG, "H=%d not a positive multiple of 16", H);
+  if (M == 0) return MOE_OK;
+  if (!x || !q8 || !scale) return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(q8) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "x and q8 must be 16-byte aligned");
+  int sms = 0;
+  if (moe_status_t st = check_device(&sms)) return st;
+  QuantTokensArgs qa{static_cast<const bf16*>(x), nullptr, M, 1, H, static_cast<uint8_t*>(q8),
+                     scale, nullptr};
+  return launch_quant_tokens_fp8(qa, stream);
 }
 
 // ------------------------------------------------------ forward_batched --

@@ -104,16 +104,32 @@ moe_status_t launch_gather(const GatherArgs& a, cudaStream_t s);
 // FP8 rows: for sorted position p < offsets[E] whose index[p] is a real
 // entry, row src[index[p] / div] (index == null: row p) is quantised with
 // its own scale = amax / 448: q8[p] = e4m3(row / scale), scale[p] = scale.
-struct QuantRowsArgs {
-  const bf16* src;
-  const int32_t* index;   // or null
-  const int32_t* offsets;
-  int32_t E, div, sentinel, H;
-  int64_t cap;
-  uint8_t* q8;
-  float* scale;
+// FP8 (E4M3) per-row quantisation of the token rows: each token's row is
+// read once, its scale and codes go to every sorted row inv[t*k + j] >= 0,
+// and row_amax[pos] (if given) is zeroed for the GEMM1 epilogue's max.
+struct QuantTokensArgs {
+  const bf16* x;          // [M, H]
+  const int32_t* inv;     // [M*k] sorted row of item (t, j), or -1
+  int64_t M;
+  int32_t k, H;
+  uint8_t* q8;            // [cap, H] codes
+  float* scale;           // [cap]
+  float* row_amax;        // [cap] or null
 };
-moe_status_t launch_quant_rows_fp8(const QuantRowsArgs& a, cudaStream_t s);
+moe_status_t launch_quant_tokens_fp8(const QuantTokensArgs& a, cudaStream_t s);
+// FP8 quantisation of the expert-sorted rows of z, whose per-row amax the
+// GEMM1 epilogue has already taken: scale_io[p] holds amax on entry and the
+// row's scale on exit; padding rows are skipped.
+struct QuantSortedArgs {
+  const bf16* src;        // [cap, H]
+  const int32_t* index;   // [cap] sorted item ids (padding >= sentinel)
+  const int32_t* offsets; // [E + 1]
+  int32_t E, sentinel, H;
+  int64_t cap;
+  uint8_t* q8;            // [cap, H]
+  float* scale_io;        // [cap]
+};
+moe_status_t launch_quant_sorted_fp8(const QuantSortedArgs& a, cudaStream_t s);
 
 // y[t, :] = bf16( sum_j o_sorted[inv[t*k + j], :] ), skipping inv < 0.
 moe_status_t launch_reduce_sorted(const float* o_sorted, const int32_t* inv, int64_t M,
@@ -145,6 +161,7 @@ struct GroupedGemmArgs {
   const float* a_scale = nullptr;
   const float* w_scale = nullptr;       // [E, 2N] / [E, N] per channel, or [E]
   int32_t w_scale_per_channel = 0;
+  float* row_amax = nullptr;            // GEMM1 FP8: max |bf16 z| of each sorted row (atomic)
 };
 moe_status_t launch_gemm1_swiglu_fp8(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_gemm2_sorted_fp8(const GroupedGemmArgs& a, cudaStream_t s);

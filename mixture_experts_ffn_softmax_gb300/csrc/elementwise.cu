@@ -271,71 +271,182 @@ namespace gbmoe {
 namespace {
 
 constexpr int kQuantWarps = 8;
+constexpr int kQuantUnroll = 4;  // 16-byte loads in flight per lane
 
-// Dynamic per-row FP8 (E4M3) quantisation, one warp per row: scale =
-// amax / 448 (1 for an all-zero row), q = e4m3(x / scale) with round to
-// nearest even and saturation ("fused_moe.py 分析": activations are
-// quantised before each GEMM).  The division is IEEE fp32.
+// x / s rounded to nearest even in fp32, for a divisor fixed along a row, by
+// Markstein's correction of the product with the reciprocal (P. Markstein,
+// "IA-64 and Elementary Functions", 2000; Handbook of Floating-Point
+// Arithmetic, division by FMA): with r = RN(1/s) and q = RN(x r) within an
+// ulp of x / s, the remainder x - q s is exact as one FMA and RN(q + rem r)
+// is the correctly rounded quotient (no overflow or underflow: the caller
+// takes the IEEE division for rows whose scale is not a normal float, and a
+// quotient below the normal range is far below E4M3's smallest code).
+__device__ __forceinline__ float div_fixed(float x, float s, float r) {
+  const float q = __fmul_rn(x, r);
+  const float rem = __fmaf_rn(-q, s, x);
+  return __fmaf_rn(rem, r, q);
+}
+
+// Row scale and its reciprocal; `fast` is false where the correction does
+// not apply (subnormal or non-finite scale) and the plain division is used.
+struct RowScale {
+  float s, r;
+  bool fast;
+};
+
+// Dynamic per-row quantisation: scale = amax / 448, or 1 for an all-zero row
+// ("fused_moe.py 分析": activations are quantised per token before each GEMM).
+__device__ __forceinline__ RowScale row_scale(float amax) {
+  RowScale rs;
+  rs.s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  rs.fast = rs.s >= 1.17549435e-38f && rs.s <= 3.0e38f;
+  rs.r = rs.fast ? __frcp_rn(rs.s) : 0.f;
+  return rs;
+}
+
+// E4M3 codes of 8 bf16 values: q = e4m3(x / scale), the quotient correctly
+// rounded in fp32, then round to nearest even with saturation to +-448.
+__device__ __forceinline__ uint2 e4m3x8(const uint4 u, const RowScale& rs) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  uint16_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    const float2 v = rs.fast ? make_float2(div_fixed(f.x, rs.s, rs.r), div_fixed(f.y, rs.s, rs.r))
+                             : make_float2(__fdiv_rn(f.x, rs.s), __fdiv_rn(f.y, rs.s));
+    b[i] = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+  }
+  return make_uint2(static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16),
+                    static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16));
+}
+
+// max |v| over 8 bf16 values, as bf16 magnitude bits in both halves
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4 u, uint32_t m) {
+  m = __vmaxu2(m, u.x & 0x7fff7fffu);
+  m = __vmaxu2(m, u.y & 0x7fff7fffu);
+  m = __vmaxu2(m, u.z & 0x7fff7fffu);
+  return __vmaxu2(m, u.w & 0x7fff7fffu);
+}
+
+// Token rows, one warp per token: amax over the row, then the codes are
+// written to each of the token's sorted rows (the gather of the permuted
+// operand and its quantisation in one pass over x).
 __global__ void __launch_bounds__(kQuantWarps * 32)
-    quant_rows_fp8_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ index,
-                          const int32_t* __restrict__ offsets, int E, int div, int32_t sentinel,
-                          int H, int64_t cap, uint8_t* __restrict__ q8,
-                          float* __restrict__ scale) {
+    quant_tokens_fp8_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ inv,
+                            int64_t M, int k, int H, uint8_t* __restrict__ q8,
+                            float* __restrict__ scale, float* __restrict__ row_amax) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = H / 8;
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
+  for (int64_t t = warp0; t < M; t += nwarps) {
+    const uint4* sv = reinterpret_cast<const uint4*>(x + t * H);
+    // loops run the same trip count on every lane (warp-uniform shuffles)
+    uint32_t m2 = 0;
+    for (int b = 0; b < nvec; b += 32 * kQuantUnroll) {
+      uint4 u[kQuantUnroll];
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int v = b + 32 * i + lane;
+        u[i] = v < nvec ? __ldg(sv + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) m2 = absmax_bits8(u[i], m2);
+    }
+    uint32_t mb = max(m2 & 0xffffu, m2 >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const RowScale rs = row_scale(__uint_as_float(mb << 16));
+    // sorted rows of the token's k items (lane j holds item j's, j < 32);
+    // without inv the rows are not permuted (k = 1, row t)
+    const int32_t mypos =
+        lane < k ? (inv != nullptr ? __ldg(inv + t * k + lane) : static_cast<int32_t>(t)) : -1;
+    for (int b = 0; b < nvec; b += 32 * kQuantUnroll) {
+      uint2 c[kQuantUnroll];
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int v = b + 32 * i + lane;
+        c[i] = e4m3x8(v < nvec ? __ldg(sv + v) : make_uint4(0, 0, 0, 0), rs);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int32_t pos = j < 32 ? __shfl_sync(0xffffffffu, mypos, j) : __ldg(inv + t * k + j);
+        if (pos < 0) continue;
+        uint2* dq = reinterpret_cast<uint2*>(q8 + static_cast<int64_t>(pos) * H);
+#pragma unroll
+        for (int i = 0; i < kQuantUnroll; ++i) {
+          const int v = b + 32 * i + lane;
+          if (v < nvec) dq[v] = c[i];
+        }
+      }
+    }
+    for (int j = lane; j < k; j += 32) {
+      const int32_t pos = inv != nullptr ? inv[t * k + j] : static_cast<int32_t>(t);
+      if (pos < 0) continue;
+      scale[pos] = rs.s;
+      if (row_amax != nullptr) row_amax[pos] = 0.f;
+    }
+  }
+}
+
+// Sorted rows of z, one warp per row, one pass: the row's amax was taken by
+// the producing GEMM's epilogue.
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quant_sorted_fp8_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ index,
+                            const int32_t* __restrict__ offsets, int E, int32_t sentinel, int H,
+                            int64_t cap, uint8_t* __restrict__ q8, float* __restrict__ scale_io) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = min(static_cast<int64_t>(offsets[E]), cap);
   const int nvec = H / 8;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
   for (int64_t p = warp0; p < rows; p += nwarps) {
-    int64_t srow = p;
-    if (index != nullptr) {
-      const int32_t idx = index[p];
-      if (idx < 0 || idx >= sentinel) continue;  // padding row
-      if (div > 0) srow = idx / div;
-    }
-    const uint4* sv = reinterpret_cast<const uint4*>(src + srow * H);
+    const int32_t idx = index[p];
+    if (idx < 0 || idx >= sentinel) continue;  // padding row
     float amax = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = __ldg(sv + v);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (lane == 0) amax = scale_io[p];
+    const RowScale rs = row_scale(__shfl_sync(0xffffffffu, amax, 0));
+    const uint4* sv = reinterpret_cast<const uint4*>(src + p * H);
     uint2* dq = reinterpret_cast<uint2*>(q8 + p * H);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = __ldg(sv + v);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-      uint16_t b[4];
+    for (int b = 0; b < nvec; b += 32 * kQuantUnroll) {
+      uint4 u[kQuantUnroll];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        b[i] = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc)),
-                                        __NV_SATFINITE, __NV_E4M3);
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int v = b + 32 * i + lane;
+        u[i] = v < nvec ? __ldcs(sv + v) : make_uint4(0, 0, 0, 0);
       }
-      dq[v] = make_uint2(static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16),
-                         static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16));
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int v = b + 32 * i + lane;
+        if (v < nvec) dq[v] = e4m3x8(u[i], rs);
+      }
     }
-    if (lane == 0) scale[p] = sc;
+    if (lane == 0) scale_io[p] = rs.s;
   }
 }
 
 }  // namespace
 
-moe_status_t launch_quant_rows_fp8(const QuantRowsArgs& a, cudaStream_t s) {
+moe_status_t launch_quant_tokens_fp8(const QuantTokensArgs& a, cudaStream_t s) {
+  if (a.M <= 0) return MOE_OK;
+  const int64_t want = ceil_div<int64_t>(a.M, kQuantWarps);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
+  prof_before("quant_tokens_fp8", s);
+  quant_tokens_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(a.x, a.inv, a.M, a.k, a.H, a.q8,
+                                                            a.scale, a.row_amax);
+  prof_after("quant_tokens_fp8", s);
+  return check_launch("quant_tokens_fp8");
+}
+
+moe_status_t launch_quant_sorted_fp8(const QuantSortedArgs& a, cudaStream_t s) {
   if (a.cap <= 0) return MOE_OK;
   const int64_t want = ceil_div<int64_t>(a.cap, kQuantWarps);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
-  prof_before("quant_rows_fp8", s);
-  quant_rows_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(a.src, a.index, a.offsets, a.E, a.div,
-                                                          a.sentinel, a.H, a.cap, a.q8, a.scale);
-  prof_after("quant_rows_fp8", s);
-  return check_launch("quant_rows_fp8");
+  prof_before("quant_z_fp8", s);
+  quant_sorted_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(a.src, a.index, a.offsets, a.E,
+                                                            a.sentinel, a.H, a.cap, a.q8,
+                                                            a.scale_io);
+  prof_after("quant_z_fp8", s);
+  return check_launch("quant_z_fp8");
 }
 
 }  // namespace gbmoe

@@ -115,6 +115,7 @@ struct KParams {
   const float* a_scale;
   const float* w_scale;
   int32_t w_scale_per_channel, w_scale_ld;
+  float* row_amax;  // SwiGLU FP8: atomic max of |bf16 z| per sorted row, or null
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
@@ -248,6 +249,49 @@ __device__ __forceinline__ void load_bias8(const bf16* bias, int64_t off, bool o
   }
 }
 
+// Per-tile values of the SwiGLU epilogue that do not depend on the
+// accumulator, loaded before its wait.  Lane = accumulator row; the warp's
+// 64 columns n_base + 32 c + lane (c = 0, 1) are spread over the lanes, one
+// per lane and array, and broadcast with shuffles when used.
+struct SwiRow {
+  float sa, zw;          // row: activation scale (FP8), weight multiplied into z
+  bool real;             // row holds a routed item (padding rows are not stored)
+  float sg[2], su[2];    // weight scales of gate / up columns (FP8)
+  float bg[2], bu[2];    // biases of gate / up columns
+};
+
+template <bool F8>
+__device__ __forceinline__ void swiglu_prefetch(const KParams& P, int e, int n_base, int64_t p,
+                                                int lane, SwiRow& r) {
+  const int N = P.N;
+  const int32_t entry = P.row_index[p];
+  r.real = entry >= 0 && entry < P.sentinel;
+  r.zw = (r.real && P.gemm1_row_weight != nullptr) ? P.gemm1_row_weight[entry] : 1.0f;
+  r.sa = F8 ? P.a_scale[p] : 1.0f;
+  const int64_t brow = static_cast<int64_t>(e) * 2 * N;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int n = n_base + 32 * c + lane;
+    const bool in = n < N;
+    if constexpr (F8) {
+      if (P.w_scale == nullptr) {
+        r.sg[c] = r.su[c] = 1.f;
+      } else if (P.w_scale_per_channel) {
+        const float* ws = P.w_scale + static_cast<int64_t>(e) * P.w_scale_ld;
+        r.sg[c] = in ? __ldg(ws + n) : 0.f;
+        r.su[c] = in ? __ldg(ws + N + n) : 0.f;
+      } else {
+        r.sg[c] = r.su[c] = __ldg(P.w_scale + e);
+      }
+    } else {
+      r.sg[c] = r.su[c] = 1.f;
+    }
+    const bool b = P.bias != nullptr && in;
+    r.bg[c] = b ? __bfloat162float(P.bias[brow + n]) : 0.f;
+    r.bu[c] = b ? __bfloat162float(P.bias[brow + N + n]) : 0.f;
+  }
+}
+
 template <Epi EPI, int CG, bool F8>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                           const CUtensorMap* tmO, const KParams& P) {
@@ -302,7 +346,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(tmA);
     ptx::prefetch_tmap(tmB);
-    if constexpr (EPI == Epi::SortedF32) ptx::prefetch_tmap(tmO);
+    if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SwiGLU) ptx::prefetch_tmap(tmO);
   }
   if (warp == 1) {
     if constexpr (CG == 2) {
@@ -460,66 +504,111 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // hand the accumulator back to the MMA warp (the even CTA's MMA waits
+    // for the epilogue warps of both CTAs)
+    auto release_acc = [&](int a) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2)
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ctl.tmem_empty[a]), 0));
+        else
+          ptx::mbar_arrive(&ctl.tmem_empty[a]);
+      }
+    };
     for (int t = unit; t < total_tiles; t += units) {
       int e, row0, nb;
       bool mine;
       tile_of(t, e, row0, nb, mine);
+      const int64_t p = row0 + row;
+      SwiRow sr;
+      const int n_base = nb * (MMA_N / 2) + half * (MMA_N / 4);  // SwiGLU: first z column
+      if constexpr (EPI == Epi::SwiGLU) {
+        if (mine) swiglu_prefetch<F8>(P, e, n_base, p, lane, sr);
+      }
       const bool got = bounded_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, P.error_word);
       if (!__all_sync(0xffffffffu, got)) break;
       ptx::tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * MMA_N);
-      const int64_t p = row0 + row;
+      bool released = false;
 
       if (!mine) {
         // this CTA's half of a pair tile has no rows of the expert
       } else if constexpr (EPI == Epi::SwiGLU) {
         bf16* z = reinterpret_cast<bf16*>(P.out);
         const int N = P.N;
-        const int32_t entry = P.row_index[p];
-        const bool real = entry >= 0 && entry < P.sentinel;  // padding rows are not stored
-        // router weight applied to the second layer's input, if asked for
-        const float zw = (real && P.gemm1_row_weight != nullptr) ? P.gemm1_row_weight[entry] : 1.0f;
-        const int64_t bias_row = static_cast<int64_t>(e) * 2 * N;
-#pragma unroll 1
-        for (int c = half * (MMA_N / 4); c < (half + 1) * (MMA_N / 4); c += 32) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32cols(taddr + c, g);
-          ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c, u);
-          ptx::tmem_ld_wait();
-          const int n0 = nb * (MMA_N / 2) + c;
-          const float sa = F8 ? P.a_scale[p] : 1.0f;
+        // all of this warp's accumulator columns at once: gate [c0, c0+64)
+        // and up [c0+128, c0+192), then the accumulator is free again
+        const int c0 = half * (MMA_N / 4);
+        uint32_t g[2][32], u[2][32];
+        ptx::tmem_ld_32cols(taddr + c0, g[0]);
+        ptx::tmem_ld_32cols(taddr + c0 + 32, g[1]);
+        ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c0, u[0]);
+        ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c0 + 32, u[1]);
+        ptx::tmem_ld_wait();
+        release_acc(acc);
+        released = true;
+        uint32_t zmax2 = 0;  // max |z| as bf16 magnitude bits, both halves
+        // z is staged as the warp's 32 rows x 64 columns (one 128-byte row
+        // each, 16-byte chunk j at j ^ (row & 7)) and written with one TMA
+        // store; a warp whose rows are all padding, or whose columns all lie
+        // past N, stores nothing (no store starts outside the tensor)
+        uint8_t* stage_buf = staging + (warp - 2) * STAGING_BYTES;
+        const bool any_real = __ballot_sync(0xffffffffu, sr.real) != 0u;
+        if (any_real && n_base < N) {
+          if (lane == 0) ptx::bulk_wait_read0();  // the buffer's previous store has read it
+          __syncwarp();
+          const bool has_bias = P.bias != nullptr;
+          auto col = [&](float v, int j) { return __shfl_sync(0xffffffffu, v, j); };
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int n = n0 + v * 8;
-            const bool in = n < N;
-            float bg[8], bu[8], sg[8], su[8];
-            load_bias8(P.bias, bias_row + n, in, bg);
-            load_bias8(P.bias, bias_row + N + n, in, bu);
-            if constexpr (F8) {
-              load_wscale8(P, e, n, in, sg);
-              load_wscale8(P, e, N + n, in, su);
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                sg[i] *= sa;
-                su[i] *= sa;
+            for (int v = 0; v < 4; ++v) {
+              uint4 pk;
+              uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                float zz[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int j = v * 8 + 2 * i + h;  // column within the 32-column chunk
+                  float gv = __uint_as_float(g[c][j]), uv = __uint_as_float(u[c][j]);
+                  if constexpr (F8) {
+                    gv *= col(sr.sg[c], j) * sr.sa;
+                    uv *= col(sr.su[c], j) * sr.sa;
+                  }
+                  if (has_bias) {
+                    gv += col(sr.bg[c], j);
+                    uv += col(sr.bu[c], j);
+                  }
+                  zz[h] = silu_f(gv) * uv * sr.zw;
+                }
+                w[i] = pack_bf16x2(zz[0], zz[1]);
               }
-            } else {
+              const int chunk = c * 4 + v;
+              *reinterpret_cast<uint4*>(stage_buf + lane * 128 + ((chunk ^ (lane & 7)) << 4)) = pk;
+              if constexpr (F8) {
+                if (sr.real && n_base + 32 * c + v * 8 < N) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) sg[i] = su[i] = 1.f;
+                  for (int i = 0; i < 4; ++i) zmax2 = __vmaxu2(zmax2, w[i] & 0x7fff7fffu);
+                }
+              }
             }
-            uint4 pk;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float g0 = __uint_as_float(g[v * 8 + 2 * i]) * sg[2 * i] + bg[2 * i];
-              const float g1 = __uint_as_float(g[v * 8 + 2 * i + 1]) * sg[2 * i + 1] + bg[2 * i + 1];
-              const float u0 = __uint_as_float(u[v * 8 + 2 * i]) * su[2 * i] + bu[2 * i];
-              const float u1 = __uint_as_float(u[v * 8 + 2 * i + 1]) * su[2 * i + 1] + bu[2 * i + 1];
-              w[i] = pack_bf16x2(silu_f(g0) * u0 * zw, silu_f(g1) * u1 * zw);
-            }
-            if (in && real) *reinterpret_cast<uint4*>(z + p * N + n) = pk;
           }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(tmO, stage_buf, n_base, row0 + q * 32);
+            ptx::bulk_commit();
+          }
+        }
+        if constexpr (F8) {
+          // the row's amax over this tile's columns, as the stored bf16 value
+          // (non-negative floats order like their bit patterns)
+          const uint32_t m = max(zmax2 & 0xffffu, zmax2 >> 16) << 16;
+          if (m != 0u && P.row_amax != nullptr)
+            atomicMax(reinterpret_cast<unsigned int*>(P.row_amax) + p, m);
         }
       } else {
         const int N = P.N;
@@ -607,15 +696,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           }
         }
       }
-      // release the accumulator (the even CTA's MMA waits for both CTAs)
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CG == 2)
-          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ctl.tmem_empty[acc]), 0));
-        else
-          ptx::mbar_arrive(&ctl.tmem_empty[acc]);
-      }
+      if (!released) release_acc(acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -623,7 +704,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     }
   }
 
-  if constexpr (EPI == Epi::SortedF32) {
+  if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SwiGLU) {
     if (warp >= 2 && lane == 0) ptx::bulk_wait0();  // TMA stores done before smem is released
   }
   __syncwarp();  // lane-0-only roles rejoin their warp before the aligned barriers
@@ -768,6 +849,15 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     if (moe_status_t st = make_map(&tmO, a.out, 2, dims, strides, box,
                                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return st;
+  } else if constexpr (EPI == Epi::SwiGLU) {
+    // z bf16 [cap, N]: one epilogue warp's 32 rows x 64 columns per store,
+    // 128-byte swizzle (matches staging)
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.cap)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
+    const uint32_t box[2] = {64, 32};
+    if (moe_status_t st = make_map(&tmO, a.out, 2, dims, strides, box,
+                                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      return st;
   } else {
     tmO = tmA;  // unused
   }
@@ -789,6 +879,7 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   P.a_scale = a.a_scale;
   P.w_scale = a.w_scale;
   P.w_scale_per_channel = a.w_scale_per_channel;
+  P.row_amax = a.row_amax;
   P.w_scale_ld = (EPI == Epi::SwiGLU) ? 2 * a.N : a.N;
   // grouped operands are padded to whole 128-row blocks; the dense one is not
   const int64_t max_blocks = (EPI == Epi::DenseF32) ? ceil_div<int64_t>(a.cap, BM) : a.cap / BM;

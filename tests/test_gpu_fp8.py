@@ -91,3 +91,59 @@ def test_fp8_validation():
         pkg.moe_forward_fp8(x, torch.ones(4, 1, device="cuda"),
                             torch.zeros(4, 1, dtype=torch.int32, device="cuda"), w13, w2, s, s)
     assert ei.value.status == 1
+
+
+def _quant_cases():
+    g = torch.Generator().manual_seed(5)
+    H = 272                                                   # 17 16-byte groups: ragged lanes
+    rows = [torch.randn(64, H, generator=g),                  # plain values
+            torch.randint(-9, 10, (64, H), generator=g).float(),   # tie-heavy small integers
+            torch.randint(-448, 449, (32, H), generator=g).float() / 7.0,
+            torch.randn(8, H, generator=g) * 1e30,
+            torch.randn(8, H, generator=g) * 1e-3,
+            torch.zeros(2, H)]                                # all-zero rows: scale 1
+    # rows whose quotients sit on E4M3 rounding midpoints: amax fixed at 448 * 2^j
+    mids = []
+    for j in (-3, 0, 5):
+        r = torch.zeros(H)
+        v = torch.tensor([1.0625, 2.125, 9.0, 17.0, 68.0, 104.0, 232.0, 440.0, 0.0009765625 * 3])
+        r[: v.numel()] = v * 2.0 ** j
+        r[-1] = 448.0 * 2.0 ** j
+        mids.append(r)
+    rows.append(torch.stack(mids))
+    tiny = torch.full((1, H), 1e-37)                          # scale below the normal range
+    tiny[0, ::3] = -3e-38
+    rows.append(tiny)
+    return torch.cat(rows).bfloat16()
+
+
+def test_quant_rows_codes_match_oracle_bit_exactly():
+    """The code of each element is an integer decided by floating point: both
+    sides decide it in fp32 (scale = amax / 448, quotient x / scale correctly
+    rounded), so codes and scales agree exactly."""
+    x = _quant_cases()
+    q8, s = pkg.moe_quant_rows_fp8(x.cuda())
+    torch.cuda.synchronize()
+    qo, so = oracle.quantize_rows_e4m3(x.float().numpy())
+    np.testing.assert_array_equal(s.cpu().numpy(), so.astype(np.float32))
+    got = q8.cpu().float().double().numpy()
+    bad = np.argwhere(got != qo)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:4].tolist()}"
+
+
+def test_quant_rows_full_size_sampled():
+    spec = wl.SPECS["mixtral_prefill"]
+    d = wl.make_moe_inputs(spec, device="cuda", weights=False)
+    q8, s = pkg.moe_quant_rows_fp8(d["hidden"])
+    torch.cuda.synchronize()
+    sel = np.random.default_rng(3).choice(spec.M, 64, replace=False)
+    qo, so = oracle.quantize_rows_e4m3(d["hidden"][sel].float().cpu().numpy())
+    np.testing.assert_array_equal(s.cpu().numpy()[sel], so.astype(np.float32))
+    np.testing.assert_array_equal(q8[sel].cpu().float().double().numpy(), qo)
+
+
+def test_quant_rows_validation_and_empty():
+    pkg.moe_quant_rows_fp8(torch.empty(0, 32, device="cuda").bfloat16())
+    with pytest.raises(pkg.MoEError) as ei:
+        pkg.moe_quant_rows_fp8(torch.zeros(4, 40, device="cuda").bfloat16())
+    assert ei.value.status == 1
