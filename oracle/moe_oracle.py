@@ -68,6 +68,8 @@ import numpy as np
 
 __all__ = [
     "e4m3_round", "quantize_rows_e4m3", "bf16_round", "forward_fp8",
+    "unpack_nibbles", "mx_decode", "ue8m0_scale", "dequant_int", "dequant_mx",
+    "forward_wq",
     "router_logits", "scores", "group_mask", "topk_select", "route_weights", "route",
     "route_with_groups", "align", "silu", "expert_ffn", "forward",
     "token_output", "forward_batched", "moe_layer",
@@ -409,3 +411,89 @@ def forward_fp8(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2_scale,
         np.add.at(y, t, a[t, j][:, None] * o)
     return y
 
+
+
+# --------------------------------------------------------------------------
+# Weight-only quantised experts.  FlagDoc fused_moe.py 分析, "WNA16 路径" and
+# "5. 特殊量化格式处理": int8 / int4 weights with a group scale and a zero
+# point, and OCP MX weights, are dequantised to the activation dtype
+# (hidden_states.dtype, bf16 here) and the layer then runs as the ordinary
+# one.  Layouts (the pages fix none; GPTQ/AWQ-style group quantisation
+# along K in the [E, K, N] orientation of the bf16 weights):
+#   int4 / fp4 codes  uint8 [E, K, N/2]: byte j of a row holds column 2j in
+#                     its low nibble and column 2j+1 in its high nibble
+#   int8 codes        int8 [E, K, N]
+#   int scales        [E, K/G, N] (group of G rows of K per scale), zero
+#                     points [E, K/G, N] in the code domain (int4: 0..15,
+#                     int8: -128..127) or absent (int4: 8, int8: 0)
+#   MX scales         uint8 UE8M0 [E, K/32, N]: 2^(s - 127), one per block
+#                     of 32 elements along K (OCP MX: block size 32)
+# --------------------------------------------------------------------------
+
+def unpack_nibbles(packed):
+    """uint8 [..., N/2] -> int64 [..., N]: column 2j = low nibble of byte j,
+    column 2j+1 = its high nibble."""
+    b = np.asarray(packed, dtype=np.uint8).astype(np.int64)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.int64)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out
+
+
+# OCP Microscaling formats (OCP MX v1.0): element formats with their bit
+# fields (sign, exponent bits, mantissa bits, exponent bias); no inf/NaN.
+MX_FORMATS = {"e2m1": (2, 1, 1), "e3m2": (3, 2, 3), "e2m3": (2, 3, 1)}
+
+
+def mx_decode(codes, fmt):
+    """Value of each MX element code: sign bit above an ebits exponent field
+    and an mbits mantissa field; exponent field 0 is subnormal
+    (m / 2^mbits * 2^(1 - bias)), otherwise 2^(e - bias) * (1 + m / 2^mbits)."""
+    ebits, mbits, bias = MX_FORMATS[fmt]
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where((c >> (ebits + mbits)) & 1, -1.0, 1.0)
+    e = (c >> mbits) & ((1 << ebits) - 1)
+    m = (c & ((1 << mbits) - 1)).astype(np.float64)
+    mag = np.where(e == 0, m / (1 << mbits) * 2.0 ** (1 - bias),
+                   2.0 ** (e.astype(np.float64) - bias) * (1.0 + m / (1 << mbits)))
+    return sign * mag
+
+
+def ue8m0_scale(s):
+    """UE8M0 block scale: 2^(s - 127) (s = 255, NaN, is not used)."""
+    return np.exp2(np.asarray(s, dtype=np.float64) - 127.0)
+
+
+def dequant_int(q, scale, zero=None, bits=4):
+    """Group dequantisation to the activation dtype:
+        w[e, k, n] = bf16((q[e, k, n] - zero[e, k // G, n]) * scale[e, k // G, n])
+    with G = K / scale.shape[1].  q: int4 codes packed as above (bits=4) or
+    int8 codes (bits=8); zero absent = 8 (int4) or 0 (int8)."""
+    codes = unpack_nibbles(q) if bits == 4 else np.asarray(q, dtype=np.int64)
+    E, K, N = codes.shape
+    sc = np.asarray(scale, dtype=np.float64)
+    G = K // sc.shape[1]
+    if zero is None:
+        zp = np.full(sc.shape, 8 if bits == 4 else 0, dtype=np.int64)
+    else:
+        zp = np.asarray(zero, dtype=np.int64)
+    kg = np.arange(K) // G
+    return bf16_round((codes - zp[:, kg, :]).astype(np.float64) * sc[:, kg, :])
+
+
+def dequant_mx(q, scale, fmt="e2m1"):
+    """MX dequantisation to the activation dtype:
+        w[e, k, n] = bf16(value(q[e, k, n]) * 2^(scale[e, k // 32, n] - 127)).
+    q: E2M1 codes packed two per byte (fmt "e2m1"), or one 6-bit code per
+    byte (fmt "e3m2" / "e2m3")."""
+    codes = unpack_nibbles(q) if fmt == "e2m1" else np.asarray(q, dtype=np.int64)
+    K = codes.shape[1]
+    kb = np.arange(K) // 32
+    s = ue8m0_scale(np.asarray(scale))
+    return bf16_round(mx_decode(codes, fmt) * s[:, kb, :])
+
+
+def forward_wq(x, topk_weights, topk_ids, w13_deq, w2_deq, w13_bias=None, w2_bias=None):
+    """The weight-only quantised layer: the ordinary layer on the dequantised
+    weights (dequant_int / dequant_mx of w13 and w2)."""
+    return forward(x, topk_weights, topk_ids, w13_deq, w2_deq, w13_bias, w2_bias)

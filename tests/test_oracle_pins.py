@@ -597,6 +597,92 @@ def test_fp8_forward_reduces_to_exact_layer_on_representable_inputs():
     np.testing.assert_allclose(y8t, y8e, rtol=1e-12, atol=1e-14)
 
 
+# ------------------------------------------------- weight-only quantisation ---
+
+def _bf16_rne_bits(v):
+    """bf16 rounding by integer arithmetic on the float32 bit pattern (round to
+    nearest, ties to even), independent of the oracle's bf16_round."""
+    b = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (b >> 16) & 1
+    r = ((b + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def test_unpack_nibbles_column_order():
+    # byte 0x21: column 0 = 1 (low nibble), column 1 = 2; byte 0xF0: 0 then 15
+    got = oracle.unpack_nibbles(np.array([[0x21, 0xF0]], dtype=np.uint8))
+    assert got.tolist() == [[1, 2, 0, 15]]
+
+
+def test_mx_element_values_against_the_format_tables():
+    # OCP MX v1.0 element values, written out from the format definitions
+    e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = oracle.mx_decode(np.arange(16), "e2m1")
+    np.testing.assert_array_equal(got[:8], e2m1)
+    np.testing.assert_array_equal(got[8:], [-v for v in e2m1])
+    # FP6 E3M2: bias 3, max 28 = 2^4 * 1.75, smallest subnormal 2^-2 * 1/4
+    e3m2 = oracle.mx_decode(np.arange(32), "e3m2")
+    assert e3m2[31] == 28.0 and e3m2[1] == 0.0625 and e3m2[12] == 1.0 and e3m2[4] == 0.25
+    assert np.all(np.diff(e3m2) > 0)
+    # FP6 E2M3: bias 1, max 7.5 = 2^2 * 1.875, smallest subnormal 1/8
+    e2m3 = oracle.mx_decode(np.arange(32), "e2m3")
+    assert e2m3[31] == 7.5 and e2m3[1] == 0.125 and e2m3[8] == 1.0 and e2m3[7] == 0.875
+    assert np.all(np.diff(e2m3) > 0)
+    assert oracle.mx_decode([0b100000], "e3m2")[0] == 0.0 and oracle.mx_decode([0b101100], "e3m2")[0] == -1.0
+    assert oracle.ue8m0_scale([127, 128, 125]).tolist() == [1.0, 2.0, 0.25]
+
+
+def test_bf16_round_against_bit_rounding():
+    rng = np.random.default_rng(4)
+    v = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-6, 6, 2000),
+                        # exact ties: 1 + (2k+1) * 2^-8 sit halfway between bf16 values
+                        1.0 + (2 * np.arange(20) + 1) * 2.0 ** -8, [0.0, -0.0, 3e38]])
+    np.testing.assert_array_equal(oracle.bf16_round(v), _bf16_rne_bits(v))
+
+
+def test_dequant_int4_groups_and_zero_points_by_hand():
+    # E=1, K=4, N=4, group G=2 (two groups), scales and zero points per (group, column)
+    codes = np.array([[0, 15, 8, 3], [1, 2, 9, 4], [7, 8, 0, 15], [12, 4, 5, 6]])
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)[None]
+    scale = np.array([[[0.5, 1.0, 2.0, 0.25], [0.125, 4.0, 1.0, 0.5]]])
+    zero = np.array([[[8, 8, 8, 3], [7, 0, 1, 15]]], dtype=np.uint8)
+    want = np.array([[-4.0, 7.0, 0.0, 0.0],        # (q - zp) * s, rows 0-1: group 0
+                     [-3.5, -6.0, 2.0, 0.25],
+                     [0.0, 32.0, -1.0, 0.0],       # rows 2-3: group 1
+                     [0.625, 16.0, 4.0, -4.5]])
+    got = oracle.dequant_int(packed, scale, zero, bits=4)
+    np.testing.assert_array_equal(got[0], want)
+    # symmetric default zero point 8
+    got = oracle.dequant_int(packed, np.ones((1, 2, 4)), None, bits=4)
+    np.testing.assert_array_equal(got[0], codes - 8)
+
+
+def test_dequant_rounds_to_bf16_once():
+    s = np.float64(_bf16_rne_bits(1.0 / 3.0))       # a bf16 scale
+    codes = np.array([[7, 9, 14, 1]])               # (q - 0) * s is not a bf16 value
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)[None]
+    got = oracle.dequant_int(packed, np.full((1, 1, 4), s), np.zeros((1, 1, 4), np.uint8), bits=4)
+    np.testing.assert_array_equal(got[0, 0], _bf16_rne_bits(codes[0] * s))
+    assert not np.array_equal(got[0, 0], codes[0] * s)
+    # int8, symmetric: codes are signed, zero point 0
+    q8 = np.array([[[-128, -1, 0, 127]]], dtype=np.int8)
+    np.testing.assert_array_equal(oracle.dequant_int(q8, np.full((1, 1, 4), 0.5), None, bits=8)[0, 0],
+                                  [-64.0, -0.5, 0.0, 63.5])
+
+
+def test_dequant_mx_blocks_of_32_by_hand():
+    K, N = 64, 2
+    codes = np.zeros((1, K, N), dtype=np.int64)
+    codes[0, 0] = [0b0011, 0b1111]     # 1.5, -6
+    codes[0, 31] = [0b0101, 0b0001]    # 3, 0.5
+    codes[0, 32] = [0b0111, 0b1010]    # 6, -1
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    scale = np.array([[[127, 128], [125, 130]]], dtype=np.uint8)   # block 0: 1, 2; block 1: 1/4, 8
+    got = oracle.dequant_mx(packed, scale, "e2m1")[0]
+    assert got[0].tolist() == [1.5, -12.0] and got[31].tolist() == [3.0, 1.0]
+    assert got[32].tolist() == [1.5, -8.0] and not got[1:31].any()
+
+
 # -------------------------------------------------------------- mutations ---
 
 def _pins_fail(golden_dir):
@@ -610,7 +696,12 @@ def _pins_fail(golden_dir):
               lambda: test_align_golden(golden_dir),
               test_e4m3_rounding_against_the_format,
               test_quantize_rows_error_bound_and_scale,
-              test_fp8_forward_reduces_to_exact_layer_on_representable_inputs]
+              test_fp8_forward_reduces_to_exact_layer_on_representable_inputs,
+              test_unpack_nibbles_column_order,
+              test_mx_element_values_against_the_format_tables,
+              test_dequant_int4_groups_and_zero_points_by_hand,
+              test_dequant_rounds_to_bf16_once,
+              test_dequant_mx_blocks_of_32_by_hand]
     for c in checks:
         try:
             c()
@@ -673,6 +764,43 @@ def _mut_quant_wrong_max(x):
     return om.e4m3_round(x32 / scale[:, None]), scale.astype(np.float64)
 
 
+def _mut_nibbles_swapped(packed):
+    b = np.asarray(packed, dtype=np.uint8).astype(np.int64)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.int64)
+    out[..., 0::2] = b >> 4
+    out[..., 1::2] = b & 0xF
+    return out
+
+
+def _mut_dequant_group_cyclic(q, scale, zero=None, bits=4):
+    codes = om.unpack_nibbles(q) if bits == 4 else np.asarray(q, dtype=np.int64)
+    K = codes.shape[1]
+    sc = np.asarray(scale, dtype=np.float64)
+    zp = np.full(sc.shape, 8 if bits == 4 else 0) if zero is None else np.asarray(zero, np.int64)
+    kg = np.arange(K) % sc.shape[1]                 # wrong: k mod groups, not k // G
+    return om.bf16_round((codes - zp[:, kg, :]) * sc[:, kg, :])
+
+
+def _mut_dequant_unrounded(q, scale, zero=None, bits=4):
+    codes = om.unpack_nibbles(q) if bits == 4 else np.asarray(q, dtype=np.int64)
+    K = codes.shape[1]
+    sc = np.asarray(scale, dtype=np.float64)
+    zp = np.full(sc.shape, 8 if bits == 4 else 0) if zero is None else np.asarray(zero, np.int64)
+    kg = np.arange(K) // (K // sc.shape[1])
+    return (codes - zp[:, kg, :]) * sc[:, kg, :]
+
+
+def _mut_mx_bias(codes, fmt):
+    c = np.asarray(codes, dtype=np.int64)
+    ebits, mbits, bias = om.MX_FORMATS[fmt]
+    bias += 1
+    sign = np.where((c >> (ebits + mbits)) & 1, -1.0, 1.0)
+    e = (c >> mbits) & ((1 << ebits) - 1)
+    m = (c & ((1 << mbits) - 1)).astype(np.float64)
+    return sign * np.where(e == 0, m / (1 << mbits) * 2.0 ** (1 - bias),
+                           2.0 ** (e - bias) * (1.0 + m / (1 << mbits)))
+
+
 _orig_align = om.align
 _ORIG_FFN = om.expert_ffn
 
@@ -686,6 +814,10 @@ _ORIG_FFN = om.expert_ffn
     ("align", _mut_sort_unstable_align),
     ("e4m3_round", _mut_e4m3_half_away),
     ("quantize_rows_e4m3", _mut_quant_wrong_max),
+    ("unpack_nibbles", _mut_nibbles_swapped),
+    ("dequant_int", _mut_dequant_group_cyclic),
+    ("dequant_int", _mut_dequant_unrounded),
+    ("mx_decode", _mut_mx_bias),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, golden_dir, target, mutant):
     monkeypatch.setattr(om, target, mutant)
