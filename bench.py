@@ -411,6 +411,7 @@ def run_ours(args, world, rank, local):
 
     if args.workload == "mixtral_prefill" and not args.no_next_rows:
         line["next_rows"] = measure_next_rows(step, spec, K, W, world, pk)
+        line["next_rows"]["weight_only_quantised"] = measure_wq(step, spec, K, W, world, pk)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, step.d, budget_s=args.cpu_budget)
@@ -501,6 +502,58 @@ def measure_next_rows(step, spec, K, W, world, pk):
                                     "unit": "TFLOP/s", "frac": round(ach / peak8, 4),
                                     "peak_source": "measured sustained bf16 x 2 (nominal ratio)"}}
     del q, ws8
+    return out
+
+
+def measure_wq(step, spec, K, W, world, pk):
+    """Weight-only quantised experts on the same layer, prefill and the
+    M = 16 decode: int4 (group 128, zero points) and MX FP4.  Decode is
+    bound by the weight bytes: touched experts' codes + scales + zero points,
+    plus x, out and logits."""
+    import mixture_experts_ffn_softmax_gb300 as pkg
+    d = step.d
+    dev = d["hidden"].device
+    dspec = wl.SPECS["mixtral_decode"]
+    dd = wl.make_moe_inputs(dspec, device=dev, weights=False)
+    dw, dids = pkg.moe_route(dd["router_logits"], dspec.top_k, "softmax", True)
+    touched = int(torch.unique(dids).numel())
+    out = {}
+    for fmt, G in (("int4", 128), ("mxfp4", 32)):
+        q = wl.make_wq_weights(spec, fmt, G, device=dev)
+        args = (q["w13_q"], q["w2_q"], q["w13_scale"], q["w2_scale"], q["w13_zero"], q["w2_zero"],
+                q["group_size"])
+        ws = pkg.alloc_workspace(pkg.workspace_size(spec.M, spec.H, spec.I, spec.E, spec.top_k,
+                                                    "separate"), dev)
+        y = torch.empty_like(d["hidden"])
+        yd = torch.empty_like(dd["hidden"])
+
+        def prefill():
+            pkg.moe_forward_wq(d["hidden"], step.w, step.ids, fmt, *args, workspace=ws, out=y)
+
+        def decode():
+            pkg.moe_forward_wq(dd["hidden"], dw, dids, fmt, *args, workspace=ws, out=yd)
+
+        ms_p = max_over_ranks(time_steps(prefill, K, W, world) / K, world)
+        Kd = max(K, 20)
+        ms_d = max_over_ranks(time_steps(decode, Kd, max(W, 3), world) / Kd, world)
+        pkg.profiler_start()
+        for _ in range(Kd):
+            decode()
+        prof = pkg.profiler_stop()
+        wbytes = sum(t.numel() * t.element_size() for k, t in q.items()
+                     if isinstance(t, torch.Tensor)) * touched // spec.E
+        dbytes = wbytes + dspec.M * dspec.H * 2 * 2 + dspec.M * dspec.E * 4
+        out[f"{fmt}_g{G}"] = {
+            "prefill_ms_per_step": round(ms_p, 4),
+            "prefill_tokens_per_s": round(spec.M * world / (ms_p / 1e3), 1),
+            "prefill_tflops": round(spec.flops() / (ms_p / 1e3) / 1e12, 1),
+            "decode_ms_per_step": round(ms_d, 4),
+            "decode_tokens_per_s": round(dspec.M * world / (ms_d / 1e3), 1),
+            "decode_weight_bytes": wbytes,
+            "decode_hbm_roofline_frac": round(dbytes / (pk["hbm_gbs"] * 1e9) / (ms_d / 1e3), 4),
+            "decode_kernels_us": {k: round(1e3 * v[1] / v[0], 2) for k, v in prof.items()},
+        }
+        del q, ws
     return out
 
 

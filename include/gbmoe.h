@@ -299,6 +299,57 @@ GBMOE_API moe_status_t moe_forward_fp8(const void* hidden, const float* topk_wei
 GBMOE_API moe_status_t moe_quant_rows_fp8(const void* x, int64_t M, int32_t H, void* q8,
                                           float* scale, moe_stream_t stream);
 
+/* ---------------------------------------------- weight-only quantised --
+ * Expert weights stored quantised, activations bf16.  Defines: "fused_moe.py
+ * 分析" (FlagDoc), "WNA16 路径" and "5. 特殊量化格式处理": int8 / int4
+ * weights with a group scale and a zero point (GPTQ/AWQ style), and OCP MX
+ * weights, are dequantised to the activation dtype and the layer runs as
+ * the bf16 one on those weights:
+ *   int4, int8  w[e, k, n] = bf16((q[e, k, n] - zp[e, k/G, n]) * s[e, k/G, n])
+ *   MX FP4      w[e, k, n] = bf16(e2m1(q[e, k, n]) * 2^(s[e, k/32, n] - 127))
+ * each value the exact product rounded once (nearest even).  Layouts, in the
+ * [E, K, N] orientation of the bf16 weights (w13: K = H, N = 2I with the
+ * gate columns first; w2: K = I, N = H), all row-major:
+ *  codes  int4 and MX FP4: uint8 [E, K, N/2], column 2j in the low nibble of
+ *         byte j, column 2j+1 in its high nibble; int8: int8 [E, K, N]
+ *  scale  int4 / int8: bf16 [E, K/G, N]; MX FP4: uint8 (UE8M0) [E, K/32, N]
+ *  zero   int4: uint8 [E, K/G, N] holding 0..15; int8: int8 [E, K/G, N];
+ *         NULL = symmetric (int4: 8, int8: 0); MX FP4: must be NULL
+ *  G      group_size along K: a multiple of 32 dividing K (MX FP4: 32)
+ * All pointers device, caller-owned, 16-byte aligned.
+ */
+typedef enum { MOE_WQ_INT4 = 0, MOE_WQ_INT8 = 1, MOE_WQ_MXFP4 = 2 } moe_wq_format_t;
+typedef struct {
+  int32_t format;     /* moe_wq_format_t */
+  int32_t group_size; /* G */
+  const void* w13;
+  const void* w2;
+  const void* w13_scale;
+  const void* w2_scale;
+  const void* w13_zero; /* NULL, or both zero-point tensors given */
+  const void* w2_zero;
+} moe_wq_weights_t;
+
+/* moe_dequant_weights: the dequantisation alone (the pages' path before the
+ * bf16 layer): out = bf16 [E, K, N] (written).  Limits: N % 16 == 0,
+ * K % G == 0.  Asynchronous on `stream`. */
+GBMOE_API moe_status_t moe_dequant_weights(int32_t format, const void* codes, const void* scale,
+                                           const void* zero, int32_t E, int32_t K, int32_t N,
+                                           int32_t group_size, void* out, moe_stream_t stream);
+
+/* moe_forward_wq: the layer with weight-only quantised w13 and w2.  The
+ * weights stay quantised in HBM: each grouped GEMM stages their codes and
+ * scales in shared memory and expands them to bf16 there.  Arguments as
+ * moe_forward with the separate weight-and-reduce; workspace >=
+ * moe_workspace_size(M, H, I, E, top_k, MOE_REDUCE_SEPARATE).
+ * Limits: as moe_forward, and H, I multiples of 32, at least 64, divisible
+ * by G. */
+GBMOE_API moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
+                                      const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                                      int32_t E, int32_t top_k, const moe_wq_weights_t* w,
+                                      const void* w13_bias, const void* w2_bias, void* workspace,
+                                      size_t workspace_bytes, void* out, moe_stream_t stream);
+
 /* ------------------------------------------------------ forward_batched --
  * moe_forward_batched: the Batched activation format.  Defines: "vLLM
  * FusedMoEModularKernel" page, Introduction (activations (num_experts,

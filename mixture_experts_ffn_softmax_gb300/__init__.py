@@ -228,6 +228,57 @@ def moe_quant_rows_fp8(x: torch.Tensor, q8: Optional[torch.Tensor] = None,
     return q8, scale
 
 
+WQ_FORMATS = {"int4": 0, "int8": 1, "mxfp4": 2}
+
+
+def _wq_shape(fmt: str, codes: torch.Tensor):
+    E, K, n = codes.shape
+    return E, K, (2 * n if fmt in ("int4", "mxfp4") else n)
+
+
+def moe_dequant_weights(fmt: str, codes: torch.Tensor, scale: torch.Tensor,
+                        zero: Optional[torch.Tensor] = None, group_size: int = 128,
+                        out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Weight-only quantised weights -> bf16 [E, K, N] (fmt "int4", "int8" or
+    "mxfp4"; layouts as moe_forward_wq)."""
+    E, K, N = _wq_shape(fmt, codes)
+    if out is None:
+        out = torch.empty(E, K, N, dtype=torch.bfloat16, device=codes.device)
+    _check(lib().moe_dequant_weights(WQ_FORMATS[fmt], _ptr(codes), _ptr(scale), _ptr(zero), E, K,
+                                     N, group_size, _ptr(out), _stream(stream)),
+           "moe_dequant_weights")
+    return out
+
+
+def moe_forward_wq(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: torch.Tensor,
+                   fmt: str, w13_q: torch.Tensor, w2_q: torch.Tensor, w13_scale: torch.Tensor,
+                   w2_scale: torch.Tensor, w13_zero: Optional[torch.Tensor] = None,
+                   w2_zero: Optional[torch.Tensor] = None, group_size: int = 128,
+                   w13_bias: Optional[torch.Tensor] = None,
+                   w2_bias: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, stream=None):
+    """Layer with weight-only quantised experts.  int4 / MX FP4 codes uint8
+    [E, K, N/2] (column 2j in the low nibble), int8 codes int8 [E, K, N];
+    scales bf16 [E, K/G, N] (int) or uint8 UE8M0 [E, K/32, N] (MX); zero
+    points uint8 / int8 [E, K/G, N] or None.  w13: K = H, N = 2I; w2: K = I,
+    N = H."""
+    M, H = hidden.shape
+    E, _, N13 = _wq_shape(fmt, w13_q)
+    I = N13 // 2
+    k = topk_ids.shape[1]
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(M, H, I, E, k, "separate"), hidden.device)
+    if out is None:
+        out = torch.empty_like(hidden)
+    wts = _lib.WqWeights(WQ_FORMATS[fmt], group_size, _ptr(w13_q), _ptr(w2_q), _ptr(w13_scale),
+                         _ptr(w2_scale), _ptr(w13_zero), _ptr(w2_zero))
+    _check(lib().moe_forward_wq(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E, k,
+                                ctypes.byref(wts), _ptr(w13_bias), _ptr(w2_bias), _ptr(workspace),
+                                workspace.numel(), _ptr(out), _stream(stream)), "moe_forward_wq")
+    return out
+
+
 def moe_forward_batched(x: torch.Tensor, expert_num_tokens: torch.Tensor, w13: torch.Tensor,
                         w2: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
                         w2_bias: Optional[torch.Tensor] = None,
@@ -324,6 +375,7 @@ def profiler_stop():
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
+           "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",
            "workspace_size", "batched_workspace_size", "alloc_workspace", "align_capacity",
            "workspace_error_word", "read_error", "launch_count", "workspace_layout",

@@ -22,6 +22,13 @@ class Fp8Weights(ctypes.Structure):
                 ("w2_scale", ctypes.c_void_p), ("scale_per_channel", ctypes.c_int32)]
 
 
+class WqWeights(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p),
+                ("w13_scale", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
+                ("w13_zero", ctypes.c_void_p), ("w2_zero", ctypes.c_void_p)]
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
                 ("total_ms", ctypes.c_double)]
@@ -45,6 +52,10 @@ SIGNATURES = {
     "moe_forward_fp8": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32,
                                 ctypes.POINTER(Fp8Weights), c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_quant_rows_fp8": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
+    "moe_dequant_weights": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp,
+                                    c_vp]),
+    "moe_forward_wq": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32,
+                               ctypes.POINTER(WqWeights), c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_align_capacity": (c_sz, [c_i64, c_i32, c_i32, c_i32]),
     "moe_align_scratch_size": (c_sz, [c_i64, c_i32, c_i32]),
     "moe_align": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,

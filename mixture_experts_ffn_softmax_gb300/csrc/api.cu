@@ -698,6 +698,149 @@ moe_status_t moe_quant_rows_fp8(const void* x, int64_t M, int32_t H, void* q8, f
   return launch_quant_tokens_fp8(qa, stream);
 }
 
+// ------------------------------------------- weight-only quantised --
+namespace {
+moe_status_t validate_wq_format(int32_t format, int32_t G, const void* zero) {
+  if (format < MOE_WQ_INT4 || format > MOE_WQ_MXFP4)
+    return set_error(MOE_ERR_INVALID_ARG, "weight format %d", format);
+  if (G < 32 || G % 32 != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "group_size=%d must be a positive multiple of 32", G);
+  if (format == MOE_WQ_MXFP4 && G != 32)
+    return set_error(MOE_ERR_INVALID_ARG, "MX FP4 scales cover blocks of 32 (group_size=%d)", G);
+  if (format == MOE_WQ_MXFP4 && zero != nullptr)
+    return set_error(MOE_ERR_INVALID_ARG, "MX FP4 has no zero points");
+  return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_dequant_weights(int32_t format, const void* codes, const void* scale,
+                                 const void* zero, int32_t E, int32_t K, int32_t N,
+                                 int32_t group_size, void* out, moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (moe_status_t st = validate_wq_format(format, group_size, zero)) return st;
+  if (E < 1 || K < 1 || N < 16 || N % 16 != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "E=%d K=%d N=%d (N a positive multiple of 16)", E, K, N);
+  if (K % group_size != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "group_size=%d does not divide K=%d", group_size, K);
+  if (static_cast<int64_t>(E) * K * N >= (int64_t(1) << 40))
+    return set_error(MOE_ERR_INVALID_ARG, "E*K*N too large");
+  if (!codes || !scale || !out) return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(codes) || !aligned16(scale) || !aligned16(out) || (zero && !aligned16(zero)))
+    return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  int sms = 0;
+  if (moe_status_t st = check_device(&sms)) return st;
+  WqDequantArgs a{format, codes, scale, zero, E, K, N, group_size, static_cast<bf16*>(out)};
+  return launch_dequant_weights(a, stream);
+}
+
+moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
+                            const int32_t* topk_ids, int64_t M, int32_t H, int32_t I, int32_t E,
+                            int32_t top_k, const moe_wq_weights_t* w, const void* w13_bias,
+                            const void* w2_bias, void* workspace, size_t workspace_bytes,
+                            void* out, moe_stream_t stream) {
+  size_t need = 0;
+  if (moe_status_t st = moe_workspace_size(M, H, I, E, top_k, MOE_REDUCE_SEPARATE, &need))
+    return st;
+  if (!w) return set_error(MOE_ERR_INVALID_ARG, "null weights");
+  if (moe_status_t st = validate_wq_format(w->format, w->group_size, w->w13_zero)) return st;
+  if (w->format == MOE_WQ_MXFP4 && w->w2_zero != nullptr)
+    return set_error(MOE_ERR_INVALID_ARG, "MX FP4 has no zero points");
+  if (H < 64 || I < 64 || H % 32 != 0 || I % 32 != 0)
+    return set_error(MOE_ERR_INVALID_ARG,
+                     "quantised weights need H and I multiples of 32, at least 64 (H=%d I=%d)", H, I);
+  if (H % w->group_size != 0 || I % w->group_size != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "group_size=%d must divide H=%d and I=%d",
+                     w->group_size, H, I);
+  if ((w->w13_zero == nullptr) != (w->w2_zero == nullptr))
+    return set_error(MOE_ERR_INVALID_ARG, "zero points for both w13 and w2, or for neither");
+  if (M == 0) return MOE_OK;
+  if (!hidden || !topk_weights || !topk_ids || !w->w13 || !w->w2 || !w->w13_scale ||
+      !w->w2_scale || !workspace || !out)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(hidden) || !aligned16(out) || !aligned16(w->w13) || !aligned16(w->w2) ||
+      !aligned16(w->w13_scale) || !aligned16(w->w2_scale) ||
+      (w->w13_zero && !aligned16(w->w13_zero)) || (w->w2_zero && !aligned16(w->w2_zero)) ||
+      (w13_bias && !aligned16(w13_bias)) || (w2_bias && !aligned16(w2_bias)))
+    return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < need)
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", need,
+                     workspace_bytes);
+  int sms = 0;
+  if (moe_status_t st = check_device(&sms)) return st;
+  cudaStream_t s = stream;
+  const int64_t Mc_max = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
+  const FwdLayout L = fwd_layout(Mc_max, H, I, E, top_k);
+  int32_t* err = at<int32_t>(workspace, L.err);
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
+  const bf16* x = static_cast<const bf16*>(hidden);
+  bf16* y = static_cast<bf16*>(out);
+  for (int64_t c0 = 0; c0 < M; c0 += Mc_max) {
+    const int64_t Mc = (M - c0) < Mc_max ? (M - c0) : Mc_max;
+    const int64_t Rc = Mc * top_k;
+    const int64_t cap = align_cap(Rc, E, MOE_BLOCK_M);
+    int32_t* sorted = at<int32_t>(workspace, L.sorted);
+    int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    int32_t* inv = at<int32_t>(workspace, L.inv);
+    AlignArgs al{topk_ids + c0 * top_k, Rc, E, MOE_BLOCK_M, sorted, offsets,
+                 at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.block_expert),
+                 at<int32_t>(workspace, L.scratch), cap, err, inv};
+    if (moe_status_t st = launch_align(al, s)) return st;
+    bf16* a_perm = at<bf16>(workspace, L.a_perm);
+    GatherArgs ga{x + c0 * H, sorted, offsets, E, top_k, static_cast<int32_t>(Rc), H, cap,
+                  a_perm};
+    if (moe_status_t st = launch_gather(ga, s)) return st;
+    bf16* z = at<bf16>(workspace, L.z);
+    GroupedGemmArgs g1{};
+    g1.a = a_perm;
+    g1.w = static_cast<const bf16*>(w->w13);
+    g1.bias = static_cast<const bf16*>(w13_bias);
+    g1.cap = cap;
+    g1.E = E;
+    g1.N = I;
+    g1.K = H;
+    g1.offsets = offsets;
+    g1.out = z;
+    g1.row_index = sorted;
+    g1.sentinel = static_cast<int32_t>(Rc);
+    g1.error_word = err;
+    g1.num_sms = sms;
+    g1.rows_hint = Rc;
+    g1.wq_format = w->format;
+    g1.wq_group = w->group_size;
+    g1.wq_scale = w->w13_scale;
+    g1.wq_zero = w->w13_zero;
+    if (moe_status_t st = launch_gemm1_swiglu_wq(g1, s)) return st;
+    float* o = at<float>(workspace, L.o);
+    GroupedGemmArgs g2{};
+    g2.a = z;
+    g2.w = static_cast<const bf16*>(w->w2);
+    g2.bias = static_cast<const bf16*>(w2_bias);
+    g2.cap = cap;
+    g2.E = E;
+    g2.N = H;
+    g2.K = I;
+    g2.offsets = offsets;
+    g2.out = o;
+    g2.row_index = sorted;
+    g2.row_weight = topk_weights + c0 * top_k;
+    g2.sentinel = static_cast<int32_t>(Rc);
+    g2.div = top_k;
+    g2.error_word = err;
+    g2.num_sms = sms;
+    g2.rows_hint = Rc;
+    g2.wq_format = w->format;
+    g2.wq_group = w->group_size;
+    g2.wq_scale = w->w2_scale;
+    g2.wq_zero = w->w2_zero;
+    if (moe_status_t st = launch_gemm2_sorted_wq(g2, s)) return st;
+    if (moe_status_t st = launch_reduce_sorted(o, inv, Mc, top_k, H, y + c0 * H, s)) return st;
+  }
+  return MOE_OK;
+}
+
 // ------------------------------------------------------ forward_batched --
 moe_status_t moe_batched_workspace_size(int32_t E, int32_t T, int32_t H, int32_t I,
                                         size_t* bytes) {

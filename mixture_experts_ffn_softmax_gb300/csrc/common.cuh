@@ -131,6 +131,18 @@ struct QuantSortedArgs {
 };
 moe_status_t launch_quant_sorted_fp8(const QuantSortedArgs& a, cudaStream_t s);
 
+// Weight-only quantised weights -> bf16 [E, K, N] (wq.cu).  format: 0 int4,
+// 1 int8, 2 MX FP4; codes, scale [E, K/G, N], zero [E, K/G, N] or null.
+struct WqDequantArgs {
+  int32_t format;
+  const void* codes;
+  const void* scale;
+  const void* zero;
+  int32_t E, K, N, G;
+  __nv_bfloat16* out;
+};
+moe_status_t launch_dequant_weights(const WqDequantArgs& a, cudaStream_t s);
+
 // y[t, :] = bf16( sum_j o_sorted[inv[t*k + j], :] ), skipping inv < 0.
 moe_status_t launch_reduce_sorted(const float* o_sorted, const int32_t* inv, int64_t M,
                                   int32_t k, int32_t H, bf16* y, cudaStream_t s);
@@ -162,6 +174,12 @@ struct GroupedGemmArgs {
   const float* w_scale = nullptr;       // [E, 2N] / [E, N] per channel, or [E]
   int32_t w_scale_per_channel = 0;
   float* row_amax = nullptr;            // GEMM1 FP8: max |bf16 z| of each sorted row (atomic)
+  // weight-only quantised w (codes in `w`): format (0 int4, 1 int8, 2 MX FP4),
+  // group size along K, scales [E, K/G, N'] and zero points (or null)
+  int32_t wq_format = -1;
+  int32_t wq_group = 0;
+  const void* wq_scale = nullptr;
+  const void* wq_zero = nullptr;
 };
 moe_status_t launch_gemm1_swiglu_fp8(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_gemm2_sorted_fp8(const GroupedGemmArgs& a, cudaStream_t s);
@@ -181,6 +199,10 @@ moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s);
 // weighted row is added into row row_index[p] / div with vector fp32 atomics.
 moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+// bf16 A x weight-only quantised w (a.wq_format), B converted to bf16 in
+// shared memory: GEMM1 with the SwiGLU epilogue, GEMM2 with sorted fp32 rows.
+moe_status_t launch_gemm1_swiglu_wq(const GroupedGemmArgs& a, cudaStream_t s);
+moe_status_t launch_gemm2_sorted_wq(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s);
 
 }  // namespace gbmoe

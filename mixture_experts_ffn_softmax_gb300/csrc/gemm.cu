@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "wq.cuh"
 
 namespace gbmoe {
 namespace {
@@ -55,6 +56,7 @@ constexpr int A_STAGE_BYTES = BM * 128;        // 16 KB: 128 rows x one 128-byte
 constexpr int TMEM_COLS = 2 * MMA_N;           // 512: two accumulators
 constexpr int MAX_E = 1024;
 constexpr int STAGING_BYTES = 32 * 128;        // per epilogue warp: 32 rows x 128 bytes
+constexpr int kMaxRaw = 8;  // raw ring stages the control block has barriers for
 
 // CG = CTAs cooperating on one MMA tile.  CG = 1: a 128 x 256 tile per CTA,
 // 48 KB per pipeline stage.  CG = 2 (a CTA pair, tcgen05 cta_group::2): a
@@ -65,7 +67,31 @@ constexpr int STAGING_BYTES = 32 * 128;        // per epilogue warp: 32 rows x 1
 // (kind::f16, K = 16).  Either way a stage holds one 128-byte swizzle row of
 // K per A row: 64 bf16 or 128 E4M3; B is staged in chunks of one 128-byte
 // row of N (64 or 128 columns) by those K rows.
-template <int CG, bool F8 = false>
+// Raw ring of the weight-only quantised B operand (no swizzle), staged by
+// TMA for the converter warps.  A stage holds, for 64 K rows of the tile's
+// 256 columns, the codes, up to two rows of group scales and of zero
+// points, in NREG regions of contiguous columns: two (gate, up) for the
+// SwiGLU GEMM, one for the other -- so that each TMA box row is as wide as
+// the region (fewer, longer rows per stage).
+template <Wq WQ, int NREG = 2>
+struct WqRing {
+  using F = WqFmt<WQ>;
+  static constexpr int RCOLS = 256 / NREG;                  // columns of a region
+  static constexpr int ROW_BYTES = RCOLS * F::CODE_BITS / 8; // codes of one K row of a region
+  static constexpr int CODES = 64 * ROW_BYTES;               // a region's codes, 64 K rows
+  static constexpr int SCALES = 2 * RCOLS * F::SCALE_BYTES;  // a region's scales, two group rows
+  static constexpr int ZEROS = F::HAS_ZERO ? 2 * RCOLS : 0;  // a region's zero points
+  static constexpr int SC_OFF = NREG * CODES;                // scales of region g at SC_OFF + g*SCALES
+  static constexpr int Z_OFF = SC_OFF + NREG * SCALES;       // zeros of region g at Z_OFF + g*ZEROS
+  static constexpr int STAGE = Z_OFF + NREG * ZEROS;
+  static constexpr int NRAW = WQ == Wq::Int8 ? 2 : 5;
+  static constexpr int BYTES = WQ == Wq::None ? 0 : NRAW * STAGE;
+  static_assert(CODES % 128 == 0 && SCALES % 128 == 0 && ZEROS % 128 == 0,
+                "raw regions keep 128-byte alignment");
+  static_assert(NRAW <= kMaxRaw, "raw ring deeper than its barriers");
+};
+
+template <int CG, bool F8 = false, Wq WQ = Wq::None>
 struct Geo {
   static constexpr int BKE = F8 ? 128 : 64;       // K elements per stage
   static constexpr int CW = F8 ? 128 : 64;        // B columns per chunk
@@ -76,10 +102,10 @@ struct Geo {
   static constexpr int UMMA_K = F8 ? 32 : 16;     // K per tcgen05.mma
   static constexpr int KSTEPS = BKE / UMMA_K;
   static constexpr int B_KSTEP = UMMA_K * 128;    // bytes per MMA K step within a chunk
-  static constexpr int NSTAGES = CG == 1 ? 4 : 5;
+  static constexpr int NSTAGES = WQ != Wq::None ? 3 : (CG == 1 ? 4 : 5);
   static constexpr size_t PREFIX_BYTES = CG == 1 ? 0 : (MAX_E + 1) * sizeof(int32_t);
-  static constexpr size_t SMEM =
-      1024 /*alignment slack*/ + NSTAGES * STAGE + EPI_WARPS * STAGING_BYTES + PREFIX_BYTES;
+  static constexpr size_t SMEM = 1024 /*alignment slack*/ + NSTAGES * STAGE +
+                                 EPI_WARPS * STAGING_BYTES + PREFIX_BYTES + WqRing<WQ>::BYTES;
   static constexpr uint32_t IDESC =
       F8 ? ptx::idesc_e4m3_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true)
          : ptx::idesc_bf16_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
@@ -87,6 +113,16 @@ struct Geo {
 static_assert(Geo<1>::SMEM <= 232448 && Geo<2>::SMEM <= 232448, "shared memory budget");
 static_assert(Geo<1, true>::SMEM <= 232448 && Geo<2, true>::SMEM <= 232448,
               "shared memory budget");
+static_assert(Geo<1, false, Wq::Int4>::SMEM <= 232448 && Geo<1, false, Wq::Int8>::SMEM <= 232448 &&
+                  Geo<1, false, Wq::Mxfp4>::SMEM <= 232448,
+              "shared memory budget");
+
+// Threads of a CTA: producer + MMA warps, converter warps (weight-only
+// quantised B), epilogue warps.
+template <Wq WQ>
+__host__ __device__ constexpr int conv_warps() { return WQ == Wq::None ? 0 : 8; }
+template <Wq WQ>
+__host__ __device__ constexpr int cta_threads() { return 64 + 32 * conv_warps<WQ>() + EPI_WARPS * 32; }
 
 enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3, DenseF32 = 4 };
 
@@ -96,6 +132,8 @@ struct Ctl {
   uint64_t empty[NS];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t raw_full[kMaxRaw];   // weight-only quantised B: raw ring
+  uint64_t raw_empty[kMaxRaw];
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -116,6 +154,9 @@ struct KParams {
   const float* w_scale;
   int32_t w_scale_per_channel, w_scale_ld;
   float* row_amax;  // SwiGLU FP8: atomic max of |bf16 z| per sorted row, or null
+  // weight-only quantised B: group size along K, group rows per 64-row
+  // stage (1 or 2), zero points present, bytes per raw stage
+  int32_t wq_G, wq_gbox, wq_has_zero, wq_raw_tx;
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
@@ -126,7 +167,9 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    // suspended rather than spinning, so waiting roles leave the issue
+    // slots to the working ones; wakes when the phase completes
+    if (ptx::mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
     if (*reinterpret_cast<volatile int32_t*>(abort)) return false;
     if (ptx::globaltimer_ns() - t0 > limit_ns) {
       *reinterpret_cast<volatile int32_t*>(abort) = 1;
@@ -292,10 +335,21 @@ __device__ __forceinline__ void swiglu_prefetch(const KParams& P, int e, int n_b
   }
 }
 
-template <Epi EPI, int CG, bool F8>
+template <Epi EPI, int CG, bool F8, Wq WQ = Wq::None>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                          const CUtensorMap* tmO, const KParams& P) {
-  using G = Geo<CG, F8>;
+                                          const CUtensorMap* tmO, const CUtensorMap* tmS,
+                                          const CUtensorMap* tmZ, const KParams& P) {
+  using G = Geo<CG, F8, WQ>;
+  using R = WqRing<WQ, EPI == Epi::SwiGLU ? 2 : 1>;
+  static_assert(R::BYTES == WqRing<WQ>::BYTES, "raw ring size does not depend on the regions");
+  constexpr bool WQM = WQ != Wq::None;
+  constexpr int CONV = conv_warps<WQ>();
+  constexpr int EPI0 = 2 + CONV;  // first epilogue warp
+  // Int4 / MX B tiles hold each aligned group of 8 columns in the order
+  // 0 4 1 5 2 6 3 7 (wq_pair_pos), and so does the accumulator: the epilogue
+  // reads column n of a group from position wq_pair_pos(n)
+  constexpr bool PERM = WQ == Wq::Int4 || WQ == Wq::Mxfp4;
+  auto acc_pos = [](int n) { return PERM ? (n & ~7) + wq_pair_pos(n & 7) : n; };
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl<G::NSTAGES> ctl;
 
@@ -308,6 +362,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* staging = tiles + G::NSTAGES * G::STAGE;  // 1024-byte aligned
   int32_t* s_pp = reinterpret_cast<int32_t*>(staging + EPI_WARPS * STAGING_BYTES);
+  uint8_t* rawbuf = staging + EPI_WARPS * STAGING_BYTES + G::PREFIX_BYTES;  // WQ raw ring
   const int32_t* off = P.offsets;
 
   if constexpr (CG == 2) {
@@ -333,8 +388,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::NSTAGES; ++i) {
-      ptx::mbar_init(&ctl.full[i], 1);
+      // the producer's arrive with A's bytes, or (quantised B) the converter
+      // warps' arrivals, one of them having raised the count by A's bytes
+      ptx::mbar_init(&ctl.full[i], WQM ? CONV : 1);
       ptx::mbar_init(&ctl.empty[i], 1);
+    }
+    if constexpr (WQM) {
+      for (int i = 0; i < R::NRAW; ++i) {
+        ptx::mbar_init(&ctl.raw_full[i], 1);
+        ptx::mbar_init(&ctl.raw_empty[i], CONV);
+      }
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ctl.tmem_full[a], 1);
@@ -347,6 +410,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     ptx::prefetch_tmap(tmA);
     ptx::prefetch_tmap(tmB);
     if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SwiGLU) ptx::prefetch_tmap(tmO);
+    if constexpr (WQM) {
+      ptx::prefetch_tmap(tmS);
+      if (P.wq_has_zero) ptx::prefetch_tmap(tmZ);
+    }
   }
   if (warp == 1) {
     if constexpr (CG == 2) {
@@ -391,7 +458,148 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     }
   };
 
-  if (warp == 0) {
+  if (WQM && warp == 0) {
+    // ------------------------------------- TMA producer (quantised B) --
+    // per 64-row K stage: the raw codes / scales / zero points of the four
+    // 64-column chunks into the raw ring, as far ahead as the ring allows
+    // (A goes to the main ring from the converter warps)
+    if (lane == 0) {
+      int rstage = 0;
+      uint32_t rphase = 0;
+      bool ok = true;
+      for (int t = unit; t < total_tiles && ok; t += units) {
+        int e, row0, nb;
+        bool mine;
+        tile_of(t, e, row0, nb, mine);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!bounded_wait(&ctl.raw_empty[rstage], rphase ^ 1u, &ctl.abort, P.error_word)) {
+            ok = false;
+            break;
+          }
+          uint64_t* rf = &ctl.raw_full[rstage];
+          ptx::mbar_arrive_expect_tx(rf, P.wq_raw_tx);
+          uint8_t* rb = rawbuf + rstage * R::STAGE;
+          const int g0 = (kb * G::BKE) / P.wq_G;
+          if constexpr (EPI == Epi::SwiGLU) {
+            // region 0: gate columns [nb*128, +128); region 1: the same up columns
+            const int col = nb * (MMA_N / 2);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              ptx::tma_load_4d(rb + g * R::CODES, tmB, rf, col * R::F::CODE_BITS / 8, g,
+                               kb * G::BKE, e);
+              ptx::tma_load_4d(rb + R::SC_OFF + g * R::SCALES, tmS, rf, col, g, g0, e);
+              if (P.wq_has_zero)
+                ptx::tma_load_4d(rb + R::Z_OFF + g * R::ZEROS, tmZ, rf, col, g, g0, e);
+            }
+          } else {
+            const int col = nb * MMA_N;
+            ptx::tma_load_3d(rb, tmB, rf, col * R::F::CODE_BITS / 8, kb * G::BKE, e);
+            ptx::tma_load_3d(rb + R::SC_OFF, tmS, rf, col, g0, e);
+            if (P.wq_has_zero) ptx::tma_load_3d(rb + R::Z_OFF, tmZ, rf, col, g0, e);
+          }
+          if (++rstage == R::NRAW) {
+            rstage = 0;
+            rphase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (WQM && warp < 2 + CONV && warp >= 2) {
+    // ------------------------------------------- converters (quantised B) --
+    // The stage's region rows (2 x 64 for the SwiGLU GEMM, 64 otherwise) are
+    // split evenly over the converter warps.  A region row is read by LPR
+    // lanes of 8 columns each (16 lanes for 128 columns, 32 for 256), so a
+    // warp reads whole rows -- no bank conflicts -- and every lane keeps one
+    // set of group parameters.  Each lane writes its 8 columns as bf16 in
+    // the 128-byte-swizzled layout TMA would have produced (16-byte unit j
+    // of K row r of a 64-column chunk at j ^ (r & 7)); then the warp arrives
+    // on the stage's barrier.
+    constexpr int NREG = (EPI == Epi::SwiGLU) ? 2 : 1;
+    constexpr int LPR = R::RCOLS / 8;                 // lanes per region row
+    constexpr int RPI = 32 / LPR;                     // rows per warp instruction
+    constexpr int ROWS = NREG * 64 / (CONV > 0 ? CONV : 1);  // region rows per warp
+    constexpr int ITERS = ROWS / RPI;
+    static_assert(!WQM || (ROWS % RPI == 0 && 32 % ROWS == 0), "converter row split");
+    const int cw = warp - 2;
+    const int first = cw * ROWS;                      // first region row of this warp
+    const int reg = first / 64;                       // region (gate / up)
+    const int k0 = first % 64 + lane / LPR;           // this lane's first K row
+    const int col = (lane % LPR) * 8;                 // first of its 8 columns in the region
+    const int gr = (first % 64) / 32;                 // group row (G = 32) of its rows
+    const int chunk = reg * (R::RCOLS / 64) + col / 64;  // 64-column chunk of the B tile
+    const int unit8 = (col % 64) / 8;
+    int stage = 0, rstage = 0;
+    uint32_t phase = 0, rphase = 0;
+    bool ok = true;
+    for (int t = unit; t < total_tiles && ok; t += units) {
+      int e, row0, nb;
+      bool mine;
+      tile_of(t, e, row0, nb, mine);
+      for (int kb = 0; kb < KB; ++kb) {
+        bool got = bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word);
+        if (cw == 0 && lane == 0 && got) {
+          // the stage's A rows: their bytes join the count before this warp arrives
+          ptx::mbar_expect_tx(&ctl.full[stage], A_STAGE_BYTES);
+          ptx::tma_load_2d(tiles + stage * G::STAGE, tmA, &ctl.full[stage], kb * G::BKE, row0);
+        }
+        got = got && bounded_wait(&ctl.raw_full[rstage], rphase, &ctl.abort, P.error_word);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* rb = rawbuf + rstage * R::STAGE;
+        const uint8_t* rc = rb + reg * R::CODES + col * R::F::CODE_BITS / 8;
+        uint8_t* dst = tiles + stage * G::STAGE + A_STAGE_BYTES + chunk * G::CHUNK_BYTES;
+        WqParams8 p;
+        {
+          const int g = P.wq_gbox == 2 ? gr : 0;
+          const uint8_t* rsc = rb + R::SC_OFF + reg * R::SCALES + (g * R::RCOLS + col) * R::F::SCALE_BYTES;
+          uint4 s8;
+          if constexpr (R::F::SCALE_BYTES == 2) {
+            s8 = *reinterpret_cast<const uint4*>(rsc);
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(rsc);
+            s8 = make_uint4(v.x, v.y, 0, 0);
+          }
+          uint2 z8 = make_uint2(0, 0);
+          if constexpr (R::F::HAS_ZERO) {
+            if (P.wq_has_zero)
+              z8 = *reinterpret_cast<const uint2*>(rb + R::Z_OFF + reg * R::ZEROS + g * R::RCOLS + col);
+          }
+          wq_params8<WQ>(s8, z8, P.wq_has_zero != 0, p);
+        }
+        uint2 c[ITERS];
+#pragma unroll
+        for (int i = 0; i < ITERS; ++i) {  // all code loads first
+          const int r = k0 + RPI * i;
+          if constexpr (R::F::CODE_BITS == 4)
+            c[i] = make_uint2(*reinterpret_cast<const uint32_t*>(rc + r * R::ROW_BYTES), 0u);
+          else
+            c[i] = *reinterpret_cast<const uint2*>(rc + r * R::ROW_BYTES);
+        }
+#pragma unroll
+        for (int i = 0; i < ITERS; ++i) {
+          const int r = k0 + RPI * i;
+          *reinterpret_cast<uint4*>(dst + r * 128 + ((unit8 ^ (r & 7)) << 4)) =
+              wq_dequant8<WQ, PERM>(c[i], p);
+        }
+        ptx::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&ctl.full[stage]);
+          ptx::mbar_arrive(&ctl.raw_empty[rstage]);
+        }
+        if (++stage == G::NSTAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++rstage == R::NRAW) {
+          rstage = 0;
+          rphase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       int stage = 0;
@@ -500,7 +708,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;               // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;     // which half of the tile's columns it owns
+    const int half = (warp - EPI0) >> 2;  // which half of the tile's columns it owns
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -536,25 +744,28 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       if (!mine) {
         // this CTA's half of a pair tile has no rows of the expert
       } else if constexpr (EPI == Epi::SwiGLU) {
-        bf16* z = reinterpret_cast<bf16*>(P.out);
         const int N = P.N;
-        // all of this warp's accumulator columns at once: gate [c0, c0+64)
-        // and up [c0+128, c0+192), then the accumulator is free again
+        // this warp's accumulator columns, gate [c0, c0+64) and up
+        // [c0+128, c0+192): read at once and the accumulator freed before the
+        // math (or, with converter warps in the CTA, one 32-column chunk at a
+        // time for the smaller register budget)
         const int c0 = half * (MMA_N / 4);
         uint32_t g[2][32], u[2][32];
-        ptx::tmem_ld_32cols(taddr + c0, g[0]);
-        ptx::tmem_ld_32cols(taddr + c0 + 32, g[1]);
-        ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c0, u[0]);
-        ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c0 + 32, u[1]);
-        ptx::tmem_ld_wait();
-        release_acc(acc);
-        released = true;
+        if constexpr (!WQM) {
+          ptx::tmem_ld_32cols(taddr + c0, g[0]);
+          ptx::tmem_ld_32cols(taddr + c0 + 32, g[1]);
+          ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c0, u[0]);
+          ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c0 + 32, u[1]);
+          ptx::tmem_ld_wait();
+          release_acc(acc);
+          released = true;
+        }
         uint32_t zmax2 = 0;  // max |z| as bf16 magnitude bits, both halves
         // z is staged as the warp's 32 rows x 64 columns (one 128-byte row
         // each, 16-byte chunk j at j ^ (row & 7)) and written with one TMA
         // store; a warp whose rows are all padding, or whose columns all lie
         // past N, stores nothing (no store starts outside the tensor)
-        uint8_t* stage_buf = staging + (warp - 2) * STAGING_BYTES;
+        uint8_t* stage_buf = staging + (warp - EPI0) * STAGING_BYTES;
         const bool any_real = __ballot_sync(0xffffffffu, sr.real) != 0u;
         if (any_real && n_base < N) {
           if (lane == 0) ptx::bulk_wait_read0();  // the buffer's previous store has read it
@@ -563,6 +774,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           auto col = [&](float v, int j) { return __shfl_sync(0xffffffffu, v, j); };
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
+            if constexpr (WQM) {
+              // fewer registers per thread here: one 32-column chunk at a time
+              ptx::tmem_ld_32cols(taddr + c0 + 32 * c, g[c]);
+              ptx::tmem_ld_32cols(taddr + MMA_N / 2 + c0 + 32 * c, u[c]);
+              ptx::tmem_ld_wait();
+              if (c == 1) {
+                release_acc(acc);
+                released = true;
+              }
+            }
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 pk;
@@ -573,7 +794,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int j = v * 8 + 2 * i + h;  // column within the 32-column chunk
-                  float gv = __uint_as_float(g[c][j]), uv = __uint_as_float(u[c][j]);
+                  const int ja = acc_pos(j);        // its accumulator position
+                  float gv = __uint_as_float(g[c][ja]), uv = __uint_as_float(u[c][ja]);
                   if constexpr (F8) {
                     gv *= col(sr.sg[c], j) * sr.sa;
                     uv *= col(sr.su[c], j) * sr.sa;
@@ -616,7 +838,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         const bool valid = entry >= 0 && entry < P.sentinel;
         const float wgt = valid ? (P.row_weight != nullptr ? P.row_weight[entry] : 1.0f) : 0.0f;
         const int64_t bias_row = static_cast<int64_t>(e) * N;
-        uint8_t* stage_buf = staging + (warp - 2) * STAGING_BYTES;
+        uint8_t* stage_buf = staging + (warp - EPI0) * STAGING_BYTES;
         // a warp whose 32 rows are all padding has nothing to store
         const bool any_real = __ballot_sync(0xffffffffu, valid) != 0u;
 #pragma unroll 1
@@ -642,7 +864,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              o[v * 8 + i] = (__uint_as_float(a[v * 8 + i]) * sc[i] + b[i]) * wgt;
+              o[v * 8 + i] = (__uint_as_float(a[acc_pos(v * 8 + i)]) * sc[i] + b[i]) * wgt;
           }
           if constexpr (EPI == Epi::SortedF32) {
             // Stage the warp's 32x32 fp32 block in the 128-byte-swizzled layout
@@ -705,7 +927,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   }
 
   if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SwiGLU) {
-    if (warp >= 2 && lane == 0) ptx::bulk_wait0();  // TMA stores done before smem is released
+    if (warp >= EPI0 && lane == 0) ptx::bulk_wait0();  // TMA stores done before smem is released
   }
   __syncwarp();  // lane-0-only roles rejoin their warp before the aligned barriers
   if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
@@ -728,7 +950,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const KParams P) {
-  gemm_body<EPI, 1, F8>(&tmA, &tmB, &tmO, P);
+  gemm_body<EPI, 1, F8>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
 }
 
 template <Epi EPI, bool F8>
@@ -736,7 +958,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmO, const KParams P) {
-  gemm_body<EPI, 2, F8>(&tmA, &tmB, &tmO, P);
+  gemm_body<EPI, 2, F8>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
+}
+
+// bf16 A x weight-only quantised B (converted to bf16 in shared memory).
+template <Epi EPI, Wq WQ>
+__global__ void __launch_bounds__(cta_threads<WQ>(), 1)
+    grouped_gemm_wq_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmO,
+                           const __grid_constant__ CUtensorMap tmS,
+                           const __grid_constant__ CUtensorMap tmZ, const KParams P) {
+  gemm_body<EPI, 1, false, WQ>(&tmA, &tmB, &tmO, &tmS, &tmZ, P);
 }
 
 // ------------------------------------------------------------------ host --
@@ -763,7 +996,8 @@ EncodeTiledFn get_encode_fn() {
 // strides are in bytes for dims 1..rank-1.
 moe_status_t make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides, const uint32_t* box,
-                      CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                      CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t gd[5], gs[4];
@@ -775,7 +1009,7 @@ moe_status_t make_map(CUtensorMap* m, const void* base, int rank, const uint64_t
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
   const CUresult r = fn(m, dtype, rank, const_cast<void*>(base), gd,
-                        gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", r);
   return MOE_OK;
@@ -791,6 +1025,32 @@ bool use_pairs(const GroupedGemmArgs& a) {
   if (mode == 1) return false;
   if (mode == 2) return a.num_sms >= 2;
   return a.rows_hint >= static_cast<int64_t>(4 * BM) * a.E && a.num_sms >= 2;
+}
+
+// Kernel parameters common to every grouped GEMM launch.
+template <Epi EPI>
+KParams base_params(const GroupedGemmArgs& a, int NB) {
+  KParams P{};
+  P.bias = a.bias;
+  P.out = a.out;
+  P.offsets = a.offsets;
+  P.row_index = a.row_index;
+  P.row_weight = a.row_weight;
+  P.error_word = a.error_word;
+  P.E = a.E;
+  P.N = a.N;
+  P.K = a.K;
+  P.NB = NB;
+  P.sentinel = a.sentinel;
+  P.div = a.div > 0 ? a.div : 1;
+  P.dense_rows = (EPI == Epi::DenseF32) ? static_cast<int32_t>(a.sentinel) : 0;
+  P.gemm1_row_weight = a.gemm1_row_weight;
+  P.a_scale = a.a_scale;
+  P.w_scale = a.w_scale;
+  P.w_scale_per_channel = a.w_scale_per_channel;
+  P.row_amax = a.row_amax;
+  P.w_scale_ld = (EPI == Epi::SwiGLU) ? 2 * a.N : a.N;
+  return P;
 }
 
 template <Epi EPI, bool F8 = false>
@@ -861,26 +1121,7 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   } else {
     tmO = tmA;  // unused
   }
-  KParams P;
-  P.bias = a.bias;
-  P.out = a.out;
-  P.offsets = a.offsets;
-  P.row_index = a.row_index;
-  P.row_weight = a.row_weight;
-  P.error_word = a.error_word;
-  P.E = a.E;
-  P.N = a.N;
-  P.K = a.K;
-  P.NB = NB;
-  P.sentinel = a.sentinel;
-  P.div = a.div > 0 ? a.div : 1;
-  P.dense_rows = (EPI == Epi::DenseF32) ? static_cast<int32_t>(a.sentinel) : 0;
-  P.gemm1_row_weight = a.gemm1_row_weight;
-  P.a_scale = a.a_scale;
-  P.w_scale = a.w_scale;
-  P.w_scale_per_channel = a.w_scale_per_channel;
-  P.row_amax = a.row_amax;
-  P.w_scale_ld = (EPI == Epi::SwiGLU) ? 2 * a.N : a.N;
+  KParams P = base_params<EPI>(a, NB);
   // grouped operands are padded to whole 128-row blocks; the dense one is not
   const int64_t max_blocks = (EPI == Epi::DenseF32) ? ceil_div<int64_t>(a.cap, BM) : a.cap / BM;
   if (max_blocks <= 0) return MOE_OK;
@@ -917,6 +1158,100 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   return check_launch(name);
 }
 
+// bf16 A x weight-only quantised B.  Single-CTA 128 x 256 tiles; the codes,
+// scales and zero points travel by TMA without swizzle into the raw ring.
+template <Epi EPI, Wq WQ>
+moe_status_t launch_gemm_wq(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
+  using G = Geo<1, false, WQ>;
+  using R = WqRing<WQ, EPI == Epi::SwiGLU ? 2 : 1>;
+  constexpr int NREG = EPI == Epi::SwiGLU ? 2 : 1;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(grouped_gemm_wq_kernel<EPI, WQ>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(G::SMEM)) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                       cudaGetErrorString(cudaGetLastError()));
+    attr_done = true;
+  }
+  const int gsize = a.wq_group;
+  const uint32_t gbox = gsize == 32 ? 2u : 1u;  // group rows per 64-row stage
+  const uint64_t KG = static_cast<uint64_t>(a.K / gsize);
+  const uint64_t E = static_cast<uint64_t>(a.E), K = static_cast<uint64_t>(a.K);
+  const uint64_t N = static_cast<uint64_t>(a.N);
+  const uint64_t sb = R::F::SCALE_BYTES;
+  const CUtensorMapDataType sdt =
+      sb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUtensorMap tmA, tmB, tmS, tmZ, tmO;
+  {
+    const uint64_t dims[2] = {K, static_cast<uint64_t>(a.cap)};
+    const uint64_t strides[1] = {K * 2};
+    const uint32_t box[2] = {G::BKE, BM};
+    if (moe_status_t st = make_map(&tmA, a.a, 2, dims, strides, box)) return st;
+  }
+  const uint64_t nbytes = N * R::F::CODE_BITS / 8;  // bytes of one K row of codes (per half)
+  int NB;
+  if constexpr (EPI == Epi::SwiGLU) {
+    // [E, K, 2, N'] viewed (n', half, k, e) for codes, (n, half, g, e) for params
+    const uint64_t cd[4] = {nbytes, 2, K, E};
+    const uint64_t cs[3] = {nbytes, 2 * nbytes, 2 * nbytes * K};
+    const uint32_t cbx[4] = {static_cast<uint32_t>(R::ROW_BYTES), 1, static_cast<uint32_t>(G::BKE), 1};
+    if (moe_status_t st = make_map(&tmB, a.w, 4, cd, cs, cbx, u8, none)) return st;
+    const uint64_t pd[4] = {N, 2, KG, E};
+    const uint64_t ps[3] = {N * sb, 2 * N * sb, 2 * N * sb * KG};
+    const uint32_t pbx[4] = {static_cast<uint32_t>(R::RCOLS), 1, gbox, 1};
+    if (moe_status_t st = make_map(&tmS, a.wq_scale, 4, pd, ps, pbx, sdt, none)) return st;
+    tmZ = tmS;
+    if (a.wq_zero != nullptr) {
+      const uint64_t zs[3] = {N, 2 * N, 2 * N * KG};
+      if (moe_status_t st = make_map(&tmZ, a.wq_zero, 4, pd, zs, pbx, u8, none)) return st;
+    }
+    NB = ceil_div(a.N, MMA_N / 2);
+    // z bf16 [cap, N], one epilogue warp's 32 x 64 block per store
+    const uint64_t od[2] = {N, static_cast<uint64_t>(a.cap)};
+    const uint64_t os[1] = {N * 2};
+    const uint32_t obx[2] = {64, 32};
+    if (moe_status_t st = make_map(&tmO, a.out, 2, od, os, obx)) return st;
+  } else {
+    const uint64_t cd[3] = {nbytes, K, E};
+    const uint64_t cs[2] = {nbytes, nbytes * K};
+    const uint32_t cbx[3] = {static_cast<uint32_t>(R::ROW_BYTES), static_cast<uint32_t>(G::BKE), 1};
+    if (moe_status_t st = make_map(&tmB, a.w, 3, cd, cs, cbx, u8, none)) return st;
+    const uint64_t pd[3] = {N, KG, E};
+    const uint64_t ps[2] = {N * sb, N * sb * KG};
+    const uint32_t pbx[3] = {static_cast<uint32_t>(R::RCOLS), gbox, 1};
+    if (moe_status_t st = make_map(&tmS, a.wq_scale, 3, pd, ps, pbx, sdt, none)) return st;
+    tmZ = tmS;
+    if (a.wq_zero != nullptr) {
+      const uint64_t zs[2] = {N, N * KG};
+      if (moe_status_t st = make_map(&tmZ, a.wq_zero, 3, pd, zs, pbx, u8, none)) return st;
+    }
+    NB = ceil_div(a.N, MMA_N);
+    // fp32 [cap, N] output, 32 x 32 boxes (matches staging)
+    const uint64_t od[2] = {N, static_cast<uint64_t>(a.cap)};
+    const uint64_t os[1] = {N * 4};
+    const uint32_t obx[2] = {32, 32};
+    if (moe_status_t st = make_map(&tmO, a.out, 2, od, os, obx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return st;
+  }
+  KParams P = base_params<EPI>(a, NB);
+  P.wq_G = gsize;
+  P.wq_gbox = static_cast<int32_t>(gbox);
+  P.wq_has_zero = a.wq_zero != nullptr ? 1 : 0;
+  P.wq_raw_tx = NREG * (R::CODES + static_cast<int32_t>(R::RCOLS * sb * gbox) +
+                        (a.wq_zero != nullptr ? static_cast<int32_t>(R::RCOLS * gbox) : 0));
+  const int64_t max_blocks = a.cap / BM;
+  if (max_blocks <= 0) return MOE_OK;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
+  prof_before(name, s);
+  grouped_gemm_wq_kernel<EPI, WQ><<<grid, cta_threads<WQ>(), G::SMEM, s>>>(tmA, tmB, tmO, tmS,
+                                                                            tmZ, P);
+  prof_after(name, s);
+  return check_launch(name);
+}
+
 }  // namespace
 
 moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s) {
@@ -946,6 +1281,28 @@ moe_status_t launch_dense_f32(const GroupedGemmArgs& a, cudaStream_t s) {
 }
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::RowsBF16>(a, "gemm2_rows_bf16", s);
+}
+
+}  // namespace gbmoe
+
+namespace gbmoe {
+
+moe_status_t launch_gemm1_swiglu_wq(const GroupedGemmArgs& a, cudaStream_t s) {
+  switch (a.wq_format) {
+    case 0: return launch_gemm_wq<Epi::SwiGLU, Wq::Int4>(a, "gemm1_swiglu_int4", s);
+    case 1: return launch_gemm_wq<Epi::SwiGLU, Wq::Int8>(a, "gemm1_swiglu_int8", s);
+    case 2: return launch_gemm_wq<Epi::SwiGLU, Wq::Mxfp4>(a, "gemm1_swiglu_mxfp4", s);
+    default: return set_error(MOE_ERR_INVALID_ARG, "weight format %d", a.wq_format);
+  }
+}
+
+moe_status_t launch_gemm2_sorted_wq(const GroupedGemmArgs& a, cudaStream_t s) {
+  switch (a.wq_format) {
+    case 0: return launch_gemm_wq<Epi::SortedF32, Wq::Int4>(a, "gemm2_sorted_int4", s);
+    case 1: return launch_gemm_wq<Epi::SortedF32, Wq::Int8>(a, "gemm2_sorted_int8", s);
+    case 2: return launch_gemm_wq<Epi::SortedF32, Wq::Mxfp4>(a, "gemm2_sorted_mxfp4", s);
+    default: return set_error(MOE_ERR_INVALID_ARG, "weight format %d", a.wq_format);
+  }
 }
 
 }  // namespace gbmoe

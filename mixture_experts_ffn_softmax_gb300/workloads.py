@@ -219,6 +219,59 @@ def make_fp8_weights(spec: MoESpec, device="cpu", seed: int = 0, per_channel: bo
     return {"w13_q": w13, "w2_q": w2, "w13_scale": s13, "w2_scale": s2}
 
 
+def _codes(shape, lo, hi, g, device, dtype):
+    """Uniform integer codes in [lo, hi], drawn in slices along dim 0."""
+    out = torch.empty(shape, dtype=dtype, device=device)
+    step = max(1, (1 << 28) // max(1, out[0].numel()))
+    for r0 in range(0, shape[0], step):
+        sl = out[r0:r0 + step]
+        sl.copy_(torch.randint(lo, hi + 1, sl.shape, generator=g, device=device,
+                               dtype=torch.int32).to(dtype))
+    return out
+
+
+def _pack_nibbles(codes: torch.Tensor) -> torch.Tensor:
+    """int codes 0..15 [..., N] -> uint8 [..., N/2]: column 2j in the low nibble."""
+    c = codes.to(torch.uint8)
+    return c[..., 0::2] | (c[..., 1::2] << 4)
+
+
+def make_wq_weights(spec: MoESpec, fmt: str = "int4", group_size: int = 128, device="cpu",
+                    seed: int = 0, zero: bool = True):
+    """Weight-only quantised expert weights for the layer:
+    int4: codes ~ U{0..15}, zero points ~ U{6..9} (or none: 8), bf16 scales
+          ~ U(0.0035, 0.0052) per (group, column) -- effective std ~0.02;
+    int8: codes ~ U{-128..127}, zero points ~ U{-4..4} (or none), scales
+          ~ U(2.2e-4, 3.2e-4);
+    mxfp4: E2M1 codes ~ U{0..15}, UE8M0 scales ~ U{118..120} per block of 32.
+    Returns codes, scales and zero points for w13 [E, H, 2I] and w2 [E, I, H]."""
+    device = torch.device(device)
+    E, H, I = spec.E, spec.H, spec.I
+    g = _gen(seed + 21, device)
+    out = {"fmt": fmt, "group_size": group_size if fmt != "mxfp4" else 32}
+    G = out["group_size"]
+    for name, K, N in (("w13", H, 2 * I), ("w2", I, H)):
+        if fmt == "int8":
+            out[name + "_q"] = _codes((E, K, N), -128, 127, g, device, torch.int8)
+        else:
+            q = _codes((E, K, N), 0, 15, g, device, torch.uint8)
+            out[name + "_q"] = _pack_nibbles(q)
+            del q
+        if fmt == "mxfp4":
+            out[name + "_scale"] = _codes((E, K // 32, N), 118, 120, g, device, torch.uint8)
+            out[name + "_zero"] = None
+            continue
+        lo, hi = (0.0035, 0.0052) if fmt == "int4" else (2.2e-4, 3.2e-4)
+        out[name + "_scale"] = (torch.rand(E, K // G, N, generator=g, device=device) * (hi - lo)
+                                + lo).bfloat16()
+        if zero:
+            zlo, zhi, zdt = (6, 9, torch.uint8) if fmt == "int4" else (-4, 4, torch.int8)
+            out[name + "_zero"] = _codes((E, K // G, N), zlo, zhi, g, device, zdt)
+        else:
+            out[name + "_zero"] = None
+    return out
+
+
 def make_batched_inputs(spec: BatchedSpec, device="cpu", seed: int = 0):
     """Returns a dict: x [E,T,H] bf16 (rows >= count are NaN), expert_num_tokens
     [E] int32 ~ U{0..T}, w13, w2, biases, row_weight [E,T] fp32 (one component
