@@ -68,6 +68,7 @@ import numpy as np
 
 __all__ = [
     "e4m3_round", "quantize_rows_e4m3", "bf16_round", "forward_fp8",
+    "quantize_groups_e4m3", "forward_fp8_block",
     "unpack_nibbles", "mx_decode", "ue8m0_scale", "dequant_int", "dequant_mx",
     "forward_wq",
     "router_logits", "scores", "group_mask", "topk_select", "route_weights", "route",
@@ -365,6 +366,61 @@ def quantize_rows_e4m3(x):
     scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
     q = e4m3_round(x32 / scale[:, None])
     return q, scale.astype(np.float64)
+
+
+def quantize_groups_e4m3(x, group=128):
+    """Per-(row, group of `group` consecutive columns) FP8 quantisation: each
+    group is quantised as its own row by quantize_rows_e4m3.  Returns (q as
+    fp64 values [M, K], scale [M, K / group] as fp64)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    M, K = x32.shape
+    G = K // group
+    q, s = quantize_rows_e4m3(x32.reshape(M * G, group))
+    return q.reshape(M, K), s.reshape(M, G)
+
+
+def forward_fp8_block(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2_scale,
+                      w13_bias=None, w2_bias=None, block=128):
+    """The FP8 W8A8 layer with block-wise scales ("fused_moe.py 分析", "FP8 W8A8",
+    block-wise: within each K block the dot product of the FP8 codes is
+    multiplied by that block's activation scale and weight scale, and the
+    blocks are summed).  Weight scales [E, K/128, N/128] (128 x 128 blocks);
+    activations quantised per (row, group of 128 along K), z as held in bf16
+    (see forward_fp8):
+        h[r, n] = sum_b (q_x[r, b] . W13q[b, n]) * s_x[r, b] * s_w13[b, n // 128]."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.asarray(topk_weights, dtype=np.float64)
+    ids = np.asarray(topk_ids)
+    M, H = x.shape
+    E = w13_q.shape[0]
+    I = w2_q.shape[1]
+    y = np.zeros((M, H), dtype=np.float64)
+    qx, sx = quantize_groups_e4m3(x, block)
+
+    def block_gemm(q, s, wq, ws):
+        K, N = wq.shape
+        out = np.zeros((q.shape[0], N), dtype=np.float64)
+        for b in range(K // block):
+            ks = slice(b * block, (b + 1) * block)
+            part = q[:, ks] @ np.asarray(wq[ks], dtype=np.float64)       # exact in fp64
+            col_scale = np.repeat(np.asarray(ws[b], dtype=np.float64), block)[:N]
+            out += part * s[:, b][:, None] * col_scale
+        return out
+
+    for e in range(E):
+        t, j = np.nonzero(ids == e)
+        if t.size == 0:
+            continue
+        h = block_gemm(qx[t], sx[t], w13_q[e], w13_scale[e])
+        if w13_bias is not None:
+            h = h + w13_bias[e]
+        z = silu(h[:, :I]) * h[:, I:]
+        qz, sz = quantize_groups_e4m3(bf16_round(z), block)
+        o = block_gemm(qz, sz, w2_q[e], w2_scale[e])
+        if w2_bias is not None:
+            o = o + w2_bias[e]
+        np.add.at(y, t, a[t, j][:, None] * o)
+    return y
 
 
 def bf16_round(v):

@@ -597,6 +597,83 @@ def test_fp8_forward_reduces_to_exact_layer_on_representable_inputs():
     np.testing.assert_allclose(y8t, y8e, rtol=1e-12, atol=1e-14)
 
 
+# ------------------------------------------------------ FP8 block-wise ---
+
+def _e4m3_grid():
+    rng = np.random.default_rng(0)
+    return np.unique(np.abs(oracle.e4m3_round(rng.standard_normal(4000) * 100)))
+
+
+def _exact_group_rows(M, K, group_scales, rng):
+    """Rows whose every 128-column group is E4M3 values (max 448) times a
+    power of two: their per-group quantisation is exact."""
+    grid = _e4m3_grid()
+    x = rng.choice(grid, size=(M, K)) * rng.choice([-1.0, 1.0], size=(M, K))
+    for g in range(K // 128):
+        x[:, g * 128] = 448.0
+        x[:, g * 128:(g + 1) * 128] *= group_scales[:, g][:, None]
+    return x
+
+
+def test_quantize_groups_scales_are_per_group():
+    rng = np.random.default_rng(5)
+    x = _exact_group_rows(2, 384, np.array([[1.0, 0.25, 8.0], [2.0 ** -6, 1.0, 0.5]]), rng)
+    q, sc = oracle.quantize_groups_e4m3(x, 128)
+    np.testing.assert_array_equal(sc, [[1.0, 0.25, 8.0], [2.0 ** -6, 1.0, 0.5]])
+    np.testing.assert_array_equal(q * np.repeat(sc, 128, axis=1), x)
+    # a group's codes depend on that group only
+    x2 = x.copy()
+    x2[:, 128:256] *= 3.0
+    q2, sc2 = oracle.quantize_groups_e4m3(x2, 128)
+    np.testing.assert_array_equal(q2[:, :128], q[:, :128])
+    np.testing.assert_array_equal(q2[:, 256:], q[:, 256:])
+    np.testing.assert_array_equal(sc2[:, [0, 2]], sc[:, [0, 2]])
+
+
+def _block_case(rng, E=3, H=256, I=128, M=6, k=2):
+    w13 = oracle.e4m3_round(rng.standard_normal((E, H, 2 * I)) * 2)
+    w2 = oracle.e4m3_round(rng.standard_normal((E, I, H)) * 2)
+    ids = np.array([rng.choice(E, k, replace=False) for _ in range(M)])
+    tw = rng.random((M, k))
+    return w13, w2, ids, tw
+
+
+def test_fp8_block_reduces_to_per_channel_layer():
+    """Weight block scales constant along K and equal group maxima within a
+    row: the block-wise layer is the per-channel FP8 layer (one z group)."""
+    rng = np.random.default_rng(6)
+    E, H, I, M = 3, 256, 128, 6
+    w13, w2, ids, tw = _block_case(rng, E, H, I, M)
+    row_scale = 2.0 ** rng.integers(-8, -3, size=M).astype(float)
+    x = _exact_group_rows(M, H, np.stack([row_scale, row_scale], 1), rng)
+    c13 = rng.uniform(0.005, 0.02, size=(E, 2 * I // 128))
+    c2 = rng.uniform(0.005, 0.02, size=(E, H // 128))
+    s13 = np.repeat(c13[:, None, :], H // 128, axis=1)
+    s2 = np.repeat(c2[:, None, :], I // 128, axis=1)
+    yb = oracle.forward_fp8_block(x, tw, ids, w13, w2, s13, s2)
+    yc = oracle.forward_fp8(x, tw, ids, w13, w2, np.repeat(c13, 128, axis=1),
+                            np.repeat(c2, 128, axis=1))
+    np.testing.assert_allclose(yb, yc, rtol=1e-12, atol=1e-12 * np.abs(yc).max())
+
+
+def test_fp8_block_matches_exact_layer_within_quantisation_error():
+    """Exactly quantisable x with different group scales, weight block scales
+    varying along K: the block-wise layer equals the exact layer on the
+    dequantised weights up to the E4M3 rounding of z (relative L2 ~2.4e-2)."""
+    rng = np.random.default_rng(0)
+    E, H, I, M = 3, 256, 128, 6
+    w13, w2, ids, tw = _block_case(rng, E, H, I, M)
+    x = _exact_group_rows(M, H, 2.0 ** rng.integers(-8, -4, size=(M, 2)).astype(float), rng)
+    s13 = rng.choice([0.5, 2.0], size=(E, H // 128, 2 * I // 128)) * 0.01
+    s2 = rng.choice([0.5, 2.0], size=(E, I // 128, H // 128)) * 0.01
+    yb = oracle.forward_fp8_block(x, tw, ids, w13, w2, s13, s2)
+    W13 = w13 * np.repeat(np.repeat(s13, 128, axis=1), 128, axis=2)
+    W2 = w2 * np.repeat(np.repeat(s2, 128, axis=1), 128, axis=2)
+    ye = oracle.forward(x, tw, ids, W13, W2)
+    rel = np.linalg.norm(yb - ye) / np.linalg.norm(ye)
+    assert rel < 0.06, rel
+
+
 # ------------------------------------------------- weight-only quantisation ---
 
 def _bf16_rne_bits(v):
@@ -701,7 +778,10 @@ def _pins_fail(golden_dir):
               test_mx_element_values_against_the_format_tables,
               test_dequant_int4_groups_and_zero_points_by_hand,
               test_dequant_rounds_to_bf16_once,
-              test_dequant_mx_blocks_of_32_by_hand]
+              test_dequant_mx_blocks_of_32_by_hand,
+              test_quantize_groups_scales_are_per_group,
+              test_fp8_block_reduces_to_per_channel_layer,
+              test_fp8_block_matches_exact_layer_within_quantisation_error]
     for c in checks:
         try:
             c()
@@ -801,6 +881,21 @@ def _mut_mx_bias(codes, fmt):
                            2.0 ** (e - bias) * (1.0 + m / (1 << mbits)))
 
 
+def _mut_groups_row_scale(x, group=128):
+    q, sc = om.quantize_rows_e4m3(x)                 # wrong: one scale per row
+    return q, np.repeat(sc[:, None], np.asarray(x).shape[1] // group, axis=1)
+
+
+_ORIG_BLOCK = om.forward_fp8_block
+
+
+def _mut_block_first_scale(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2_scale,
+                           w13_bias=None, w2_bias=None, block=128):
+    s13 = np.repeat(np.asarray(w13_scale)[:, :1], np.asarray(w13_scale).shape[1], axis=1)
+    return _ORIG_BLOCK(x, topk_weights, topk_ids, w13_q, w2_q, s13, w2_scale, w13_bias,
+                       w2_bias, block)                 # wrong: first K block's scale everywhere
+
+
 _orig_align = om.align
 _ORIG_FFN = om.expert_ffn
 
@@ -818,6 +913,8 @@ _ORIG_FFN = om.expert_ffn
     ("dequant_int", _mut_dequant_group_cyclic),
     ("dequant_int", _mut_dequant_unrounded),
     ("mx_decode", _mut_mx_bias),
+    ("quantize_groups_e4m3", _mut_groups_row_scale),
+    ("forward_fp8_block", _mut_block_first_scale),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, golden_dir, target, mutant):
     monkeypatch.setattr(om, target, mutant)
