@@ -501,7 +501,32 @@ def measure_next_rows(step, spec, K, W, world, pk):
                                     "achieved": round(ach, 1), "peak": round(peak8, 1),
                                     "unit": "TFLOP/s", "frac": round(ach / peak8, 4),
                                     "peak_source": "measured sustained bf16 x 2 (nominal ratio)"}}
-    del q, ws8
+    del q
+
+    # the same with 128 x 128 weight-block scales (activations per row and
+    # 128-wide group)
+    qb = wl.make_fp8_weights(spec, device=dev, block=True)
+
+    def fp8_block():
+        pkg.moe_forward_fp8(d["hidden"], step.w, step.ids, qb["w13_q"], qb["w2_q"],
+                            qb["w13_scale"], qb["w2_scale"], None, None, ws8, step.out)
+
+    ms = max_over_ranks(time_steps(fp8_block, K, W, world) / K, world)
+    pkg.profiler_start()
+    for _ in range(K):
+        fp8_block()
+    prof = pkg.profiler_stop()
+    us = {k: 1e3 * v[1] / max(v[0], 1) for k, v in prof.items()}
+    ach = f1 / (us["gemm1_swiglu_fp8_block"] * 1e-6) / 1e12
+    out["fp8_w8a8_block"] = {"ms_per_step": round(ms, 4),
+                             "tokens_per_s": round(spec.M * world / (ms / 1e3), 1),
+                             "tflops": round(spec.flops() / (ms / 1e3) / 1e12, 1),
+                             "kernels_us": {k: round(v, 2) for k, v in us.items()},
+                             "roofline": {"kernel": "gemm1_swiglu_fp8_block", "bound": "tensor",
+                                          "achieved": round(ach, 1), "peak": round(peak8, 1),
+                                          "unit": "TFLOP/s", "frac": round(ach / peak8, 4),
+                                          "peak_source": "measured sustained bf16 x 2 (nominal ratio)"}}
+    del qb, ws8
     return out
 
 

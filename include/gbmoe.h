@@ -262,20 +262,31 @@ GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_we
  * Activations (each routed row of x, and of z as held in bf16) are
  * quantised dynamically per row: scale = fp32(max|row| / 448) (1 for an
  * all-zero row), q = e4m3(fp32(row / scale)), round to nearest even,
- * saturating; the quotient is the correctly rounded fp32 one.  Weight scales are per expert ([E]) or per output
- * channel ([E, 2I] and [E, H]).  Block-wise (128 x 128) weight scales are
- * not offered.
+ * saturating; the quotient is the correctly rounded fp32 one.  Weight scales
+ * are per expert, per output channel, or per 128 x 128 block (scale_mode).
+ * Block mode follows the page's block-wise path: within each 128-wide K
+ * block the FP8 dot product is multiplied by that block's activation scale
+ * and weight scale, and the blocks are summed; activations are then
+ * quantised per (row, group of 128 along K) instead of per row.
  *  w13, w2       device E4M3 bytes [E, H, 2I] and [E, I, H]
  *  biases        bf16 as in moe_forward, or NULL
  *  workspace     >= moe_workspace_size_fp8(...) bytes, 256-byte aligned
- * Limits: as moe_forward, and H % 16 == 0, I % 16 == 0.
+ * Limits: as moe_forward, and H % 16 == 0, I % 16 == 0 (block mode:
+ * H % 128 == 0, I % 128 == 0).
  */
+typedef enum {
+  MOE_FP8_SCALE_EXPERT = 0,  /* w13_scale, w2_scale [E]                               */
+  MOE_FP8_SCALE_CHANNEL = 1, /* [E, 2I] and [E, H], per output channel               */
+  MOE_FP8_SCALE_BLOCK = 2    /* [E, H/128, 2I/128] and [E, I/128, H/128], per 128 x 128
+                                block of the weights; activations then quantised per
+                                (row, group of 128 along K)                           */
+} moe_fp8_scale_mode_t;
 typedef struct {
   const void* w13;
   const void* w2;
   const float* w13_scale;
   const float* w2_scale;
-  int32_t scale_per_channel; /* 0: scales [E]; 1: [E, 2I] and [E, H] */
+  int32_t scale_mode; /* moe_fp8_scale_mode_t */
 } moe_fp8_weights_t;
 GBMOE_API moe_status_t moe_workspace_size_fp8(int64_t M, int32_t H, int32_t I, int32_t E,
                                               int32_t top_k, size_t* bytes);

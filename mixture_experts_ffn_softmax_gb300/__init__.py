@@ -194,19 +194,21 @@ def moe_forward_fp8(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: 
                     workspace: Optional[torch.Tensor] = None,
                     out: Optional[torch.Tensor] = None, stream=None):
     """FP8 W8A8 layer: w13_q [E, H, 2I] / w2_q [E, I, H] E4M3 (torch.float8_e4m3fn
-    or uint8 bytes), scales fp32 per expert [E] or per output channel
-    ([E, 2I] / [E, H]); activations are quantised per row on the GPU."""
+    or uint8 bytes), scales fp32 per expert [E], per output channel
+    ([E, 2I] / [E, H]) or per 128 x 128 block ([E, H/128, 2I/128] /
+    [E, I/128, H/128]); activations are quantised on the GPU per row, or per
+    (row, group of 128) with block scales."""
     M, H = hidden.shape
     E, _, I2 = w13_q.shape
     I = I2 // 2
     k = topk_ids.shape[1]
-    per_channel = int(w13_scale.dim() == 2)
+    scale_mode = w13_scale.dim() - 1          # 0 per expert, 1 per channel, 2 per block
     assert w13_scale.dtype == torch.float32 and w2_scale.dtype == torch.float32
     if workspace is None:
         workspace = alloc_workspace(workspace_size_fp8(M, H, I, E, k), hidden.device)
     if out is None:
         out = torch.empty_like(hidden)
-    wts = _lib.Fp8Weights(_ptr(w13_q), _ptr(w2_q), _ptr(w13_scale), _ptr(w2_scale), per_channel)
+    wts = _lib.Fp8Weights(_ptr(w13_q), _ptr(w2_q), _ptr(w13_scale), _ptr(w2_scale), scale_mode)
     _check(lib().moe_forward_fp8(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E, k,
                                  ctypes.byref(wts), _ptr(w13_bias), _ptr(w2_bias),
                                  _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)),

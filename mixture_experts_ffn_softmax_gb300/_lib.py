@@ -19,7 +19,7 @@ class ForwardOpts(ctypes.Structure):
 
 class Fp8Weights(ctypes.Structure):
     _fields_ = [("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
-                ("w2_scale", ctypes.c_void_p), ("scale_per_channel", ctypes.c_int32)]
+                ("w2_scale", ctypes.c_void_p), ("scale_mode", ctypes.c_int32)]
 
 
 class WqWeights(ctypes.Structure):

@@ -555,10 +555,11 @@ Fp8Layout fp8_layout(int64_t Mc, int32_t H, int32_t I, int32_t E, int32_t k) {
   L.scratch = take(align_scratch_bytes(Rc, E));
   L.inv = take(sizeof(int32_t) * Rc);
   L.a8 = take(static_cast<size_t>(L.cap) * H);
-  L.a_scale = take(sizeof(float) * L.cap);
+  // scales per sorted row, or per (row, 128-wide group) in block mode
+  L.a_scale = take(sizeof(float) * L.cap * static_cast<size_t>(ceil_div(H, 128)));
   L.z = take(sizeof(bf16) * L.cap * I);
   L.z8 = take(static_cast<size_t>(L.cap) * I);
-  L.z_scale = take(sizeof(float) * L.cap);
+  L.z_scale = take(sizeof(float) * L.cap * static_cast<size_t>(ceil_div(I, 128)));
   L.o = take(sizeof(float) * L.cap * H);
   L.total = off;
   return L;
@@ -589,8 +590,13 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
   if (M == 0) return MOE_OK;
   if (!w || !w->w13 || !w->w2 || !w->w13_scale || !w->w2_scale)
     return set_error(MOE_ERR_INVALID_ARG, "null FP8 weights or scales");
-  if (w->scale_per_channel != 0 && w->scale_per_channel != 1)
-    return set_error(MOE_ERR_INVALID_ARG, "scale_per_channel must be 0 or 1");
+  if (w->scale_mode < MOE_FP8_SCALE_EXPERT || w->scale_mode > MOE_FP8_SCALE_BLOCK)
+    return set_error(MOE_ERR_INVALID_ARG, "scale_mode=%d", w->scale_mode);
+  const bool block = w->scale_mode == MOE_FP8_SCALE_BLOCK;
+  if (block && (H % 128 != 0 || I % 128 != 0 || I > 32768))
+    return set_error(MOE_ERR_INVALID_ARG,
+                     "block-wise FP8 scales need H and I multiples of 128, I <= 32768 (H=%d I=%d)",
+                     H, I);
   if (!hidden || !topk_weights || !topk_ids || !workspace || !out)
     return set_error(MOE_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(hidden) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(out) ||
@@ -629,7 +635,11 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     float* a_scale = at<float>(workspace, L.a_scale);
     float* z_scale = at<float>(workspace, L.z_scale);
     QuantTokensArgs qa{x + c0 * H, inv, Mc, top_k, H, a8, a_scale, z_scale};
-    if (moe_status_t st = launch_quant_tokens_fp8(qa, s)) return st;
+    if (block) {
+      if (moe_status_t st = launch_quant_tokens_group_fp8(qa, cap, I / 128, s)) return st;
+    } else {
+      if (moe_status_t st = launch_quant_tokens_fp8(qa, s)) return st;
+    }
     bf16* z = at<bf16>(workspace, L.z);
     GroupedGemmArgs g1{};
     g1.a = reinterpret_cast<const bf16*>(a8);
@@ -648,13 +658,15 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     g1.rows_hint = Rc;
     g1.a_scale = a_scale;
     g1.w_scale = w->w13_scale;
-    g1.w_scale_per_channel = w->scale_per_channel;
+    g1.w_scale_per_channel = w->scale_mode == MOE_FP8_SCALE_CHANNEL;
     g1.row_amax = z_scale;
-    if (moe_status_t st = launch_gemm1_swiglu_fp8(g1, s)) return st;
+    if (moe_status_t st = block ? launch_gemm1_swiglu_fp8_block(g1, s) : launch_gemm1_swiglu_fp8(g1, s))
+      return st;
     // quantise z per row for the second GEMM (amax taken by GEMM1)
     uint8_t* z8 = at<uint8_t>(workspace, L.z8);
     QuantSortedArgs qz{z, sorted, offsets, E, static_cast<int32_t>(Rc), I, cap, z8, z_scale};
-    if (moe_status_t st = launch_quant_sorted_fp8(qz, s)) return st;
+    if (moe_status_t st = block ? launch_quant_sorted_group_fp8(qz, s) : launch_quant_sorted_fp8(qz, s))
+      return st;
     float* o = at<float>(workspace, L.o);
     GroupedGemmArgs g2{};
     g2.a = reinterpret_cast<const bf16*>(z8);
@@ -675,8 +687,9 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     g2.rows_hint = Rc;
     g2.a_scale = z_scale;
     g2.w_scale = w->w2_scale;
-    g2.w_scale_per_channel = w->scale_per_channel;
-    if (moe_status_t st = launch_gemm2_sorted_fp8(g2, s)) return st;
+    g2.w_scale_per_channel = w->scale_mode == MOE_FP8_SCALE_CHANNEL;
+    if (moe_status_t st = block ? launch_gemm2_sorted_fp8_block(g2, s) : launch_gemm2_sorted_fp8(g2, s))
+      return st;
     if (moe_status_t st = launch_reduce_sorted(o, inv, Mc, top_k, H, y + c0 * H, s)) return st;
   }
   return MOE_OK;

@@ -130,6 +130,12 @@ struct QuantSortedArgs {
   float* scale_io;        // [cap]
 };
 moe_status_t launch_quant_sorted_fp8(const QuantSortedArgs& a, cudaStream_t s);
+// The same per (row, group of 128 columns), scales group-major [H/128][ld]
+// (tokens: ld = cap, also zeroing zgroups z-amax slots per sorted row;
+// sorted rows: ld = cap, scale_io group-major).
+moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld, int zgroups,
+                                           cudaStream_t s);
+moe_status_t launch_quant_sorted_group_fp8(const QuantSortedArgs& a, cudaStream_t s);
 
 // Weight-only quantised weights -> bf16 [E, K, N] (wq.cu).  format: 0 int4,
 // 1 int8, 2 MX FP4; codes, scale [E, K/G, N], zero [E, K/G, N] or null.
@@ -199,6 +205,11 @@ moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s);
 // weighted row is added into row row_index[p] / div with vector fp32 atomics.
 moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+// FP8 with block-wise scales: a.w_scale [E, K/128, N'/128] per 128 x 128
+// weight block, a.a_scale [K/128][cap] per (sorted row, 128-wide K group),
+// a.row_amax (GEMM1) [N/128][cap] z amax per row and 128-column group.
+moe_status_t launch_gemm1_swiglu_fp8_block(const GroupedGemmArgs& a, cudaStream_t s);
+moe_status_t launch_gemm2_sorted_fp8_block(const GroupedGemmArgs& a, cudaStream_t s);
 // bf16 A x weight-only quantised w (a.wq_format), B converted to bf16 in
 // shared memory: GEMM1 with the SwiGLU epilogue, GEMM2 with sorted fp32 rows.
 moe_status_t launch_gemm1_swiglu_wq(const GroupedGemmArgs& a, cudaStream_t s);

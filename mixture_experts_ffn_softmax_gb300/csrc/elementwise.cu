@@ -424,7 +424,124 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   }
 }
 
+// Per-(row, group of 128) quantisation ("fused_moe.py 分析", FP8 W8A8,
+// block-wise activations).  Lane l holds 8 elements; each half-warp covers
+// one 128-wide group, reduced over its 16 lanes.  Scales are stored group
+// major, scale[g * ld + row], so a warp's 32 rows read one line in the GEMM.
+
+constexpr int kMaxGroups = 256;  // 128-wide groups per row the z quantisation handles (H <= 32768)
+
+__device__ __forceinline__ float half_warp_amax(uint32_t mb) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+  return __uint_as_float(mb << 16);
+}
+
+// Token rows: each token's groups are quantised once and the codes written
+// to each of its k sorted rows; the z amax slots of those rows are zeroed.
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quant_tokens_group_fp8_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ inv,
+                                  int64_t M, int k, int H, uint8_t* __restrict__ q8,
+                                  float* __restrict__ scale, int64_t ld, float* __restrict__ zmax,
+                                  int zgroups) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
+  for (int64_t t = warp0; t < M; t += nwarps) {
+    const int32_t mypos = lane < k ? __ldg(inv + t * k + lane) : -1;
+    for (int b = 0; b < H; b += 256) {  // two groups per pass, the same count on every lane
+      const int v = b + lane * 8;
+      const bool in = v < H;
+      const uint4 u = in ? __ldg(reinterpret_cast<const uint4*>(x + t * H + v)) : make_uint4(0, 0, 0, 0);
+      uint32_t m2 = absmax_bits8(u, 0u);
+      const RowScale rs = row_scale(half_warp_amax(max(m2 & 0xffffu, m2 >> 16)));
+      const uint2 c = e4m3x8(u, rs);
+      const int g = v / 128;
+      for (int j = 0; j < k; ++j) {
+        const int32_t pos = j < 32 ? __shfl_sync(0xffffffffu, mypos, j) : __ldg(inv + t * k + j);
+        if (pos < 0 || !in) continue;
+        *reinterpret_cast<uint2*>(q8 + static_cast<int64_t>(pos) * H + v) = c;
+        if ((lane & 15) == 0) scale[static_cast<int64_t>(g) * ld + pos] = rs.s;
+      }
+    }
+    if (zmax != nullptr) {
+      for (int j = 0; j < k; ++j) {
+        const int32_t pos = j < 32 ? __shfl_sync(0xffffffffu, mypos, j) : __ldg(inv + t * k + j);
+        if (pos < 0) continue;
+        for (int g = lane; g < zgroups; g += 32) zmax[static_cast<int64_t>(g) * ld + pos] = 0.f;
+      }
+    }
+  }
+}
+
+// Sorted rows of z, one pass: each group's amax was taken by GEMM1's
+// epilogue (scale_io[g * ld + p] holds it on entry, the group scale on exit).
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quant_sorted_group_fp8_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ index,
+                                  const int32_t* __restrict__ offsets, int E, int32_t sentinel,
+                                  int H, int64_t cap, uint8_t* __restrict__ q8,
+                                  float* __restrict__ scale_io) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = min(static_cast<int64_t>(offsets[E]), cap);
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
+  const int groups = H / 128;
+  for (int64_t p = warp0; p < rows; p += nwarps) {
+    const int32_t idx = index[p];
+    if (idx < 0 || idx >= sentinel) continue;  // padding row
+    // the row's group amaxes, read once: group g is lane g % 32, slot g / 32
+    float am[kMaxGroups / 32];
+#pragma unroll
+    for (int j = 0; j < kMaxGroups / 32; ++j) {
+      const int g = lane + 32 * j;
+      am[j] = g < groups ? scale_io[static_cast<int64_t>(g) * cap + p] : 0.f;
+    }
+    __syncwarp();  // all reads of the row's amaxes before any scale is written
+    for (int b = 0; b < H; b += 256) {
+      const int v = b + lane * 8;
+      const bool in = v < H;
+      const int g = v / 128;
+      const int gh = b / 128 + (lane >> 4);        // this half-warp's group
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxGroups / 32; ++j) {
+        const float a = __shfl_sync(0xffffffffu, am[j], gh & 31);
+        if ((gh >> 5) == j) amax = a;
+      }
+      const RowScale rs = row_scale(in ? amax : 0.f);
+      if (in) {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src + p * H + v));
+        *reinterpret_cast<uint2*>(q8 + p * H + v) = e4m3x8(u, rs);
+        if ((lane & 15) == 0) scale_io[static_cast<int64_t>(g) * cap + p] = rs.s;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld, int zgroups,
+                                           cudaStream_t s) {
+  if (a.M <= 0) return MOE_OK;
+  const int64_t want = ceil_div<int64_t>(a.M, kQuantWarps);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
+  prof_before("quant_tokens_fp8", s);
+  quant_tokens_group_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(
+      a.x, a.inv, a.M, a.k, a.H, a.q8, a.scale, ld, a.row_amax, zgroups);
+  prof_after("quant_tokens_fp8", s);
+  return check_launch("quant_tokens_fp8");
+}
+
+moe_status_t launch_quant_sorted_group_fp8(const QuantSortedArgs& a, cudaStream_t s) {
+  if (a.cap <= 0) return MOE_OK;
+  const int64_t want = ceil_div<int64_t>(a.cap, kQuantWarps);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
+  prof_before("quant_z_fp8", s);
+  quant_sorted_group_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(
+      a.src, a.index, a.offsets, a.E, a.sentinel, a.H, a.cap, a.q8, a.scale_io);
+  prof_after("quant_z_fp8", s);
+  return check_launch("quant_z_fp8");
+}
 
 moe_status_t launch_quant_tokens_fp8(const QuantTokensArgs& a, cudaStream_t s) {
   if (a.M <= 0) return MOE_OK;

@@ -157,6 +157,9 @@ struct KParams {
   // weight-only quantised B: group size along K, group rows per 64-row
   // stage (1 or 2), zero points present, bytes per raw stage
   int32_t wq_G, wq_gbox, wq_has_zero, wq_raw_tx;
+  // block-scaled FP8: activation scales [K/128][a_ld] (group-major), weight
+  // scales [E][K/128][w_scale_ld] per 128 x 128 block
+  int64_t bs_a_ld;
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
@@ -335,7 +338,7 @@ __device__ __forceinline__ void swiglu_prefetch(const KParams& P, int e, int n_b
   }
 }
 
-template <Epi EPI, int CG, bool F8, Wq WQ = Wq::None>
+template <Epi EPI, int CG, bool F8, Wq WQ = Wq::None, bool BS = false>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                           const CUtensorMap* tmO, const CUtensorMap* tmS,
                                           const CUtensorMap* tmZ, const KParams& P) {
@@ -345,6 +348,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   constexpr bool WQM = WQ != Wq::None;
   constexpr int CONV = conv_warps<WQ>();
   constexpr int EPI0 = 2 + CONV;  // first epilogue warp
+  constexpr int NEPI = BS ? 16 : EPI_WARPS;  // epilogue warps
   // Int4 / MX B tiles hold each aligned group of 8 columns in the order
   // 0 4 1 5 2 6 3 7 (wq_pair_pos), and so does the accumulator: the epilogue
   // reads column n of a group from position wq_pair_pos(n)
@@ -401,7 +405,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ctl.tmem_full[a], 1);
-      ptx::mbar_init(&ctl.tmem_empty[a], CG * EPI_WARPS);
+      ptx::mbar_init(&ctl.tmem_empty[a], CG * NEPI);
     }
     ctl.abort = 0;
     ptx::fence_barrier_init();
@@ -664,10 +668,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = unit; t < total_tiles && ok; t += units) {
-        if (!bounded_wait(&ctl.tmem_empty[acc], acc_phase ^ 1u, &ctl.abort, P.error_word)) break;
+        // block-scaled FP8: every K stage is its own accumulation, into the
+        // two accumulators in turn, handed to the epilogue stage by stage
+        if (!BS && !bounded_wait(&ctl.tmem_empty[acc], acc_phase ^ 1u, &ctl.abort, P.error_word)) break;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
+        uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
         for (int kb = 0; kb < KB; ++kb) {
+          if constexpr (BS) {
+            if (!bounded_wait(&ctl.tmem_empty[acc], acc_phase ^ 1u, &ctl.abort, P.error_word)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
+          }
           if (!bounded_wait(&ctl.full[stage], phase, &ctl.abort, P.error_word)) {
             ok = false;
             break;
@@ -683,7 +697,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             // CHUNK_BYTES apart, 8-row k groups 1024 bytes apart.
             const uint64_t bdesc =
                 ptx::smem_desc_sw128(sb + ks * G::B_KSTEP, G::CHUNK_BYTES, 1024);
-            const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
+            const uint32_t accum = (BS ? ks : (kb | ks)) != 0 ? 1u : 0u;
             if constexpr (CG == 2 && F8) ptx::mma_e4m3_pair(d_tmem, adesc, bdesc, G::IDESC, accum);
             else if constexpr (CG == 2) ptx::mma_bf16_pair(d_tmem, adesc, bdesc, G::IDESC, accum);
             else if constexpr (F8) ptx::mma_e4m3(d_tmem, adesc, bdesc, G::IDESC, accum);
@@ -695,13 +709,22 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             stage = 0;
             phase ^= 1u;
           }
+          if constexpr (BS) {
+            ptx::mma_commit(&ctl.tmem_full[acc]);
+            if (++acc == 2) {
+              acc = 0;
+              acc_phase ^= 1u;
+            }
+          }
         }
         if (!ok) break;
-        if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.tmem_full[acc], 0x3);
-        else ptx::mma_commit(&ctl.tmem_full[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
+        if constexpr (!BS) {
+          if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.tmem_full[acc], 0x3);
+          else ptx::mma_commit(&ctl.tmem_full[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
         }
       }
     }
@@ -724,6 +747,135 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           ptx::mbar_arrive(&ctl.tmem_empty[a]);
       }
     };
+    if constexpr (BS) {
+      // ------------------------------------------- block-scaled FP8 epilogue --
+      // "fused_moe.py 分析", FP8 W8A8, block-wise: each K block's dot product
+      // (one stage's accumulator) times that block's activation scale (per
+      // row and 128-wide K group) and weight scale (per 128 x 128 block),
+      // summed over the K blocks in registers.  This warp's four 32-column
+      // accumulator chunks: SwiGLU gate [h*64, +64) and up [128 + h*64, +64);
+      // otherwise [h*128, +128).
+      // CH accumulator chunks of 32 columns per warp: the quadrant's 8
+      // chunks split over its NEPI / 4 warps (SwiGLU: matching gate and up
+      // chunks, the gate ones first)
+      constexpr int CH = 8 / (NEPI / 4);
+      const int sub = (warp - EPI0) >> 2;
+      auto chunk_col = [&](int c) {
+        if constexpr (EPI == Epi::SwiGLU)
+          return c < CH / 2 ? 32 * (sub * (CH / 2) + c) : MMA_N / 2 + 32 * (sub * (CH / 2) + c - CH / 2);
+        else
+          return 32 * (sub * CH + c);
+      };
+      bool ok = true;
+      for (int t = unit; t < total_tiles && ok; t += units) {
+        int e, row0, nb;
+        bool mine;
+        tile_of(t, e, row0, nb, mine);
+        const int64_t p = row0 + row;
+        const int32_t entry = P.row_index[p];
+        const bool real = entry >= 0 && entry < P.sentinel;
+        const int N = P.N;
+        // weight blocks: SwiGLU gate block nb and up block N/128 + nb; the
+        // other GEMM's 256-column tile spans blocks 2 nb and 2 nb + 1 (a
+        // block past N stores nothing; its scale load is kept in range)
+        const int blk_a = (EPI == Epi::SwiGLU) ? nb : min(2 * nb + (sub * CH * 32) / 128, P.w_scale_ld - 1);
+        const int blk_b = (EPI == Epi::SwiGLU) ? N / 128 + nb : blk_a;
+        const float* wsc = P.w_scale + static_cast<int64_t>(e) * KB * P.w_scale_ld;
+        float accv[CH][32];
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) accv[c][j] = 0.f;
+        for (int kb = 0; kb < KB; ++kb) {
+          // the block's scales, loaded before the wait for its accumulator
+          const float sa = P.a_scale[static_cast<int64_t>(kb) * P.bs_a_ld + p];
+          const float swa = __ldg(wsc + kb * P.w_scale_ld + blk_a);
+          const float swb = __ldg(wsc + kb * P.w_scale_ld + blk_b);
+          const bool got = bounded_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, P.error_word);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t taddr =
+              tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * MMA_N);
+          const float sca = sa * swa, scb = sa * swb;
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            const float sc = (EPI == Epi::SwiGLU && c >= CH / 2) ? scb : sca;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {  // 16 columns at a time (register budget)
+              uint32_t v[16];
+              ptx::tmem_ld_16cols(taddr + chunk_col(c) + 16 * hh, v);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                accv[c][16 * hh + j] = fmaf(__uint_as_float(v[j]), sc, accv[c][16 * hh + j]);
+            }
+          }
+          release_acc(acc);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+        if (!ok || !mine || !real) continue;
+        if constexpr (EPI == Epi::SwiGLU) {
+          bf16* z = reinterpret_cast<bf16*>(P.out);
+          const int64_t brow = static_cast<int64_t>(e) * 2 * N;
+          uint32_t zmax2 = 0;
+#pragma unroll
+          for (int c = 0; c < CH / 2; ++c) {
+            const int n0 = nb * (MMA_N / 2) + chunk_col(c);  // z column of the chunk
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int n = n0 + 8 * v;
+              if (n >= N) break;
+              float bg[8], bu[8];
+              load_bias8(P.bias, brow + n, true, bg);
+              load_bias8(P.bias, brow + N + n, true, bu);
+              uint4 pk;
+              uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int j = 8 * v + 2 * i;
+                const float z0 = silu_f(accv[c][j] + bg[2 * i]) * (accv[c + CH / 2][j] + bu[2 * i]);
+                const float z1 = silu_f(accv[c][j + 1] + bg[2 * i + 1]) *
+                                 (accv[c + CH / 2][j + 1] + bu[2 * i + 1]);
+                w[i] = pack_bf16x2(z0, z1);
+                zmax2 = __vmaxu2(zmax2, w[i] & 0x7fff7fffu);
+              }
+              *reinterpret_cast<uint4*>(z + p * N + n) = pk;
+            }
+          }
+          // the row's amax over this z group (the tile's 128 z columns)
+          const uint32_t m = max(zmax2 & 0xffffu, zmax2 >> 16) << 16;
+          if (m != 0u && P.row_amax != nullptr)
+            atomicMax(reinterpret_cast<unsigned int*>(P.row_amax) +
+                          static_cast<int64_t>(nb) * P.bs_a_ld + p,
+                      m);
+        } else {
+          float* o = reinterpret_cast<float*>(P.out);
+          const float wgt = P.row_weight != nullptr ? P.row_weight[entry] : 1.0f;
+          const int64_t brow = static_cast<int64_t>(e) * N;
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int n = nb * MMA_N + chunk_col(c) + 8 * v;
+              if (n >= N) break;
+              float b[8];
+              load_bias8(P.bias, brow + n, true, b);
+              float4* d = reinterpret_cast<float4*>(o + p * N + n);
+              d[0] = make_float4((accv[c][8 * v] + b[0]) * wgt, (accv[c][8 * v + 1] + b[1]) * wgt,
+                                 (accv[c][8 * v + 2] + b[2]) * wgt, (accv[c][8 * v + 3] + b[3]) * wgt);
+              d[1] = make_float4((accv[c][8 * v + 4] + b[4]) * wgt, (accv[c][8 * v + 5] + b[5]) * wgt,
+                                 (accv[c][8 * v + 6] + b[6]) * wgt, (accv[c][8 * v + 7] + b[7]) * wgt);
+            }
+          }
+        }
+      }
+    } else
     for (int t = unit; t < total_tiles; t += units) {
       int e, row0, nb;
       bool mine;
@@ -961,6 +1113,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   gemm_body<EPI, 2, F8>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
 }
 
+// FP8 with block-wise (128 x 128) weight scales and per-(row, 128-group)
+// activation scales: single-CTA tiles, one accumulation per K stage.
+constexpr int BS_THREADS = 64 + 16 * 32;  // producer + MMA + 16 epilogue warps
+
+template <Epi EPI>
+__global__ void __launch_bounds__(BS_THREADS, 1)
+    grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const KParams P) {
+  gemm_body<EPI, 1, true, Wq::None, true>(&tmA, &tmB, &tmB, nullptr, nullptr, P);
+}
+
 // bf16 A x weight-only quantised B (converted to bf16 in shared memory).
 template <Epi EPI, Wq WQ>
 __global__ void __launch_bounds__(cta_threads<WQ>(), 1)
@@ -1053,13 +1216,47 @@ KParams base_params(const GroupedGemmArgs& a, int NB) {
   return P;
 }
 
+// Tensor maps of A (sorted rows, K-major) and B (expert weights, MN-major)
+// and the number of column blocks, shared by the grouped GEMM launchers.
+template <Epi EPI, bool F8>
+moe_status_t make_ab_maps(const GroupedGemmArgs& a, CUtensorMap* tmA, CUtensorMap* tmB, int* NB) {
+  using G1 = Geo<1, F8>;
+  const CUtensorMapDataType dt =
+      F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t eb = F8 ? 1 : 2;  // bytes per operand element
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.cap)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * eb};
+    const uint32_t box[2] = {G1::BKE, BM};
+    if (moe_status_t st = make_map(tmA, a.a, 2, dims, strides, box, dt)) return st;
+  }
+  if constexpr (EPI == Epi::SwiGLU) {
+    // w13 [E, K, 2, N] viewed 4-D: (n, half, k, e)
+    const uint64_t dims[4] = {static_cast<uint64_t>(a.N), 2, static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.E)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(a.N) * eb,
+                                 static_cast<uint64_t>(a.N) * 2 * eb,
+                                 static_cast<uint64_t>(a.N) * 2 * eb * a.K};
+    const uint32_t box[4] = {G1::CW, 1, G1::BKE, 1};
+    if (moe_status_t st = make_map(tmB, a.w, 4, dims, strides, box, dt)) return st;
+    *NB = ceil_div(a.N, MMA_N / 2);
+  } else {
+    // w2 [E, K, N] viewed 3-D: (n, k, e)
+    const uint64_t dims[3] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(a.N) * eb,
+                                 static_cast<uint64_t>(a.N) * eb * a.K};
+    const uint32_t box[3] = {G1::CW, G1::BKE, 1};
+    if (moe_status_t st = make_map(tmB, a.w, 3, dims, strides, box, dt)) return st;
+    *NB = ceil_div(a.N, MMA_N);
+  }
+  return MOE_OK;
+}
+
 template <Epi EPI, bool F8 = false>
 moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
   using G1 = Geo<1, F8>;
   using G2 = Geo<2, F8>;
-  const CUtensorMapDataType dt =
-      F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t eb = F8 ? 1 : 2;  // bytes per operand element
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(grouped_gemm_kernel<EPI, F8>,
@@ -1073,33 +1270,8 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     attr_done = true;
   }
   CUtensorMap tmA, tmB;
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.cap)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * eb};
-    const uint32_t box[2] = {G1::BKE, BM};
-    if (moe_status_t st = make_map(&tmA, a.a, 2, dims, strides, box, dt)) return st;
-  }
   int NB;
-  if constexpr (EPI == Epi::SwiGLU) {
-    // w13 [E, K, 2, N] viewed 4-D: (n, half, k, e)
-    const uint64_t dims[4] = {static_cast<uint64_t>(a.N), 2, static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.E)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(a.N) * eb,
-                                 static_cast<uint64_t>(a.N) * 2 * eb,
-                                 static_cast<uint64_t>(a.N) * 2 * eb * a.K};
-    const uint32_t box[4] = {G1::CW, 1, G1::BKE, 1};
-    if (moe_status_t st = make_map(&tmB, a.w, 4, dims, strides, box, dt)) return st;
-    NB = ceil_div(a.N, MMA_N / 2);
-  } else {
-    // w2 [E, K, N] viewed 3-D: (n, k, e)
-    const uint64_t dims[3] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.E)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(a.N) * eb,
-                                 static_cast<uint64_t>(a.N) * eb * a.K};
-    const uint32_t box[3] = {G1::CW, G1::BKE, 1};
-    if (moe_status_t st = make_map(&tmB, a.w, 3, dims, strides, box, dt)) return st;
-    NB = ceil_div(a.N, MMA_N);
-  }
+  if (moe_status_t st = make_ab_maps<EPI, F8>(a, &tmA, &tmB, &NB)) return st;
   CUtensorMap tmO;
   if constexpr (EPI == Epi::SortedF32) {
     // fp32 [cap, N] output, 32 x 32 boxes, 128-byte swizzle (matches staging)
@@ -1154,6 +1326,34 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
   prof_before(name, s);
   grouped_gemm_kernel<EPI, F8><<<grid, NTHREADS, G1::SMEM, s>>>(tmA, tmB, tmO, P);
+  prof_after(name, s);
+  return check_launch(name);
+}
+
+// FP8 with block scales: single-CTA 128 x 256 tiles, 128 K per stage.
+template <Epi EPI>
+moe_status_t launch_gemm_bs(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
+  using G = Geo<1, true>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(grouped_gemm_bs_kernel<EPI>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(G::SMEM)) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                       cudaGetErrorString(cudaGetLastError()));
+    attr_done = true;
+  }
+  CUtensorMap tmA, tmB;
+  int NB;
+  if (moe_status_t st = make_ab_maps<EPI, true>(a, &tmA, &tmB, &NB)) return st;
+  KParams P = base_params<EPI>(a, NB);
+  P.w_scale_ld = ((EPI == Epi::SwiGLU) ? 2 * a.N : a.N) / 128;  // weight blocks per K block
+  P.bs_a_ld = a.cap;
+  const int64_t max_blocks = a.cap / BM;
+  if (max_blocks <= 0) return MOE_OK;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
+  prof_before(name, s);
+  grouped_gemm_bs_kernel<EPI><<<grid, BS_THREADS, G::SMEM, s>>>(tmA, tmB, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -1286,6 +1486,13 @@ moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
 }  // namespace gbmoe
 
 namespace gbmoe {
+
+moe_status_t launch_gemm1_swiglu_fp8_block(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm_bs<Epi::SwiGLU>(a, "gemm1_swiglu_fp8_block", s);
+}
+moe_status_t launch_gemm2_sorted_fp8_block(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm_bs<Epi::SortedF32>(a, "gemm2_sorted_fp8_block", s);
+}
 
 moe_status_t launch_gemm1_swiglu_wq(const GroupedGemmArgs& a, cudaStream_t s) {
   switch (a.wq_format) {

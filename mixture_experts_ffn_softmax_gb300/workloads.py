@@ -202,10 +202,12 @@ def make_moe_inputs(spec: MoESpec, device="cpu", seed: int = 0, weights: bool = 
     return d
 
 
-def make_fp8_weights(spec: MoESpec, device="cpu", seed: int = 0, per_channel: bool = True):
+def make_fp8_weights(spec: MoESpec, device="cpu", seed: int = 0, per_channel: bool = True,
+                     block: bool = False):
     """FP8 (E4M3) expert weights for the W8A8 layer: codes drawn as N(0, 1)
     values cast to float8_e4m3fn, and scales ~ U(0.015, 0.025) per output
-    channel ([E, 2I] and [E, H]) or per expert ([E]) -- effective weights of
+    channel ([E, 2I] and [E, H]), per expert ([E]), or (block) per 128 x 128
+    block ([E, H/128, 2I/128] and [E, I/128, H/128]) -- effective weights of
     standard deviation ~0.02, like the bf16 workloads."""
     device = torch.device(device)
     E, H, I = spec.E, spec.H, spec.I
@@ -213,7 +215,12 @@ def make_fp8_weights(spec: MoESpec, device="cpu", seed: int = 0, per_channel: bo
     w13 = _normal((E, H, 2 * I), 1.0, g, device, torch.float8_e4m3fn)
     w2 = _normal((E, I, H), 1.0, g, device, torch.float8_e4m3fn)
     gs = _gen(seed + 14, device)
-    shape13, shape2 = ((E, 2 * I), (E, H)) if per_channel else ((E,), (E,))
+    if block:
+        shape13, shape2 = (E, H // 128, 2 * I // 128), (E, I // 128, H // 128)
+    elif per_channel:
+        shape13, shape2 = (E, 2 * I), (E, H)
+    else:
+        shape13, shape2 = (E,), (E,)
     s13 = torch.rand(shape13, generator=gs, device=device) * 0.01 + 0.015
     s2 = torch.rand(shape2, generator=gs, device=device) * 0.01 + 0.015
     return {"w13_q": w13, "w2_q": w2, "w13_scale": s13, "w2_scale": s2}

@@ -147,3 +147,68 @@ def test_quant_rows_validation_and_empty():
     with pytest.raises(pkg.MoEError) as ei:
         pkg.moe_quant_rows_fp8(torch.zeros(4, 40, device="cuda").bfloat16())
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small"])
+def test_fp8_block_scales_small_workloads(name):
+    """128 x 128 weight-block scales, activations per (row, group of 128):
+    against the oracle's block-wise FP8 layer."""
+    spec = wl.SMALL_SPECS[name]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    q = wl.make_fp8_weights(spec, device="cuda", block=True)
+    w32, ids = _route(spec, d)
+    y = pkg.moe_forward_fp8(d["hidden"], torch.from_numpy(w32).cuda(), torch.from_numpy(ids).cuda(),
+                            q["w13_q"], q["w2_q"], q["w13_scale"], q["w2_scale"], d["w13_bias"],
+                            d["w2_bias"])
+    torch.cuda.synchronize()
+    ref = oracle.forward_fp8_block(f64(d["hidden"]), w32.astype(np.float64), ids, f64(q["w13_q"]),
+                                   f64(q["w2_q"]), f64(q["w13_scale"]), f64(q["w2_scale"]),
+                                   f64(d["w13_bias"]), f64(d["w2_bias"]))
+    check_out(f64(y), ref, f"{name} fp8 block")
+
+
+def test_fp8_block_scales_with_bias_and_ragged_rows():
+    """Biases, M not a multiple of the tile, experts with a few rows each."""
+    spec = wl.MoESpec(name="block_ragged", M=77, H=256, I=384, E=6, top_k=3,
+                      routing_method="softmax", renormalize=True, bias=True)
+    d = wl.make_moe_inputs(spec, device="cuda")
+    q = wl.make_fp8_weights(spec, device="cuda", block=True)
+    w32, ids = _route(spec, d)
+    y = pkg.moe_forward_fp8(d["hidden"], torch.from_numpy(w32).cuda(), torch.from_numpy(ids).cuda(),
+                            q["w13_q"], q["w2_q"], q["w13_scale"], q["w2_scale"], d["w13_bias"],
+                            d["w2_bias"])
+    torch.cuda.synchronize()
+    ref = oracle.forward_fp8_block(f64(d["hidden"]), w32.astype(np.float64), ids, f64(q["w13_q"]),
+                                   f64(q["w2_q"]), f64(q["w13_scale"]), f64(q["w2_scale"]),
+                                   f64(d["w13_bias"]), f64(d["w2_bias"]))
+    check_out(f64(y), ref, "ragged fp8 block")
+
+
+def test_fp8_block_scales_full_size_mixtral_sampled():
+    spec = wl.SPECS["mixtral_prefill"]
+    d = wl.make_moe_inputs(spec, device="cuda", weights=False)
+    q = wl.make_fp8_weights(spec, device="cuda", block=True)
+    w, ids = pkg.moe_route(d["router_logits"], spec.top_k, "softmax", True)
+    ws = pkg.alloc_workspace(pkg.workspace_size_fp8(spec.M, spec.H, spec.I, spec.E, spec.top_k))
+    y = pkg.moe_forward_fp8(d["hidden"], w, ids, q["w13_q"], q["w2_q"], q["w13_scale"],
+                            q["w2_scale"], workspace=ws)
+    torch.cuda.synchronize()
+    assert pkg.read_error(pkg.workspace_error_word(ws)) == 0
+    sel = np.sort(np.random.default_rng(2).choice(spec.M, 12, replace=False))
+    ref = oracle.forward_fp8_block(f64(d["hidden"])[sel], w.cpu().numpy()[sel].astype(np.float64),
+                                   ids.cpu().numpy()[sel], LazyF64(q["w13_q"]), LazyF64(q["w2_q"]),
+                                   f64(q["w13_scale"]), f64(q["w2_scale"]))
+    check_out(f64(y)[sel], ref, "mixtral fp8 block")
+
+
+def test_fp8_block_scales_validation():
+    spec = wl.MoESpec(name="bad", M=8, H=192, I=256, E=2, top_k=1)   # H % 128 != 0
+    d = wl.make_moe_inputs(spec, device="cuda", weights=False)
+    w13 = torch.zeros(2, 192, 512, dtype=torch.uint8, device="cuda")
+    w2 = torch.zeros(2, 256, 192, dtype=torch.uint8, device="cuda")
+    s13 = torch.ones(2, 1, 4, device="cuda")
+    s2 = torch.ones(2, 2, 1, device="cuda")
+    with pytest.raises(pkg.MoEError) as ei:
+        pkg.moe_forward_fp8(d["hidden"], torch.ones(8, 1, device="cuda"),
+                            torch.zeros(8, 1, dtype=torch.int32, device="cuda"), w13, w2, s13, s2)
+    assert ei.value.status == 1
