@@ -71,3 +71,15 @@ def test_align_bad_ids_set_error_word():
     assert counts == [1, 1, 1, 1]                     # bad items dropped, others placed
     assert pkg.read_error(err.data_ptr()) == 4
     assert int(err.item()) == 0                       # reset by read_error
+
+
+@pytest.mark.parametrize("E,M,k", [(8, 2049, 2), (8, 8192, 2), (16, 4096, 4), (8, 8193, 2),
+                                   (17, 1500, 3), (2, 16384, 1)])
+def test_align_one_block_plan_bounds(E, M, k):
+    """Around the bounds of the one-block plan for few experts (items up to
+    16384 with at most 16 experts) and just past them; a skewed draw."""
+    rng = np.random.default_rng(M + E)
+    p = rng.dirichlet(np.ones(E) * 0.3)
+    ids = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(M)]).astype(np.int32)
+    _check_align(ids, E, 128)
+    _check_align(ids, E, 16)
