@@ -265,6 +265,8 @@ def run_batched(args, world, rank, local):
                      "unit": "GB/s", "frac": round(b1 / (g1 * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
                      "traffic": None, "peak_source": pk["source"] + " copy"},
         "kernels_us": {k: round(v, 2) for k, v in kern.items()},
+        "graph": {"ms_per_step": round(ms_graph, 4),
+                  "tokens_per_s": round(spec.M * world / (ms_graph / 1e3), 1)},
         "gpu_launches": launches, "clocks": ck,
         "e2e": {"value": round(R * world / (ms_e2e / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hy.numel() * 2},
@@ -346,6 +348,19 @@ def run_ours(args, world, rank, local):
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                 "traffic": None, "peak_source": pk["source"] + " copy"}
 
+    # the same step captured once into a CUDA graph and replayed (launch
+    # overhead removed; matters for the small shapes)
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        step()
+    torch.cuda.current_stream().wait_stream(gs)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    ms_graph = max_over_ranks(time_steps(graph.replay, K, W, world) / K, world)
+    del graph
+
     # end to end through the public API with host buffers
     hx = step.d["hidden"].cpu().pin_memory()
     hl = step.d["router_logits"].cpu().pin_memory()
@@ -380,6 +395,8 @@ def run_ours(args, world, rank, local):
                           "peaks": "measured sustained bf16, measured copy GB/s"},
         "roofline": roof,
         "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
+        "graph": {"ms_per_step": round(ms_graph, 4),
+                  "tokens_per_s": round(spec.M * world / (ms_graph / 1e3), 1)},
         "gpu_launches": launches,
         "clocks": ck,
         "e2e": e2e,
@@ -396,6 +413,16 @@ def run_ours(args, world, rank, local):
         for _ in range(Kd):
             dstep()
         dprof = pkg.profiler_stop()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gs):
+            dstep()
+        torch.cuda.current_stream().wait_stream(gs)
+        dgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(dgraph):
+            dstep()
+        dms_graph = max_over_ranks(time_steps(dgraph.replay, Kd, max(W, 3), world) / Kd, world)
+        del dgraph
         dids = dstep.ids.cpu().numpy()
         dfl, dby, dt = algorithmic(dspec, dids)
         g1d = 1e3 * dprof["gemm1_swiglu"][1] / dprof["gemm1_swiglu"][0]
@@ -405,6 +432,7 @@ def run_ours(args, world, rank, local):
             "tokens_per_s": round(dspec.M * world / (dms / 1e3), 1),
             "experts_touched": dt,
             "hbm_roofline_frac": round((dby / (pk["hbm_gbs"] * 1e9)) / (dms / 1e3), 4),
+            "graph_ms_per_step": round(dms_graph, 4),
             "gemm1_hbm_gbs": round(b1 / (g1d * 1e-6) / 1e9, 1),
             "kernels_us": {k: round(1e3 * v[1] / v[0], 2) for k, v in dprof.items()},
         }
