@@ -560,7 +560,7 @@ def measure_next_rows(step, spec, K, W, world, pk):
 
 def measure_wq(step, spec, K, W, world, pk):
     """Weight-only quantised experts on the same layer, prefill and the
-    M = 16 decode: int4 (group 128, zero points) and MX FP4.  Decode is
+    M = 16 decode: int4 (group 128, zero points), MX FP4 and MX FP6 (E2M3).  Decode is
     bound by the weight bytes: touched experts' codes + scales + zero points,
     plus x, out and logits."""
     import mixture_experts_ffn_softmax_gb300 as pkg
@@ -571,7 +571,7 @@ def measure_wq(step, spec, K, W, world, pk):
     dw, dids = pkg.moe_route(dd["router_logits"], dspec.top_k, "softmax", True)
     touched = int(torch.unique(dids).numel())
     out = {}
-    for fmt, G in (("int4", 128), ("mxfp4", 32)):
+    for fmt, G in (("int4", 128), ("mxfp4", 32), ("mxfp6_e2m3", 32)):
         q = wl.make_wq_weights(spec, fmt, G, device=dev)
         args = (q["w13_q"], q["w2_q"], q["w13_scale"], q["w2_scale"], q["w13_zero"], q["w2_zero"],
                 q["group_size"])

@@ -317,19 +317,28 @@ GBMOE_API moe_status_t moe_quant_rows_fp8(const void* x, int64_t M, int32_t H, v
  * weights, are dequantised to the activation dtype and the layer runs as
  * the bf16 one on those weights:
  *   int4, int8  w[e, k, n] = bf16((q[e, k, n] - zp[e, k/G, n]) * s[e, k/G, n])
- *   MX FP4      w[e, k, n] = bf16(e2m1(q[e, k, n]) * 2^(s[e, k/32, n] - 127))
+ *   MX FP4/FP6  w[e, k, n] = bf16(value(q[e, k, n]) * 2^(s[e, k/32, n] - 127)),
+ *               value = the E2M1 / E3M2 / E2M3 element of the code
  * each value the exact product rounded once (nearest even).  Layouts, in the
  * [E, K, N] orientation of the bf16 weights (w13: K = H, N = 2I with the
  * gate columns first; w2: K = I, N = H), all row-major:
  *  codes  int4 and MX FP4: uint8 [E, K, N/2], column 2j in the low nibble of
- *         byte j, column 2j+1 in its high nibble; int8: int8 [E, K, N]
- *  scale  int4 / int8: bf16 [E, K/G, N]; MX FP4: uint8 (UE8M0) [E, K/32, N]
+ *         byte j, column 2j+1 in its high nibble; int8: int8 [E, K, N];
+ *         MX FP6: uint8 [E, K, N], the 6-bit code in the low bits (not the
+ *         packed four-codes-in-three-bytes form)
+ *  scale  int4 / int8: bf16 [E, K/G, N]; MX: uint8 (UE8M0) [E, K/32, N]
  *  zero   int4: uint8 [E, K/G, N] holding 0..15; int8: int8 [E, K/G, N];
- *         NULL = symmetric (int4: 8, int8: 0); MX FP4: must be NULL
- *  G      group_size along K: a multiple of 32 dividing K (MX FP4: 32)
+ *         NULL = symmetric (int4: 8, int8: 0); MX: must be NULL
+ *  G      group_size along K: a multiple of 32 dividing K (MX: 32)
  * All pointers device, caller-owned, 16-byte aligned.
  */
-typedef enum { MOE_WQ_INT4 = 0, MOE_WQ_INT8 = 1, MOE_WQ_MXFP4 = 2 } moe_wq_format_t;
+typedef enum {
+  MOE_WQ_INT4 = 0,
+  MOE_WQ_INT8 = 1,
+  MOE_WQ_MXFP4 = 2,       /* OCP MX E2M1, two codes per byte */
+  MOE_WQ_MXFP6_E3M2 = 3,  /* OCP MX FP6 E3M2, one code per byte (low 6 bits) */
+  MOE_WQ_MXFP6_E2M3 = 4   /* OCP MX FP6 E2M3, one code per byte (low 6 bits) */
+} moe_wq_format_t;
 typedef struct {
   int32_t format;     /* moe_wq_format_t */
   int32_t group_size; /* G */

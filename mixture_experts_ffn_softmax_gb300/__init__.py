@@ -230,7 +230,7 @@ def moe_quant_rows_fp8(x: torch.Tensor, q8: Optional[torch.Tensor] = None,
     return q8, scale
 
 
-WQ_FORMATS = {"int4": 0, "int8": 1, "mxfp4": 2}
+WQ_FORMATS = {"int4": 0, "int8": 1, "mxfp4": 2, "mxfp6_e3m2": 3, "mxfp6_e2m3": 4}
 
 
 def _wq_shape(fmt: str, codes: torch.Tensor):
@@ -241,8 +241,8 @@ def _wq_shape(fmt: str, codes: torch.Tensor):
 def moe_dequant_weights(fmt: str, codes: torch.Tensor, scale: torch.Tensor,
                         zero: Optional[torch.Tensor] = None, group_size: int = 128,
                         out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Weight-only quantised weights -> bf16 [E, K, N] (fmt "int4", "int8" or
-    "mxfp4"; layouts as moe_forward_wq)."""
+    """Weight-only quantised weights -> bf16 [E, K, N] (fmt "int4", "int8",
+    "mxfp4", "mxfp6_e3m2" or "mxfp6_e2m3"; layouts as moe_forward_wq)."""
     E, K, N = _wq_shape(fmt, codes)
     if out is None:
         out = torch.empty(E, K, N, dtype=torch.bfloat16, device=codes.device)
@@ -261,10 +261,10 @@ def moe_forward_wq(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: t
                    workspace: Optional[torch.Tensor] = None,
                    out: Optional[torch.Tensor] = None, stream=None):
     """Layer with weight-only quantised experts.  int4 / MX FP4 codes uint8
-    [E, K, N/2] (column 2j in the low nibble), int8 codes int8 [E, K, N];
-    scales bf16 [E, K/G, N] (int) or uint8 UE8M0 [E, K/32, N] (MX); zero
-    points uint8 / int8 [E, K/G, N] or None.  w13: K = H, N = 2I; w2: K = I,
-    N = H."""
+    [E, K, N/2] (column 2j in the low nibble), int8 codes int8 [E, K, N],
+    MX FP6 codes uint8 [E, K, N] (6-bit code in the low bits); scales bf16
+    [E, K/G, N] (int) or uint8 UE8M0 [E, K/32, N] (MX); zero points uint8 /
+    int8 [E, K/G, N] or None.  w13: K = H, N = 2I; w2: K = I, N = H."""
     M, H = hidden.shape
     E, _, N13 = _wq_shape(fmt, w13_q)
     I = N13 // 2

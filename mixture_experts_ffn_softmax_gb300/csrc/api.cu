@@ -714,14 +714,14 @@ moe_status_t moe_quant_rows_fp8(const void* x, int64_t M, int32_t H, void* q8, f
 // ------------------------------------------- weight-only quantised --
 namespace {
 moe_status_t validate_wq_format(int32_t format, int32_t G, const void* zero) {
-  if (format < MOE_WQ_INT4 || format > MOE_WQ_MXFP4)
+  if (format < MOE_WQ_INT4 || format > MOE_WQ_MXFP6_E2M3)
     return set_error(MOE_ERR_INVALID_ARG, "weight format %d", format);
   if (G < 32 || G % 32 != 0)
     return set_error(MOE_ERR_INVALID_ARG, "group_size=%d must be a positive multiple of 32", G);
-  if (format == MOE_WQ_MXFP4 && G != 32)
-    return set_error(MOE_ERR_INVALID_ARG, "MX FP4 scales cover blocks of 32 (group_size=%d)", G);
-  if (format == MOE_WQ_MXFP4 && zero != nullptr)
-    return set_error(MOE_ERR_INVALID_ARG, "MX FP4 has no zero points");
+  const bool mx = format >= MOE_WQ_MXFP4;
+  if (mx && G != 32)
+    return set_error(MOE_ERR_INVALID_ARG, "MX scales cover blocks of 32 (group_size=%d)", G);
+  if (mx && zero != nullptr) return set_error(MOE_ERR_INVALID_ARG, "MX formats have no zero points");
   return MOE_OK;
 }
 }  // namespace
@@ -756,8 +756,8 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
     return st;
   if (!w) return set_error(MOE_ERR_INVALID_ARG, "null weights");
   if (moe_status_t st = validate_wq_format(w->format, w->group_size, w->w13_zero)) return st;
-  if (w->format == MOE_WQ_MXFP4 && w->w2_zero != nullptr)
-    return set_error(MOE_ERR_INVALID_ARG, "MX FP4 has no zero points");
+  if (w->format >= MOE_WQ_MXFP4 && w->w2_zero != nullptr)
+    return set_error(MOE_ERR_INVALID_ARG, "MX formats have no zero points");
   if (H < 64 || I < 64 || H % 32 != 0 || I % 32 != 0)
     return set_error(MOE_ERR_INVALID_ARG,
                      "quantised weights need H and I multiples of 32, at least 64 (H=%d I=%d)", H, I);

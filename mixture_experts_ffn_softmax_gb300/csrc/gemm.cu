@@ -84,7 +84,7 @@ struct WqRing {
   static constexpr int SC_OFF = NREG * CODES;                // scales of region g at SC_OFF + g*SCALES
   static constexpr int Z_OFF = SC_OFF + NREG * SCALES;       // zeros of region g at Z_OFF + g*ZEROS
   static constexpr int STAGE = Z_OFF + NREG * ZEROS;
-  static constexpr int NRAW = WQ == Wq::Int8 ? 2 : 5;
+  static constexpr int NRAW = F::CODE_BITS == 8 ? 2 : 5;
   static constexpr int BYTES = WQ == Wq::None ? 0 : NRAW * STAGE;
   static_assert(CODES % 128 == 0 && SCALES % 128 == 0 && ZEROS % 128 == 0,
                 "raw regions keep 128-byte alignment");
@@ -114,7 +114,8 @@ static_assert(Geo<1>::SMEM <= 232448 && Geo<2>::SMEM <= 232448, "shared memory b
 static_assert(Geo<1, true>::SMEM <= 232448 && Geo<2, true>::SMEM <= 232448,
               "shared memory budget");
 static_assert(Geo<1, false, Wq::Int4>::SMEM <= 232448 && Geo<1, false, Wq::Int8>::SMEM <= 232448 &&
-                  Geo<1, false, Wq::Mxfp4>::SMEM <= 232448,
+                  Geo<1, false, Wq::Mxfp4>::SMEM <= 232448 &&
+                  Geo<1, false, Wq::Mxfp6e3m2>::SMEM <= 232448,
               "shared memory budget");
 
 // Threads of a CTA: producer + MMA warps, converter warps (weight-only
@@ -352,7 +353,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   // Int4 / MX B tiles hold each aligned group of 8 columns in the order
   // 0 4 1 5 2 6 3 7 (wq_pair_pos), and so does the accumulator: the epilogue
   // reads column n of a group from position wq_pair_pos(n)
-  constexpr bool PERM = WQ == Wq::Int4 || WQ == Wq::Mxfp4;
+  constexpr bool PERM = WQ != Wq::None && WqFmt<WQ>::PAIRS;
   auto acc_pos = [](int n) { return PERM ? (n & ~7) + wq_pair_pos(n & 7) : n; };
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl<G::NSTAGES> ctl;
@@ -1499,6 +1500,8 @@ moe_status_t launch_gemm1_swiglu_wq(const GroupedGemmArgs& a, cudaStream_t s) {
     case 0: return launch_gemm_wq<Epi::SwiGLU, Wq::Int4>(a, "gemm1_swiglu_int4", s);
     case 1: return launch_gemm_wq<Epi::SwiGLU, Wq::Int8>(a, "gemm1_swiglu_int8", s);
     case 2: return launch_gemm_wq<Epi::SwiGLU, Wq::Mxfp4>(a, "gemm1_swiglu_mxfp4", s);
+    case 3: return launch_gemm_wq<Epi::SwiGLU, Wq::Mxfp6e3m2>(a, "gemm1_swiglu_mxfp6", s);
+    case 4: return launch_gemm_wq<Epi::SwiGLU, Wq::Mxfp6e2m3>(a, "gemm1_swiglu_mxfp6", s);
     default: return set_error(MOE_ERR_INVALID_ARG, "weight format %d", a.wq_format);
   }
 }
@@ -1508,6 +1511,8 @@ moe_status_t launch_gemm2_sorted_wq(const GroupedGemmArgs& a, cudaStream_t s) {
     case 0: return launch_gemm_wq<Epi::SortedF32, Wq::Int4>(a, "gemm2_sorted_int4", s);
     case 1: return launch_gemm_wq<Epi::SortedF32, Wq::Int8>(a, "gemm2_sorted_int8", s);
     case 2: return launch_gemm_wq<Epi::SortedF32, Wq::Mxfp4>(a, "gemm2_sorted_mxfp4", s);
+    case 3: return launch_gemm_wq<Epi::SortedF32, Wq::Mxfp6e3m2>(a, "gemm2_sorted_mxfp6", s);
+    case 4: return launch_gemm_wq<Epi::SortedF32, Wq::Mxfp6e2m3>(a, "gemm2_sorted_mxfp6", s);
     default: return set_error(MOE_ERR_INVALID_ARG, "weight format %d", a.wq_format);
   }
 }

@@ -82,6 +82,8 @@ moe_status_t launch_dequant_weights(const WqDequantArgs& a, cudaStream_t s) {
     case 0: return launch_dequant_t<Wq::Int4>(a, s);
     case 1: return launch_dequant_t<Wq::Int8>(a, s);
     case 2: return launch_dequant_t<Wq::Mxfp4>(a, s);
+    case 3: return launch_dequant_t<Wq::Mxfp6e3m2>(a, s);
+    case 4: return launch_dequant_t<Wq::Mxfp6e2m3>(a, s);
     default: return set_error(MOE_ERR_INVALID_ARG, "weight format %d", a.format);
   }
 }

@@ -11,6 +11,8 @@
 //   Int8   signed codes, w = bf16((q - zp) * s), zp int8 (default 0)
 //   Mxfp4  OCP MX E2M1 codes, two per byte, UE8M0 scale 2^(s - 127) per
 //          block of 32 rows of K: w = bf16(value(q) * 2^(s - 127))
+//   Mxfp6  OCP MX E3M2 or E2M3 codes, one per byte (low 6 bits), UE8M0
+//          scales as MX FP4
 // bf16 arithmetic keeps subnormals, so 2^-127 scales and products below the
 // normal range round like the exact product does.
 // Every value is the exact product rounded once to bf16 (nearest even).
@@ -21,14 +23,17 @@
 
 namespace gbmoe {
 
-enum class Wq : int { None = 0, Int4 = 1, Int8 = 2, Mxfp4 = 3 };
+enum class Wq : int { None = 0, Int4 = 1, Int8 = 2, Mxfp4 = 3, Mxfp6e3m2 = 4, Mxfp6e2m3 = 5 };
 
 template <Wq WQ>
 struct WqFmt {
-  static constexpr int CODE_BITS = WQ == Wq::Int8 ? 8 : 4;
+  static constexpr bool MX = WQ == Wq::Mxfp4 || WQ == Wq::Mxfp6e3m2 || WQ == Wq::Mxfp6e2m3;
+  static constexpr int CODE_BITS = (WQ == Wq::Int4 || WQ == Wq::Mxfp4) ? 4 : 8;
   static constexpr int CODE_BYTES8 = CODE_BITS;        // bytes of 8 codes
-  static constexpr int SCALE_BYTES = WQ == Wq::Mxfp4 ? 1 : 2;
-  static constexpr bool HAS_ZERO = WQ != Wq::Mxfp4;
+  static constexpr int SCALE_BYTES = MX ? 1 : 2;
+  static constexpr bool HAS_ZERO = !MX;
+  // codes come out in the pair order (j, j + 4) (see wq_dequant8)
+  static constexpr bool PAIRS = WQ != Wq::Int8;
 };
 
 // Per-group parameters of 8 columns, prepared for the conversion.
@@ -86,33 +91,46 @@ __device__ __forceinline__ void wq_params8(const uint4 scale8, const uint2 zero8
 }
 
 // 8 codes of one K row -> 8 bf16 values (16 bytes), in column order, or
-// with PAIR_ORDER (Int4, Mxfp4) in the order WQ_PAIR_COL, which saves the
-// final byte permutes.  codes: Int4 / Mxfp4 in c.x (8 nibbles); Int8 in
-// c.x, c.y (8 bytes).
+// with PAIR_ORDER (all but Int8) in the pair order 0 4 1 5 2 6 3 7, which
+// saves the final byte permutes.  codes: Int4 / Mxfp4 in c.x (8 nibbles);
+// Int8 / Mxfp6 in c.x, c.y (8 bytes).
 template <Wq WQ, bool PAIR_ORDER = false>
 __device__ __forceinline__ uint4 wq_dequant8(const uint2 c, const WqParams8& p) {
   uint4 r;
   uint32_t* o = &r.x;
-  if constexpr (WQ == Wq::Int4 || WQ == Wq::Mxfp4) {
-    // Column i sits at bits 4i: shifted by 4j, one mask takes the nibbles of
-    // columns j and j + 4 into the two halves of a bf16 pair.
+  if constexpr (WQ != Wq::Int8) {
+    // Int4 / Mxfp4: column i sits at bits 4i; shifted by 4j, one mask takes
+    // the nibbles of columns j and j + 4 into the two halves of a bf16 pair.
+    // Mxfp6: bytes j of c.x and c.y (columns j, j + 4) into the two halves.
     uint32_t h[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t t = c.x >> (4 * j);
+      const uint32_t t = WqFmt<WQ>::CODE_BITS == 4 ? c.x >> (4 * j)
+                                                  : __byte_perm(c.x, c.y, j | ((4 + j) << 8));
       __nv_bfloat162 r2;
       if constexpr (WQ == Wq::Int4) {
         // (128 + q) - (128 + zp) = q - zp exactly; one rounding in the product
         const uint32_t v = (t & 0x000F000Fu) | 0x43004300u;
         r2 = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), p.zb2[j]), p.s2[j]);
       } else {
-        // E2M1 (s e1 e0 m) as bf16 bits: sign to bit 15, (e, m) to bits 8..6
-        // -- value(q) * 2^-126 for normal and subnormal codes alike; times
-        // 2^126 is exact, times the block scale rounds once
-        const uint32_t v = ((t & 0x00070007u) << 6) | ((t & 0x00080008u) << 12);
-        const uint32_t two126 = 0x7E807E80u;
+        // The code's exponent and mantissa bits placed as the low exponent
+        // and high mantissa bits of a bf16, the sign to bit 15: the value
+        // times 2^-(127 - bias) for normal and subnormal codes alike (E2M1:
+        // bits 8..6, 2^-126; E3M2: bits 9..5, 2^-124; E2M3: bits 8..4,
+        // 2^-126); the power of two back is exact, the block scale rounds once
+        uint32_t v, back;
+        if constexpr (WQ == Wq::Mxfp4) {
+          v = ((t & 0x00070007u) << 6) | ((t & 0x00080008u) << 12);
+          back = 0x7E807E80u;  // 2^126
+        } else if constexpr (WQ == Wq::Mxfp6e3m2) {
+          v = ((t & 0x001F001Fu) << 5) | ((t & 0x00200020u) << 10);
+          back = 0x7D807D80u;  // 2^124
+        } else {
+          v = ((t & 0x001F001Fu) << 4) | ((t & 0x00200020u) << 10);
+          back = 0x7E807E80u;  // 2^126
+        }
         r2 = __hmul2(__hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v),
-                             *reinterpret_cast<const __nv_bfloat162*>(&two126)),
+                             *reinterpret_cast<const __nv_bfloat162*>(&back)),
                      p.s2[j]);
       }
       h[j] = *reinterpret_cast<const uint32_t*>(&r2);

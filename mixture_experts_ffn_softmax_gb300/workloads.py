@@ -250,22 +250,28 @@ def make_wq_weights(spec: MoESpec, fmt: str = "int4", group_size: int = 128, dev
           ~ U(0.0035, 0.0052) per (group, column) -- effective std ~0.02;
     int8: codes ~ U{-128..127}, zero points ~ U{-4..4} (or none), scales
           ~ U(2.2e-4, 3.2e-4);
-    mxfp4: E2M1 codes ~ U{0..15}, UE8M0 scales ~ U{118..120} per block of 32.
+    mxfp4: E2M1 codes ~ U{0..15}, UE8M0 scales ~ U{118..120} per block of 32;
+    mxfp6_e3m2 / mxfp6_e2m3: codes ~ U{0..63} one per byte, UE8M0 scales
+    ~ U{117..119} / U{119..121}.
     Returns codes, scales and zero points for w13 [E, H, 2I] and w2 [E, I, H]."""
     device = torch.device(device)
     E, H, I = spec.E, spec.H, spec.I
     g = _gen(seed + 21, device)
-    out = {"fmt": fmt, "group_size": group_size if fmt != "mxfp4" else 32}
+    mx = fmt.startswith("mxfp")
+    out = {"fmt": fmt, "group_size": 32 if mx else group_size}
     G = out["group_size"]
     for name, K, N in (("w13", H, 2 * I), ("w2", I, H)):
         if fmt == "int8":
             out[name + "_q"] = _codes((E, K, N), -128, 127, g, device, torch.int8)
+        elif fmt.startswith("mxfp6"):
+            out[name + "_q"] = _codes((E, K, N), 0, 63, g, device, torch.uint8)
         else:
             q = _codes((E, K, N), 0, 15, g, device, torch.uint8)
             out[name + "_q"] = _pack_nibbles(q)
             del q
-        if fmt == "mxfp4":
-            out[name + "_scale"] = _codes((E, K // 32, N), 118, 120, g, device, torch.uint8)
+        if mx:
+            lo, hi = {"mxfp4": (118, 120), "mxfp6_e3m2": (117, 119), "mxfp6_e2m3": (119, 121)}[fmt]
+            out[name + "_scale"] = _codes((E, K // 32, N), lo, hi, g, device, torch.uint8)
             out[name + "_zero"] = None
             continue
         lo, hi = (0.0035, 0.0052) if fmt == "int4" else (2.2e-4, 3.2e-4)

@@ -16,10 +16,13 @@ from helpers import check_out, f64, route_args
 pytestmark = pytest.mark.gpu
 
 
+MX_ELEMENT = {"mxfp4": "e2m1", "mxfp6_e3m2": "e3m2", "mxfp6_e2m3": "e2m3"}
+
+
 def _oracle_dequant(fmt, q, scale, zero):
     q = q.cpu().numpy()
-    if fmt == "mxfp4":
-        return oracle.dequant_mx(q, scale.cpu().numpy(), "e2m1")
+    if fmt in MX_ELEMENT:
+        return oracle.dequant_mx(q, scale.cpu().numpy(), MX_ELEMENT[fmt])
     z = None if zero is None else zero.cpu().numpy()
     return oracle.dequant_int(q, scale.float().cpu().numpy(), z, bits=4 if fmt == "int4" else 8)
 
@@ -31,7 +34,7 @@ class LazyDequant:
     def __init__(self, fmt, q, scale, zero):
         self.args = (fmt, q, scale, zero)
         E, K, n = q.shape
-        self.shape = (E, K, 2 * n if fmt != "int8" else n)
+        self.shape = (E, K, 2 * n if fmt in ("int4", "mxfp4") else n)
         self._cache = {}
 
     def __getitem__(self, e):
@@ -53,7 +56,8 @@ def _route(spec, d):
 
 
 CASES = [("int4", 128, True), ("int4", 32, False), ("int4", 64, True),
-         ("int8", 64, True), ("int8", 128, False), ("mxfp4", 32, False)]
+         ("int8", 64, True), ("int8", 128, False), ("mxfp4", 32, False),
+         ("mxfp6_e3m2", 32, False), ("mxfp6_e2m3", 32, False)]
 
 
 @pytest.mark.parametrize("fmt,G,zero", CASES)
@@ -68,17 +72,22 @@ def test_dequant_weights_bit_exact(fmt, G, zero):
         np.testing.assert_array_equal(got.float().cpu().numpy(), want.astype(np.float32))
 
 
-def test_dequant_mx_extreme_scales_bit_exact():
-    """UE8M0 scales at the ends of the range: bf16 subnormal results
-    (2^-127), and powers of two far above one."""
-    E, K, N = 2, 64, 32
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp6_e3m2", "mxfp6_e2m3"])
+def test_dequant_mx_extreme_scales_bit_exact(fmt):
+    """Every element code with UE8M0 scales at the ends of the range: bf16
+    subnormal results (2^-127), and powers of two far above one."""
+    E, K, N = 2, 64, 64
     g = torch.Generator().manual_seed(3)
-    codes = torch.randint(0, 256, (E, K, N // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+    if fmt == "mxfp4":
+        codes = torch.randint(0, 256, (E, K, N // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+    else:
+        codes = torch.arange(E * K * N, dtype=torch.int32).reshape(E, K, N).remainder(64)
+        codes = codes.to(torch.uint8)
     scale = torch.tensor([0, 1, 2, 100, 127, 130, 200, 250], dtype=torch.uint8)
     scale = scale[torch.randint(0, 8, (E, K // 32, N), generator=g)]
-    got = pkg.moe_dequant_weights("mxfp4", codes.cuda(), scale.cuda(), None, 32)
+    got = pkg.moe_dequant_weights(fmt, codes.cuda(), scale.cuda(), None, 32)
     torch.cuda.synchronize()
-    want = oracle.dequant_mx(codes.numpy(), scale.numpy(), "e2m1")
+    want = oracle.dequant_mx(codes.numpy(), scale.numpy(), MX_ELEMENT[fmt])
     np.testing.assert_array_equal(got.float().cpu().numpy(), want.astype(np.float32))
 
 
@@ -103,7 +112,7 @@ def test_wq_layer_small_workloads(name, fmt, G, zero):
     check_out(f64(y), ref, f"{name} {fmt} G={G}")
 
 
-@pytest.mark.parametrize("fmt", ["int4", "int8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["int4", "int8", "mxfp4", "mxfp6_e3m2", "mxfp6_e2m3"])
 def test_wq_layer_equals_bf16_layer_on_dequantised_weights(fmt):
     """The fused conversion feeds the same bf16 weights to the same MMA
     sequence as the bf16 layer (single-CTA tiles): identical outputs."""
