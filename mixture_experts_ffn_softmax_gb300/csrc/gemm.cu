@@ -40,6 +40,7 @@
 // Every mbarrier wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT,
 // all roles stop, in-flight copies are given time to land, TMEM is freed.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -73,10 +74,10 @@ constexpr int kMaxRaw = 8;  // raw ring stages the control block has barriers fo
 // points, in NREG regions of contiguous columns: two (gate, up) for the
 // SwiGLU GEMM, one for the other -- so that each TMA box row is as wide as
 // the region (fewer, longer rows per stage).
-template <Wq WQ, int NREG = 2>
+template <Wq WQ, int NREG = 2, int RCOLS_ = 256 / NREG>
 struct WqRing {
   using F = WqFmt<WQ>;
-  static constexpr int RCOLS = 256 / NREG;                  // columns of a region
+  static constexpr int RCOLS = RCOLS_;                      // columns of a region
   static constexpr int ROW_BYTES = RCOLS * F::CODE_BITS / 8; // codes of one K row of a region
   static constexpr int CODES = 64 * ROW_BYTES;               // a region's codes, 64 K rows
   static constexpr int SCALES = 2 * RCOLS * F::SCALE_BYTES;  // a region's scales, two group rows
@@ -84,7 +85,10 @@ struct WqRing {
   static constexpr int SC_OFF = NREG * CODES;                // scales of region g at SC_OFF + g*SCALES
   static constexpr int Z_OFF = SC_OFF + NREG * SCALES;       // zeros of region g at Z_OFF + g*ZEROS
   static constexpr int STAGE = Z_OFF + NREG * ZEROS;
-  static constexpr int NRAW = F::CODE_BITS == 8 ? 2 : 5;
+  // as many raw stages as fit beside the main ring (int8 / FP6 codes are
+  // twice the bytes of int4 / FP4)
+  static constexpr int NRAW = NREG * RCOLS == 256 ? (F::CODE_BITS == 8 ? 2 : 5)
+                                                  : (F::CODE_BITS == 8 ? 4 : 8);
   static constexpr int BYTES = WQ == Wq::None ? 0 : NRAW * STAGE;
   static_assert(CODES % 128 == 0 && SCALES % 128 == 0 && ZEROS % 128 == 0,
                 "raw regions keep 128-byte alignment");
@@ -102,10 +106,13 @@ struct Geo {
   static constexpr int UMMA_K = F8 ? 32 : 16;     // K per tcgen05.mma
   static constexpr int KSTEPS = BKE / UMMA_K;
   static constexpr int B_KSTEP = UMMA_K * 128;    // bytes per MMA K step within a chunk
-  static constexpr int NSTAGES = WQ != Wq::None ? 3 : (CG == 1 ? 4 : 5);
-  static constexpr size_t PREFIX_BYTES = CG == 1 ? 0 : (MAX_E + 1) * sizeof(int32_t);
+  static constexpr int NSTAGES = WQ != Wq::None ? (CG == 1 ? 3 : 4) : (CG == 1 ? 4 : 5);
+  // the pair tile prefix, rounded up so that what follows stays 1024-aligned
+  static constexpr size_t PREFIX_BYTES = CG == 1 ? 0 : ((MAX_E + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
+  // raw ring: a CTA of a pair converts one 128-column region per stage
+  using Raw = std::conditional_t<CG == 1, WqRing<WQ, 2, 128>, WqRing<WQ, 1, 128>>;
   static constexpr size_t SMEM = 1024 /*alignment slack*/ + NSTAGES * STAGE +
-                                 EPI_WARPS * STAGING_BYTES + PREFIX_BYTES + WqRing<WQ>::BYTES;
+                                 EPI_WARPS * STAGING_BYTES + PREFIX_BYTES + Raw::BYTES;
   static constexpr uint32_t IDESC =
       F8 ? ptx::idesc_e4m3_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true)
          : ptx::idesc_bf16_f32(BM * CG, MMA_N, /*a_mn=*/false, /*b_mn=*/true);
@@ -115,7 +122,8 @@ static_assert(Geo<1, true>::SMEM <= 232448 && Geo<2, true>::SMEM <= 232448,
               "shared memory budget");
 static_assert(Geo<1, false, Wq::Int4>::SMEM <= 232448 && Geo<1, false, Wq::Int8>::SMEM <= 232448 &&
                   Geo<1, false, Wq::Mxfp4>::SMEM <= 232448 &&
-                  Geo<1, false, Wq::Mxfp6e3m2>::SMEM <= 232448,
+                  Geo<1, false, Wq::Mxfp6e3m2>::SMEM <= 232448 &&
+                  Geo<2, false, Wq::Int4>::SMEM <= 232448 && Geo<2, false, Wq::Int8>::SMEM <= 232448,
               "shared memory budget");
 
 // Threads of a CTA: producer + MMA warps, converter warps (weight-only
@@ -166,14 +174,20 @@ struct KParams {
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
 // when another role of the CTA has aborted, or after limit_ns, in which case
 // it records MOE_ERR_TIMEOUT and raises the CTA's abort flag.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* abort,
                                              int32_t* err, uint64_t limit_ns = kWaitLimitNs) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  // CLUSTER: acquire at cluster scope (arrivals from the other CTA of a pair
+  // that publish that CTA's own writes)
+  if (CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity, 0u) : ptx::mbar_try_wait(bar, parity))
+    return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
     // suspended rather than spinning, so waiting roles leave the issue
     // slots to the working ones; wakes when the phase completes
-    if (ptx::mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
+    if (CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity, 1000000u)
+                : ptx::mbar_try_wait_suspend(bar, parity, 1000000u))
+      return true;
     if (*reinterpret_cast<volatile int32_t*>(abort)) return false;
     if (ptx::globaltimer_ns() - t0 > limit_ns) {
       *reinterpret_cast<volatile int32_t*>(abort) = 1;
@@ -344,8 +358,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
                                           const CUtensorMap* tmO, const CUtensorMap* tmS,
                                           const CUtensorMap* tmZ, const KParams& P) {
   using G = Geo<CG, F8, WQ>;
-  using R = WqRing<WQ, EPI == Epi::SwiGLU ? 2 : 1>;
-  static_assert(R::BYTES == WqRing<WQ>::BYTES, "raw ring size does not depend on the regions");
+  // raw ring regions: single CTA, the tile's 256 columns (SwiGLU: gate and
+  // up halves); CTA pair, this CTA's 128 columns (SwiGLU: gate for the even
+  // CTA, up for the odd one)
+  using R = std::conditional_t<CG == 2, WqRing<WQ, 1, 128>,
+                               WqRing<WQ, EPI == Epi::SwiGLU ? 2 : 1>>;
+  static_assert(R::BYTES == G::Raw::BYTES, "raw ring as sized in the shared-memory budget");
   constexpr bool WQM = WQ != Wq::None;
   constexpr int CONV = conv_warps<WQ>();
   constexpr int EPI0 = 2 + CONV;  // first epilogue warp
@@ -368,6 +386,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   uint8_t* staging = tiles + G::NSTAGES * G::STAGE;  // 1024-byte aligned
   int32_t* s_pp = reinterpret_cast<int32_t*>(staging + EPI_WARPS * STAGING_BYTES);
   uint8_t* rawbuf = staging + EPI_WARPS * STAGING_BYTES + G::PREFIX_BYTES;  // WQ raw ring
+  static_assert((EPI_WARPS * STAGING_BYTES + G::PREFIX_BYTES) % 1024 == 0 &&
+                    (G::NSTAGES * G::STAGE) % 1024 == 0,
+                "staging, prefix and raw ring start 1024-byte aligned");
   const int32_t* off = P.offsets;
 
   if constexpr (CG == 2) {
@@ -395,7 +416,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     for (int i = 0; i < G::NSTAGES; ++i) {
       // the producer's arrive with A's bytes, or (quantised B) the converter
       // warps' arrivals, one of them having raised the count by A's bytes
-      ptx::mbar_init(&ctl.full[i], WQM ? CONV : 1);
+      ptx::mbar_init(&ctl.full[i], WQM ? CG * CONV : 1);  // (pairs: the even CTA's counts both)
       ptx::mbar_init(&ctl.empty[i], 1);
     }
     if constexpr (WQM) {
@@ -485,7 +506,22 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           ptx::mbar_arrive_expect_tx(rf, P.wq_raw_tx);
           uint8_t* rb = rawbuf + rstage * R::STAGE;
           const int g0 = (kb * G::BKE) / P.wq_G;
-          if constexpr (EPI == Epi::SwiGLU) {
+          if constexpr (CG == 2) {
+            // this CTA's 128 columns: SwiGLU gate (even CTA) or up (odd CTA)
+            // columns [nb*128, +128); otherwise [nb*256 + rank*128, +128)
+            if constexpr (EPI == Epi::SwiGLU) {
+              const int col = nb * (MMA_N / 2);
+              const int hf = static_cast<int>(rank);
+              ptx::tma_load_4d(rb, tmB, rf, col * R::F::CODE_BITS / 8, hf, kb * G::BKE, e);
+              ptx::tma_load_4d(rb + R::SC_OFF, tmS, rf, col, hf, g0, e);
+              if (P.wq_has_zero) ptx::tma_load_4d(rb + R::Z_OFF, tmZ, rf, col, hf, g0, e);
+            } else {
+              const int col = nb * MMA_N + static_cast<int>(rank) * (MMA_N / 2);
+              ptx::tma_load_3d(rb, tmB, rf, col * R::F::CODE_BITS / 8, kb * G::BKE, e);
+              ptx::tma_load_3d(rb + R::SC_OFF, tmS, rf, col, g0, e);
+              if (P.wq_has_zero) ptx::tma_load_3d(rb + R::Z_OFF, tmZ, rf, col, g0, e);
+            }
+          } else if constexpr (EPI == Epi::SwiGLU) {
             // region 0: gate columns [nb*128, +128); region 1: the same up columns
             const int col = nb * (MMA_N / 2);
 #pragma unroll
@@ -519,7 +555,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     // the 128-byte-swizzled layout TMA would have produced (16-byte unit j
     // of K row r of a 64-column chunk at j ^ (r & 7)); then the warp arrives
     // on the stage's barrier.
-    constexpr int NREG = (EPI == Epi::SwiGLU) ? 2 : 1;
+    // regions of this CTA's B tile (a CTA of a pair converts one: its 128 columns)
+    constexpr int NREG = (CG == 1 && EPI == Epi::SwiGLU) ? 2 : 1;
+    static_assert(NREG * R::RCOLS == 256 / CG, "converted columns = this CTA's B tile");
     constexpr int LPR = R::RCOLS / 8;                 // lanes per region row
     constexpr int RPI = 32 / LPR;                     // rows per warp instruction
     constexpr int ROWS = NREG * 64 / (CONV > 0 ? CONV : 1);  // region rows per warp
@@ -543,9 +581,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       for (int kb = 0; kb < KB; ++kb) {
         bool got = bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word);
         if (cw == 0 && lane == 0 && got) {
-          // the stage's A rows: their bytes join the count before this warp arrives
-          ptx::mbar_expect_tx(&ctl.full[stage], A_STAGE_BYTES);
-          ptx::tma_load_2d(tiles + stage * G::STAGE, tmA, &ctl.full[stage], kb * G::BKE, row0);
+          // the stage's A rows: their bytes join the count before this warp
+          // arrives (pairs: both CTAs' rows complete on the even CTA's barrier,
+          // which counts the bytes of both)
+          if constexpr (CG == 2) {
+            if (rank == 0) ptx::mbar_expect_tx(&ctl.full[stage], 2 * A_STAGE_BYTES);
+            ptx::tma_load_2d_pair(tiles + stage * G::STAGE, tmA,
+                                  ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0),
+                                  kb * G::BKE, row0);
+          } else {
+            ptx::mbar_expect_tx(&ctl.full[stage], A_STAGE_BYTES);
+            ptx::tma_load_2d(tiles + stage * G::STAGE, tmA, &ctl.full[stage], kb * G::BKE, row0);
+          }
         }
         got = got && bounded_wait(&ctl.raw_full[rstage], rphase, &ctl.abort, P.error_word);
         if (!__all_sync(0xffffffffu, got)) {
@@ -591,7 +638,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         ptx::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) {
-          ptx::mbar_arrive(&ctl.full[stage]);
+          if constexpr (CG == 2)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0));
+          else
+            ptx::mbar_arrive(&ctl.full[stage]);
           ptx::mbar_arrive(&ctl.raw_empty[rstage]);
         }
         if (++stage == G::NSTAGES) {
@@ -683,7 +733,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             ptx::tc_fence_after();
             d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
           }
-          if (!bounded_wait(&ctl.full[stage], phase, &ctl.abort, P.error_word)) {
+          // (pairs with converters: the odd CTA's converted B arrives by its
+          // threads' release.cluster arrivals, hence the cluster-scope acquire)
+          if (!bounded_wait<CG == 2 && WQM>(&ctl.full[stage], phase, &ctl.abort, P.error_word)) {
             ok = false;
             break;
           }
@@ -1136,6 +1188,18 @@ __global__ void __launch_bounds__(cta_threads<WQ>(), 1)
   gemm_body<EPI, 1, false, WQ>(&tmA, &tmB, &tmO, &tmS, &tmZ, P);
 }
 
+// The same on CTA pairs: each CTA converts its 128 of the tile's 256
+// columns, the even CTA's MMA reads both.
+template <Epi EPI, Wq WQ>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<WQ>(), 1)
+    grouped_gemm_wq_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                                const __grid_constant__ CUtensorMap tmB,
+                                const __grid_constant__ CUtensorMap tmO,
+                                const __grid_constant__ CUtensorMap tmS,
+                                const __grid_constant__ CUtensorMap tmZ, const KParams P) {
+  gemm_body<EPI, 2, false, WQ>(&tmA, &tmB, &tmO, &tmS, &tmZ, P);
+}
+
 // ------------------------------------------------------------------ host --
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1361,15 +1425,16 @@ moe_status_t launch_gemm_bs(const GroupedGemmArgs& a, const char* name, cudaStre
 
 // bf16 A x weight-only quantised B.  Single-CTA 128 x 256 tiles; the codes,
 // scales and zero points travel by TMA without swizzle into the raw ring.
-template <Epi EPI, Wq WQ>
-moe_status_t launch_gemm_wq(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
-  using G = Geo<1, false, WQ>;
-  using R = WqRing<WQ, EPI == Epi::SwiGLU ? 2 : 1>;
-  constexpr int NREG = EPI == Epi::SwiGLU ? 2 : 1;
+template <Epi EPI, Wq WQ, int CG>
+moe_status_t launch_gemm_wq_cg(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
+  using G = Geo<CG, false, WQ>;
+  using R = std::conditional_t<CG == 2, WqRing<WQ, 1, 128>,
+                               WqRing<WQ, EPI == Epi::SwiGLU ? 2 : 1>>;
+  constexpr int NREG = (CG == 1 && EPI == Epi::SwiGLU) ? 2 : 1;
+  auto kernel = CG == 2 ? grouped_gemm_wq_pair_kernel<EPI, WQ> : grouped_gemm_wq_kernel<EPI, WQ>;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(grouped_gemm_wq_kernel<EPI, WQ>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(G::SMEM)) != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
                        cudaGetErrorString(cudaGetLastError()));
@@ -1445,12 +1510,37 @@ moe_status_t launch_gemm_wq(const GroupedGemmArgs& a, const char* name, cudaStre
                         (a.wq_zero != nullptr ? static_cast<int32_t>(R::RCOLS * gbox) : 0));
   const int64_t max_blocks = a.cap / BM;
   if (max_blocks <= 0) return MOE_OK;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
+  unsigned grid;
+  if constexpr (CG == 2) {
+    // persistent pairs: no more clusters than can be resident at once
+    static int resident = -1;
+    if (resident < 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (a.num_sms / 2));
+      cfg.blockDim = dim3(cta_threads<WQ>());
+      cfg.dynamicSmemBytes = G::SMEM;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = a.num_sms / 2;
+      }
+      resident = std::min(n, a.num_sms / 2);
+    }
+    const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
+    grid = 2 * static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
+  } else {
+    grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
+  }
   prof_before(name, s);
-  grouped_gemm_wq_kernel<EPI, WQ><<<grid, cta_threads<WQ>(), G::SMEM, s>>>(tmA, tmB, tmO, tmS,
-                                                                            tmZ, P);
+  kernel<<<grid, cta_threads<WQ>(), G::SMEM, s>>>(tmA, tmB, tmO, tmS, tmZ, P);
   prof_after(name, s);
   return check_launch(name);
+}
+
+template <Epi EPI, Wq WQ>
+moe_status_t launch_gemm_wq(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
+  if (use_pairs(a)) return launch_gemm_wq_cg<EPI, WQ, 2>(a, name, s);
+  return launch_gemm_wq_cg<EPI, WQ, 1>(a, name, s);
 }
 
 }  // namespace

@@ -91,9 +91,16 @@ def test_dequant_mx_extreme_scales_bit_exact(fmt):
     np.testing.assert_array_equal(got.float().cpu().numpy(), want.astype(np.float32))
 
 
+@pytest.fixture(params=["single", "pairs"])
+def tiles(request):
+    pkg.set_gemm_tiles(request.param)
+    yield request.param
+    pkg.set_gemm_tiles("auto")
+
+
 @pytest.mark.parametrize("fmt,G,zero", CASES)
 @pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small", "qwen_small"])
-def test_wq_layer_small_workloads(name, fmt, G, zero):
+def test_wq_layer_small_workloads(name, fmt, G, zero, tiles):
     spec = wl.SMALL_SPECS[name]
     if spec.H % G or spec.I % G:
         pytest.skip("group size does not divide H and I")
@@ -109,24 +116,25 @@ def test_wq_layer_small_workloads(name, fmt, G, zero):
     w2 = _oracle_dequant(fmt, q["w2_q"], q["w2_scale"], q["w2_zero"])
     ref = oracle.forward_wq(f64(d["hidden"]), w32.astype(np.float64), ids, w13, w2, f64(b13),
                             f64(b2))
-    check_out(f64(y), ref, f"{name} {fmt} G={G}")
+    check_out(f64(y), ref, f"{name} {fmt} G={G} {tiles}")
 
 
+@pytest.mark.parametrize("mode", ["single", "pairs"])
 @pytest.mark.parametrize("fmt", ["int4", "int8", "mxfp4", "mxfp6_e3m2", "mxfp6_e2m3"])
-def test_wq_layer_equals_bf16_layer_on_dequantised_weights(fmt):
+def test_wq_layer_equals_bf16_layer_on_dequantised_weights(fmt, mode):
     """The fused conversion feeds the same bf16 weights to the same MMA
-    sequence as the bf16 layer (single-CTA tiles): identical outputs."""
+    sequence as the bf16 layer (same tile shape): identical outputs."""
     spec = wl.SMALL_SPECS["mixtral_small"]
     d = wl.make_moe_inputs(spec, device="cuda", weights=False)
     q = wl.make_wq_weights(spec, fmt, 64, device="cuda")
     w32, ids = _route(spec, d)
     tw, tids = torch.from_numpy(w32).cuda(), torch.from_numpy(ids).cuda()
-    y = pkg.moe_forward_wq(d["hidden"], tw, tids, fmt, q["w13_q"], q["w2_q"], q["w13_scale"],
-                           q["w2_scale"], q["w13_zero"], q["w2_zero"], q["group_size"])
     w13 = pkg.moe_dequant_weights(fmt, q["w13_q"], q["w13_scale"], q["w13_zero"], q["group_size"])
     w2 = pkg.moe_dequant_weights(fmt, q["w2_q"], q["w2_scale"], q["w2_zero"], q["group_size"])
-    pkg.set_gemm_tiles("single")
+    pkg.set_gemm_tiles(mode)
     try:
+        y = pkg.moe_forward_wq(d["hidden"], tw, tids, fmt, q["w13_q"], q["w2_q"], q["w13_scale"],
+                               q["w2_scale"], q["w13_zero"], q["w2_zero"], q["group_size"])
         yb = pkg.moe_forward(d["hidden"], tw, tids, w13, w2, reduce="separate")
         torch.cuda.synchronize()
     finally:
