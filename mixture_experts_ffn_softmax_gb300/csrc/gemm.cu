@@ -57,7 +57,8 @@ constexpr int A_STAGE_BYTES = BM * 128;        // 16 KB: 128 rows x one 128-byte
 constexpr int TMEM_COLS = 2 * MMA_N;           // 512: two accumulators
 constexpr int MAX_E = 1024;
 constexpr int STAGING_BYTES = 32 * 128;        // per epilogue warp: 32 rows x 128 bytes
-constexpr int kMaxRaw = 8;  // raw ring stages the control block has barriers for
+constexpr int kMaxRaw = 8;
+constexpr uint32_t kRelayBytes = 16;  // CTA-pair stage signal (bulk copy size)  // raw ring stages the control block has barriers for
 
 // CG = CTAs cooperating on one MMA tile.  CG = 1: a 128 x 256 tile per CTA,
 // 48 KB per pipeline stage.  CG = 2 (a CTA pair, tcgen05 cta_group::2): a
@@ -145,6 +146,11 @@ struct Ctl {
   uint64_t raw_empty[kMaxRaw];
   uint32_t tmem_base;
   int32_t abort;
+  // CTA pairs with converters: the odd CTA signals a converted stage to the
+  // even CTA by a 16-byte bulk copy into relay_dst[stage] (completing on the
+  // even CTA's full barrier); relay_src is its (ignored) source
+  alignas(16) uint8_t relay_dst[NS][16];
+  alignas(16) uint8_t relay_src[16];
 };
 
 struct KParams {
@@ -174,20 +180,14 @@ struct KParams {
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
 // when another role of the CTA has aborted, or after limit_ns, in which case
 // it records MOE_ERR_TIMEOUT and raises the CTA's abort flag.
-template <bool CLUSTER = false>
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* abort,
                                              int32_t* err, uint64_t limit_ns = kWaitLimitNs) {
-  // CLUSTER: acquire at cluster scope (arrivals from the other CTA of a pair
-  // that publish that CTA's own writes)
-  if (CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity, 0u) : ptx::mbar_try_wait(bar, parity))
-    return true;
+  if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
     // suspended rather than spinning, so waiting roles leave the issue
     // slots to the working ones; wakes when the phase completes
-    if (CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity, 1000000u)
-                : ptx::mbar_try_wait_suspend(bar, parity, 1000000u))
-      return true;
+    if (ptx::mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
     if (*reinterpret_cast<volatile int32_t*>(abort)) return false;
     if (ptx::globaltimer_ns() - t0 > limit_ns) {
       *reinterpret_cast<volatile int32_t*>(abort) = 1;
@@ -416,7 +416,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     for (int i = 0; i < G::NSTAGES; ++i) {
       // the producer's arrive with A's bytes, or (quantised B) the converter
       // warps' arrivals, one of them having raised the count by A's bytes
-      ptx::mbar_init(&ctl.full[i], WQM ? CG * CONV : 1);  // (pairs: the even CTA's counts both)
+      ptx::mbar_init(&ctl.full[i], WQM ? CONV : 1);
       ptx::mbar_init(&ctl.empty[i], 1);
     }
     if constexpr (WQM) {
@@ -582,10 +582,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         bool got = bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word);
         if (cw == 0 && lane == 0 && got) {
           // the stage's A rows: their bytes join the count before this warp
-          // arrives (pairs: both CTAs' rows complete on the even CTA's barrier,
-          // which counts the bytes of both)
+          // arrives (pairs: both CTAs' rows and the odd CTA's relay copy
+          // complete on the even CTA's barrier, which counts all their bytes)
           if constexpr (CG == 2) {
-            if (rank == 0) ptx::mbar_expect_tx(&ctl.full[stage], 2 * A_STAGE_BYTES);
+            if (rank == 0) ptx::mbar_expect_tx(&ctl.full[stage], 2 * A_STAGE_BYTES + kRelayBytes);
             ptx::tma_load_2d_pair(tiles + stage * G::STAGE, tmA,
                                   ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0),
                                   kb * G::BKE, row0);
@@ -638,10 +638,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         ptx::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) {
-          if constexpr (CG == 2)
-            ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0));
-          else
-            ptx::mbar_arrive(&ctl.full[stage]);
+          // (pairs: the odd CTA's relay thread forwards its CTA's completed
+          // stage to the even CTA's barrier)
+          ptx::mbar_arrive(&ctl.full[stage]);
           ptx::mbar_arrive(&ctl.raw_empty[rstage]);
         }
         if (++stage == G::NSTAGES) {
@@ -733,9 +732,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             ptx::tc_fence_after();
             d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
           }
-          // (pairs with converters: the odd CTA's converted B arrives by its
-          // threads' release.cluster arrivals, hence the cluster-scope acquire)
-          if (!bounded_wait<CG == 2 && WQM>(&ctl.full[stage], phase, &ctl.abort, P.error_word)) {
+          if (!bounded_wait(&ctl.full[stage], phase, &ctl.abort, P.error_word)) {
             ok = false;
             break;
           }
@@ -777,6 +774,32 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
+          }
+        }
+      }
+    } else if (CG == 2 && WQM && lane == 0) {
+      // ---------------------------------- relay (odd CTA, quantised B) --
+      // Once this CTA's converter warps have all arrived for a stage (each
+      // after fencing its writes for the async proxy), a 16-byte bulk copy
+      // into the even CTA completes on that CTA's full barrier: the
+      // converted tile is signalled through the async proxy, the way this
+      // CTA's TMA loads signal theirs.  (An arrive with release at cluster
+      // scope costs a cluster-wide memory barrier, ~1500 cycles, per stage.)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = unit; t < total_tiles && ok; t += units) {
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!bounded_wait(&ctl.full[stage], phase, &ctl.abort, P.error_word)) {
+            ok = false;
+            break;
+          }
+          ptx::bulk_copy_to_cluster(ptx::mapa_shared(ptx::smem_u32(ctl.relay_dst[stage]), 0),
+                                    ctl.relay_src, kRelayBytes,
+                                    ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0));
+          if (++stage == G::NSTAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }

@@ -73,22 +73,6 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// As mbar_try_wait_suspend, acquiring at cluster scope: for a barrier that
-// threads of the other CTA of a pair arrive at (release.cluster) after
-// writing the data the waiter then consumes.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity,
-                                                      uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
 // --------------------------------------------------------------- TMA ---
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -144,6 +128,16 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16, 16-byte aligned addresses) from
+// this CTA's shared memory into shared memory of a CTA of the cluster,
+// completing on an mbarrier of that CTA (shared::cluster addresses).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, const void* src,
+                                                     uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst_cluster), "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
 }
 // TMA loads into this CTA's shared memory that complete on an mbarrier of
 // either CTA of the pair (shared::cluster address).

@@ -1,13 +1,14 @@
 """Small, self-checking invocations of one layer variant each, sized for
 profiler captures (a few GB on the device at most, three calls):
 
-    python -m mixture_experts_ffn_softmax_gb300.profile_cases <case>
+    python -m mixture_experts_ffn_softmax_gb300.profile_cases <case> [auto|single|pairs]
 
 Cases:
   fp8_mixtral_m2048     FP8 W8A8 layer, Mixtral-8x7B expert shape, M = 2048
   int4_mixtral_decode   int4 (group 128, zero points) layer, Mixtral shape, M = 16
   mxfp4_mixtral_decode  MX FP4 layer, Mixtral shape, M = 16
   int4_mixtral_m2048    int4 (group 128) layer, Mixtral shape, M = 2048
+The optional second argument picks the GEMM tile mode (default auto).
 Exits non-zero if the layer reports an error."""
 import dataclasses
 import sys
@@ -16,14 +17,15 @@ import torch
 
 from . import workloads as wl
 from . import (alloc_workspace, moe_forward_fp8, moe_forward_wq, moe_route, read_error,
-               workspace_error_word, workspace_size, workspace_size_fp8)
+               set_gemm_tiles, workspace_error_word, workspace_size, workspace_size_fp8)
 
 
 def _spec(M):
     return dataclasses.replace(wl.SPECS["mixtral_prefill"], M=M, name=f"mixtral_m{M}")
 
 
-def run(case: str, calls: int = 3) -> None:
+def run(case: str, calls: int = 3, tiles: str = "auto") -> None:
+    set_gemm_tiles(tiles)
     kind, _, shape = case.partition("_mixtral_")
     M = 16 if shape == "decode" else int(shape.lstrip("m"))
     spec = _spec(M)
@@ -52,4 +54,4 @@ def run(case: str, calls: int = 3) -> None:
 
 
 if __name__ == "__main__":
-    run(sys.argv[1])
+    run(sys.argv[1], tiles=sys.argv[2] if len(sys.argv) > 2 else "auto")
