@@ -18,6 +18,12 @@
 // The 512 TMEM columns hold two 128x256 fp32 accumulators so the epilogue of
 // tile i overlaps the MMAs of tile i+1.
 //
+// Weight-only quantised B (608 threads): warp 0 lane 0 streams the raw codes,
+// scales and zero points into a raw ring; warps 2..9 convert them to bf16 in
+// the B tile's layout; warp 10 lane 0 loads A; warps 11..18 are the epilogue.
+// On CTA pairs the odd CTA's warp 1 lane 0 relays its converted stages to
+// the even CTA's barrier.
+//
 // Tiles are enumerated expert by expert, column block by column block, with
 // the row blocks of one expert innermost, so CTAs running at the same time
 // share the same weight columns in L2.  The tile count is read on the device
@@ -132,7 +138,9 @@ static_assert(Geo<1, false, Wq::Int4>::SMEM <= 232448 && Geo<1, false, Wq::Int8>
 template <Wq WQ>
 __host__ __device__ constexpr int conv_warps() { return WQ == Wq::None ? 0 : 8; }
 template <Wq WQ>
-__host__ __device__ constexpr int cta_threads() { return 64 + 32 * conv_warps<WQ>() + EPI_WARPS * 32; }
+__host__ __device__ constexpr int cta_threads() {
+  return 64 + 32 * conv_warps<WQ>() + (WQ == Wq::None ? 0 : 32) + EPI_WARPS * 32;
+}
 
 enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3, DenseF32 = 4 };
 
@@ -366,7 +374,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   static_assert(R::BYTES == G::Raw::BYTES, "raw ring as sized in the shared-memory budget");
   constexpr bool WQM = WQ != Wq::None;
   constexpr int CONV = conv_warps<WQ>();
-  constexpr int EPI0 = 2 + CONV;  // first epilogue warp
+  constexpr int AWARP = 2 + CONV;  // quantised B: the warp loading A
+  constexpr int EPI0 = WQM ? AWARP + 1 : 2;  // first epilogue warp
   constexpr int NEPI = BS ? 16 : EPI_WARPS;  // epilogue warps
   // Int4 / MX B tiles hold each aligned group of 8 columns in the order
   // 0 4 1 5 2 6 3 7 (wq_pair_pos), and so does the accumulator: the epilogue
@@ -416,7 +425,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     for (int i = 0; i < G::NSTAGES; ++i) {
       // the producer's arrive with A's bytes, or (quantised B) the converter
       // warps' arrivals, one of them having raised the count by A's bytes
-      ptx::mbar_init(&ctl.full[i], WQM ? CONV : 1);
+      // quantised B: the converter warps and the A warp (arrive + bytes);
+      // the odd CTA of a pair loads A onto the even CTA's barrier, so its
+      // own (read by its relay) counts the converters alone
+      ptx::mbar_init(&ctl.full[i], WQM ? CONV + (CG == 1 || rank == 0 ? 1 : 0) : 1);
       ptx::mbar_init(&ctl.empty[i], 1);
     }
     if constexpr (WQM) {
@@ -488,7 +500,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     // ------------------------------------- TMA producer (quantised B) --
     // per 64-row K stage: the raw codes / scales / zero points of the four
     // 64-column chunks into the raw ring, as far ahead as the ring allows
-    // (A goes to the main ring from the converter warps)
+    // (A goes to the main ring from the A warp)
     if (lane == 0) {
       int rstage = 0;
       uint32_t rphase = 0;
@@ -580,20 +592,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       tile_of(t, e, row0, nb, mine);
       for (int kb = 0; kb < KB; ++kb) {
         bool got = bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word);
-        if (cw == 0 && lane == 0 && got) {
-          // the stage's A rows: their bytes join the count before this warp
-          // arrives (pairs: both CTAs' rows and the odd CTA's relay copy
-          // complete on the even CTA's barrier, which counts all their bytes)
-          if constexpr (CG == 2) {
-            if (rank == 0) ptx::mbar_expect_tx(&ctl.full[stage], 2 * A_STAGE_BYTES + kRelayBytes);
-            ptx::tma_load_2d_pair(tiles + stage * G::STAGE, tmA,
-                                  ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0),
-                                  kb * G::BKE, row0);
-          } else {
-            ptx::mbar_expect_tx(&ctl.full[stage], A_STAGE_BYTES);
-            ptx::tma_load_2d(tiles + stage * G::STAGE, tmA, &ctl.full[stage], kb * G::BKE, row0);
-          }
-        }
         got = got && bounded_wait(&ctl.raw_full[rstage], rphase, &ctl.abort, P.error_word);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
@@ -650,6 +648,42 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         if (++rstage == R::NRAW) {
           rstage = 0;
           rphase ^= 1u;
+        }
+      }
+    }
+  } else if (WQM && warp == AWARP) {
+    // ----------------------------------------- A producer (quantised B) --
+    // each stage's A rows as soon as the stage is free; the arrival carries
+    // the bytes, so the phase cannot complete before they are counted
+    // (pairs: both CTAs' rows and the odd CTA's relay copy complete on the
+    // even CTA's barrier, which counts all their bytes)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = unit; t < total_tiles && ok; t += units) {
+        int e, row0, nb;
+        bool mine;
+        tile_of(t, e, row0, nb, mine);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word)) {
+            ok = false;
+            break;
+          }
+          if constexpr (CG == 2) {
+            if (rank == 0)
+              ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * A_STAGE_BYTES + kRelayBytes);
+            ptx::tma_load_2d_pair(tiles + stage * G::STAGE, tmA,
+                                  ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0),
+                                  kb * G::BKE, row0);
+          } else {
+            ptx::mbar_arrive_expect_tx(&ctl.full[stage], A_STAGE_BYTES);
+            ptx::tma_load_2d(tiles + stage * G::STAGE, tmA, &ctl.full[stage], kb * G::BKE, row0);
+          }
+          if (++stage == G::NSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
