@@ -109,11 +109,16 @@ struct Geo {
   static constexpr int CHUNKS = MMA_N / CW;       // B chunks per tile
   static constexpr int CHUNK_BYTES = BKE * 128;   // one chunk: BKE k-rows x 128 bytes
   static constexpr int B_CHUNKS_CTA = CHUNKS / CG;
-  static constexpr int STAGE = A_STAGE_BYTES + B_CHUNKS_CTA * CHUNK_BYTES;
+  // row sub-tiles per tile: quantised B on CTA pairs feeds each converted B
+  // stage to two MMAs (rows +0 and +256 of a 512-row tile), one per
+  // accumulator, halving the conversion per MMA
+  static constexpr int SUB = (WQ != Wq::None && CG == 2) ? 2 : 1;
+  static constexpr int B_OFF = SUB * A_STAGE_BYTES;  // B after the stage's A tiles
+  static constexpr int STAGE = B_OFF + B_CHUNKS_CTA * CHUNK_BYTES;
   static constexpr int UMMA_K = F8 ? 32 : 16;     // K per tcgen05.mma
   static constexpr int KSTEPS = BKE / UMMA_K;
   static constexpr int B_KSTEP = UMMA_K * 128;    // bytes per MMA K step within a chunk
-  static constexpr int NSTAGES = WQ != Wq::None ? (CG == 1 ? 3 : 4) : (CG == 1 ? 4 : 5);
+  static constexpr int NSTAGES = WQ != Wq::None ? 3 : (CG == 1 ? 4 : 5);
   // the pair tile prefix, rounded up so that what follows stays 1024-aligned
   static constexpr size_t PREFIX_BYTES = CG == 1 ? 0 : ((MAX_E + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
   // raw ring: a CTA of a pair converts one 128-column region per stage
@@ -130,7 +135,9 @@ static_assert(Geo<1, true>::SMEM <= 232448 && Geo<2, true>::SMEM <= 232448,
 static_assert(Geo<1, false, Wq::Int4>::SMEM <= 232448 && Geo<1, false, Wq::Int8>::SMEM <= 232448 &&
                   Geo<1, false, Wq::Mxfp4>::SMEM <= 232448 &&
                   Geo<1, false, Wq::Mxfp6e3m2>::SMEM <= 232448 &&
-                  Geo<2, false, Wq::Int4>::SMEM <= 232448 && Geo<2, false, Wq::Int8>::SMEM <= 232448,
+                  Geo<2, false, Wq::Int4>::SMEM <= 232448 && Geo<2, false, Wq::Int8>::SMEM <= 232448 &&
+                  Geo<2, false, Wq::Mxfp4>::SMEM <= 232448 &&
+                  Geo<2, false, Wq::Mxfp6e3m2>::SMEM <= 232448,
               "shared memory budget");
 
 // Threads of a CTA: producer + MMA warps, converter warps (weight-only
@@ -252,7 +259,11 @@ struct PairTile {
   int e, row0, nb;
   bool mine;  // this CTA's row block belongs to the expert
 };
-__device__ __forceinline__ PairTile map_pair_tile(int t, const int32_t* s_pp,
+// Tile t of a CTA pair: expert, column block, and this CTA's row block of
+// row sub-tile h (a tile spans 2 * SUB row blocks: sub-tile h holds blocks
+// 2 SUB q + 2 h + rank).  s_pp: prefix over the experts of their tiles.
+template <int SUB>
+__device__ __forceinline__ PairTile map_pair_tile(int t, int h, const int32_t* s_pp,
                                                   const int32_t* __restrict__ off, int E,
                                                   int NB, int rank) {
   int lo = 0, hi = E - 1;  // largest e with s_pp[e] * NB <= t
@@ -263,7 +274,7 @@ __device__ __forceinline__ PairTile map_pair_tile(int t, const int32_t* s_pp,
   const int e = lo;
   const int pairs = s_pp[e + 1] - s_pp[e];
   const int local = t - s_pp[e] * NB;
-  const int mb = 2 * (local % pairs) + rank;
+  const int mb = 2 * SUB * (local % pairs) + 2 * h + rank;
   PairTile tl;
   tl.e = e;
   tl.nb = local / pairs;
@@ -406,7 +417,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       const int per = ceil_div(P.E, 32);
       const int e0 = lane * per, e1 = min(P.E, e0 + per);
       int32_t part = 0;
-      for (int e = e0; e < e1; ++e) part += (((off[e + 1] - off[e]) / BM) + 1) >> 1;
+      for (int e = e0; e < e1; ++e) part += ((off[e + 1] - off[e]) / BM + 2 * G::SUB - 1) / (2 * G::SUB);
       int32_t incl = part;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -416,7 +427,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       int32_t run = incl - part;
       for (int e = e0; e < e1; ++e) {
         s_pp[e] = run;
-        run += (((off[e + 1] - off[e]) / BM) + 1) >> 1;
+        run += ((off[e + 1] - off[e]) / BM + 2 * G::SUB - 1) / (2 * G::SUB);
       }
       if (lane == 31) s_pp[P.E] = incl;
     }
@@ -475,9 +486,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   const int units = (CG == 2) ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int KB = ceil_div(P.K, G::BKE);
 
-  auto tile_of = [&](int t, int& e, int& row0, int& nb, bool& mine) {
+  // (h: row sub-tile, always 0 unless G::SUB = 2)
+  auto tile_of = [&](int t, int& e, int& row0, int& nb, bool& mine, int h = 0) {
     if constexpr (CG == 2) {
-      const PairTile pt = map_pair_tile(t, s_pp, off, P.E, P.NB, static_cast<int>(rank));
+      const PairTile pt = map_pair_tile<G::SUB>(t, h, s_pp, off, P.E, P.NB, static_cast<int>(rank));
       e = pt.e;
       row0 = pt.row0;
       nb = pt.nb;
@@ -599,7 +611,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         }
         const uint8_t* rb = rawbuf + rstage * R::STAGE;
         const uint8_t* rc = rb + reg * R::CODES + col * R::F::CODE_BITS / 8;
-        uint8_t* dst = tiles + stage * G::STAGE + A_STAGE_BYTES + chunk * G::CHUNK_BYTES;
+        uint8_t* dst = tiles + stage * G::STAGE + G::B_OFF + chunk * G::CHUNK_BYTES;
         WqParams8 p;
         {
           const int g = P.wq_gbox == 2 ? gr : 0;
@@ -671,11 +683,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             break;
           }
           if constexpr (CG == 2) {
+            // this CTA's rows of both row sub-tiles (row blocks past the
+            // expert's, or past the tensor, load rows of the next expert or
+            // zeros: their results are not stored)
             if (rank == 0)
-              ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * A_STAGE_BYTES + kRelayBytes);
-            ptx::tma_load_2d_pair(tiles + stage * G::STAGE, tmA,
-                                  ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0),
-                                  kb * G::BKE, row0);
+              ptx::mbar_arrive_expect_tx(&ctl.full[stage],
+                                         2 * G::SUB * A_STAGE_BYTES + kRelayBytes);
+#pragma unroll
+            for (int h = 0; h < G::SUB; ++h)
+              ptx::tma_load_2d_pair(tiles + stage * G::STAGE + h * A_STAGE_BYTES, tmA,
+                                    ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0),
+                                    kb * G::BKE, row0 + h * 2 * BM);
           } else {
             ptx::mbar_arrive_expect_tx(&ctl.full[stage], A_STAGE_BYTES);
             ptx::tma_load_2d(tiles + stage * G::STAGE, tmA, &ctl.full[stage], kb * G::BKE, row0);
@@ -754,7 +772,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       for (int t = unit; t < total_tiles && ok; t += units) {
         // block-scaled FP8: every K stage is its own accumulation, into the
         // two accumulators in turn, handed to the epilogue stage by stage
+        // (two row sub-tiles: both accumulators, sub-tile h in accumulator h)
         if (!BS && !bounded_wait(&ctl.tmem_empty[acc], acc_phase ^ 1u, &ctl.abort, P.error_word)) break;
+        if (G::SUB == 2 &&
+            !bounded_wait(&ctl.tmem_empty[1], acc_phase ^ 1u, &ctl.abort, P.error_word))
+          break;
         ptx::tc_fence_after();
         uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MMA_N);
         for (int kb = 0; kb < KB; ++kb) {
@@ -772,20 +794,24 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           }
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_u32(tiles + stage * G::STAGE);
-          const uint32_t sb = sa + A_STAGE_BYTES;
+          const uint32_t sb = sa + G::B_OFF;
 #pragma unroll
           for (int ks = 0; ks < G::KSTEPS; ++ks) {
-            // A (K-major): advance UMMA_K elements = 32 bytes along the swizzled row.
-            const uint64_t adesc = ptx::smem_desc_sw128(sa + ks * 32, 16, 1024);
             // B (MN-major): advance UMMA_K k-rows; column chunks are
             // CHUNK_BYTES apart, 8-row k groups 1024 bytes apart.
             const uint64_t bdesc =
                 ptx::smem_desc_sw128(sb + ks * G::B_KSTEP, G::CHUNK_BYTES, 1024);
             const uint32_t accum = (BS ? ks : (kb | ks)) != 0 ? 1u : 0u;
-            if constexpr (CG == 2 && F8) ptx::mma_e4m3_pair(d_tmem, adesc, bdesc, G::IDESC, accum);
-            else if constexpr (CG == 2) ptx::mma_bf16_pair(d_tmem, adesc, bdesc, G::IDESC, accum);
-            else if constexpr (F8) ptx::mma_e4m3(d_tmem, adesc, bdesc, G::IDESC, accum);
-            else ptx::mma_bf16(d_tmem, adesc, bdesc, G::IDESC, accum);
+#pragma unroll
+            for (int h = 0; h < G::SUB; ++h) {
+              // A (K-major): advance UMMA_K elements = 32 bytes along the swizzled row.
+              const uint64_t adesc = ptx::smem_desc_sw128(sa + h * A_STAGE_BYTES + ks * 32, 16, 1024);
+              const uint32_t d = d_tmem + static_cast<uint32_t>(h * MMA_N);
+              if constexpr (CG == 2 && F8) ptx::mma_e4m3_pair(d, adesc, bdesc, G::IDESC, accum);
+              else if constexpr (CG == 2) ptx::mma_bf16_pair(d, adesc, bdesc, G::IDESC, accum);
+              else if constexpr (F8) ptx::mma_e4m3(d, adesc, bdesc, G::IDESC, accum);
+              else ptx::mma_bf16(d, adesc, bdesc, G::IDESC, accum);
+            }
           }
           if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.empty[stage], 0x3);
           else ptx::mma_commit(&ctl.empty[stage]);
@@ -803,11 +829,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         }
         if (!ok) break;
         if constexpr (!BS) {
-          if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.tmem_full[acc], 0x3);
-          else ptx::mma_commit(&ctl.tmem_full[acc]);
-          if (++acc == 2) {
-            acc = 0;
-            acc_phase ^= 1u;
+#pragma unroll
+          for (int h = 0; h < G::SUB; ++h) {
+            if constexpr (CG == 2) ptx::mma_commit_pair(&ctl.tmem_full[acc], 0x3);
+            else ptx::mma_commit(&ctl.tmem_full[acc]);
+            if (++acc == 2) {
+              acc = 0;
+              acc_phase ^= 1u;
+            }
           }
         }
       }
@@ -986,10 +1015,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         }
       }
     } else
-    for (int t = unit; t < total_tiles; t += units) {
+    // row sub-tile h of tile t (one per tile unless G::SUB = 2)
+    for (int t = unit, h = 0; t < total_tiles;
+         (h + 1 == G::SUB) ? (h = 0, t += units) : ++h) {
       int e, row0, nb;
       bool mine;
-      tile_of(t, e, row0, nb, mine);
+      tile_of(t, e, row0, nb, mine, h);
       const int64_t p = row0 + row;
       SwiRow sr;
       const int n_base = nb * (MMA_N / 2) + half * (MMA_N / 4);  // SwiGLU: first z column
