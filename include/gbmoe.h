@@ -252,6 +252,59 @@ GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_we
                                         size_t workspace_bytes, const moe_forward_opts_t* opts,
                                         void* out, moe_stream_t stream);
 
+/* ----------------------------------------------- step from host memory --
+ * moe_forward_host: one layer step whose inputs and output live in host
+ * memory: the routing of moe_route, then moe_forward, with the copies --
+ * router logits and hidden rows host -> device, out device -> host -- inside
+ * the call.  Defines: "MindIE-SD Fused MoE" page, function signature
+ * (hidden_states and router_logits in, the layer's output out, the router's
+ * top-k inside the operator); "vLLM FusedMoEModularKernel" page, apply() steps.
+ *  io->h_hidden      host bf16 [M, H];  io->h_logits host fp32 [M, E]
+ *  io->h_out         host bf16 [M, H], written
+ *                    (page-locked host memory gives full copy bandwidth and
+ *                    keeps the copies asynchronous)
+ *  io->d_hidden      device bf16 [M, H];  io->d_logits device fp32 [M, E]
+ *  io->topk_weights  device fp32 [M, top_k];  io->topk_ids device int32 [M, top_k]
+ *  io->d_out         device bf16 [M, H]
+ *                    (device staging, owned by the caller; 16-byte aligned)
+ *  route             routing parameters, with moe_route's meaning and limits
+ *  w13, w2, w13_bias, w2_bias, workspace, workspace_bytes, reduce_mode:
+ *                    as moe_forward
+ * Order on `stream`: the logits' copy, routing and the expert-sorted plan,
+ * while the hidden rows are copied on a copy stream the library keeps per
+ * host thread and device (joined by an event before the rows are gathered);
+ * then the GEMMs, the reduce and the copy of out to io->h_out.  Returns after
+ * enqueueing; io->h_out holds the result once `stream` has passed the call
+ * (cudaStreamSynchronize or an event).  The call can be captured in a CUDA
+ * graph.  Errors: as moe_route and moe_forward (checked before anything is
+ * enqueued); a failed copy or stream operation returns MOE_ERR_CUDA.
+ */
+typedef struct {
+  const void* h_hidden;
+  const float* h_logits;
+  void* h_out;
+  void* d_hidden;
+  float* d_logits;
+  float* topk_weights;
+  int32_t* topk_ids;
+  void* d_out;
+} moe_host_io_t;
+typedef struct {
+  int32_t top_k;
+  int32_t routing_method; /* moe_routing_t */
+  int32_t renormalize;
+  int32_t k_group;
+  int32_t group_count;
+  int32_t group_select_mode;
+  float routed_scaling_factor;
+} moe_route_params_t;
+GBMOE_API moe_status_t moe_forward_host(const moe_host_io_t* io, int64_t M, int32_t H,
+                                        int32_t I, int32_t E, const moe_route_params_t* route,
+                                        const void* w13, const void* w2, const void* w13_bias,
+                                        const void* w2_bias, void* workspace,
+                                        size_t workspace_bytes, int32_t reduce_mode,
+                                        moe_stream_t stream);
+
 /* ------------------------------------------------------------ FP8 W8A8 --
  * moe_forward_fp8: the layer with FP8 (E4M3) weights and activations
  * ("fused_moe.py 分析", "FP8 W8A8": the inputs of both GEMMs are quantised

@@ -281,6 +281,54 @@ def moe_forward_wq(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: t
     return out
 
 
+class HostStaging:
+    """Device buffers of moe_forward_host for M tokens: hidden [M, H] bf16,
+    router logits [M, E] fp32, top-k weights [M, k] fp32 and ids [M, k]
+    int32, out [M, H] bf16, and the forward's workspace."""
+
+    def __init__(self, M: int, H: int, I: int, E: int, top_k: int, device="cuda",
+                 reduce: str = "auto"):
+        self.hidden = torch.empty(M, H, dtype=torch.bfloat16, device=device)
+        self.logits = torch.empty(M, E, dtype=torch.float32, device=device)
+        self.topk_weights = torch.empty(M, top_k, dtype=torch.float32, device=device)
+        self.topk_ids = torch.empty(M, top_k, dtype=torch.int32, device=device)
+        self.out = torch.empty(M, H, dtype=torch.bfloat16, device=device)
+        self.workspace = alloc_workspace(workspace_size(M, H, I, E, top_k, reduce), device)
+
+
+def moe_forward_host(hidden: torch.Tensor, router_logits: torch.Tensor, w13: torch.Tensor,
+                     w2: torch.Tensor, top_k: int, routing_method: str = "softmax",
+                     renormalize: bool = False, k_group: int = 1, group_count: int = 1,
+                     group_select_mode: int = 0, routed_scaling_factor: float = 1.0,
+                     w13_bias: Optional[torch.Tensor] = None,
+                     w2_bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                     staging: Optional[HostStaging] = None, reduce: str = "auto", stream=None):
+    """One layer step from host memory: hidden bf16 [M, H] and router_logits
+    fp32 [M, E] on the host (pinned for full copy speed) -> out bf16 [M, H]
+    on the host, routed as moe_route and computed as moe_forward, the copies
+    inside the call.  Asynchronous on `stream`: out is complete once the
+    stream has passed the call."""
+    M, H = hidden.shape
+    E, _, I2 = w13.shape
+    assert hidden.device.type == "cpu" and router_logits.device.type == "cpu"
+    assert hidden.dtype == torch.bfloat16 and router_logits.dtype == torch.float32
+    assert hidden.is_contiguous() and router_logits.is_contiguous()
+    if staging is None:
+        staging = HostStaging(M, H, I2 // 2, E, top_k, w13.device, reduce)
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.bfloat16, pin_memory=True)
+    io = _lib.HostIo(_ptr(hidden), _ptr(router_logits), _ptr(out), _ptr(staging.hidden),
+                     _ptr(staging.logits), _ptr(staging.topk_weights), _ptr(staging.topk_ids),
+                     _ptr(staging.out))
+    rp = _lib.RouteParams(top_k, ROUTING[routing_method], int(bool(renormalize)), k_group,
+                          group_count, group_select_mode, float(routed_scaling_factor))
+    _check(lib().moe_forward_host(ctypes.byref(io), M, H, I2 // 2, E, ctypes.byref(rp),
+                                  _ptr(w13), _ptr(w2), _ptr(w13_bias), _ptr(w2_bias),
+                                  _ptr(staging.workspace), staging.workspace.numel(),
+                                  REDUCE[reduce], _stream(stream)), "moe_forward_host")
+    return out
+
+
 def moe_forward_batched(x: torch.Tensor, expert_num_tokens: torch.Tensor, w13: torch.Tensor,
                         w2: torch.Tensor, w13_bias: Optional[torch.Tensor] = None,
                         w2_bias: Optional[torch.Tensor] = None,
@@ -376,6 +424,7 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
+           "moe_forward_host", "HostStaging",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
            "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",

@@ -29,6 +29,20 @@ class WqWeights(ctypes.Structure):
                 ("w13_zero", ctypes.c_void_p), ("w2_zero", ctypes.c_void_p)]
 
 
+class HostIo(ctypes.Structure):
+    _fields_ = [("h_hidden", ctypes.c_void_p), ("h_logits", ctypes.c_void_p),
+                ("h_out", ctypes.c_void_p), ("d_hidden", ctypes.c_void_p),
+                ("d_logits", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
+                ("topk_ids", ctypes.c_void_p), ("d_out", ctypes.c_void_p)]
+
+
+class RouteParams(ctypes.Structure):
+    _fields_ = [("top_k", ctypes.c_int32), ("routing_method", ctypes.c_int32),
+                ("renormalize", ctypes.c_int32), ("k_group", ctypes.c_int32),
+                ("group_count", ctypes.c_int32), ("group_select_mode", ctypes.c_int32),
+                ("routed_scaling_factor", ctypes.c_float)]
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
                 ("total_ms", ctypes.c_double)]
@@ -54,6 +68,8 @@ SIGNATURES = {
     "moe_quant_rows_fp8": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
     "moe_dequant_weights": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp,
                                     c_vp]),
+    "moe_forward_host": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                 c_vp, ctypes.c_size_t, c_i32, c_vp]),
     "moe_forward_wq": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32,
                                ctypes.POINTER(WqWeights), c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_align_capacity": (c_sz, [c_i64, c_i32, c_i32, c_i32]),

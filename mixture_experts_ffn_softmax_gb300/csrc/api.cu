@@ -233,12 +233,9 @@ moe_status_t moe_set_gemm_tiles(int32_t mode) {
 }
 
 // ---------------------------------------------------------------- route --
-static moe_status_t route_impl(const void* router_logits, int32_t logits_bf16, int64_t M,
-                               int32_t E, int32_t top_k, int32_t routing_method,
-                               int32_t renormalize, int32_t k_group, int32_t group_count,
-                               int32_t group_select_mode, float routed_scaling_factor,
-                               float* topk_weights, int32_t* topk_ids, moe_stream_t stream) {
-  g_detail[0] = 0;
+static moe_status_t route_check(int64_t M, int32_t E, int32_t top_k, int32_t routing_method,
+                                int32_t k_group, int32_t group_count, int32_t group_select_mode,
+                                float routed_scaling_factor) {
   if (M < 0) return set_error(MOE_ERR_INVALID_ARG, "M=%lld < 0", (long long)M);
   if (E < 1 || E > 1024) return set_error(MOE_ERR_INVALID_ARG, "E=%d outside [1, 1024]", E);
   if (routing_method != MOE_ROUTE_SOFTMAX && routing_method != MOE_ROUTE_SIGMOID)
@@ -258,6 +255,18 @@ static moe_status_t route_impl(const void* router_logits, int32_t logits_bf16, i
   if (!(routed_scaling_factor == routed_scaling_factor) ||
       routed_scaling_factor > 3.0e38f || routed_scaling_factor < -3.0e38f)
     return set_error(MOE_ERR_INVALID_ARG, "routed_scaling_factor is not finite");
+  return MOE_OK;
+}
+
+static moe_status_t route_impl(const void* router_logits, int32_t logits_bf16, int64_t M,
+                               int32_t E, int32_t top_k, int32_t routing_method,
+                               int32_t renormalize, int32_t k_group, int32_t group_count,
+                               int32_t group_select_mode, float routed_scaling_factor,
+                               float* topk_weights, int32_t* topk_ids, moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (moe_status_t st = route_check(M, E, top_k, routing_method, k_group, group_count,
+                                    group_select_mode, routed_scaling_factor))
+    return st;
   if (M == 0) return MOE_OK;
   if (!router_logits || !topk_weights || !topk_ids)
     return set_error(MOE_ERR_INVALID_ARG, "null pointer");
@@ -417,15 +426,16 @@ moe_status_t moe_forward(const void* hidden, const float* topk_weights,
                           w2_bias, workspace, workspace_bytes, &o, out, stream);
 }
 
-moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
-                              const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
-                              int32_t E, int32_t top_k, const void* w13, const void* w2,
-                              const void* w13_bias, const void* w2_bias, void* workspace,
-                              size_t workspace_bytes, const moe_forward_opts_t* opts, void* out,
-                              moe_stream_t stream) {
+// Argument checks of moe_forward_opts (nothing is enqueued); *sms gets the
+// device's SM count when M > 0.
+static moe_status_t forward_check(const void* hidden, const float* topk_weights,
+                                  const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                                  int32_t E, int32_t top_k, const void* w13, const void* w2,
+                                  const void* w13_bias, const void* w2_bias,
+                                  const void* workspace, size_t workspace_bytes,
+                                  const moe_forward_opts_t* opts, const void* out, int* sms) {
   if (!opts) return set_error(MOE_ERR_INVALID_ARG, "null opts");
   const int32_t reduce_mode = opts->reduce_mode;
-  const bool weight_on_input = opts->apply_router_weight_on_input != 0;
   if (opts->apply_router_weight_on_input != 0 && opts->apply_router_weight_on_input != 1)
     return set_error(MOE_ERR_INVALID_ARG, "apply_router_weight_on_input must be 0 or 1");
   if (opts->expert_map != nullptr &&
@@ -446,10 +456,20 @@ moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
   if (workspace_bytes < need)
     return set_error(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", need,
                      workspace_bytes);
-  int sms = 0;
-  if (moe_status_t st = check_device(&sms)) return st;
-  cudaStream_t s = stream;
+  return check_device(sms);
+}
 
+// The forward's launches (arguments already checked, M > 0).  wait_rows: an
+// event the stream waits for before the hidden rows are first read (their
+// copy on another stream), or null.
+static moe_status_t forward_launch(const void* hidden, const float* topk_weights,
+                                   const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                                   int32_t E, int32_t top_k, const void* w13, const void* w2,
+                                   const void* w13_bias, const void* w2_bias, void* workspace,
+                                   const moe_forward_opts_t* opts, void* out, int sms,
+                                   cudaEvent_t wait_rows, cudaStream_t s) {
+  const int32_t reduce_mode = opts->reduce_mode;
+  const bool weight_on_input = opts->apply_router_weight_on_input != 0;
   const int64_t Mc_max = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
   const FwdLayout L = fwd_layout(Mc_max, H, I, E, top_k);
   int32_t* err = at<int32_t>(workspace, L.err);
@@ -475,6 +495,9 @@ moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
     bf16* a_perm = at<bf16>(workspace, L.a_perm);
     GatherArgs ga{x + c0 * H, sorted, offsets, E, top_k, static_cast<int32_t>(Rc), H, cap,
                   a_perm};
+    if (wait_rows != nullptr && c0 == 0 && cudaStreamWaitEvent(s, wait_rows, 0) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaStreamWaitEvent: %s",
+                       cudaGetErrorString(cudaGetLastError()));
     if (moe_status_t st = launch_gather(ga, s)) return st;
 
     bf16* z = at<bf16>(workspace, L.z);
@@ -526,6 +549,103 @@ moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
       if (moe_status_t st = launch_reduce_sorted(o, inv, Mc, top_k, H, y + c0 * H, s)) return st;
     }
   }
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
+                              const int32_t* topk_ids, int64_t M, int32_t H, int32_t I,
+                              int32_t E, int32_t top_k, const void* w13, const void* w2,
+                              const void* w13_bias, const void* w2_bias, void* workspace,
+                              size_t workspace_bytes, const moe_forward_opts_t* opts, void* out,
+                              moe_stream_t stream) {
+  int sms = 0;
+  if (moe_status_t st = forward_check(hidden, topk_weights, topk_ids, M, H, I, E, top_k, w13, w2,
+                                      w13_bias, w2_bias, workspace, workspace_bytes, opts, out,
+                                      &sms))
+    return st;
+  if (M == 0) return MOE_OK;
+  return forward_launch(hidden, topk_weights, topk_ids, M, H, I, E, top_k, w13, w2, w13_bias,
+                        w2_bias, workspace, opts, out, sms, nullptr, stream);
+}
+
+// ------------------------------------------------------- host-memory step --
+namespace {
+// Per host thread and device: the stream the hidden rows are copied on and
+// the events that fork it from, and join it to, the caller's stream.
+struct CopyLane {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, rows = nullptr;
+};
+constexpr int kMaxDevices = 64;
+
+moe_status_t copy_lane(CopyLane** lane) {
+  thread_local CopyLane lanes[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return set_error(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(cudaGetLastError()));
+  CopyLane& l = lanes[dev];
+  if (l.stream == nullptr) {
+    if (cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&l.rows, cudaEventDisableTiming) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "copy stream: %s", cudaGetErrorString(cudaGetLastError()));
+  }
+  *lane = &l;
+  return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_forward_host(const moe_host_io_t* io, int64_t M, int32_t H, int32_t I,
+                              int32_t E, const moe_route_params_t* route, const void* w13,
+                              const void* w2, const void* w13_bias, const void* w2_bias,
+                              void* workspace, size_t workspace_bytes, int32_t reduce_mode,
+                              moe_stream_t stream) {
+  g_detail[0] = 0;
+  if (!io || !route) return set_error(MOE_ERR_INVALID_ARG, "null io or route");
+  if (moe_status_t st = route_check(M, E, route->top_k, route->routing_method, route->k_group,
+                                    route->group_count, route->group_select_mode,
+                                    route->routed_scaling_factor))
+    return st;
+  moe_forward_opts_t o{};
+  o.reduce_mode = reduce_mode;
+  int sms = 0;
+  if (moe_status_t st = forward_check(io->d_hidden, io->topk_weights, io->topk_ids, M, H, I, E,
+                                      route->top_k, w13, w2, w13_bias, w2_bias, workspace,
+                                      workspace_bytes, &o, io->d_out, &sms))
+    return st;
+  if (M == 0) return MOE_OK;
+  if (!io->h_hidden || !io->h_logits || !io->h_out || !io->d_logits)
+    return set_error(MOE_ERR_INVALID_ARG, "null pointer");
+  CopyLane* lane = nullptr;
+  if (moe_status_t st = copy_lane(&lane)) return st;
+  cudaStream_t s = stream;
+  auto cuda_fail = [](const char* what) {
+    return set_error(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(cudaGetLastError()));
+  };
+  const size_t row_bytes = static_cast<size_t>(M) * H * sizeof(bf16);
+  if (cudaMemcpyAsync(io->d_logits, io->h_logits, static_cast<size_t>(M) * E * sizeof(float),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return cuda_fail("cudaMemcpyAsync(logits)");
+  // fork: the hidden rows' copy overlaps routing and the expert-sorted plan
+  if (cudaEventRecord(lane->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(lane->stream, lane->fork, 0) != cudaSuccess ||
+      cudaMemcpyAsync(io->d_hidden, io->h_hidden, row_bytes, cudaMemcpyHostToDevice,
+                      lane->stream) != cudaSuccess ||
+      cudaEventRecord(lane->rows, lane->stream) != cudaSuccess)
+    return cuda_fail("hidden rows copy");
+  moe_status_t st = route_impl(io->d_logits, 0, M, E, route->top_k, route->routing_method,
+                               route->renormalize, route->k_group, route->group_count,
+                               route->group_select_mode, route->routed_scaling_factor,
+                               io->topk_weights, io->topk_ids, s);
+  if (st == MOE_OK)
+    st = forward_launch(io->d_hidden, io->topk_weights, io->topk_ids, M, H, I, E, route->top_k,
+                        w13, w2, w13_bias, w2_bias, workspace, &o, io->d_out, sms, lane->rows, s);
+  if (st != MOE_OK) {
+    cudaStreamWaitEvent(s, lane->rows, 0);  // join the copy stream on the way out as well
+    return st;
+  }
+  if (cudaMemcpyAsync(io->h_out, io->d_out, row_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return cuda_fail("cudaMemcpyAsync(out)");
   return MOE_OK;
 }
 

@@ -129,6 +129,31 @@ def test_forward_validation():
                            ctypes.c_void_p(1 << 20), need, 0, p, None) == INVALID
 
 
+def test_forward_host_validation():
+    """The host-memory step checks routing and forward arguments before it
+    enqueues anything (no GPU here: valid arguments reach the device check)."""
+    lib = pkg.lib()
+    p = ctypes.c_void_p(4096)
+    n = ctypes.c_size_t(0)
+    lib.moe_workspace_size(8, 64, 64, 4, 2, 0, ctypes.byref(n))
+    need = n.value
+    io = _lib.HostIo(4096, 4096, 4096, 4096, 4096, 4096, 4096, 4096)
+
+    def step(M=8, H=64, I=64, E=4, k=2, ws=need, io_=io, method=0, groups=1):
+        rp = _lib.RouteParams(k, method, 1, 1, groups, 0, 1.0)
+        return lib.moe_forward_host(ctypes.byref(io_) if io_ is not None else None, M, H, I, E,
+                                    ctypes.byref(rp), p, p, None, None, ctypes.c_void_p(1 << 20),
+                                    ws, 0, None)
+    assert step(M=0) == OK
+    assert step(io_=None) == INVALID
+    assert step(k=5) == INVALID          # top_k > E
+    assert step(method=2) == INVALID
+    assert step(groups=3) == INVALID     # E % group_count
+    assert step(H=60) == INVALID
+    assert step(ws=need - 1) == WS_SMALL
+    assert step() == NO_DEVICE
+
+
 def test_batched_validation():
     lib = pkg.lib()
     n = ctypes.c_size_t(0)
