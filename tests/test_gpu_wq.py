@@ -200,3 +200,40 @@ def test_wq_validation():
                                 q["w13_zero"], 32)
     pkg.moe_forward_wq(d["hidden"][:0], w[:0], ids[:0], "int4", q["w13_q"], q["w2_q"],
                        q["w13_scale"], q["w2_scale"], q["w13_zero"], q["w2_zero"], 64)
+
+
+@pytest.mark.parametrize("fmt,G", [("int4", 128), ("mxfp4", 32), ("int8", 64)])
+def test_wq_pair_tiles_every_block_count(fmt, G):
+    """CTA-pair tiles hold four row blocks of one expert: experts with 0..9
+    row blocks (every remainder mod 4, a ragged last block) give the same
+    outputs on pairs as on single-CTA tiles, bit for bit."""
+    E, H, I, k = 10, 256, 384, 1
+    counts = [0, 128, 256, 384, 512, 640, 700, 896, 1024, 1100]   # rows per expert
+    M = sum(counts)
+    ids = torch.cat([torch.full((c,), e, dtype=torch.int32) for e, c in enumerate(counts)])
+    ids = ids[torch.randperm(M, generator=torch.Generator().manual_seed(5))].view(M, k).cuda()
+    w = torch.rand(M, k, generator=torch.Generator().manual_seed(6)).cuda()
+    spec = wl.SMALL_SPECS["mixtral_small"].scaled("blocks", M=M, H=H, I=I, E=E, top_k=k)
+    d = wl.make_moe_inputs(spec, device="cuda", weights=False)
+    q = wl.make_wq_weights(spec, fmt, G, device="cuda")
+    args = (d["hidden"], w, ids, fmt, q["w13_q"], q["w2_q"], q["w13_scale"], q["w2_scale"],
+            q["w13_zero"], q["w2_zero"], q["group_size"])
+    ys = {}
+    for mode in ("single", "pairs"):
+        pkg.set_gemm_tiles(mode)
+        try:
+            ws = pkg.alloc_workspace(pkg.workspace_size(M, H, I, E, k, "separate"))
+            ys[mode] = pkg.moe_forward_wq(*args, workspace=ws)
+            torch.cuda.synchronize()
+            assert pkg.read_error(pkg.workspace_error_word(ws)) == 0
+        finally:
+            pkg.set_gemm_tiles("auto")
+    assert torch.equal(ys["single"], ys["pairs"])
+    # and against the oracle on a row sample from every expert
+    sel = np.sort(np.concatenate([np.flatnonzero(ids.cpu().numpy()[:, 0] == e)[:3]
+                                  for e in range(E) if counts[e]]))
+    ref = oracle.forward_wq(f64(d["hidden"])[sel], w.cpu().numpy()[sel].astype(np.float64),
+                            ids.cpu().numpy()[sel],
+                            LazyDequant(fmt, q["w13_q"], q["w13_scale"], q["w13_zero"]),
+                            LazyDequant(fmt, q["w2_q"], q["w2_scale"], q["w2_zero"]))
+    check_out(f64(ys["pairs"])[sel], ref, f"{fmt} every block count")
