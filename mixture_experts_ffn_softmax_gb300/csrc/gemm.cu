@@ -942,15 +942,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
 #pragma unroll
           for (int c = 0; c < CH; ++c) {
             const float sc = (EPI == Epi::SwiGLU && c >= CH / 2) ? scb : sca;
+            // the chunk's 32 columns as two 16-column loads behind one wait
+            uint32_t v[2][16];
+            ptx::tmem_ld_16cols(taddr + chunk_col(c), v[0]);
+            ptx::tmem_ld_16cols(taddr + chunk_col(c) + 16, v[1]);
+            ptx::tmem_ld_wait();
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {  // 16 columns at a time (register budget)
-              uint32_t v[16];
-              ptx::tmem_ld_16cols(taddr + chunk_col(c) + 16 * hh, v);
-              ptx::tmem_ld_wait();
+            for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                accv[c][16 * hh + j] = fmaf(__uint_as_float(v[j]), sc, accv[c][16 * hh + j]);
-            }
+                accv[c][16 * hh + j] = fmaf(__uint_as_float(v[hh][j]), sc, accv[c][16 * hh + j]);
           }
           release_acc(acc);
           if (++acc == 2) {
