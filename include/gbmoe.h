@@ -504,6 +504,13 @@ GBMOE_API moe_status_t moe_profiler_stop(moe_kernel_time_t* out, int32_t capacit
  * 256x256 tiles (tcgen05 cta_group::2).  Results are the same up to fp32
  * summation order.  Invalid values return MOE_ERR_INVALID_ARG. */
 GBMOE_API moe_status_t moe_set_gemm_tiles(int32_t mode);
+/* Where moe_forward / moe_forward_opts / moe_forward_host take GEMM1's rows
+ * from (process-wide tuning / testing knob): 0 = automatic (fused when the
+ * routed rows of a token chunk hold at most 16 MiB), 1 = a separate gather
+ * kernel writes the expert-sorted rows first, 2 = GEMM1 copies them from the
+ * token rows itself (a gather warp, 16-byte asynchronous copies).
+ * Results are identical.  Invalid values return MOE_ERR_INVALID_ARG. */
+GBMOE_API moe_status_t moe_set_gather_mode(int32_t mode);
 
 /* Total kernel launches issued by the library on this thread since load. */
 GBMOE_API int64_t moe_launch_count(void);

@@ -410,6 +410,14 @@ def launch_count() -> int:
     return lib().moe_launch_count()
 
 
+def set_gather_mode(mode: str = "auto"):
+    """Where GEMM1 takes its rows from: "auto", "separate" (a gather kernel
+    writes the expert-sorted rows first) or "fused" (GEMM1 copies them from
+    the token rows itself).  Results are identical."""
+    _check(lib().moe_set_gather_mode({"auto": 0, "separate": 1, "fused": 2}[mode]),
+           "moe_set_gather_mode")
+
+
 def profiler_start():
     _check(lib().moe_profiler_start(), "moe_profiler_start")
 
@@ -424,7 +432,7 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
-           "moe_forward_host", "HostStaging",
+           "moe_forward_host", "HostStaging", "set_gather_mode",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
            "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",

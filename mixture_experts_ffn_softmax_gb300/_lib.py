@@ -68,6 +68,7 @@ SIGNATURES = {
     "moe_quant_rows_fp8": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
     "moe_dequant_weights": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp,
                                     c_vp]),
+    "moe_set_gather_mode": (c_i32, [c_i32]),
     "moe_forward_host": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                  c_vp, ctypes.c_size_t, c_i32, c_vp]),
     "moe_forward_wq": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32,

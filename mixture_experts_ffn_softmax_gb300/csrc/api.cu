@@ -45,9 +45,24 @@ cudaEvent_t take_event() {
 
 namespace {
 std::atomic<int> g_gemm_tile_mode{0};
+std::atomic<int> g_gather_mode{0};
 }  // namespace
 
 int gemm_tile_mode() { return g_gemm_tile_mode.load(std::memory_order_relaxed); }
+
+// Automatic choice: fused when the routed rows are few (<= 16 MiB of them).
+// The gather warp's 16-byte copies move ~16 B per cycle per SM, half of what
+// GEMM1's MMAs consume on large shapes (Mixtral prefill GEMM1 1257 -> 2446
+// us fused), while on small ones the fused copy saves the gather's launch
+// and the padding rows' loads (M=64 test shape 34 -> 29 us, DeepSeek-V3
+// M=64 2.90 -> 2.83 ms).
+bool gemm1_fused_gather(int64_t rows, int32_t H, int32_t I, int32_t E) {
+  const int mode = g_gather_mode.load(std::memory_order_relaxed);
+  if (mode != 0) return mode == 2;
+  (void)I;
+  (void)E;
+  return rows * static_cast<int64_t>(H) * 2 <= (int64_t{16} << 20);
+}
 
 moe_status_t set_error(moe_status_t st, const char* fmt, ...) {
   va_list ap;
@@ -229,6 +244,12 @@ int64_t moe_launch_count(void) { return g_launches; }
 moe_status_t moe_set_gemm_tiles(int32_t mode) {
   if (mode < 0 || mode > 2) return set_error(MOE_ERR_INVALID_ARG, "gemm tile mode %d", mode);
   g_gemm_tile_mode.store(mode, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_set_gather_mode(int32_t mode) {
+  if (mode < 0 || mode > 2) return set_error(MOE_ERR_INVALID_ARG, "gather mode %d", mode);
+  g_gather_mode.store(mode, std::memory_order_relaxed);
   return MOE_OK;
 }
 
@@ -498,7 +519,11 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
     if (wait_rows != nullptr && c0 == 0 && cudaStreamWaitEvent(s, wait_rows, 0) != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaStreamWaitEvent: %s",
                        cudaGetErrorString(cudaGetLastError()));
-    if (moe_status_t st = launch_gather(ga, s)) return st;
+    // GEMM1 copies its A rows from the token rows itself, or they are
+    // gathered into a_perm first
+    const bool fused_gather = gemm1_fused_gather(Rc, H, I, E);
+    if (!fused_gather)
+      if (moe_status_t st = launch_gather(ga, s)) return st;
 
     bf16* z = at<bf16>(workspace, L.z);
     GroupedGemmArgs g1{};
@@ -517,6 +542,10 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
     g1.error_word = err;
     g1.num_sms = sms;
     g1.rows_hint = Rc;
+    if (fused_gather) {
+      g1.a_rows = x + c0 * H;
+      g1.div = top_k;
+    }
     if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
 
     float* o = at<float>(workspace, L.o);

@@ -186,7 +186,14 @@ struct GroupedGemmArgs {
   int32_t wq_group = 0;
   const void* wq_scale = nullptr;
   const void* wq_zero = nullptr;
+  // GEMM1 with the gather fused (bf16): the token rows [M, K] that A's rows
+  // are copied from (row r = token row_index[r] / div), or null (A = a)
+  const bf16* a_rows = nullptr;
 };
+// Whether GEMM1 copies its A rows from the token rows itself: the mode set
+// by moe_set_gather_mode (0 auto, 1 separate gather kernel, 2 fused) and,
+// for auto, the call's shape.
+bool gemm1_fused_gather(int64_t rows, int32_t H, int32_t I, int32_t E);
 moe_status_t launch_gemm1_swiglu_fp8(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_gemm2_sorted_fp8(const GroupedGemmArgs& a, cudaStream_t s);
 // Dense GEMM with fp32 output: out [M, N] = a [M, K] @ w [K, N] + bias [N]

@@ -176,6 +176,7 @@ struct KParams {
   const float* row_weight;
   int32_t* error_word;
   int32_t E, N, K, NB, sentinel, div;
+  const void* a_rows;  // gathered A: token rows [M, K] (row r: token row_index[r] / div)
   int32_t dense_rows;             // > 0: one expert, rows [0, dense_rows), no offsets
   const float* gemm1_row_weight;  // SwiGLU: per-item weight multiplied into z, or null
   // FP8 dequantisation: acc * a_scale[row] * w_scale[e, col] (per channel,
@@ -372,7 +373,7 @@ __device__ __forceinline__ void swiglu_prefetch(const KParams& P, int e, int n_b
   }
 }
 
-template <Epi EPI, int CG, bool F8, Wq WQ = Wq::None, bool BS = false>
+template <Epi EPI, int CG, bool F8, Wq WQ = Wq::None, bool BS = false, bool GA = false>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                           const CUtensorMap* tmO, const CUtensorMap* tmS,
                                           const CUtensorMap* tmZ, const KParams& P) {
@@ -388,6 +389,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   constexpr int AWARP = 2 + CONV;  // quantised B: the warp loading A
   constexpr int EPI0 = WQM ? AWARP + 1 : 2;  // first epilogue warp
   constexpr int NEPI = BS ? 16 : EPI_WARPS;  // epilogue warps
+  // GA (gathered A): A rows copied from the token rows by the gather warp
+  // that follows the epilogue warps, instead of TMA loads of permuted rows
+  constexpr int GWARP = EPI0 + NEPI;
+  static_assert(!GA || (!WQM && !BS && !F8 && EPI == Epi::SwiGLU), "gathered A: bf16 GEMM1");
   // Int4 / MX B tiles hold each aligned group of 8 columns in the order
   // 0 4 1 5 2 6 3 7 (wq_pair_pos), and so does the accumulator: the epilogue
   // reads column n of a group from position wq_pair_pos(n)
@@ -439,7 +444,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       // quantised B: the converter warps and the A warp (arrive + bytes);
       // the odd CTA of a pair loads A onto the even CTA's barrier, so its
       // own (read by its relay) counts the converters alone
-      ptx::mbar_init(&ctl.full[i], WQM ? CONV + (CG == 1 || rank == 0 ? 1 : 0) : 1);
+      // gathered A: the producer's arrival (B's bytes) and the gather warp's
+      // 32 lanes; the odd CTA of a pair counts its gather lanes alone (read
+      // by its relay)
+      ptx::mbar_init(&ctl.full[i], WQM  ? CONV + (CG == 1 || rank == 0 ? 1 : 0)
+                                   : GA ? 32 + (CG == 1 || rank == 0 ? 1 : 0)
+                                        : 1);
       ptx::mbar_init(&ctl.empty[i], 1);
     }
     if constexpr (WQM) {
@@ -456,7 +466,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(tmA);
+    if constexpr (!GA) ptx::prefetch_tmap(tmA);
     ptx::prefetch_tmap(tmB);
     if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SwiGLU) ptx::prefetch_tmap(tmO);
     if constexpr (WQM) {
@@ -721,10 +731,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             break;
           }
           uint8_t* sa = tiles + stage * G::STAGE;
-          uint8_t* sb = sa + A_STAGE_BYTES;
+          uint8_t* sb = sa + G::B_OFF;
+          // (gathered A: the stage's B bytes only)
           if constexpr (CG == 1) {
-            ptx::mbar_arrive_expect_tx(&ctl.full[stage], G::STAGE);
-            ptx::tma_load_2d(sa, tmA, &ctl.full[stage], kb * G::BKE, row0);
+            ptx::mbar_arrive_expect_tx(&ctl.full[stage], GA ? G::STAGE - G::B_OFF : G::STAGE);
+            if constexpr (!GA) ptx::tma_load_2d(sa, tmA, &ctl.full[stage], kb * G::BKE, row0);
 #pragma unroll
             for (int c = 0; c < G::CHUNKS; ++c) {
               if constexpr (EPI == Epi::SwiGLU)  // gate cols [nb*128,+128), then the up half
@@ -739,8 +750,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             // both CTAs' copies complete on the even CTA's barrier, which
             // expects the bytes of the whole pair
             const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(&ctl.full[stage]), 0);
-            if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * G::STAGE);
-            ptx::tma_load_2d_pair(sa, tmA, full0, kb * G::BKE, row0);
+            if (rank == 0)
+              ptx::mbar_arrive_expect_tx(&ctl.full[stage],
+                                         GA ? 2 * (G::STAGE - G::B_OFF) + kRelayBytes : 2 * G::STAGE);
+            if constexpr (!GA) ptx::tma_load_2d_pair(sa, tmA, full0, kb * G::BKE, row0);
 #pragma unroll
             for (int c = 0; c < G::B_CHUNKS_CTA; ++c) {
               const int gc = static_cast<int>(rank) * G::B_CHUNKS_CTA + c;  // chunk of the tile
@@ -840,7 +853,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           }
         }
       }
-    } else if (CG == 2 && WQM && lane == 0) {
+    } else if (CG == 2 && (WQM || GA) && lane == 0) {
       // ---------------------------------- relay (odd CTA, quantised B) --
       // Once this CTA's converter warps have all arrived for a stage (each
       // after fencing its writes for the async proxy), a 16-byte bulk copy
@@ -867,6 +880,72 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         }
       }
     }
+  } else if (GA && warp == GWARP) {
+    // ------------------------------------------------ A gatherer (GA) --
+    // The stage's A rows straight from the token rows: row r of the tile is
+    // item row_index[row0 + r] of token item / top_k; padding slots, rows
+    // past the expert and columns past K are zero-filled.  Lane l copies rows
+    // l, l + 32, l + 64, l + 96: eight 16-byte cp.async per row into the
+    // 128-byte-swizzled K-major layout TMA would have produced (16-byte chunk
+    // c of row r at c ^ (r & 7)).  A lane waits for its own copies kGaLag
+    // stages behind, fences them for the async proxy and then arrives on
+    // that stage's barrier (the odd CTA of a pair: its own, for the relay).
+    constexpr int kGaLag = 2;
+    static_assert(!GA || kGaLag < G::NSTAGES, "gather lag within the ring");
+    const bf16* xa = reinterpret_cast<const bf16*>(P.a_rows);
+    int stage = 0, sig = 0;
+    uint32_t phase = 0;
+    int pending = 0;  // stages copied but not yet signalled (the oldest is `sig`)
+    bool ok = true;
+    auto signal_oldest = [&]() {
+      ptx::fence_proxy_async_smem();  // this lane's completed copies -> the tensor core
+      ptx::mbar_arrive(&ctl.full[sig]);
+      if (++sig == G::NSTAGES) sig = 0;
+      --pending;
+    };
+    for (int t = unit; t < total_tiles && ok; t += units) {
+      int e, row0, nb;
+      bool mine;
+      tile_of(t, e, row0, nb, mine);
+      const bf16* src[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int32_t item = mine ? P.row_index[row0 + lane + 32 * i] : P.sentinel;
+        src[i] = (item >= 0 && item < P.sentinel)
+                     ? xa + static_cast<int64_t>(item / P.div) * P.K : nullptr;
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        const bool got = bounded_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort, P.error_word);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = tiles + stage * G::STAGE;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane + 32 * i;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int col = kb * G::BKE + 8 * c;
+            const bool live = src[i] != nullptr && col < P.K;  // K % 8 == 0
+            ptx::cp_async_16(dst + r * 128 + ((c ^ (r & 7)) << 4), live ? src[i] + col : xa,
+                             live ? 16u : 0u);
+          }
+        }
+        ptx::cp_async_commit();
+        ++pending;
+        if (pending > kGaLag) {
+          ptx::cp_async_wait<kGaLag>();
+          signal_oldest();
+        }
+        if (++stage == G::NSTAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    ptx::cp_async_wait<0>();
+    while (pending > 0) signal_oldest();
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;               // TMEM lane quadrant this warp may access
@@ -1255,6 +1334,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   gemm_body<EPI, 2, F8>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
 }
 
+// bf16 GEMM1 with the gather fused: the gather warp after the epilogue
+// warps copies A's rows from the token rows.
+constexpr int GA_THREADS = NTHREADS + 32;
+template <Epi EPI>
+__global__ void __launch_bounds__(GA_THREADS, 1)
+    grouped_gemm_ga_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  gemm_body<EPI, 1, false, Wq::None, false, true>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
+}
+template <Epi EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA_THREADS, 1)
+    grouped_gemm_ga_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                                const __grid_constant__ CUtensorMap tmB,
+                                const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  gemm_body<EPI, 2, false, Wq::None, false, true>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
+}
+
 // FP8 with block-wise (128 x 128) weight scales and per-(row, 128-group)
 // activation scales: single-CTA tiles, one accumulation per K stage.
 constexpr int BS_THREADS = 64 + 16 * 32;  // producer + MMA + 16 epilogue warps
@@ -1360,6 +1457,7 @@ KParams base_params(const GroupedGemmArgs& a, int NB) {
   P.NB = NB;
   P.sentinel = a.sentinel;
   P.div = a.div > 0 ? a.div : 1;
+  P.a_rows = a.a_rows;
   P.dense_rows = (EPI == Epi::DenseF32) ? static_cast<int32_t>(a.sentinel) : 0;
   P.gemm1_row_weight = a.gemm1_row_weight;
   P.a_scale = a.a_scale;
@@ -1480,6 +1578,70 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
   prof_before(name, s);
   grouped_gemm_kernel<EPI, F8><<<grid, NTHREADS, G1::SMEM, s>>>(tmA, tmB, tmO, P);
+  prof_after(name, s);
+  return check_launch(name);
+}
+
+// bf16 GEMM1 with the gather fused (a.a_rows: the token rows); tiles as
+// launch_gemm's.  tmA is built on a.a but not read.
+moe_status_t launch_gemm1_ga(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
+  constexpr Epi EPI = Epi::SwiGLU;
+  using G1 = Geo<1, false>;
+  using G2 = Geo<2, false>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(grouped_gemm_ga_kernel<EPI>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(G1::SMEM)) != cudaSuccess ||
+        cudaFuncSetAttribute(grouped_gemm_ga_pair_kernel<EPI>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(G2::SMEM)) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                       cudaGetErrorString(cudaGetLastError()));
+    attr_done = true;
+  }
+  if ((a.K & 7) != 0 || (reinterpret_cast<uintptr_t>(a.a_rows) & 15u) != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "%s: token rows must be 16-byte aligned rows", name);
+  CUtensorMap tmA, tmB, tmO;
+  int NB;
+  if (moe_status_t st = make_ab_maps<EPI, false>(a, &tmA, &tmB, &NB)) return st;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.cap)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
+    const uint32_t box[2] = {64, 32};
+    if (moe_status_t st = make_map(&tmO, a.out, 2, dims, strides, box,
+                                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      return st;
+  }
+  KParams P = base_params<EPI>(a, NB);
+  const int64_t max_blocks = a.cap / BM;
+  if (max_blocks <= 0) return MOE_OK;
+  if (use_pairs(a)) {
+    static int resident = -1;
+    if (resident < 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (a.num_sms / 2));
+      cfg.blockDim = dim3(GA_THREADS);
+      cfg.dynamicSmemBytes = G2::SMEM;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_ga_pair_kernel<EPI>, &cfg) !=
+              cudaSuccess ||
+          n <= 0) {
+        cudaGetLastError();
+        n = a.num_sms / 2;
+      }
+      resident = std::min(n, a.num_sms / 2);
+    }
+    const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
+    const unsigned clusters = static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
+    prof_before(name, s);
+    grouped_gemm_ga_pair_kernel<EPI><<<2 * clusters, GA_THREADS, G2::SMEM, s>>>(tmA, tmB, tmO, P);
+    prof_after(name, s);
+    return check_launch(name);
+  }
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
+  prof_before(name, s);
+  grouped_gemm_ga_kernel<EPI><<<grid, GA_THREADS, G1::SMEM, s>>>(tmA, tmB, tmO, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -1642,6 +1804,7 @@ moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStre
 }
 
 moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s) {
+  if (a.a_rows != nullptr) return launch_gemm1_ga(a, "gemm1_swiglu", s);
   return launch_gemm<Epi::SwiGLU>(a, "gemm1_swiglu", s);
 }
 moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s) {

@@ -30,17 +30,26 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert (y.float() == 0).all()
 
 
-def test_profiler_counts_launches():
+@pytest.mark.parametrize("gather", ["separate", "fused"])
+def test_profiler_counts_launches(gather):
     M, H, I, E, k = 32, 64, 64, 2, 1
     x = torch.ones(M, H, device="cuda").bfloat16()
     w13 = torch.zeros(E, H, 2 * I, device="cuda").bfloat16()
     w2 = torch.zeros(E, I, H, device="cuda").bfloat16()
-    n0 = pkg.launch_count()
-    pkg.profiler_start()
-    pkg.moe_forward(x, torch.ones(M, k, device="cuda"),
-                    torch.zeros(M, k, dtype=torch.int32, device="cuda"), w13, w2)
-    prof = pkg.profiler_stop()
+    pkg.set_gather_mode(gather)
+    try:
+        n0 = pkg.launch_count()
+        pkg.profiler_start()
+        pkg.moe_forward(x, torch.ones(M, k, device="cuda"),
+                        torch.zeros(M, k, dtype=torch.int32, device="cuda"), w13, w2)
+        prof = pkg.profiler_stop()
+    finally:
+        pkg.set_gather_mode("auto")
     assert pkg.launch_count() - n0 == sum(v[0] for v in prof.values())
-    for name in ("align_small", "gather_rows", "gemm1_swiglu",
-                 "gemm2_sorted", "reduce_sorted"):
+    names = ["align_small", "gemm1_swiglu", "gemm2_sorted", "reduce_sorted"]
+    if gather == "separate":
+        names.append("gather_rows")
+    else:
+        assert "gather_rows" not in prof
+    for name in names:
         assert prof[name][0] == 1 and prof[name][1] > 0

@@ -77,8 +77,9 @@ def test_fused_layer_small_workloads(name):
 def test_intermediate_stages():
     """Inside the forward's workspace: the sorted item list and the inverse
     permutation are bit-exact against the oracle's align, the permuted rows
-    are bit-exact copies of the routed tokens, and z (GEMM1 output) matches
-    SiLU(gate) * up of the oracle within bf16 rounding."""
+    (written by the separate gather kernel) are bit-exact copies of the
+    routed tokens, and z (GEMM1 output) matches SiLU(gate) * up of the oracle
+    within bf16 rounding."""
     spec = wl.SMALL_SPECS["mixtral_small"]
     d = wl.make_moe_inputs(spec, device="cuda")
     w, ids, _ = _oracle_route(spec, d["router_logits"])
@@ -86,8 +87,12 @@ def test_intermediate_stages():
     tids = torch.from_numpy(ids).cuda()
     M, H, I, E, k = spec.M, spec.H, spec.I, spec.E, spec.top_k
     ws = pkg.alloc_workspace(pkg.workspace_size(M, H, I, E, k))
-    pkg.moe_forward(d["hidden"], tw, tids, d["w13"], d["w2"], workspace=ws)
-    torch.cuda.synchronize()
+    pkg.set_gather_mode("separate")
+    try:
+        pkg.moe_forward(d["hidden"], tw, tids, d["w13"], d["w2"], workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        pkg.set_gather_mode("auto")
     lay = pkg.workspace_layout(M, H, I, E, k)
     al = oracle.align(ids, E, pkg.BLOCK_M)
     n = al["num_tokens_post_padded"]
