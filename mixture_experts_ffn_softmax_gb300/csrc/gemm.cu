@@ -400,6 +400,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   auto acc_pos = [](int n) { return PERM ? (n & ~7) + wq_pair_pos(n & 7) : n; };
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl<G::NSTAGES> ctl;
+  static_assert(G::SMEM + sizeof(Ctl<G::NSTAGES>) <= 232448,
+                "dynamic + static shared memory within the per-block limit");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
