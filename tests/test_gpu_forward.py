@@ -150,6 +150,8 @@ def test_forward_in_place_and_reuse():
     dict(M=20000, H=64, I=64, E=4, k=2),   # crosses the 16384-token chunk
     dict(M=3, H=16, I=8, E=2, k=2),        # H, I below one 64-wide TMA box
     dict(M=70, H=8, I=24, E=3, k=1),
+    dict(M=100, H=64, I=64, E=1024, k=64),  # the largest expert count and top_k
+    dict(M=50, H=64, I=64, E=64, k=64),     # every expert, top_k = E = 64
 ])
 def test_forward_edge_cases(case, reduce, tiles):
     g = torch.Generator(device="cuda").manual_seed(5)
