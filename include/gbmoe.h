@@ -270,10 +270,16 @@ GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_we
  *  route             routing parameters, with moe_route's meaning and limits
  *  w13, w2, w13_bias, w2_bias, workspace, workspace_bytes, reduce_mode:
  *                    as moe_forward
- * Order on `stream`: the logits' copy, routing and the expert-sorted plan,
- * while the hidden rows are copied on a copy stream the library keeps per
- * host thread and device (joined by an event before the rows are gathered);
- * then the GEMMs, the reduce and the copy of out to io->h_out.  Returns after
+ * Order: the copies in run on a host-to-device stream and the copies out on
+ * a device-to-host stream, both kept by the library per host thread and
+ * device and ordered with `stream` by events; routing, the plan, the GEMMs
+ * and the reduce run on `stream`, each token chunk's rows awaited right
+ * before they are first read.  Layers whose halves still average >= 512
+ * routed rows per expert and whose copies are large against their weights
+ * (copied bytes x 11 > weight bytes) run as two token chunks (results
+ * identical to one pass), so the second chunk's rows are copied in while
+ * the first is computed and the first chunk's output is copied out while
+ * the second is computed.  Returns after
  * enqueueing; io->h_out holds the result once `stream` has passed the call
  * (cudaStreamSynchronize or an event).  The call can be captured in a CUDA
  * graph.  Errors: as moe_route and moe_forward (checked before anything is

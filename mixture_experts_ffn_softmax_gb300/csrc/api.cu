@@ -488,13 +488,14 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
                                    int32_t E, int32_t top_k, const void* w13, const void* w2,
                                    const void* w13_bias, const void* w2_bias, void* workspace,
                                    const moe_forward_opts_t* opts, void* out, int sms,
-                                   cudaEvent_t wait_rows, cudaStream_t s) {
+                                   cudaEvent_t wait_rows, cudaStream_t s,
+                                   bool reset_error = true) {
   const int32_t reduce_mode = opts->reduce_mode;
   const bool weight_on_input = opts->apply_router_weight_on_input != 0;
   const int64_t Mc_max = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
   const FwdLayout L = fwd_layout(Mc_max, H, I, E, top_k);
   int32_t* err = at<int32_t>(workspace, L.err);
-  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+  if (reset_error && cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
 
   const bf16* x = static_cast<const bf16*>(hidden);
@@ -601,9 +602,11 @@ moe_status_t moe_forward_opts(const void* hidden, const float* topk_weights,
 namespace {
 // Per host thread and device: the stream the hidden rows are copied on and
 // the events that fork it from, and join it to, the caller's stream.
+constexpr int kMaxHostChunks = 2;
 struct CopyLane {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, rows = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t fork = nullptr, join_in = nullptr, join_out = nullptr;
+  cudaEvent_t logits[kMaxHostChunks] = {}, rows[kMaxHostChunks] = {}, out[kMaxHostChunks] = {};
 };
 constexpr int kMaxDevices = 64;
 
@@ -613,11 +616,18 @@ moe_status_t copy_lane(CopyLane** lane) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return set_error(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(cudaGetLastError()));
   CopyLane& l = lanes[dev];
-  if (l.stream == nullptr) {
-    if (cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&l.rows, cudaEventDisableTiming) != cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "copy stream: %s", cudaGetErrorString(cudaGetLastError()));
+  if (l.h2d == nullptr) {
+    bool ok = cudaStreamCreateWithFlags(&l.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&l.d2h, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* ev : {&l.fork, &l.join_in, &l.join_out})
+      ok = ok && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < kMaxHostChunks; ++i)
+      for (cudaEvent_t* ev : {&l.logits[i], &l.rows[i], &l.out[i]})
+        ok = ok && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      l.h2d = nullptr;
+      return set_error(MOE_ERR_CUDA, "copy streams: %s", cudaGetErrorString(cudaGetLastError()));
+    }
   }
   *lane = &l;
   return MOE_OK;
@@ -651,30 +661,78 @@ moe_status_t moe_forward_host(const moe_host_io_t* io, int64_t M, int32_t H, int
   auto cuda_fail = [](const char* what) {
     return set_error(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(cudaGetLastError()));
   };
-  const size_t row_bytes = static_cast<size_t>(M) * H * sizeof(bf16);
-  if (cudaMemcpyAsync(io->d_logits, io->h_logits, static_cast<size_t>(M) * E * sizeof(float),
-                      cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return cuda_fail("cudaMemcpyAsync(logits)");
-  // fork: the hidden rows' copy overlaps routing and the expert-sorted plan
+  // Two token chunks -- the second chunk's rows copied in while the first is
+  // computed, the first chunk's output copied out while the second is --
+  // when each half still averages >= 512 routed rows per expert (the GEMMs
+  // keep their tile shape, so the results are those of one pass) and the
+  // copies are large against the weights, which each chunk reads again:
+  // about half the copy time (host link ~300 GB/s) is hidden, one more
+  // pass over the weights (HBM ~6.8 TB/s) is paid.  Measured through this
+  // call: Qwen-MoE shape (142 MB copied, 1.2 GB of weights) 1.985 -> 1.870
+  // ms in two chunks; Mixtral shape (67 MB, 2.8 GB) 2.111 -> 2.300 ms.
+  const int32_t k = route->top_k;
+  const int64_t copy_bytes = M * (int64_t{4} * H + int64_t{4} * E);
+  const int64_t weight_bytes = int64_t{6} * E * H * I;
+  const int chunks =
+      ((M / 2) * k >= int64_t{512} * E && copy_bytes * 11 > weight_bytes) ? 2 : 1;
+  int64_t m0s[kMaxHostChunks + 1];
+  for (int c = 0; c <= chunks; ++c) m0s[c] = M * c / chunks;
+  // fork the copy streams off the caller's stream; join them on every way out
   if (cudaEventRecord(lane->fork, s) != cudaSuccess ||
-      cudaStreamWaitEvent(lane->stream, lane->fork, 0) != cudaSuccess ||
-      cudaMemcpyAsync(io->d_hidden, io->h_hidden, row_bytes, cudaMemcpyHostToDevice,
-                      lane->stream) != cudaSuccess ||
-      cudaEventRecord(lane->rows, lane->stream) != cudaSuccess)
-    return cuda_fail("hidden rows copy");
-  moe_status_t st = route_impl(io->d_logits, 0, M, E, route->top_k, route->routing_method,
-                               route->renormalize, route->k_group, route->group_count,
-                               route->group_select_mode, route->routed_scaling_factor,
-                               io->topk_weights, io->topk_ids, s);
-  if (st == MOE_OK)
-    st = forward_launch(io->d_hidden, io->topk_weights, io->topk_ids, M, H, I, E, route->top_k,
-                        w13, w2, w13_bias, w2_bias, workspace, &o, io->d_out, sms, lane->rows, s);
-  if (st != MOE_OK) {
-    cudaStreamWaitEvent(s, lane->rows, 0);  // join the copy stream on the way out as well
-    return st;
+      cudaStreamWaitEvent(lane->h2d, lane->fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(lane->d2h, lane->fork, 0) != cudaSuccess)
+    return cuda_fail("copy stream fork");
+  auto join = [&]() {
+    cudaEventRecord(lane->join_in, lane->h2d);
+    cudaEventRecord(lane->join_out, lane->d2h);
+    cudaStreamWaitEvent(s, lane->join_in, 0);
+    cudaStreamWaitEvent(s, lane->join_out, 0);
+  };
+  const bf16* hx = static_cast<const bf16*>(io->h_hidden);
+  bf16* hy = static_cast<bf16*>(io->h_out);
+  bf16* dx = static_cast<bf16*>(io->d_hidden);
+  bf16* dy = static_cast<bf16*>(io->d_out);
+  for (int c = 0; c < chunks; ++c) {
+    const int64_t m0 = m0s[c], mc = m0s[c + 1] - m0s[c];
+    if (cudaMemcpyAsync(io->d_logits + m0 * E, io->h_logits + m0 * E,
+                        static_cast<size_t>(mc) * E * sizeof(float), cudaMemcpyHostToDevice,
+                        lane->h2d) != cudaSuccess ||
+        cudaEventRecord(lane->logits[c], lane->h2d) != cudaSuccess ||
+        cudaMemcpyAsync(dx + m0 * H, hx + m0 * H, static_cast<size_t>(mc) * H * sizeof(bf16),
+                        cudaMemcpyHostToDevice, lane->h2d) != cudaSuccess ||
+        cudaEventRecord(lane->rows[c], lane->h2d) != cudaSuccess) {
+      join();
+      return cuda_fail("host-to-device copy");
+    }
   }
-  if (cudaMemcpyAsync(io->h_out, io->d_out, row_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return cuda_fail("cudaMemcpyAsync(out)");
+  for (int c = 0; c < chunks; ++c) {
+    const int64_t m0 = m0s[c], mc = m0s[c + 1] - m0s[c];
+    moe_status_t st = MOE_OK;
+    if (cudaStreamWaitEvent(s, lane->logits[c], 0) != cudaSuccess) st = cuda_fail("logits wait");
+    if (st == MOE_OK)
+      st = route_impl(io->d_logits + m0 * E, 0, mc, E, k, route->routing_method,
+                      route->renormalize, route->k_group, route->group_count,
+                      route->group_select_mode, route->routed_scaling_factor,
+                      io->topk_weights + m0 * k, io->topk_ids + m0 * k, s);
+    // the rows' copy overlaps routing and the plan: the forward waits for it
+    // right before the rows are first read
+    if (st == MOE_OK)
+      st = forward_launch(dx + m0 * H, io->topk_weights + m0 * k, io->topk_ids + m0 * k, mc, H,
+                          I, E, k, w13, w2, w13_bias, w2_bias, workspace, &o, dy + m0 * H, sms,
+                          lane->rows[c], s, /*reset_error=*/c == 0);
+    if (st == MOE_OK &&
+        (cudaEventRecord(lane->out[c], s) != cudaSuccess ||
+         cudaStreamWaitEvent(lane->d2h, lane->out[c], 0) != cudaSuccess ||
+         cudaMemcpyAsync(hy + m0 * H, dy + m0 * H, static_cast<size_t>(mc) * H * sizeof(bf16),
+                         cudaMemcpyDeviceToHost, lane->d2h) != cudaSuccess))
+      st = cuda_fail("device-to-host copy");
+    if (st != MOE_OK) {
+      cudaStreamWaitEvent(s, lane->rows[c], 0);
+      join();
+      return st;
+    }
+  }
+  join();
   return MOE_OK;
 }
 

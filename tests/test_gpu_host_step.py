@@ -44,11 +44,16 @@ def test_host_step_equals_device_layer(name, pinned):
     assert torch.equal(y, want.cpu())
 
 
-def test_host_step_full_size_mixtral_prefill():
-    spec = wl.SPECS["mixtral_prefill"]
+@pytest.mark.parametrize("name", ["mixtral_prefill", "qwen_skew", "deepseek_m64"])
+def test_host_step_full_size(name):
+    """Full-size layers: the Qwen shape runs as two token chunks with the
+    copies overlapping the compute, the Mixtral and DeepSeek shapes in one
+    pass; the output equals one device pass bit for bit."""
+    spec = wl.SPECS[name]
     d = wl.make_moe_inputs(spec, device="cuda")
     hx, hl = d["hidden"].cpu().pin_memory(), d["router_logits"].cpu().pin_memory()
-    y = pkg.moe_forward_host(hx, hl, d["w13"], d["w2"], stream=torch.cuda.current_stream(),
+    y = pkg.moe_forward_host(hx, hl, d["w13"], d["w2"], w13_bias=d["w13_bias"],
+                             w2_bias=d["w2_bias"], stream=torch.cuda.current_stream(),
                              **_route_kw(spec))
     torch.cuda.synchronize()
     assert torch.equal(y, _device_layer(spec, d).cpu())
