@@ -37,7 +37,7 @@ Sources (page title, section):
   format (num_experts, max_tokens, K) with expert_num_tokens, where not
   every row is valid.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * w13 columns [0, I) are the gate half and [I, 2I) the up half.
 * b13 is added to both halves before SiLU-and-mul; b2 is added per routed
