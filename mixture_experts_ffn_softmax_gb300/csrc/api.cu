@@ -103,7 +103,8 @@ moe_status_t check_device(int* num_sms) {
     cudaGetLastError();
     return set_error(MOE_ERR_NO_DEVICE, "no CUDA device");
   }
-  static int cached_dev = -1, cached_ok = 0, cached_sms = 0;
+  // per host thread: the last device asked about (no shared mutable state)
+  thread_local int cached_dev = -1, cached_ok = 0, cached_sms = 0;
   if (dev != cached_dev) {
     int major = 0, minor = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);

@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/gbmoe.h"
 
@@ -36,6 +37,37 @@ moe_status_t check_launch(const char* name);
 
 // GEMM tile shape selection: 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles.
 int gemm_tile_mode();
+
+// A value computed once per device (function attributes, occupancy), safely
+// from several host threads: get(f) returns f()'s result for the current
+// device, calling f the first time for that device (again after a failure).
+class PerDevice {
+ public:
+  template <typename F>
+  cudaError_t get(F&& f, int* value = nullptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) {
+      cudaGetLastError();
+      return cudaErrorInvalidDevice;
+    }
+    std::lock_guard<std::mutex> lock(mutex_);
+    if (!have_[dev]) {
+      int v = 0;
+      const cudaError_t e = f(&v);
+      if (e != cudaSuccess) return e;
+      value_[dev] = v;
+      have_[dev] = true;
+    }
+    if (value) *value = value_[dev];
+    return cudaSuccess;
+  }
+
+ private:
+  static constexpr int kDevices = 64;
+  std::mutex mutex_;
+  bool have_[kDevices] = {};
+  int value_[kDevices] = {};
+};
 
 // ---- launchers (one per .cu file) ----
 struct RouteArgs {

@@ -86,13 +86,19 @@ __global__ void __launch_bounds__(256)
 }
 
 int device_sms() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  static PerDevice sms_per_device;
+  int sms = 148;
+  sms_per_device.get(
+      [](int* v) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            *v <= 0)
+          *v = 148;
+        cudaGetLastError();
+        return cudaSuccess;
+      },
+      &sms);
   return sms;
 }
 
@@ -232,14 +238,12 @@ template <int EMAX>
 moe_status_t launch_router_small_t(const bf16* x, const bf16* wg, const bf16* bg, int64_t M,
                                    int H, int E, float* s, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(H) * EMAX * sizeof(float) + (H / 8) * 16;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(router_small_kernel<EMAX>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
-        cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(router_small)");
-    attr = true;
-  }
+  static PerDevice attrs;
+  if (attrs.get([](int*) {
+        return cudaFuncSetAttribute(router_small_kernel<EMAX>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+      }) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(router_small)");
   const unsigned grid = static_cast<unsigned>(
       std::min<int64_t>(ceil_div<int64_t>(M, kRouterWarps), device_sms()));
   prof_before("router_small", st);

@@ -1511,18 +1511,19 @@ template <Epi EPI, bool F8 = false>
 moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
   using G1 = Geo<1, F8>;
   using G2 = Geo<2, F8>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<EPI, F8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(G1::SMEM)) != cudaSuccess ||
-        cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI, F8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(G2::SMEM)) != cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
-                       cudaGetErrorString(cudaGetLastError()));
-    attr_done = true;
-  }
+  static PerDevice attrs;
+  if (attrs.get([](int*) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, F8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(G1::SMEM));
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI, F8>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(G2::SMEM));
+        return e;
+      }) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                     cudaGetErrorString(cudaGetLastError()));
   CUtensorMap tmA, tmB;
   int NB;
   if (moe_status_t st = make_ab_maps<EPI, F8>(a, &tmA, &tmB, &NB)) return st;
@@ -1554,21 +1555,23 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   if (EPI != Epi::DenseF32 && use_pairs(a)) {
     // Persistent pairs: no more clusters than can be resident at once (the
     // tiles are split statically among them).
-    static int resident = -1;
-    if (resident < 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (a.num_sms / 2));
-      cfg.blockDim = dim3(NTHREADS);
-      cfg.dynamicSmemBytes = G2::SMEM;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI, F8>, &cfg) !=
-              cudaSuccess ||
-          n <= 0) {
-        cudaGetLastError();
-        n = a.num_sms / 2;
-      }
-      resident = std::min(n, a.num_sms / 2);
-    }
+    static PerDevice clusters_per_device;
+    int resident = a.num_sms / 2;
+    clusters_per_device.get(
+        [&](int* v) {
+          cudaLaunchConfig_t cfg = {};
+          cfg.gridDim = dim3(2 * (a.num_sms / 2));
+          cfg.blockDim = dim3(NTHREADS);
+          cfg.dynamicSmemBytes = G2::SMEM;
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI, F8>, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = a.num_sms / 2;
+          }
+          *v = std::min(n, a.num_sms / 2);
+          return cudaSuccess;
+        },
+        &resident);
     // at most blocks/2 + E/2 pair tiles per column block
     const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
     const unsigned clusters = static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
@@ -1590,18 +1593,19 @@ moe_status_t launch_gemm1_ga(const GroupedGemmArgs& a, const char* name, cudaStr
   constexpr Epi EPI = Epi::SwiGLU;
   using G1 = Geo<1, false>;
   using G2 = Geo<2, false>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(grouped_gemm_ga_kernel<EPI>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(G1::SMEM)) != cudaSuccess ||
-        cudaFuncSetAttribute(grouped_gemm_ga_pair_kernel<EPI>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(G2::SMEM)) != cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
-                       cudaGetErrorString(cudaGetLastError()));
-    attr_done = true;
-  }
+  static PerDevice attrs;
+  if (attrs.get([](int*) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_ga_kernel<EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(G1::SMEM));
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(grouped_gemm_ga_pair_kernel<EPI>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(G2::SMEM));
+        return e;
+      }) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                     cudaGetErrorString(cudaGetLastError()));
   if ((a.K & 7) != 0 || (reinterpret_cast<uintptr_t>(a.a_rows) & 15u) != 0)
     return set_error(MOE_ERR_INVALID_ARG, "%s: token rows must be 16-byte aligned rows", name);
   CUtensorMap tmA, tmB, tmO;
@@ -1619,21 +1623,22 @@ moe_status_t launch_gemm1_ga(const GroupedGemmArgs& a, const char* name, cudaStr
   const int64_t max_blocks = a.cap / BM;
   if (max_blocks <= 0) return MOE_OK;
   if (use_pairs(a)) {
-    static int resident = -1;
-    if (resident < 0) {
+    // persistent pairs: no more clusters than can be resident at once
+    static PerDevice clusters_per_device;
+    int resident = a.num_sms / 2;
+    clusters_per_device.get([&](int* v) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * (a.num_sms / 2));
       cfg.blockDim = dim3(GA_THREADS);
       cfg.dynamicSmemBytes = G2::SMEM;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_ga_pair_kernel<EPI>, &cfg) !=
-              cudaSuccess ||
-          n <= 0) {
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_ga_pair_kernel<EPI>, &cfg) != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = a.num_sms / 2;
       }
-      resident = std::min(n, a.num_sms / 2);
-    }
+      *v = std::min(n, a.num_sms / 2);
+      return cudaSuccess;
+    }, &resident);
     const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
     const unsigned clusters = static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
     prof_before(name, s);
@@ -1652,15 +1657,13 @@ moe_status_t launch_gemm1_ga(const GroupedGemmArgs& a, const char* name, cudaStr
 template <Epi EPI>
 moe_status_t launch_gemm_bs(const GroupedGemmArgs& a, const char* name, cudaStream_t s) {
   using G = Geo<1, true>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(grouped_gemm_bs_kernel<EPI>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(G::SMEM)) != cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
-                       cudaGetErrorString(cudaGetLastError()));
-    attr_done = true;
-  }
+  static PerDevice attrs;
+  if (attrs.get([&](int*) {
+        return cudaFuncSetAttribute(grouped_gemm_bs_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(G::SMEM));
+      }) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                     cudaGetErrorString(cudaGetLastError()));
   CUtensorMap tmA, tmB;
   int NB;
   if (moe_status_t st = make_ab_maps<EPI, true>(a, &tmA, &tmB, &NB)) return st;
@@ -1685,14 +1688,13 @@ moe_status_t launch_gemm_wq_cg(const GroupedGemmArgs& a, const char* name, cudaS
                                WqRing<WQ, EPI == Epi::SwiGLU ? 2 : 1>>;
   constexpr int NREG = (CG == 1 && EPI == Epi::SwiGLU) ? 2 : 1;
   auto kernel = CG == 2 ? grouped_gemm_wq_pair_kernel<EPI, WQ> : grouped_gemm_wq_kernel<EPI, WQ>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(G::SMEM)) != cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
-                       cudaGetErrorString(cudaGetLastError()));
-    attr_done = true;
-  }
+  static PerDevice attrs;
+  if (attrs.get([&](int*) {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(G::SMEM));
+      }) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
+                     cudaGetErrorString(cudaGetLastError()));
   const int gsize = a.wq_group;
   const uint32_t gbox = gsize == 32 ? 2u : 1u;  // group rows per 64-row stage
   const uint64_t KG = static_cast<uint64_t>(a.K / gsize);
@@ -1766,19 +1768,23 @@ moe_status_t launch_gemm_wq_cg(const GroupedGemmArgs& a, const char* name, cudaS
   unsigned grid;
   if constexpr (CG == 2) {
     // persistent pairs: no more clusters than can be resident at once
-    static int resident = -1;
-    if (resident < 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (a.num_sms / 2));
-      cfg.blockDim = dim3(cta_threads<WQ>());
-      cfg.dynamicSmemBytes = G::SMEM;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        n = a.num_sms / 2;
-      }
-      resident = std::min(n, a.num_sms / 2);
-    }
+    static PerDevice clusters_per_device;
+    int resident = a.num_sms / 2;
+    clusters_per_device.get(
+        [&](int* v) {
+          cudaLaunchConfig_t cfg = {};
+          cfg.gridDim = dim3(2 * (a.num_sms / 2));
+          cfg.blockDim = dim3(cta_threads<WQ>());
+          cfg.dynamicSmemBytes = G::SMEM;
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = a.num_sms / 2;
+          }
+          *v = std::min(n, a.num_sms / 2);
+          return cudaSuccess;
+        },
+        &resident);
     const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
     grid = 2 * static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
   } else {

@@ -11,13 +11,19 @@ namespace gbmoe {
 namespace {
 
 int sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  static PerDevice sms_per_device;
+  int sms = 148;
+  sms_per_device.get(
+      [](int* v) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            *v <= 0)
+          *v = 148;
+        cudaGetLastError();
+        return cudaSuccess;
+      },
+      &sms);
   return sms;
 }
 
