@@ -496,7 +496,10 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
   const int64_t Mc_max = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
   const FwdLayout L = fwd_layout(Mc_max, H, I, E, top_k);
   int32_t* err = at<int32_t>(workspace, L.err);
-  if (reset_error && cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+  // the error word and, after it, the GEMMs' tile-schedule counters
+  int32_t* sched1 = err + 16;  // GEMM1 {next tile, CTAs done}
+  int32_t* sched2 = err + 24;  // GEMM2
+  if (reset_error && cudaMemsetAsync(err, 0, 32 * sizeof(int32_t), s) != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
 
   const bf16* x = static_cast<const bf16*>(hidden);
@@ -548,6 +551,7 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
       g1.a_rows = x + c0 * H;
       g1.div = top_k;
     }
+    g1.sched = sched1;
     if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
 
     float* o = at<float>(workspace, L.o);
@@ -569,6 +573,7 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
     g2.row_weight = weight_on_input ? nullptr : topk_weights + c0 * top_k;
     g2.sentinel = static_cast<int32_t>(Rc);
     g2.div = top_k;
+    g2.sched = sched2;
     g2.error_word = err;
     g2.num_sms = sms;
     g2.rows_hint = Rc;

@@ -221,6 +221,10 @@ struct GroupedGemmArgs {
   // GEMM1 with the gather fused (bf16): the token rows [M, K] that A's rows
   // are copied from (row r = token row_index[r] / div), or null (A = a)
   const bf16* a_rows = nullptr;
+  // bf16 grouped GEMMs: two int32 {next tile, CTAs done}, zero at launch
+  // (reset by the kernel itself when it ends), for the dynamic tile
+  // schedule; null: static schedule
+  int32_t* sched = nullptr;
 };
 // Whether GEMM1 copies its A rows from the token rows itself: the mode set
 // by moe_set_gather_mode (0 auto, 1 separate gather kernel, 2 fused) and,

@@ -64,7 +64,11 @@ constexpr int TMEM_COLS = 2 * MMA_N;           // 512: two accumulators
 constexpr int MAX_E = 1024;
 constexpr int STAGING_BYTES = 32 * 128;        // per epilogue warp: 32 rows x 128 bytes
 constexpr int kMaxRaw = 8;
-constexpr uint32_t kRelayBytes = 16;  // CTA-pair stage signal (bulk copy size)  // raw ring stages the control block has barriers for
+constexpr uint32_t kRelayBytes = 16;  // CTA-pair stage signal (bulk copy size)
+// Slots of the dynamic tile ring: more than the producer can run ahead of the
+// slowest reader (at most NSTAGES tiles ahead of the MMA, which is at most
+// two tiles ahead of the epilogue).
+constexpr int kTileSlots = 16;  // raw ring stages the control block has barriers for
 
 // CG = CTAs cooperating on one MMA tile.  CG = 1: a 128 x 256 tile per CTA,
 // 48 KB per pipeline stage.  CG = 2 (a CTA pair, tcgen05 cta_group::2): a
@@ -166,6 +170,11 @@ struct Ctl {
   // even CTA's full barrier); relay_src is its (ignored) source
   alignas(16) uint8_t relay_dst[NS][16];
   alignas(16) uint8_t relay_src[16];
+  // dynamic tile schedule: the tile of the i-th unit of work in slot i % 16
+  // (16 bytes each: the odd CTA of a pair receives it by bulk copy), ready
+  // when tile_full[i % 16] completes phase (i / 16) & 1
+  alignas(16) int32_t tile_slot[kTileSlots][4];
+  uint64_t tile_full[kTileSlots];
 };
 
 struct KParams {
@@ -177,6 +186,9 @@ struct KParams {
   int32_t* error_word;
   int32_t E, N, K, NB, sentinel, div;
   const void* a_rows;  // gathered A: token rows [M, K] (row r: token row_index[r] / div)
+  // dynamic tile schedule (bf16 grouped GEMMs): {next tile, CTAs done}, zero
+  // at launch, reset by the last CTA to finish; null: static schedule
+  int32_t* sched;
   int32_t dense_rows;             // > 0: one expert, rows [0, dense_rows), no offsets
   const float* gemm1_row_weight;  // SwiGLU: per-item weight multiplied into z, or null
   // FP8 dequantisation: acc * a_scale[row] * w_scale[e, col] (per channel,
@@ -464,6 +476,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       ptx::mbar_init(&ctl.tmem_full[a], 1);
       ptx::mbar_init(&ctl.tmem_empty[a], CG * NEPI);
     }
+    // the producer's arrival (the odd CTA's with the 16 bytes it expects)
+    for (int i = 0; i < kTileSlots; ++i) ptx::mbar_init(&ctl.tile_full[i], 1);
     ctl.abort = 0;
     ptx::fence_barrier_init();
   }
@@ -497,6 +511,24 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   const int unit = (CG == 2) ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int units = (CG == 2) ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int KB = ceil_div(P.K, G::BKE);
+  // Dynamic tile schedule (bf16 grouped GEMMs with P.sched): the producer
+  // claims tiles from a global counter in order as its unit becomes free, so
+  // the units working on the row blocks that share a weight tile start it
+  // together and find it in L2 (a static round-robin lets them drift up to
+  // most of a tile apart).  The producer publishes each claim in the tile
+  // ring; the other roles read it from there.  Static: unit + i * units.
+  const bool dyn = !WQM && !GA && !BS && P.sched != nullptr;
+  auto tile_at = [&](int i) -> int {  // the i-th tile of this unit, or -1 past the last
+    if (!dyn) {
+      const int t = unit + i * units;
+      return t < total_tiles ? t : -1;
+    }
+    const int slot = i % kTileSlots;
+    if (!bounded_wait(&ctl.tile_full[slot], static_cast<uint32_t>(i / kTileSlots) & 1u, &ctl.abort,
+                      P.error_word))
+      return -1;
+    return *reinterpret_cast<volatile int32_t*>(&ctl.tile_slot[slot][0]);
+  };
 
   // (h: row sub-tile, always 0 unless G::SUB = 2)
   auto tile_of = [&](int t, int& e, int& row0, int& nb, bool& mine, int h = 0) {
@@ -723,7 +755,34 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = unit; t < total_tiles && ok; t += units) {
+      const bool claimer = dyn && (CG == 1 || rank == 0);
+      int early = -1;  // the next tile's claim, made during this tile's last stage
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (dyn) {
+          // claim the next tile and publish it (pairs: the even CTA claims
+          // and hands the claim to the odd CTA by a 16-byte bulk copy)
+          const int slot = i % kTileSlots;
+          if (claimer) {
+            const int c = early >= 0 ? early : atomicAdd(P.sched, 1);
+            early = -1;
+            t = c < total_tiles ? c : -1;
+            ctl.tile_slot[slot][0] = t;
+            if constexpr (CG == 2) {
+              ptx::fence_proxy_async_smem();  // the slot as the copy's source
+              ptx::bulk_copy_to_cluster(ptx::mapa_shared(ptx::smem_u32(ctl.tile_slot[slot]), 1),
+                                        ctl.tile_slot[slot], 16,
+                                        ptx::mapa_shared(ptx::smem_u32(&ctl.tile_full[slot]), 1));
+            }
+            ptx::mbar_arrive(&ctl.tile_full[slot]);
+          } else {
+            ptx::mbar_arrive_expect_tx(&ctl.tile_full[slot], 16);
+            t = tile_at(i);
+          }
+        } else {
+          t = tile_at(i);
+        }
+        if (t < 0) break;
         int e, row0, nb;
         bool mine;
         tile_of(t, e, row0, nb, mine);
@@ -732,6 +791,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             ok = false;
             break;
           }
+          // the round trip of the next claim overlaps this last stage's loads
+          if (claimer && kb == KB - 1) early = atomicAdd(P.sched, 1);
           uint8_t* sa = tiles + stage * G::STAGE;
           uint8_t* sb = sa + G::B_OFF;
           // (gathered A: the stage's B bytes only)
@@ -784,7 +845,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = unit; t < total_tiles && ok; t += units) {
+      for (int i = 0; ok && tile_at(i) >= 0; ++i) {
         // block-scaled FP8: every K stage is its own accumulation, into the
         // two accumulators in turn, handed to the epilogue stage by stage
         // (two row sub-tiles: both accumulators, sub-tile h in accumulator h)
@@ -1098,8 +1159,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       }
     } else
     // row sub-tile h of tile t (one per tile unless G::SUB = 2)
-    for (int t = unit, h = 0; t < total_tiles;
-         (h + 1 == G::SUB) ? (h = 0, t += units) : ++h) {
+    for (int i = 0, h = 0, t = tile_at(0); t >= 0;
+         (h + 1 == G::SUB) ? (h = 0, t = tile_at(++i)) : ++h) {
       int e, row0, nb;
       bool mine;
       tile_of(t, e, row0, nb, mine, h);
@@ -1313,6 +1374,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     while (ptx::globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
   }
   if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+  if (dyn && threadIdx.x == 0 && (CG == 1 || rank == 0)) {
+    // the last claiming CTA to finish zeroes the counters for the next
+    // launch (every claim precedes its CTA's count)
+    __threadfence();
+    if (atomicAdd(P.sched + 1, 1) == units - 1) {
+      atomicExch(P.sched, 0);
+      atomicExch(P.sched + 1, 0);
+    }
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     if constexpr (CG == 2) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
@@ -1460,6 +1530,7 @@ KParams base_params(const GroupedGemmArgs& a, int NB) {
   P.sentinel = a.sentinel;
   P.div = a.div > 0 ? a.div : 1;
   P.a_rows = a.a_rows;
+  P.sched = a.sched;
   P.dense_rows = (EPI == Epi::DenseF32) ? static_cast<int32_t>(a.sentinel) : 0;
   P.gemm1_row_weight = a.gemm1_row_weight;
   P.a_scale = a.a_scale;
@@ -1581,6 +1652,11 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     return check_launch(name);
   }
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
+  // single-CTA tiles keep the static schedule: with two row blocks per weight
+  // tile (the shapes that take them) adjacent units already share it, and the
+  // dynamic one measured slower there (DeepSeek-V3 M=8192 layer 5.8-6.0 ->
+  // 6.0-6.3 ms)
+  P.sched = nullptr;
   prof_before(name, s);
   grouped_gemm_kernel<EPI, F8><<<grid, NTHREADS, G1::SMEM, s>>>(tmA, tmB, tmO, P);
   prof_after(name, s);
