@@ -827,7 +827,8 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
   const int64_t Mc_max = M < MOE_CHUNK_TOKENS ? M : MOE_CHUNK_TOKENS;
   const Fp8Layout L = fp8_layout(Mc_max, H, I, E, top_k);
   int32_t* err = at<int32_t>(workspace, L.err);
-  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+  // the error word and the GEMMs' tile-schedule counters after it
+  if (cudaMemsetAsync(err, 0, 32 * sizeof(int32_t), s) != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
   const bf16* x = static_cast<const bf16*>(hidden);
   bf16* y = static_cast<bf16*>(out);
@@ -867,6 +868,7 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     g1.row_index = sorted;
     g1.sentinel = static_cast<int32_t>(Rc);
     g1.error_word = err;
+    g1.sched = err + 16;  // used by the CTA-pair tiles
     g1.num_sms = sms;
     g1.rows_hint = Rc;
     g1.a_scale = a_scale;
@@ -896,6 +898,7 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     g2.sentinel = static_cast<int32_t>(Rc);
     g2.div = top_k;
     g2.error_word = err;
+    g2.sched = err + 24;
     g2.num_sms = sms;
     g2.rows_hint = Rc;
     g2.a_scale = z_scale;
