@@ -756,7 +756,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       uint32_t phase = 0;
       bool ok = true;
       const bool claimer = dyn && (CG == 1 || rank == 0);
-      int early = -1;  // the next tile's claim, made during this tile's last stage
+      int early = -1;  // the next tile's claim, made during this tile's last stages
       for (int i = 0; ok; ++i) {
         int t;
         if (dyn) {
@@ -791,8 +791,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             ok = false;
             break;
           }
-          // the round trip of the next claim overlaps this last stage's loads
-          if (claimer && kb == KB - 1) early = atomicAdd(P.sched, 1);
+          // the next claim's round trip (~1-2 us) overlaps this tile's last
+          // four stages (a short tile: all of it)
+          if (claimer && kb == (KB > 4 ? KB - 4 : 0)) early = atomicAdd(P.sched, 1);
           uint8_t* sa = tiles + stage * G::STAGE;
           uint8_t* sb = sa + G::B_OFF;
           // (gathered A: the stage's B bytes only)
@@ -1646,6 +1647,11 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     // at most blocks/2 + E/2 pair tiles per column block
     const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
     const unsigned clusters = static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
+    // the dynamic schedule pays where weight tiles are large (K >= 3072:
+    // Mixtral-shape gemm1 DRAM reads 1.99-2.55 -> 1.95 GB, FP8 gemm1 ~620 ->
+    // 594 us); with short K (Qwen-MoE shape, K = 2048 / 768) it measured
+    // 1-2.5 % slower, so those keep the static round-robin
+    if (a.K < 3072) P.sched = nullptr;
     prof_before(name, s);
     grouped_gemm_pair_kernel<EPI, F8><<<2 * clusters, NTHREADS, G2::SMEM, s>>>(tmA, tmB, tmO, P);
     prof_after(name, s);
