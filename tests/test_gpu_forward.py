@@ -264,3 +264,30 @@ def test_forward_full_size_sampled(name):
                          None if d["w2_bias"] is None else LazyF64(d["w2_bias"]))
     check_out(f64(y)[sel], ref, name)
     assert np.isfinite(f64(y)).all()
+
+
+@pytest.mark.parametrize("reduce", ["separate", "epilogue_atomic"])
+def test_forward_dynamic_schedule_across_chunks_and_calls(reduce):
+    """CTA-pair GEMMs with K >= 3072 take their tiles from a counter that each
+    launch resets when it ends: a forward of two token chunks (20000 > 16384
+    tokens) repeated three times gives the oracle's result and the same bits
+    every time."""
+    M, H, I, E, k = 20000, 3072, 64, 4, 2
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = torch.randn(M, H, generator=g, device="cuda").bfloat16()
+    w13 = (torch.randn(E, H, 2 * I, generator=g, device="cuda") * 0.02).bfloat16()
+    w2 = (torch.randn(E, I, H, generator=g, device="cuda") * 0.05).bfloat16()
+    rng = np.random.default_rng(3)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+    wts = rng.random((M, k)).astype(np.float32)
+    tw, tids = torch.from_numpy(wts).cuda(), torch.from_numpy(ids).cuda()
+    ws = pkg.alloc_workspace(pkg.workspace_size(M, H, I, E, k, reduce))
+    outs = []
+    for _ in range(3):
+        outs.append(pkg.moe_forward(x, tw, tids, w13, w2, workspace=ws, reduce=reduce))
+        torch.cuda.synchronize()
+        assert pkg.read_error(pkg.workspace_error_word(ws)) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    sel = np.r_[0:16, 16376:16392, M - 16:M]
+    ref = oracle.forward(f64(x)[sel], wts[sel], ids[sel], f64(w13), f64(w2))
+    check_out(f64(outs[0])[sel], ref, f"dynamic schedule {reduce}")
