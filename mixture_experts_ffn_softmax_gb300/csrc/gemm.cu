@@ -1093,8 +1093,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                accv[c][16 * hh + j] = fmaf(__uint_as_float(v[hh][j]), sc, accv[c][16 * hh + j]);
+              for (int j = 0; j < 16; j += 2)  // packed pairs: half the FMA issues
+                ptx::fma2(accv[c][16 * hh + j], accv[c][16 * hh + j + 1],
+                          __uint_as_float(v[hh][j]), __uint_as_float(v[hh][j + 1]), sc);
           }
           release_acc(acc);
           if (++acc == 2) {

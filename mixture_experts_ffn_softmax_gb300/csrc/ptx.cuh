@@ -211,6 +211,17 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// c = a * b + c on a pair of fp32 values (packed fma.rn.f32x2: one
+// instruction, each lane rounded as fmaf), b the same for both.
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b) {
+  uint64_t a, bb, c;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(c) : "f"(c0), "f"(c1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(bb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(c));
+}
+
 // ------------------------------------------------------------ tcgen05 ---
 // TMEM allocation: executed by one full warp; the allocated base address is
 // written to shared memory at `dst`.
