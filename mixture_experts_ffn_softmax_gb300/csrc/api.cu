@@ -843,18 +843,20 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
                  at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.block_expert),
                  at<int32_t>(workspace, L.scratch), cap, err, inv};
     if (moe_status_t st = launch_align(al, s)) return st;
-    // quantise each token row once (E4M3, one scale per row) into its k
-    // sorted rows; zero those rows' z amax for GEMM1's epilogue
+    // quantise each token row once (E4M3, one scale per row, or per row and
+    // 128-column group) into its k sorted rows; per row, zero those rows' z
+    // amax for GEMM1's epilogue
     uint8_t* a8 = at<uint8_t>(workspace, L.a8);
     float* a_scale = at<float>(workspace, L.a_scale);
     float* z_scale = at<float>(workspace, L.z_scale);
-    QuantTokensArgs qa{x + c0 * H, inv, Mc, top_k, H, a8, a_scale, z_scale};
+    QuantTokensArgs qa{x + c0 * H, inv, Mc, top_k, H, a8, a_scale, block ? nullptr : z_scale};
     if (block) {
-      if (moe_status_t st = launch_quant_tokens_group_fp8(qa, cap, I / 128, s)) return st;
+      if (moe_status_t st = launch_quant_tokens_group_fp8(qa, cap, s)) return st;
     } else {
       if (moe_status_t st = launch_quant_tokens_fp8(qa, s)) return st;
     }
     bf16* z = at<bf16>(workspace, L.z);
+    uint8_t* z8 = at<uint8_t>(workspace, L.z8);
     GroupedGemmArgs g1{};
     g1.a = reinterpret_cast<const bf16*>(a8);
     g1.w = static_cast<const bf16*>(w->w13);
@@ -864,7 +866,7 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     g1.N = I;
     g1.K = H;
     g1.offsets = offsets;
-    g1.out = z;
+    g1.out = block ? static_cast<void*>(z8) : static_cast<void*>(z);
     g1.row_index = sorted;
     g1.sentinel = static_cast<int32_t>(Rc);
     g1.error_word = err;
@@ -874,14 +876,17 @@ moe_status_t moe_forward_fp8(const void* hidden, const float* topk_weights,
     g1.a_scale = a_scale;
     g1.w_scale = w->w13_scale;
     g1.w_scale_per_channel = w->scale_mode == MOE_FP8_SCALE_CHANNEL;
-    g1.row_amax = z_scale;
+    // block scales: GEMM1 quantises z itself (its tile's 128 z columns are
+    // one group); per row: it takes each row's amax for the pass below
+    if (block) g1.z_group_scale = z_scale;
+    else g1.row_amax = z_scale;
     if (moe_status_t st = block ? launch_gemm1_swiglu_fp8_block(g1, s) : launch_gemm1_swiglu_fp8(g1, s))
       return st;
-    // quantise z per row for the second GEMM (amax taken by GEMM1)
-    uint8_t* z8 = at<uint8_t>(workspace, L.z8);
-    QuantSortedArgs qz{z, sorted, offsets, E, static_cast<int32_t>(Rc), I, cap, z8, z_scale};
-    if (moe_status_t st = block ? launch_quant_sorted_group_fp8(qz, s) : launch_quant_sorted_fp8(qz, s))
-      return st;
+    if (!block) {
+      // quantise z per row for the second GEMM (amax taken by GEMM1)
+      QuantSortedArgs qz{z, sorted, offsets, E, static_cast<int32_t>(Rc), I, cap, z8, z_scale};
+      if (moe_status_t st = launch_quant_sorted_fp8(qz, s)) return st;
+    }
     float* o = at<float>(workspace, L.o);
     GroupedGemmArgs g2{};
     g2.a = reinterpret_cast<const bf16*>(z8);

@@ -162,12 +162,10 @@ struct QuantSortedArgs {
   float* scale_io;        // [cap]
 };
 moe_status_t launch_quant_sorted_fp8(const QuantSortedArgs& a, cudaStream_t s);
-// The same per (row, group of 128 columns), scales group-major [H/128][ld]
-// (tokens: ld = cap, also zeroing zgroups z-amax slots per sorted row;
-// sorted rows: ld = cap, scale_io group-major).
-moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld, int zgroups,
-                                           cudaStream_t s);
-moe_status_t launch_quant_sorted_group_fp8(const QuantSortedArgs& a, cudaStream_t s);
+// The token rows' quantisation per (row, group of 128 columns), scales
+// group-major [H/128][ld] (ld = cap; row_amax unused).  z of the block-scaled
+// layer is quantised the same way by GEMM1's epilogue.
+moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld, cudaStream_t s);
 
 // Weight-only quantised weights -> bf16 [E, K, N] (wq.cu).  format: 0 int4,
 // 1 int8, 2 MX FP4; codes, scale [E, K/G, N], zero [E, K/G, N] or null.
@@ -212,6 +210,10 @@ struct GroupedGemmArgs {
   const float* w_scale = nullptr;       // [E, 2N] / [E, N] per channel, or [E]
   int32_t w_scale_per_channel = 0;
   float* row_amax = nullptr;            // GEMM1 FP8: max |bf16 z| of each sorted row (atomic)
+  // GEMM1 with block-scaled FP8 (required there): z leaves as E4M3 codes in
+  // `out` ([cap, N] bytes) with one scale per row and 128-column group here,
+  // [N / 128][cap] -- the quantisation the second GEMM's A takes
+  float* z_group_scale = nullptr;
   // weight-only quantised w (codes in `w`): format (0 int4, 1 int8, 2 MX FP4),
   // group size along K, scales [E, K/G, N'] and zero points (or null)
   int32_t wq_format = -1;

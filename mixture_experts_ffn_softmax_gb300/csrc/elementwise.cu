@@ -8,6 +8,7 @@
 // top-k expert outputs.  "Fused MoE Modular Kernel" (vLLM): the permute /
 // unpermute steps of apply() and TopKWeightAndReduce.
 #include "common.cuh"
+#include "fp8q.cuh"
 
 namespace gbmoe {
 namespace {
@@ -291,60 +292,11 @@ moe_status_t launch_router_small(const bf16* x, const bf16* wg, const bf16* bg, 
 
 }  // namespace gbmoe
 
-#include <cuda_fp8.h>
-
 namespace gbmoe {
 namespace {
 
 constexpr int kQuantWarps = 8;
 constexpr int kQuantUnroll = 4;  // 16-byte loads in flight per lane
-
-// x / s rounded to nearest even in fp32, for a divisor fixed along a row, by
-// Markstein's correction of the product with the reciprocal (P. Markstein,
-// "IA-64 and Elementary Functions", 2000; Handbook of Floating-Point
-// Arithmetic, division by FMA): with r = RN(1/s) and q = RN(x r) within an
-// ulp of x / s, the remainder x - q s is exact as one FMA and RN(q + rem r)
-// is the correctly rounded quotient (no overflow or underflow: the caller
-// takes the IEEE division for rows whose scale is not a normal float, and a
-// quotient below the normal range is far below E4M3's smallest code).
-__device__ __forceinline__ float div_fixed(float x, float s, float r) {
-  const float q = __fmul_rn(x, r);
-  const float rem = __fmaf_rn(-q, s, x);
-  return __fmaf_rn(rem, r, q);
-}
-
-// Row scale and its reciprocal; `fast` is false where the correction does
-// not apply (subnormal or non-finite scale) and the plain division is used.
-struct RowScale {
-  float s, r;
-  bool fast;
-};
-
-// Dynamic per-row quantisation: scale = amax / 448, or 1 for an all-zero row
-// ("fused_moe.py 分析": activations are quantised per token before each GEMM).
-__device__ __forceinline__ RowScale row_scale(float amax) {
-  RowScale rs;
-  rs.s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-  rs.fast = rs.s >= 1.17549435e-38f && rs.s <= 3.0e38f;
-  rs.r = rs.fast ? __frcp_rn(rs.s) : 0.f;
-  return rs;
-}
-
-// E4M3 codes of 8 bf16 values: q = e4m3(x / scale), the quotient correctly
-// rounded in fp32, then round to nearest even with saturation to +-448.
-__device__ __forceinline__ uint2 e4m3x8(const uint4 u, const RowScale& rs) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-  uint16_t b[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(h[i]);
-    const float2 v = rs.fast ? make_float2(div_fixed(f.x, rs.s, rs.r), div_fixed(f.y, rs.s, rs.r))
-                             : make_float2(__fdiv_rn(f.x, rs.s), __fdiv_rn(f.y, rs.s));
-    b[i] = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-  }
-  return make_uint2(static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16),
-                    static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16));
-}
 
 // max |v| over 8 bf16 values, as bf16 magnitude bits in both halves
 __device__ __forceinline__ uint32_t absmax_bits8(const uint4 u, uint32_t m) {
@@ -455,8 +407,6 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 // one 128-wide group, reduced over its 16 lanes.  Scales are stored group
 // major, scale[g * ld + row], so a warp's 32 rows read one line in the GEMM.
 
-constexpr int kMaxGroups = 256;  // 128-wide groups per row the z quantisation handles (H <= 32768)
-
 __device__ __forceinline__ float half_warp_amax(uint32_t mb) {
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
@@ -464,12 +414,11 @@ __device__ __forceinline__ float half_warp_amax(uint32_t mb) {
 }
 
 // Token rows: each token's groups are quantised once and the codes written
-// to each of its k sorted rows; the z amax slots of those rows are zeroed.
+// to each of its k sorted rows.
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_tokens_group_fp8_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ inv,
                                   int64_t M, int k, int H, uint8_t* __restrict__ q8,
-                                  float* __restrict__ scale, int64_t ld, float* __restrict__ zmax,
-                                  int zgroups) {
+                                  float* __restrict__ scale, int64_t ld) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
@@ -490,109 +439,20 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         if ((lane & 15) == 0) scale[static_cast<int64_t>(g) * ld + pos] = rs.s;
       }
     }
-    if (zmax != nullptr) {
-      for (int j = 0; j < k; ++j) {
-        const int32_t pos = j < 32 ? __shfl_sync(0xffffffffu, mypos, j) : __ldg(inv + t * k + j);
-        if (pos < 0) continue;
-        for (int g = lane; g < zgroups; g += 32) zmax[static_cast<int64_t>(g) * ld + pos] = 0.f;
-      }
-    }
-  }
-}
-
-// Sorted rows of z, one pass: each group's amax was taken by GEMM1's
-// epilogue (scale_io[g * ld + p] holds it on entry, the group scale on exit).
-__global__ void __launch_bounds__(kQuantWarps * 32)
-    quant_sorted_group_fp8_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ index,
-                                  const int32_t* __restrict__ offsets, int E, int32_t sentinel,
-                                  int H, int64_t cap, uint8_t* __restrict__ q8,
-                                  float* __restrict__ scale_io) {
-  const int lane = threadIdx.x & 31;
-  const int64_t rows = min(static_cast<int64_t>(offsets[E]), cap);
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
-  const int groups = H / 128;
-  for (int64_t p = warp0; p < rows; p += nwarps) {
-    const int32_t idx = index[p];
-    if (idx < 0 || idx >= sentinel) continue;  // padding row
-    // the row's group amaxes, read once: group g is lane g % 32, slot g / 32
-    float am[kMaxGroups / 32];
-#pragma unroll
-    for (int j = 0; j < kMaxGroups / 32; ++j) {
-      const int g = lane + 32 * j;
-      am[j] = g < groups ? scale_io[static_cast<int64_t>(g) * cap + p] : 0.f;
-    }
-    __syncwarp();  // all reads of the row's amaxes before any scale is written
-    // kQuantUnroll passes of 256 columns per iteration, their loads issued
-    // first (one 16-byte load per lane at a time left this pass at ~0.5 of
-    // copy bandwidth: 111 us on the Mixtral-shape z)
-    for (int b0 = 0; b0 < H; b0 += 256 * kQuantUnroll) {
-      uint4 u[kQuantUnroll];
-#pragma unroll
-      for (int i = 0; i < kQuantUnroll; ++i) {
-        const int v = b0 + 256 * i + lane * 8;
-        u[i] = v < H ? __ldcs(reinterpret_cast<const uint4*>(src + p * H + v)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int i = 0; i < kQuantUnroll; ++i) {
-        const int b = b0 + 256 * i;
-        const int v = b + lane * 8;
-        const bool in = v < H;
-        const int g = v / 128;
-        const int gh = b / 128 + (lane >> 4);        // this half-warp's group
-        float amax = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxGroups / 32; ++j) {
-          const float a = __shfl_sync(0xffffffffu, am[j], gh & 31);
-          if ((gh >> 5) == j) amax = a;
-        }
-        const RowScale rs = row_scale(in ? amax : 0.f);
-        if (in) {
-          *reinterpret_cast<uint2*>(q8 + p * H + v) = e4m3x8(u[i], rs);
-          if ((lane & 15) == 0) scale_io[static_cast<int64_t>(g) * cap + p] = rs.s;
-        }
-      }
-    }
   }
 }
 
 }  // namespace
 
-moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld, int zgroups,
-                                           cudaStream_t s) {
+moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld, cudaStream_t s) {
   if (a.M <= 0) return MOE_OK;
   const int64_t want = ceil_div<int64_t>(a.M, kQuantWarps);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
   prof_before("quant_tokens_fp8", s);
   quant_tokens_group_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(
-      a.x, a.inv, a.M, a.k, a.H, a.q8, a.scale, ld, a.row_amax, zgroups);
+      a.x, a.inv, a.M, a.k, a.H, a.q8, a.scale, ld);
   prof_after("quant_tokens_fp8", s);
   return check_launch("quant_tokens_fp8");
-}
-
-moe_status_t launch_quant_sorted_group_fp8(const QuantSortedArgs& a, cudaStream_t s) {
-  if (a.cap <= 0) return MOE_OK;
-  // as many blocks as are resident at once (each strides over the same
-  // share of rows)
-  static PerDevice blocks_per_sm;
-  int per_sm = 4;
-  blocks_per_sm.get(
-      [](int* v) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, quant_sorted_group_fp8_kernel,
-                                                          kQuantWarps * 32, 0) != cudaSuccess ||
-            *v <= 0)
-          *v = 4;
-        cudaGetLastError();
-        return cudaSuccess;
-      },
-      &per_sm);
-  const int64_t want = ceil_div<int64_t>(a.cap, kQuantWarps);
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * per_sm));
-  prof_before("quant_z_fp8", s);
-  quant_sorted_group_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(
-      a.src, a.index, a.offsets, a.E, a.sentinel, a.H, a.cap, a.q8, a.scale_io);
-  prof_after("quant_z_fp8", s);
-  return check_launch("quant_z_fp8");
 }
 
 moe_status_t launch_quant_tokens_fp8(const QuantTokensArgs& a, cudaStream_t s) {

@@ -49,6 +49,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "fp8q.cuh"
 #include "ptx.cuh"
 #include "wq.cuh"
 
@@ -197,6 +198,9 @@ struct KParams {
   const float* w_scale;
   int32_t w_scale_per_channel, w_scale_ld;
   float* row_amax;  // SwiGLU FP8: atomic max of |bf16 z| per sorted row, or null
+  // block-scaled SwiGLU: z is quantised in the epilogue, E4M3 codes in out
+  // and one scale per row and 128-column group here, [N / 128][bs_a_ld]
+  float* z_group_scale;
   // weight-only quantised B: group size along K, group rows per 64-row
   // stage (1 or 2), zero points present, bytes per raw stage
   int32_t wq_G, wq_gbox, wq_has_zero, wq_raw_tx;
@@ -429,6 +433,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
                     (G::NSTAGES * G::STAGE) % 1024 == 0,
                 "staging, prefix and raw ring start 1024-byte aligned");
   const int32_t* off = P.offsets;
+  // Block-scaled SwiGLU quantising z: the four epilogue warps of a TMEM lane
+  // quadrant each hold 32 of a row's 128 z columns and exchange their rows'
+  // partial maxima here, in the staging area (which that epilogue does not
+  // use): parts by tile parity, quadrant, warp and row, and one barrier per
+  // quadrant that completes when its four warps have written theirs.
+  struct ZExchange {
+    uint32_t part[2][4][4][32];
+    uint64_t bar[4];
+  };
+  static_assert(sizeof(ZExchange) <= EPI_WARPS * STAGING_BYTES, "exchange within the staging area");
+  ZExchange* zx = reinterpret_cast<ZExchange*>(staging);
 
   if constexpr (CG == 2) {
     // prefix of ceil(row blocks / 2) over the experts: lane chunks + warp scan
@@ -478,6 +493,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     }
     // the producer's arrival (the odd CTA's with the 16 bytes it expects)
     for (int i = 0; i < kTileSlots; ++i) ptx::mbar_init(&ctl.tile_full[i], 1);
+    if constexpr (BS && EPI == Epi::SwiGLU)
+      for (int i = 0; i < 4; ++i) ptx::mbar_init(&zx->bar[i], 4);
     ctl.abort = 0;
     ptx::fence_barrier_init();
   }
@@ -1034,9 +1051,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       // "fused_moe.py 分析", FP8 W8A8, block-wise: each K block's dot product
       // (one stage's accumulator) times that block's activation scale (per
       // row and 128-wide K group) and weight scale (per 128 x 128 block),
-      // summed over the K blocks in registers.  This warp's four 32-column
-      // accumulator chunks: SwiGLU gate [h*64, +64) and up [128 + h*64, +64);
-      // otherwise [h*128, +128).
+      // summed over the K blocks in registers.  The SwiGLU GEMM leaves z
+      // quantised for the second GEMM (E4M3 codes and one scale per row and
+      // 128-column group: its tile's z columns), not as bf16 for a pass of
+      // its own.
       // CH accumulator chunks of 32 columns per warp: the quadrant's 8
       // chunks split over its NEPI / 4 warps (SwiGLU: matching gate and up
       // chunks, the gate ones first)
@@ -1049,6 +1067,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           return 32 * (sub * CH + c);
       };
       bool ok = true;
+      int zt = 0;  // tiles done (the z exchange's parity)
       for (int t = unit; t < total_tiles && ok; t += units) {
         int e, row0, nb;
         bool mine;
@@ -1103,42 +1122,60 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             acc_phase ^= 1u;
           }
         }
-        if (!ok || !mine || !real) continue;
+        if (!ok) continue;
         if constexpr (EPI == Epi::SwiGLU) {
-          bf16* z = reinterpret_cast<bf16*>(P.out);
-          const int64_t brow = static_cast<int64_t>(e) * 2 * N;
-          uint32_t zmax2 = 0;
-#pragma unroll
-          for (int c = 0; c < CH / 2; ++c) {
-            const int n0 = nb * (MMA_N / 2) + chunk_col(c);  // z column of the chunk
+          {
+            // z rounded to bf16 and quantised for the second GEMM as its A
+            // rows are: E4M3 codes with one scale per row for the tile's 128
+            // z columns (one group), from the row's max |z| over the
+            // quadrant's four warps (N is a multiple of 128: every column of
+            // the tile exists)
+            static_assert(NEPI != 16 || CH == 2, "one gate and one up chunk per warp");
+            const int64_t brow = static_cast<int64_t>(e) * 2 * N;
+            const int n0 = nb * (MMA_N / 2) + chunk_col(0);
+            uint4 zz[4];
+            uint32_t zmax2 = 0;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               const int n = n0 + 8 * v;
-              if (n >= N) break;
               float bg[8], bu[8];
               load_bias8(P.bias, brow + n, true, bg);
               load_bias8(P.bias, brow + N + n, true, bu);
-              uint4 pk;
-              uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+              uint32_t* w = reinterpret_cast<uint32_t*>(&zz[v]);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const int j = 8 * v + 2 * i;
-                const float z0 = silu_f(accv[c][j] + bg[2 * i]) * (accv[c + CH / 2][j] + bu[2 * i]);
-                const float z1 = silu_f(accv[c][j + 1] + bg[2 * i + 1]) *
-                                 (accv[c + CH / 2][j + 1] + bu[2 * i + 1]);
+                const float z0 = silu_f(accv[0][j] + bg[2 * i]) * (accv[CH / 2][j] + bu[2 * i]);
+                const float z1 = silu_f(accv[0][j + 1] + bg[2 * i + 1]) *
+                                 (accv[CH / 2][j + 1] + bu[2 * i + 1]);
                 w[i] = pack_bf16x2(z0, z1);
                 zmax2 = __vmaxu2(zmax2, w[i] & 0x7fff7fffu);
               }
-              *reinterpret_cast<uint4*>(z + p * N + n) = pk;
+            }
+            const int par = zt & 1;
+            ++zt;
+            zx->part[par][q][sub][lane] = max(zmax2 & 0xffffu, zmax2 >> 16);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&zx->bar[q]);
+            const bool got = bounded_wait(&zx->bar[q], static_cast<uint32_t>(par), &ctl.abort,
+                                          P.error_word);
+            if (!__all_sync(0xffffffffu, got)) {
+              ok = false;
+              continue;
+            }
+            uint32_t m = 0;
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) m = max(m, zx->part[par][q][w4][lane]);
+            const RowScale rs = row_scale(__uint_as_float(m << 16));
+            if (mine && real) {
+              uint8_t* zq = reinterpret_cast<uint8_t*>(P.out) + p * N + n0;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) *reinterpret_cast<uint2*>(zq + 8 * v) = e4m3x8(zz[v], rs);
+              if (sub == 0) P.z_group_scale[static_cast<int64_t>(nb) * P.bs_a_ld + p] = rs.s;
             }
           }
-          // the row's amax over this z group (the tile's 128 z columns)
-          const uint32_t m = max(zmax2 & 0xffffu, zmax2 >> 16) << 16;
-          if (m != 0u && P.row_amax != nullptr)
-            atomicMax(reinterpret_cast<unsigned int*>(P.row_amax) +
-                          static_cast<int64_t>(nb) * P.bs_a_ld + p,
-                      m);
         } else {
+          if (!mine || !real) continue;
           float* o = reinterpret_cast<float*>(P.out);
           const float wgt = P.row_weight != nullptr ? P.row_weight[entry] : 1.0f;
           const int64_t brow = static_cast<int64_t>(e) * N;
@@ -1539,6 +1576,7 @@ KParams base_params(const GroupedGemmArgs& a, int NB) {
   P.w_scale = a.w_scale;
   P.w_scale_per_channel = a.w_scale_per_channel;
   P.row_amax = a.row_amax;
+  P.z_group_scale = a.z_group_scale;
   P.w_scale_ld = (EPI == Epi::SwiGLU) ? 2 * a.N : a.N;
   return P;
 }
@@ -1747,6 +1785,8 @@ moe_status_t launch_gemm_bs(const GroupedGemmArgs& a, const char* name, cudaStre
       }) != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
                      cudaGetErrorString(cudaGetLastError()));
+  if (EPI == Epi::SwiGLU && (a.z_group_scale == nullptr || a.N % 128 != 0))
+    return set_error(MOE_ERR_INVALID_ARG, "%s: z group scales and N %% 128 == 0 required", name);
   CUtensorMap tmA, tmB;
   int NB;
   if (moe_status_t st = make_ab_maps<EPI, true>(a, &tmA, &tmB, &NB)) return st;
