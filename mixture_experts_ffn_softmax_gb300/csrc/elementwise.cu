@@ -424,30 +424,60 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
   for (int64_t t = warp0; t < M; t += nwarps) {
     const int32_t mypos = lane < k ? __ldg(inv + t * k + lane) : -1;
-    for (int b = 0; b < H; b += 256) {  // two groups per pass, the same count on every lane
-      const int v = b + lane * 8;
-      const bool in = v < H;
-      const uint4 u = in ? __ldg(reinterpret_cast<const uint4*>(x + t * H + v)) : make_uint4(0, 0, 0, 0);
-      uint32_t m2 = absmax_bits8(u, 0u);
-      const RowScale rs = row_scale(half_warp_amax(max(m2 & 0xffffu, m2 >> 16)));
-      const uint2 c = e4m3x8(u, rs);
-      const int g = v / 128;
-      for (int j = 0; j < k; ++j) {
-        const int32_t pos = j < 32 ? __shfl_sync(0xffffffffu, mypos, j) : __ldg(inv + t * k + j);
-        if (pos < 0 || !in) continue;
-        *reinterpret_cast<uint2*>(q8 + static_cast<int64_t>(pos) * H + v) = c;
-        if ((lane & 15) == 0) scale[static_cast<int64_t>(g) * ld + pos] = rs.s;
+    // passes of 256 columns (two groups, the same count on every lane),
+    // kQuantUnroll of them per iteration with their loads issued first
+    for (int b0 = 0; b0 < H; b0 += 256 * kQuantUnroll) {
+      uint4 u[kQuantUnroll];
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int v = b0 + 256 * i + lane * 8;
+        u[i] = v < H ? __ldg(reinterpret_cast<const uint4*>(x + t * H + v)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int v = b0 + 256 * i + lane * 8;
+        const bool in = v < H;
+        uint32_t m2 = absmax_bits8(u[i], 0u);
+        const RowScale rs = row_scale(half_warp_amax(max(m2 & 0xffffu, m2 >> 16)));
+        const uint2 c = e4m3x8(u[i], rs);
+        const int g = v / 128;
+        for (int j = 0; j < k; ++j) {
+          const int32_t pos = j < 32 ? __shfl_sync(0xffffffffu, mypos, j) : __ldg(inv + t * k + j);
+          if (pos < 0 || !in) continue;
+          *reinterpret_cast<uint2*>(q8 + static_cast<int64_t>(pos) * H + v) = c;
+          if ((lane & 15) == 0) scale[static_cast<int64_t>(g) * ld + pos] = rs.s;
+        }
       }
     }
   }
+}
+
+// Blocks of `kernel` resident on one SM at once (cached per device): a
+// grid-stride kernel launched with more gives every block the same share of
+// rows, and the blocks past that run as a thin second wave.
+template <typename Kernel>
+int resident_blocks(Kernel kernel, int threads, PerDevice& cache) {
+  int per_sm = 4;
+  cache.get(
+      [&](int* v) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kernel, threads, 0) != cudaSuccess ||
+            *v <= 0)
+          *v = 4;
+        cudaGetLastError();
+        return cudaSuccess;
+      },
+      &per_sm);
+  return per_sm;
 }
 
 }  // namespace
 
 moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld, cudaStream_t s) {
   if (a.M <= 0) return MOE_OK;
+  static PerDevice blocks_per_sm;
+  const int per_sm = resident_blocks(quant_tokens_group_fp8_kernel, kQuantWarps * 32, blocks_per_sm);
   const int64_t want = ceil_div<int64_t>(a.M, kQuantWarps);
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * per_sm));
   prof_before("quant_tokens_fp8", s);
   quant_tokens_group_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(
       a.x, a.inv, a.M, a.k, a.H, a.q8, a.scale, ld);
