@@ -5,6 +5,7 @@ profiler captures (a few GB on the device at most, three calls):
 
 Cases:
   fp8_mixtral_m2048     FP8 W8A8 layer, Mixtral-8x7B expert shape, M = 2048
+  fp8block_mixtral_m2048  the same with 128 x 128 weight-block scales
   int4_mixtral_decode   int4 (group 128, zero points) layer, Mixtral shape, M = 16
   mxfp4_mixtral_decode  MX FP4 layer, Mixtral shape, M = 16
   int4_mixtral_m2048    int4 (group 128) layer, Mixtral shape, M = 2048
@@ -32,8 +33,8 @@ def run(case: str, calls: int = 3, tiles: str = "auto") -> None:
     d = wl.make_moe_inputs(spec, device="cuda", weights=False)
     w, ids = moe_route(d["router_logits"], spec.top_k, "softmax", True)
     out = torch.empty_like(d["hidden"])
-    if kind == "fp8":
-        q = wl.make_fp8_weights(spec, device="cuda")
+    if kind in ("fp8", "fp8block"):
+        q = wl.make_fp8_weights(spec, device="cuda", block=kind == "fp8block")
         ws = alloc_workspace(workspace_size_fp8(spec.M, spec.H, spec.I, spec.E, spec.top_k))
         for _ in range(calls):
             moe_forward_fp8(d["hidden"], w, ids, q["w13_q"], q["w2_q"], q["w13_scale"],
