@@ -184,6 +184,26 @@ def test_fp8_block_scales_with_bias_and_ragged_rows():
     check_out(f64(y), ref, "ragged fp8 block")
 
 
+@pytest.mark.parametrize("M,H,I,E,k", [(1, 128, 128, 3, 2), (5, 256, 128, 4, 3), (3, 128, 384, 2, 1)])
+def test_fp8_block_scales_edge_shapes(M, H, I, E, k):
+    """One token or a few, a single 128-wide z group (one z column tile), and
+    tiles that are almost all padding: z's codes and group scales come from
+    GEMM1's epilogue, whose per-row maxima are exchanged across warps."""
+    spec = wl.MoESpec(name="block_edge", M=M, H=H, I=I, E=E, top_k=k,
+                      routing_method="softmax", renormalize=True, bias=True)
+    d = wl.make_moe_inputs(spec, device="cuda")
+    q = wl.make_fp8_weights(spec, device="cuda", block=True)
+    w32, ids = _route(spec, d)
+    y = pkg.moe_forward_fp8(d["hidden"], torch.from_numpy(w32).cuda(), torch.from_numpy(ids).cuda(),
+                            q["w13_q"], q["w2_q"], q["w13_scale"], q["w2_scale"], d["w13_bias"],
+                            d["w2_bias"])
+    torch.cuda.synchronize()
+    ref = oracle.forward_fp8_block(f64(d["hidden"]), w32.astype(np.float64), ids, f64(q["w13_q"]),
+                                   f64(q["w2_q"]), f64(q["w13_scale"]), f64(q["w2_scale"]),
+                                   f64(d["w13_bias"]), f64(d["w2_bias"]))
+    check_out(f64(y), ref, f"fp8 block M={M} H={H} I={I} E={E} k={k}")
+
+
 def test_fp8_block_scales_full_size_mixtral_sampled():
     spec = wl.SPECS["mixtral_prefill"]
     d = wl.make_moe_inputs(spec, device="cuda", weights=False)
