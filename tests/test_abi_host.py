@@ -182,6 +182,16 @@ def test_gemm_tile_mode_validation():
         assert lib.moe_set_gemm_tiles(m) == OK
 
 
+def test_gather_mode_validation():
+    lib = pkg.lib()
+    assert lib.moe_set_gather_mode(3) == INVALID
+    assert lib.moe_set_gather_mode(-1) == INVALID
+    for m in (2, 1, 0):
+        assert lib.moe_set_gather_mode(m) == OK
+    with pytest.raises(KeyError):
+        pkg.set_gather_mode("tma")
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     _lib._lib_saved = _lib._lib
     try:
