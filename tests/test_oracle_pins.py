@@ -146,6 +146,73 @@ def test_route_brute_force(seed):
     assert n_cases > 200
 
 
+def _brute_best_groups(l_row, method, k_group, G, mode):
+    """The kept group subset by enumeration (largest summed group score, ties
+    to the lexicographically smallest subset), scored as in _brute_route."""
+    E = len(l_row)
+    if method == "softmax":
+        ex = [math.exp(v - max(l_row)) for v in l_row]
+        tot = math.fsum(ex)
+        p = [v / tot for v in ex]
+    else:
+        p = [1.0 / (1.0 + math.exp(-v)) for v in l_row]
+    gs = E // G
+    gscore = []
+    for g in range(G):
+        members = range(g * gs, (g + 1) * gs)
+        if mode == 0:
+            gscore.append(max(p[e] for e in members))
+        else:
+            gscore.append(max(p[a] + p[b] for a, b in itertools.combinations(members, 2)))
+    best = min(itertools.combinations(range(G), k_group),
+               key=lambda s: (-sum(sorted(gscore[g] for g in s)), s))
+    return p, list(best)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_route_with_groups_brute_force(seed):
+    """MindIE-SD "Fused MoE", 路由选择 (grouped selection): once the kept
+    groups are fixed, the result is the top-k over exactly those groups'
+    experts.  For EVERY k_group-subset of groups, route_with_groups must equal
+    enumeration of all top_k-subsets of that subset's experts (so a wrong
+    group-to-expert index map or a mask over the wrong groups fails), and
+    with the subset that enumeration of the group choice keeps it must equal
+    route() itself."""
+    rng = np.random.default_rng(300 + seed)
+    n_cases = 0
+    for E, G in ((6, 2), (6, 3), (8, 2), (8, 4), (12, 4)):
+        gs = E // G
+        for method in ("softmax", "sigmoid"):
+            for k_group in range(1, G + 1):
+                for top_k in range(1, min(3, k_group * gs) + 1):
+                    # continuous logits, with a few exact ties planted
+                    l = rng.standard_normal((3, E))
+                    l[:, rng.integers(0, E)] = l[:, rng.integers(0, E)]
+                    for renorm in (False, True):
+                        scale = 1.0 if renorm else 2.5
+                        for t in range(l.shape[0]):
+                            row = [float(v) for v in l[t]]
+                            p = _brute_best_groups(row, method, k_group, G, 0)[0]
+                            for gsub in itertools.combinations(range(G), k_group):
+                                experts = [e for g in gsub for e in range(g * gs, (g + 1) * gs)]
+                                bw, bids = _brute_route_in(p, experts, top_k, method,
+                                                           renorm, scale)
+                                w, ids = oracle.route_with_groups(
+                                    l[t], list(gsub), top_k, method, renorm, G, scale)
+                                assert ids.tolist() == bids, (E, G, gsub, top_k, l[t])
+                                np.testing.assert_allclose(w, bw, rtol=1e-12, atol=1e-14)
+                                n_cases += 1
+                            for mode in ((0, 1) if gs >= 2 else (0,)):
+                                _, kept = _brute_best_groups(row, method, k_group, G, mode)
+                                rw, rids, _ = oracle.route(l[t:t + 1], top_k, method, renorm,
+                                                           k_group, G, mode, scale)
+                                w, ids = oracle.route_with_groups(
+                                    l[t], kept, top_k, method, renorm, G, scale)
+                                assert ids.tolist() == rids[0].tolist(), (E, G, mode, kept)
+                                np.testing.assert_allclose(w, rw[0], rtol=1e-12, atol=1e-14)
+    assert n_cases > 500
+
+
 def test_route_matches_printed_routing_function():
     """Without groups, softmax routing is the page's printed custom routing
     function: softmax over experts, torch.topk, then divide by the sum of the
@@ -766,6 +833,7 @@ def _pins_fail(golden_dir):
     """Run the cheap pins; return True if at least one fails."""
     checks = [lambda: test_route_golden(golden_dir),
               lambda: test_route_brute_force(0),
+              lambda: test_route_with_groups_brute_force(0),
               test_ffn_closed_form,
               test_single_expert_is_dense_swiglu,
               test_uniform_topk_all_is_mean_of_experts,
@@ -896,6 +964,37 @@ def _mut_block_first_scale(x, topk_weights, topk_ids, w13_q, w2_q, w13_scale, w2
                        w2_bias, block)                 # wrong: first K block's scale everywhere
 
 
+_ORIG_RWG = om.route_with_groups
+
+
+def _mut_groups_shifted(logits_row, groups, top_k, method, renormalize, group_count,
+                        routed_scaling_factor):
+    """Group g mapped to experts g*gs+1 .. g*gs+gs (an off-by-one)."""
+    l = np.asarray(logits_row, dtype=np.float64)[None, :]
+    E = l.shape[1]
+    gs = E // group_count
+    allowed = np.zeros((1, E), dtype=bool)
+    for g in groups:
+        allowed[0, (g * gs + 1) % E:min(E, (g + 1) * gs + 1)] = True
+    ids = om.topk_select(l, allowed, top_k)
+    w = om.route_weights(om.scores(l, method), ids, method, renormalize, routed_scaling_factor)
+    return w[0], ids[0].astype(np.int32)
+
+
+def _mut_groups_strided(logits_row, groups, top_k, method, renormalize, group_count,
+                        routed_scaling_factor):
+    """Groups taken as strided expert sets e % group_count == g (the mask
+    over the wrong axis of an (gs, G) reshape)."""
+    l = np.asarray(logits_row, dtype=np.float64)[None, :]
+    E = l.shape[1]
+    allowed = np.zeros((1, E), dtype=bool)
+    for g in groups:
+        allowed[0, g::group_count] = True
+    ids = om.topk_select(l, allowed, top_k)
+    w = om.route_weights(om.scores(l, method), ids, method, renormalize, routed_scaling_factor)
+    return w[0], ids[0].astype(np.int32)
+
+
 _orig_align = om.align
 _ORIG_FFN = om.expert_ffn
 
@@ -915,6 +1014,8 @@ _ORIG_FFN = om.expert_ffn
     ("mx_decode", _mut_mx_bias),
     ("quantize_groups_e4m3", _mut_groups_row_scale),
     ("forward_fp8_block", _mut_block_first_scale),
+    ("route_with_groups", _mut_groups_shifted),
+    ("route_with_groups", _mut_groups_strided),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, golden_dir, target, mutant):
     monkeypatch.setattr(om, target, mutant)
