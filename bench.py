@@ -5,10 +5,20 @@ grouped GEMM + down-projection grouped GEMM + top-k weight-and-reduce).
                     [--workload mixtral_prefill]
 
 One step = one pass of the whole path over one batch of synthetic inputs of
-the named workload (default: the Mixtral-8x7B-shape layer, prefill M=4096;
-the same layer's M=16 decode is measured alongside and reported under
-"decode").  Weights and inputs are resident in HBM before timing; the
-weights (2.8 GB) exceed the 129 MB L2, so no flush is needed between steps.
+the named workload (default: the Mixtral-8x7B-shape layer, prefill M=4096).
+Weights and inputs are resident in HBM before timing; the weights (2.8 GB)
+exceed the 129 MB L2, so no flush is needed between steps.
+
+With the default workload the line also carries, under "configs", every
+other workload of the layer family measured the same way (its own step
+count, stated): the tiny layer (warm, and cold-L2 with a 256 MB write
+between steps), the Mixtral-shape M=16 decode, DeepSeek-V3-shape M=64 and
+M=8192, the Qwen-MoE shape with skewed routing (Zipf popularity and the
+literal Zipf draw), and the batched layout -- each with its step roofline
+fraction, its dominant kernel's roofline and a bounded-sample CPU oracle
+baseline.  Roofline peaks: the measured burst bf16 GEMM rate and the
+measured copy bandwidth (every kernel here is timed in a region well under
+a second); the sustained and the nominal dense peaks are given beside them.
 
 --impl reference times the CPU oracle (test infrastructure, fp64 numpy) on a
 bounded sample of the same workload on the host cores.
@@ -40,6 +50,10 @@ from mixture_experts_ffn_softmax_gb300 import workloads as wl  # noqa: E402
 METRIC = "fused-MoE fwd tokens/s and TFLOP/s (1×GB300), % of roofline"
 
 
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0   # GB300 datasheet, dense bf16 (context only)
+L2_FLUSH_BYTES = 256 << 20
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -53,22 +67,30 @@ def peaks():
 
 
 def measured_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source has changed since those counters were taken."""
+    """(DRAM bytes per launch, note) from the committed record
+    profiles/traffic_<kernel>_<workload>.json (written from an ncu export by
+    mixture_experts_ffn_softmax_gb300/ncu_traffic.py).  The bytes are None
+    when there is no record or when the kernel source has changed since the
+    counters were taken (the record holds the source's hash)."""
     import hashlib
-    import re
-    src = os.path.join(ROOT, "mixture_experts_ffn_softmax_gb300", "csrc", "gemm.cu")
-    summ = os.path.join(ROOT, "profiles", f"gemm_{workload}_ncu_full.md")
-    if not (os.path.exists(src) and os.path.exists(summ)):
-        return None
-    txt = open(summ).read()
-    sha = re.search(r"sha256\[:16\] = ([0-9a-f]{16})", txt)
-    val = re.search(rf"traffic_bytes_per_launch {kernel} {workload}: (\d+)", txt)
-    if not sha or not val:
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != sha.group(1):
-        return None
-    return int(val.group(1))
+    rec_path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
+    if not os.path.exists(rec_path):
+        return None, "no ncu record"
+    try:
+        with open(rec_path) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, rec["source"])
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec["kernel"] != kernel or rec["workload"] != workload:
+            return None, "record names another kernel or workload"
+        if sha != rec["source_sha256_16"]:
+            return None, f"stale: {rec['source']} changed since the ncu capture"
+        return int(rec["traffic_bytes_per_launch"]), (
+            f"profiles/traffic_{kernel}_{workload}.json, {rec['source']} "
+            f"sha256[:16] {rec['source_sha256_16']}")
+    except (OSError, KeyError, ValueError) as e:
+        return None, f"unreadable record: {e}"
 
 
 # ----------------------------------------------------------- distributed --
@@ -173,14 +195,101 @@ def algorithmic(spec, ids_np):
     return spec.flops(), wbytes + io, touched
 
 
+def kernel_work(name, H, I, E, k, M, R, touched, bias=False):
+    """Algorithmic (FLOPs, bytes) of one launch of a kernel of the step.
+    R routed rows (M*k, or the valid rows of the batched layout), `touched`
+    experts with at least one row; bf16 weights and activations, fp32 item
+    rows.  GEMM1: 4HI FLOPs per row; its touched experts' w13 (4HI bytes each)
+    + the rows read (2H) + z written (2I).  GEMM2: 2HI FLOPs per row; w2
+    (2HI bytes each) + z read (2I) + the fp32 (4H) or bf16 (2H) row written.
+    Gather 2H read + 2H written per row; reduce 4kH read + 2H written per
+    token; route 4E read + 8k written per token; align 4 B read twice and
+    8 B written per row.  Returns None for a kernel not listed."""
+    b13 = touched * 2 * I * 2 if bias else 0
+    b2 = touched * H * 2 if bias else 0
+    if name == "gemm1_swiglu":
+        return 4.0 * R * H * I, touched * 4 * H * I + b13 + R * (2 * H + 2 * I)
+    if name == "gemm2_sorted":
+        return 2.0 * R * H * I, touched * 2 * H * I + b2 + R * (2 * I + 4 * H)
+    if name == "gemm2_atomic":
+        return 2.0 * R * H * I, touched * 2 * H * I + b2 + R * 2 * I + M * H * 4
+    if name == "gemm2_rows_bf16":
+        return 2.0 * R * H * I, touched * 2 * H * I + b2 + R * (2 * I + 2 * H)
+    if name == "gather_rows":
+        return 0.0, R * 4 * H
+    if name == "reduce_sorted":
+        return 0.0, M * (4 * k * H + 2 * H)
+    if name == "cast_f32_bf16":
+        return 0.0, M * 6 * H
+    if name == "route":
+        return 0.0, M * (4 * E + 8 * k)
+    if name.startswith("align") or name == "batched_plan":
+        return 0.0, R * 16
+    return None
+
+
+def roofline_of(flops, nbytes, seconds, pk):
+    """Roofline of work (flops, bytes) done in `seconds`: t_roof = max(flops /
+    burst bf16 peak, bytes / copy bandwidth); frac = t_roof / seconds."""
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_tc >= t_hbm:
+        ach = flops / seconds / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(t_tc / seconds, 4),
+                "frac_of_sustained_peak": round(ach / pk["bf16_tflops_sustained"], 4),
+                "frac_of_nominal_dense_peak": round(ach / NOMINAL_DENSE_BF16_TFLOPS, 4)}
+    ach = nbytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(t_hbm / seconds, 4)}
+
+
+def dominant_kernel(kern, work):
+    """The kernel with the largest share of the step's device time, with its
+    roofline.  kern: name -> {"launches", "avg_us"} over the profiled steps;
+    work: name -> (flops, bytes) per launch."""
+    total = sum(v["launches"] * v["avg_us"] for v in kern.values())
+    name = max(kern, key=lambda n: kern[n]["launches"] * kern[n]["avg_us"])
+    v = kern[name]
+    return name, v["launches"] * v["avg_us"] / max(total, 1e-9), work.get(name)
+
+
+def time_steps_cold(step, K, W, flush):
+    """Per-step device time with L2 flushed before every step: a write of
+    `flush` (larger than L2) between steps, outside the timed events.
+    Returns the summed milliseconds of the K timed steps."""
+    for _ in range(W):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    evs = []
+    for _ in range(K):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        step()
+        e1.record(s)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
 class OurStep:
     reduce = "auto"
 
-    def __init__(self, spec, device):
+    def __init__(self, spec, device, weights_from=None):
+        """weights_from: the input dict of another workload of the same layer
+        (same E, H, I, seed): its weights are used instead of drawing them
+        again (they are the same draws)."""
         import mixture_experts_ffn_softmax_gb300 as pkg
         self.pkg = pkg
         self.spec = spec
-        self.d = wl.make_moe_inputs(spec, device=device)
+        self.d = wl.make_moe_inputs(spec, device=device, weights=weights_from is None)
+        if weights_from is not None:
+            for key in ("w13", "w2", "w13_bias", "w2_bias"):
+                self.d[key] = weights_from[key]
         M, E, k = spec.M, spec.E, spec.top_k
         self.w = torch.empty(M, k, dtype=torch.float32, device=device)
         self.ids = torch.empty(M, k, dtype=torch.int32, device=device)
@@ -196,6 +305,96 @@ class OurStep:
                         d["w2"], d["w13_bias"], d["w2_bias"], self.ws, self.out,
                         reduce=self.reduce)
         return self.out
+
+
+def _graph_ms(step, K, W, world):
+    """The same step captured once into a CUDA graph and replayed (launch
+    overhead removed; matters for the small shapes)."""
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        step()
+    torch.cuda.current_stream().wait_stream(gs)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    ms = max_over_ranks(time_steps(graph.replay, K, W, world) / K, world)
+    del graph
+    return ms
+
+
+def _steps_for(step, K, W, world, target_ms=50.0):
+    """At least K timed steps, more for short steps (about target_ms of timed
+    work, at most 1000 steps), from a 3-step probe after the warm-up."""
+    probe = time_steps(step, 3, W, world) / 3
+    return int(min(1000, max(K, round(target_ms / max(probe, 1e-3)))))
+
+
+def _profile(step, n):
+    import mixture_experts_ffn_softmax_gb300 as pkg
+    pkg.profiler_start()
+    for _ in range(n):
+        step()
+    prof = pkg.profiler_stop()
+    return {k: {"launches": v[0] // n, "avg_us": 1e3 * v[1] / max(v[0], 1)}
+            for k, v in prof.items()}
+
+
+def _summary(kern, work, ms, flops, nbytes, pk):
+    """Step roofline + dominant kernel roofline of one measured config."""
+    step_roof = roofline_of(flops, nbytes, ms * 1e-3, pk)
+    t_roof = max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)) * 1e3
+    name, share, w = dominant_kernel(kern, work)
+    dom = {"kernel": name, "avg_us": round(kern[name]["avg_us"], 2),
+           "share_of_step": round(share, 4)}
+    if w is not None:
+        dom.update(roofline_of(w[0], w[1], kern[name]["avg_us"] * 1e-6, pk))
+        dom["algorithmic_flops"], dom["algorithmic_bytes"] = w[0], int(w[1])
+    return {"t_roof_ms": round(t_roof, 4), "frac": step_roof["frac"],
+            "bound": step_roof["bound"]}, dom
+
+
+def measure_config(spec, device, K, W, world, pk, weights_from=None, cold_l2=False,
+                   cpu=True, cpu_budget=3.0, graph=True):
+    """One contiguous-layout workload measured like the headline: timed steps
+    (device-resident inputs), per-kernel events, the step roofline, the
+    dominant kernel's roofline, a CUDA-graph replay, optionally a cold-L2
+    timing, and a bounded-sample CPU oracle baseline."""
+    import mixture_experts_ffn_softmax_gb300 as pkg
+    step = OurStep(spec, device, weights_from=weights_from)
+    Kc = _steps_for(step, K, W, world)
+    n0 = pkg.launch_count()
+    ms = max_over_ranks(time_steps(step, Kc, W, world) / Kc, world)
+    launches = (pkg.launch_count() - n0) // (Kc + W)
+    flops, nbytes, touched = algorithmic(spec, step.ids.cpu().numpy())
+    kern = _profile(step, min(Kc, 50))
+    work = {n: kernel_work(n, spec.H, spec.I, spec.E, spec.top_k, spec.M, spec.R, touched,
+                           spec.bias) for n in kern}
+    work = {n: w for n, w in work.items() if w is not None}
+    roof_step, dom = _summary(kern, work, ms, flops, nbytes, pk)
+    out = {"workload": spec.name, "M": spec.M, "H": spec.H, "I": spec.I, "E": spec.E,
+           "top_k": spec.top_k, "routing": spec.routing_method, "steps": Kc,
+           "ms_per_step": round(ms, 4), "tokens_per_s": round(job_rate(spec.M, world, ms), 1),
+           "tflops": round(flops * world / (ms / 1e3) / 1e12, 2), "experts_touched": touched,
+           "algorithmic_bytes": int(nbytes), "roofline_step": roof_step,
+           "dominant_kernel": dom, "gpu_launches": launches,
+           "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()}}
+    if graph:
+        gms = _graph_ms(step, Kc, W, world)
+        out["graph"] = {"ms_per_step": round(gms, 4),
+                        "tokens_per_s": round(job_rate(spec.M, world, gms), 1)}
+    if cold_l2:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        cms = max_over_ranks(time_steps_cold(step, Kc, W, flush) / Kc, world)
+        out["cold_l2"] = {"ms_per_step": round(cms, 4),
+                          "tokens_per_s": round(job_rate(spec.M, world, cms), 1),
+                          "roofline_frac": round(roof_step["t_roof_ms"] / cms, 4),
+                          "flush": f"{L2_FLUSH_BYTES >> 20} MB written between steps, "
+                                   "outside the timed events"}
+        del flush
+    if cpu and world == 1:
+        out["cpu_baseline"] = cpu_baseline(spec, step.d, budget_s=cpu_budget)
+    return out, step
 
 
 class BatchedStep:
@@ -219,14 +418,47 @@ class BatchedStep:
                                             d["row_weight"], self.ws, self.out)
 
 
-def run_batched(args, world, rank, local):
+def measure_batched(spec, device, K, W, world, pk, cpu=True, cpu_budget=3.0):
+    """The batched layout measured like measure_config; FLOPs = 6 * valid
+    rows * H * I, bytes = touched experts' weights + valid rows in and out."""
     import mixture_experts_ffn_softmax_gb300 as pkg
+    step = BatchedStep(spec, device)
+    Kc = _steps_for(step, K, W, world)
+    n0 = pkg.launch_count()
+    ms = max_over_ranks(time_steps(step, Kc, W, world) / Kc, world)
+    launches = (pkg.launch_count() - n0) // (Kc + W)
+    R = step.rows
+    flops = 6.0 * R * spec.H * spec.I
+    touched = int((step.d["expert_num_tokens"] > 0).sum().item())
+    nbytes = touched * 3 * spec.H * spec.I * 2 + 2 * R * spec.H * 2
+    kern = _profile(step, min(Kc, 50))
+    work = {n: kernel_work(n, spec.H, spec.I, spec.E, 1, R, R, touched, spec.bias)
+            for n in kern}
+    work = {n: w for n, w in work.items() if w is not None}
+    roof_step, dom = _summary(kern, work, ms, flops, nbytes, pk)
+    gms = _graph_ms(step, Kc, W, world)
+    out = {"workload": spec.name, "E": spec.E, "T": spec.T, "H": spec.H, "I": spec.I,
+           "valid_rows": R, "steps": Kc, "ms_per_step": round(ms, 4),
+           "tokens_per_s": round(job_rate(R, world, ms), 1),
+           "tflops": round(flops * world / (ms / 1e3) / 1e12, 2), "experts_touched": touched,
+           "algorithmic_bytes": int(nbytes), "roofline_step": roof_step,
+           "dominant_kernel": dom, "gpu_launches": launches,
+           "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
+           "graph": {"ms_per_step": round(gms, 4),
+                     "tokens_per_s": round(job_rate(R, world, gms), 1)}}
+    if cpu and world == 1:
+        out["cpu_baseline"] = cpu_baseline_batched(spec, step.d, budget_s=cpu_budget)
+    return out, step
+
+
+def run_batched(args, world, rank, local):
     pk = peaks()
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
     spec = wl.BATCHED_SPECS[args.workload]
-    step = BatchedStep(spec, device)
     K, W = args.steps, args.warmup
+    step = BatchedStep(spec, device)
+    import mixture_experts_ffn_softmax_gb300 as pkg
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -236,28 +468,14 @@ def run_batched(args, world, rank, local):
     ck = clocks.stop()
     ms_step = max_over_ranks(ms / K, world)
     R = step.rows
-    flops = 6.0 * R * spec.H * spec.I
-    touched = int((step.d["expert_num_tokens"] > 0).sum().item())
-    nbytes = touched * 3 * spec.H * spec.I * 2 + 2 * R * spec.H * 2
-    pkg.profiler_start()
-    for _ in range(K):
-        step()
-    prof = pkg.profiler_stop()
-    kern = {k: 1e3 * v[1] / max(v[0], 1) for k, v in prof.items()}
-    roof_ms = 1e3 * max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
-    g1 = kern["gemm1_swiglu"]
-    b1 = touched * spec.H * 2 * spec.I * 2 + R * spec.H * 2
-    # the same step captured once into a CUDA graph and replayed
-    gs = torch.cuda.Stream()
-    gs.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(gs):
-        step()
-    torch.cuda.current_stream().wait_stream(gs)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    ms_graph = max_over_ranks(time_steps(graph.replay, K, W, world) / K, world)
-    del graph
+    del step
+    m, step = measure_batched(spec, device, K, W, world, pk, cpu=False)
+    dom = m["dominant_kernel"]
+    roof = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac") if k in dom}
+    roof.update({"kernel": dom["kernel"], "traffic": None,
+                 "traffic_note": "no ncu record for this kernel and workload",
+                 "peak_source": pk["source"] + (" burst bf16" if dom.get("bound") == "tensor"
+                                                else " copy")})
 
     hx = step.d["x"].cpu().pin_memory()
     hy = torch.empty_like(hx).pin_memory()
@@ -269,6 +487,7 @@ def run_batched(args, world, rank, local):
         hy.copy_(y, non_blocking=True)
 
     ms_e2e = max_over_ranks(time_steps(e2e_step, K, W, world) / K, world)
+    flops = 6.0 * R * spec.H * spec.I
     line = {
         "metric": METRIC, "value": round(job_rate(R, world, ms_step), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4),
@@ -278,14 +497,8 @@ def run_batched(args, world, rank, local):
                    "T": spec.T, "H": spec.H, "I": spec.I, "valid_rows": R,
                    "parallelism": f"replicas x{world}", "l2": "inputs larger than L2"},
         "tflops": round(flops * world / (ms_step / 1e3) / 1e12, 2),
-        "roofline_step": {"t_roof_ms": round(roof_ms, 4), "frac": round(roof_ms / ms_step, 4)},
-        "roofline": {"kernel": "gemm1_swiglu", "bound": "hbm",
-                     "achieved": round(b1 / (g1 * 1e-6) / 1e9, 1), "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(b1 / (g1 * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
-                     "traffic": None, "peak_source": pk["source"] + " copy"},
-        "kernels_us": {k: round(v, 2) for k, v in kern.items()},
-        "graph": {"ms_per_step": round(ms_graph, 4),
-                  "tokens_per_s": round(R * world / (ms_graph / 1e3), 1)},
+        "roofline_step": m["roofline_step"], "roofline": roof,
+        "kernels_us": m["kernels_us"], "graph": m["graph"],
         "gpu_launches": launches, "clocks": ck,
         "e2e": {"value": round(R * world / (ms_e2e / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hy.numel() * 2},
@@ -338,47 +551,26 @@ def run_ours(args, world, rank, local):
     tflops = flops * world / (ms_step / 1e3) / 1e12
 
     # per-kernel timing with events on the launching stream (second timed pass)
-    pkg.profiler_start()
-    for _ in range(K):
-        step()
-    prof = pkg.profiler_stop()
-    kern = {k: {"launches": v[0], "avg_us": 1e3 * v[1] / max(v[0], 1)} for k, v in prof.items()}
+    kern = _profile(step, K)
+    work = {n: kernel_work(n, spec.H, spec.I, spec.E, spec.top_k, spec.M, spec.R, touched,
+                           spec.bias) for n in kern}
+    work = {n: w for n, w in work.items() if w is not None}
+    roof_step, dom = _summary(kern, work, ms_step, flops, nbytes, pk)
+    # The roofline object is GEMM1's (the step's dominant kernel on the
+    # prefill shapes): algorithmic work per launch / its average event time.
+    g1 = kern["gemm1_swiglu"]["avg_us"]
+    f1, b1 = work["gemm1_swiglu"]
+    roof = {"kernel": "gemm1_swiglu", **roofline_of(f1, b1, g1 * 1e-6, pk),
+            "algorithmic_flops": f1, "algorithmic_bytes": int(b1),
+            "share_of_step": round(kern["gemm1_swiglu"]["launches"] * g1 / (ms_step * 1e3), 4)}
+    traffic, note = measured_traffic("gemm1_swiglu", spec.name)
+    roof["traffic"] = traffic
+    roof["traffic_note"] = note
+    roof["peak_source"] = pk["source"] + (
+        " burst bf16 (the kernel is timed in a region well under a second)"
+        if roof["bound"] == "tensor" else " copy")
 
-    g1 = kern.get("gemm1_swiglu", {}).get("avg_us")
-    g2 = kern.get("gemm2_scatter", {}).get("avg_us")
-    step_roof_ms = 1e3 * max(flops / (pk["bf16_tflops_sustained"] * 1e12),
-                             nbytes / (pk["hbm_gbs"] * 1e9))
-    if spec.M >= 1024:
-        # tensor-bound: GEMM1 carries 4 R H I of the 6 R H I FLOPs
-        f1 = 4.0 * spec.R * spec.H * spec.I
-        ach = f1 / (g1 * 1e-6) / 1e12
-        # timed inside a long loop of steps (power cap engages): the sustained peak
-        peak = pk["bf16_tflops_sustained"]
-        roof = {"kernel": "gemm1_swiglu", "bound": "tensor", "achieved": round(ach, 1),
-                "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                "traffic": measured_traffic("gemm1_swiglu", "mixtral_prefill")
-                if spec.name == "mixtral_prefill" else None,
-                "peak_source": pk["source"] + " sustained bf16 (kernel timed inside the step loop)",
-                "frac_of_burst_peak": round(ach / pk["bf16_tflops"], 4)}
-    else:
-        b1 = touched * spec.H * 2 * spec.I * 2 + spec.M * spec.H * 2
-        ach = b1 / (g1 * 1e-6) / 1e9
-        roof = {"kernel": "gemm1_swiglu", "bound": "hbm", "achieved": round(ach, 1),
-                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                "traffic": None, "peak_source": pk["source"] + " copy"}
-
-    # the same step captured once into a CUDA graph and replayed (launch
-    # overhead removed; matters for the small shapes)
-    gs = torch.cuda.Stream()
-    gs.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(gs):
-        step()
-    torch.cuda.current_stream().wait_stream(gs)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    ms_graph = max_over_ranks(time_steps(graph.replay, K, W, world) / K, world)
-    del graph
+    ms_graph = _graph_ms(step, K, W, world)
 
     # end to end through the C ABI with host buffers (moe_forward_host: the
     # copies of hidden and logits in, routing, the forward, the copy of out
@@ -401,8 +593,9 @@ def run_ours(args, world, rank, local):
            "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
            "d2h_bytes_per_step": hy.numel() * 2, "ms_per_step": round(ms_e2e, 4),
            "call": "moe_forward_host"}
-    del st
+    del st, hx, hl, hy
 
+    big = spec.M * spec.H * spec.top_k * 2 + 3 * spec.E * spec.H * spec.I * 2 > (129 << 20)
     line = {
         "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
@@ -411,13 +604,13 @@ def run_ours(args, world, rank, local):
                    else spec.name, "M": spec.M, "H": spec.H, "I": spec.I, "E": spec.E,
                    "top_k": spec.top_k, "routing": spec.routing_method,
                    "renormalize": spec.renormalize, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (weights 2.8 GB)"},
+                   "l2": "inputs larger than L2 (weights of every touched expert are read "
+                         "each step)" if big else "inputs fit in L2 (warm)"},
         "tflops": round(tflops, 2),
-        "roofline_step": {"t_roof_ms": round(step_roof_ms, 4),
-                          "frac": round(step_roof_ms / ms_step, 4),
-                          "bound": "tensor" if flops / pk["bf16_tflops_sustained"] / 1e12 > nbytes / pk["hbm_gbs"] / 1e9 else "hbm",
-                          "peaks": "measured sustained bf16, measured copy GB/s"},
+        "roofline_step": {**roof_step,
+                          "peaks": "measured burst bf16 GEMM, measured copy GB/s"},
         "roofline": roof,
+        "dominant_kernel": dom,
         "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
         "graph": {"ms_per_step": round(ms_graph, 4),
                   "tokens_per_s": round(spec.M * world / (ms_graph / 1e3), 1)},
@@ -426,49 +619,53 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
     }
 
-    # the decode shape of the same layer, reported alongside
-    if args.workload == "mixtral_prefill" and not args.no_decode:
-        dspec = wl.SPECS["mixtral_decode"]
-        dstep = OurStep(dspec, device)
-        dstep.d["w13"], dstep.d["w2"] = step.d["w13"], step.d["w2"]
-        Kd = max(K, 20)
-        dms = max_over_ranks(time_steps(dstep, Kd, max(W, 3), world) / Kd, world)
-        pkg.profiler_start()
-        for _ in range(Kd):
-            dstep()
-        dprof = pkg.profiler_stop()
-        gs = torch.cuda.Stream()
-        gs.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(gs):
-            dstep()
-        torch.cuda.current_stream().wait_stream(gs)
-        dgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(dgraph):
-            dstep()
-        dms_graph = max_over_ranks(time_steps(dgraph.replay, Kd, max(W, 3), world) / Kd, world)
-        del dgraph
-        dids = dstep.ids.cpu().numpy()
-        dfl, dby, dt = algorithmic(dspec, dids)
-        g1d = 1e3 * dprof["gemm1_swiglu"][1] / dprof["gemm1_swiglu"][0]
-        b1 = dt * dspec.H * 2 * dspec.I * 2 + dspec.M * dspec.H * 2
-        line["decode"] = {
-            "M": dspec.M, "ms_per_step": round(dms, 4),
-            "tokens_per_s": round(dspec.M * world / (dms / 1e3), 1),
-            "experts_touched": dt,
-            "hbm_roofline_frac": round((dby / (pk["hbm_gbs"] * 1e9)) / (dms / 1e3), 4),
-            "graph_ms_per_step": round(dms_graph, 4),
-            "gemm1_hbm_gbs": round(b1 / (g1d * 1e-6) / 1e9, 1),
-            "kernels_us": {k: round(1e3 * v[1] / v[0], 2) for k, v in dprof.items()},
-        }
-
     if args.workload == "mixtral_prefill" and not args.no_next_rows:
         line["next_rows"] = measure_next_rows(step, spec, K, W, world, pk)
         line["next_rows"]["weight_only_quantised"] = measure_wq(step, spec, K, W, world, pk)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, step.d, budget_s=args.cpu_budget)
+
+    if args.workload == "mixtral_prefill":
+        line["configs"] = measure_all_configs(args, step, device, K, W, world, pk)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def measure_all_configs(args, head_step, device, K, W, world, pk):
+    """Every other workload of the layer family, one after the other (each
+    freed before the next), measured by measure_config / measure_batched."""
+    cpu = world == 1 and not args.no_cpu_baseline
+    out = {}
+
+    def free():
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    if not args.no_decode:
+        out["mixtral_decode"], _ = measure_config(wl.SPECS["mixtral_decode"], device, K, W,
+                                                  world, pk, weights_from=head_step.d, cpu=cpu)
+    if args.no_configs:
+        return out
+    out["tiny"], _ = measure_config(wl.SPECS["tiny"], device, K, W, world, pk, cold_l2=True,
+                                    cpu=cpu)
+    free()
+    ds64, st = measure_config(wl.SPECS["deepseek_m64"], device, K, W, world, pk, cpu=cpu)
+    out["deepseek_m64"] = ds64
+    out["deepseek_m8192"], _ = measure_config(wl.SPECS["deepseek_m8192"], device, K, W, world,
+                                              pk, weights_from=st.d, cpu=cpu, graph=False)
+    del st
+    free()
+    q, st = measure_config(wl.SPECS["qwen_skew"], device, K, W, world, pk, cpu=cpu)
+    out["qwen_skew"] = q
+    out["qwen_skew_lit"], _ = measure_config(wl.SPECS["qwen_skew_lit"], device, K, W, world,
+                                             pk, weights_from=st.d, cpu=cpu)
+    del st
+    free()
+    out["batched"], _ = measure_batched(wl.BATCHED_SPECS["batched"], device, K, W, world, pk,
+                                        cpu=cpu)
+    free()
+    return out
 
 
 def measure_next_rows(step, spec, K, W, world, pk):
@@ -527,7 +724,7 @@ def measure_next_rows(step, spec, K, W, world, pk):
 
     # FP8 W8A8: E4M3 weights with per-output-channel scales, activations
     # quantised per row on the GPU; the fp8 tensor peak is the measured
-    # sustained bf16 peak x 2 (nominal dense fp8 : bf16 = 4.5 : 2.25)
+    # burst bf16 peak x 2 (nominal dense fp8 : bf16 = 4.5 : 2.25)
     q = wl.make_fp8_weights(spec, device=dev, per_channel=True)
     ws8 = pkg.alloc_workspace(pkg.workspace_size_fp8(spec.M, spec.H, spec.I, spec.E,
                                                      spec.top_k), dev)
@@ -543,7 +740,7 @@ def measure_next_rows(step, spec, K, W, world, pk):
     prof = pkg.profiler_stop()
     us = {k: 1e3 * v[1] / max(v[0], 1) for k, v in prof.items()}
     f1 = 4.0 * spec.R * spec.H * spec.I
-    peak8 = 2.0 * pk["bf16_tflops_sustained"]
+    peak8 = 2.0 * pk["bf16_tflops"]
     ach = f1 / (us["gemm1_swiglu_fp8"] * 1e-6) / 1e12
     out["fp8_w8a8"] = {"ms_per_step": round(ms, 4),
                        "tokens_per_s": round(spec.M * world / (ms / 1e3), 1),
@@ -552,7 +749,7 @@ def measure_next_rows(step, spec, K, W, world, pk):
                        "roofline": {"kernel": "gemm1_swiglu_fp8", "bound": "tensor",
                                     "achieved": round(ach, 1), "peak": round(peak8, 1),
                                     "unit": "TFLOP/s", "frac": round(ach / peak8, 4),
-                                    "peak_source": "measured sustained bf16 x 2 (nominal ratio)"}}
+                                    "peak_source": "measured burst bf16 x 2 (nominal fp8 : bf16 ratio)"}}
     del q
 
     # the same with 128 x 128 weight-block scales (activations per row and
@@ -577,7 +774,7 @@ def measure_next_rows(step, spec, K, W, world, pk):
                              "roofline": {"kernel": "gemm1_swiglu_fp8_block", "bound": "tensor",
                                           "achieved": round(ach, 1), "peak": round(peak8, 1),
                                           "unit": "TFLOP/s", "frac": round(ach / peak8, 4),
-                                          "peak_source": "measured sustained bf16 x 2 (nominal ratio)"}}
+                                          "peak_source": "measured burst bf16 x 2 (nominal fp8 : bf16 ratio)"}}
     del qb, ws8
     return out
 
@@ -635,23 +832,52 @@ def measure_wq(step, spec, K, W, world, pk):
 
 
 # ------------------------------------------------------- CPU oracle legs --
-def _oracle_sample(spec, d, n_tokens):
-    """Host fp64 copies of a token sample and the experts it touches."""
-    sel = np.arange(n_tokens)
-    x = wl.to_f64(d["hidden"][:n_tokens])
-    logits = wl.to_f64(d["router_logits"][:n_tokens])
-    return sel, x, logits
+class _ExpertsF64:
+    """Host fp64 copies of just the experts a sample uses, indexable like the
+    [E, ...] weight tensor (the oracle reads w[e] only for experts with
+    routed rows).  Widening happens here, before any timing."""
+
+    def __init__(self, t, experts):
+        self.shape = tuple(t.shape)
+        self._w = {int(e): wl.to_f64(t[int(e)]) for e in experts}
+
+    def __getitem__(self, e):
+        return self._w[int(e)]
+
+
+def _sample_tokens(spec, n_small=None):
+    """Tokens in the CPU sample.  Each expert the sample touches is widened
+    to fp64 on the host (3 H I 8 bytes): when all experts fit in 12 GB the
+    sample is 256 tokens for E <= 8 and 128 routed rows otherwise (n_small
+    overrides), else as many tokens as keep the touched experts within 6 GB."""
+    per_expert = 3 * spec.H * spec.I * 8
+    if spec.E * per_expert <= 12e9:
+        n = n_small or (256 if spec.E <= 8 else max(1, 128 // spec.top_k))
+        return min(spec.M, n)
+    return min(spec.M, max(1, int(6e9 // per_expert) // spec.top_k))
+
+
+def _oracle_inputs(spec, d, n):
+    import oracle
+    x = wl.to_f64(d["hidden"][:n])
+    logits = wl.to_f64(d["router_logits"][:n])
+    _, ids, _ = oracle.route(logits, spec.top_k, spec.routing_method, spec.renormalize,
+                             spec.k_group, spec.group_count, spec.group_select_mode,
+                             spec.routed_scaling_factor)
+    experts = np.unique(ids)
+    w13 = _ExpertsF64(d["w13"], experts)
+    w2 = _ExpertsF64(d["w2"], experts)
+    b13 = wl.to_f64(d["w13_bias"]) if d.get("w13_bias") is not None else None
+    b2 = wl.to_f64(d["w2_bias"]) if d.get("w2_bias") is not None else None
+    return x, logits, w13, w2, b13, b2, experts.size
 
 
 def cpu_baseline(spec, d, budget_s=15.0, kind="oracle"):
-    """Times the CPU oracle (as it stands) on a bounded token sample."""
+    """Times the CPU oracle (as it stands) on a bounded token sample: the
+    whole layer (routing + the experts of each sampled token) in fp64."""
     import oracle
-    n = min(spec.M, 256 if spec.H * spec.I >= 4096 * 4096 else 1024)
-    _, x, logits = _oracle_sample(spec, d, n)
-    w13 = wl.to_f64(d["w13"])
-    w2 = wl.to_f64(d["w2"])
-    b13 = wl.to_f64(d["w13_bias"]) if d.get("w13_bias") is not None else None
-    b2 = wl.to_f64(d["w2_bias"]) if d.get("w2_bias") is not None else None
+    n = _sample_tokens(spec)
+    x, logits, w13, w2, b13, b2, n_exp = _oracle_inputs(spec, d, n)
     t0 = time.perf_counter()
     reps = 0
     while True:
@@ -664,22 +890,48 @@ def cpu_baseline(spec, d, budget_s=15.0, kind="oracle"):
     dt = (time.perf_counter() - t0) / reps
     return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": os.cpu_count(),
             "kind": kind,
-            "sample": f"{n} of {spec.M} tokens of {spec.name}, full routing + {spec.top_k} "
-                      f"experts per token in fp64 numpy, {reps} rep(s), {dt:.2f} s each"}
+            "sample": f"{n} of {spec.M} tokens of {spec.name} ({n_exp} experts touched), full "
+                      f"routing + {spec.top_k} experts per token in fp64 numpy, {reps} rep(s), "
+                      f"{dt:.3f} s each"}
+
+
+def cpu_baseline_batched(spec, d, budget_s=3.0, n_experts=2):
+    """The oracle's batched forward on the valid rows of the first n_experts
+    experts (their weights widened to fp64 beforehand)."""
+    import oracle
+    counts = d["expert_num_tokens"][:n_experts].cpu().numpy()
+    xb = wl.to_f64(d["x"][:n_experts])
+    rw = wl.to_f64(d["row_weight"][:n_experts])
+    ex = range(n_experts)
+    w13, w2 = _ExpertsF64(d["w13"], ex), _ExpertsF64(d["w2"], ex)
+    w13.shape = (n_experts,) + w13.shape[1:]
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.forward_batched(xb, counts, w13, w2, None, None, rw)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s / 2 or reps >= 3:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    rows = int(counts.sum())
+    return {"value": round(rows / dt, 2), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"the {rows} valid rows of experts 0..{n_experts - 1} of {spec.E} "
+                      f"({spec.name}) in fp64 numpy, {reps} rep(s), {dt:.3f} s each"}
 
 
 def run_reference(args, world, rank, local):
     if rank != 0:
         return
-    spec = wl.SPECS[args.workload]
+    if args.workload in wl.BATCHED_SPECS:
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the reference arm times the contiguous-layout workloads only"}))
+        return
+    spec = {**wl.SPECS, **wl.PROFILE_SPECS}[args.workload]
     d = wl.make_moe_inputs(spec, device="cpu")
     import oracle
-    n = min(spec.M, 128)
-    x = wl.to_f64(d["hidden"][:n])
-    logits = wl.to_f64(d["router_logits"][:n])
-    w13, w2 = wl.to_f64(d["w13"]), wl.to_f64(d["w2"])
-    b13 = wl.to_f64(d["w13_bias"]) if d["w13_bias"] is not None else None
-    b2 = wl.to_f64(d["w2_bias"]) if d["w2_bias"] is not None else None
+    n = _sample_tokens(spec, n_small=128)
+    x, logits, w13, w2, b13, b2, n_exp = _oracle_inputs(spec, d, n)
 
     def step():
         oracle.moe_layer(x, logits, w13, w2, spec.top_k, spec.routing_method, spec.renormalize,
@@ -701,7 +953,8 @@ def run_reference(args, world, rank, local):
                        "E": spec.E, "top_k": spec.top_k, "parallelism": "cpu oracle"},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
                              "kind": "oracle",
-                             "sample": f"{n} of {spec.M} tokens per step (fp64 numpy oracle)"},
+                             "sample": f"{n} of {spec.M} tokens per step ({n_exp} experts "
+                                       f"touched; fp64 numpy oracle)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -718,6 +971,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads of the layer family (decode still runs)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--tiles", default="auto", choices=["auto", "single", "pairs"],
                     help="grouped-GEMM tile shape (default: the library's automatic choice)")

@@ -170,15 +170,23 @@ GBMOE_API moe_status_t moe_align(const int32_t* topk_ids, int64_t M, int32_t top
  *
  * Same arguments, outputs and errors as moe_align, minus `scratch`: the
  * per-chunk count table lives in a library-owned static device array of
- * MOE_ALIGN_STATIC_SCRATCH_INTS int32 (1 MiB), allocated when the library is
- * loaded on a GPU and held by every GPU that loads it until the process
+ * MOE_ALIGN_STATIC_SCRATCH_INTS int32 (1 MiB).  The array belongs to the
+ * library's device code module: with CUDA's lazy module loading (the default)
+ * the module, and with it the array, is loaded on a device by the first
+ * call of this entry point (or of any other kernel of the library) there, so
+ * THAT first call may allocate; every later call allocates nothing.  Once
+ * loaded, every GPU that uses the library holds the array until the process
  * exits.  Sizes with ceil(M * top_k / 256) * E > MOE_ALIGN_STATIC_SCRATCH_INTS
- * are rejected with MOE_ERR_WORKSPACE_TOO_SMALL.  The entry point calls no
- * allocating routine.  The first call on each device looks up the array's
- * device address (set-up); make that first call before any stream capture.
- * All calls share the one array and it keeps the last call's contents (every
- * entry a call reads is written earlier in that same call, so nothing has to
- * start at zero); calls that overlap on the GPU, on any streams, race on it.
+ * are rejected with MOE_ERR_WORKSPACE_TOO_SMALL.  The entry point itself calls
+ * no cudaMalloc / cudaFree or allocating library routine.  The first call on
+ * each device also looks up the array's device address (set-up) and caches
+ * it for that device; make that first call before any stream capture.  A
+ * device reset (cudaDeviceReset, or tearing down and re-creating the primary
+ * context) invalidates the cached address: do not call this entry point in a
+ * process after such a reset.  All calls share the one array and it keeps the
+ * last call's contents (every entry a call reads is written earlier in that
+ * same call, so nothing has to start at zero); calls that overlap on the GPU,
+ * on any streams, race on it.
  */
 #define MOE_ALIGN_STATIC_SCRATCH_INTS (1 << 18)
 GBMOE_API moe_status_t moe_align_static_scratch(const int32_t* topk_ids, int64_t M,

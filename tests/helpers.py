@@ -84,6 +84,29 @@ def check_out(out, ref, what=""):
     return rel, mx / max(rms, 1e-30)
 
 
+def covering_tokens(ids, n_random, rng, block_m=128):
+    """Token sample for full-size parity: for every expert that receives
+    items, the tokens of its first item, of the first item of its last
+    block_m-row block and of its last item (items of one expert sit in
+    ascending item order r = t * top_k + j in the sorted layout, so these
+    reach the first and the last row block of every expert's GEMM tiles),
+    plus n_random tokens drawn at random.  Returns sorted token indices."""
+    ids = np.asarray(ids)
+    M, k = ids.shape
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    bounds = np.searchsorted(flat[order], np.arange(flat.max() + 2))
+    sel = set()
+    for e in range(flat.max() + 1):
+        items = order[bounds[e]:bounds[e + 1]]
+        if items.size == 0:
+            continue
+        for pos in (0, (items.size - 1) // block_m * block_m, items.size - 1):
+            sel.add(int(items[pos]) // k)
+    sel.update(int(t) for t in rng.choice(M, size=min(M, n_random), replace=False))
+    return np.array(sorted(sel))
+
+
 class LazyF64:
     """Indexable view of a (possibly device, bf16) weight tensor that widens one
     expert at a time to float64 on the host, so full-size layers never need a

@@ -13,7 +13,7 @@ import oracle
 import mixture_experts_ffn_softmax_gb300 as pkg
 from mixture_experts_ffn_softmax_gb300 import workloads as wl
 
-from helpers import LazyF64, check_out, check_route, f64, route_args
+from helpers import LazyF64, check_out, check_route, covering_tokens, f64, route_args
 
 pytestmark = pytest.mark.gpu
 
@@ -234,13 +234,18 @@ def test_tile_shapes_agree_full_size_mixtral():
     check_out(f64(ys[1]), f64(ys[0]), "pairs vs single")
 
 
-FULL = ["mixtral_prefill", "mixtral_decode", "deepseek_m64", "deepseek_m8192", "qwen_skew"]
+FULL = ["mixtral_prefill", "mixtral_decode", "deepseek_m64", "deepseek_m8192", "qwen_skew",
+        "qwen_skew_lit"]
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_forward_full_size_sampled(name):
     """Full-size layer in the benchmark's launch configuration; sampled tokens
-    checked against the oracle one by one."""
+    checked against the oracle.  The sample holds, for every expert that
+    receives items, the tokens of its first item, of the first item of its
+    last 128-row block and of its last item (so every touched expert's first
+    and last row block of the grouped GEMMs is compared), plus random
+    tokens."""
     spec = wl.SPECS[name]
     d = wl.make_moe_inputs(spec, device="cuda")
     a = route_args(spec)
@@ -255,8 +260,9 @@ def test_forward_full_size_sampled(name):
     gw_np, gids_np = gw.cpu().numpy(), gids.cpu().numpy()
     check_route(d["router_logits"].cpu().numpy(), gw_np, gids_np, a)
     rng = np.random.default_rng(0)
-    n = min(spec.M, 12 if spec.E > 64 else 24)
-    sel = np.sort(rng.choice(spec.M, size=n, replace=False))
+    sel = covering_tokens(gids_np, 12 if spec.E > 64 else 24, rng)
+    touched = np.unique(gids_np)
+    assert set(np.unique(gids_np[sel])) == set(touched)
     xs = f64(d["hidden"][torch.from_numpy(sel).cuda()])
     ref = oracle.forward(xs, gw_np[sel].astype(np.float64), gids_np[sel], LazyF64(d["w13"]),
                          LazyF64(d["w2"]),

@@ -39,7 +39,7 @@ def _ranks(rank, world, port, out):
 
 def test_max_over_ranks_and_job_rate_gloo():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_ranks, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)

@@ -3,11 +3,14 @@ allocate device memory (an operator inside another framework with no handle
 to its allocator, or a latency-critical loop where cudaMalloc is not
 allowed).  Its scratch is a static device array owned by the library.
 
-Checks, through the C ABI, that two calls in a row give exactly what the
+Checks, through the C ABI, that calls in a row give exactly what the
 regular moe_align (caller-provided scratch) gives: the outputs are integer
-index data, so the comparison is bit-exact.  The second call uses a smaller
-problem than the first, so stale contents left in the shared static array
-by the first call would show up as a mismatch.  This file is collected last.
+index data, so the comparison is bit-exact.  Every case is large enough to
+take the four-kernel align path (more than 4096 routed items with more than
+16 experts), the only path that uses the static array; the second and third
+calls are smaller than the first and use other expert counts, so the table
+is laid out differently in the array each time, and stale contents left by
+an earlier call would show up as a mismatch.  This file is collected last.
 """
 import ctypes
 
@@ -60,8 +63,10 @@ def _ids(M, k, E, seed):
 
 def test_static_scratch_align_matches_regular_align_twice():
     dev = torch.device("cuda")
-    for M, k, E, bm, seed in ((8192, 8, 256, 128, 0), (777, 3, 40, 16, 1)):
+    for M, k, E, bm, seed in ((8192, 8, 256, 128, 0), (1000, 6, 64, 16, 1),
+                              (3000, 8, 100, 64, 2)):
         assert -(-(M * k) // 256) * E <= MAX_INTS
+        assert M * k > 4096 and E > 16        # the four-kernel path, which uses the array
         ids = _ids(M, k, E, seed)
         a, b = _outputs(M, k, E, bm, dev), _outputs(M, k, E, bm, dev)
         _call_static(ids, M, k, E, bm, a)
