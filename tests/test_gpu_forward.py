@@ -234,6 +234,34 @@ def test_tile_shapes_agree_full_size_mixtral():
     check_out(f64(ys[1]), f64(ys[0]), "pairs vs single")
 
 
+@pytest.mark.parametrize("tiles", ["single", "pairs"], indirect=True)
+@pytest.mark.parametrize("reduce", ["separate", "epilogue_atomic"])
+def test_odd_and_even_row_blocks(reduce, tiles):
+    """Experts with 0, 1, 2, 3 and 5 row blocks (a pair tile's second row
+    block is absent for the odd ones: its rows are computed, never stored),
+    ragged N in both GEMMs, biases, and a repeated call giving the same bits."""
+    counts = [0, 100, 128, 129, 300, 600, 256]
+    E, H, I = len(counts), 392, 328
+    rng = np.random.default_rng(21)
+    ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)]).astype(np.int32)
+    rng.shuffle(ids)
+    M, k = ids.size, 1
+    ids = ids.reshape(M, k)
+    wts = rng.random((M, k)).astype(np.float32)
+    g = torch.Generator(device="cuda").manual_seed(21)
+    x = torch.randn(M, H, generator=g, device="cuda").bfloat16()
+    w13 = (torch.randn(E, H, 2 * I, generator=g, device="cuda") * 0.05).bfloat16()
+    w2 = (torch.randn(E, I, H, generator=g, device="cuda") * 0.05).bfloat16()
+    b13 = (torch.randn(E, 2 * I, generator=g, device="cuda") * 0.1).bfloat16()
+    b2 = (torch.randn(E, H, generator=g, device="cuda") * 0.1).bfloat16()
+    tw, tids = torch.from_numpy(wts).cuda(), torch.from_numpy(ids).cuda()
+    ys = [pkg.moe_forward(x, tw, tids, w13, w2, b13, b2, reduce=reduce) for _ in range(2)]
+    torch.cuda.synchronize()
+    ref = oracle.forward(f64(x), wts, ids, f64(w13), f64(w2), f64(b13), f64(b2))
+    check_out(f64(ys[0]), ref, f"odd/even row blocks {tiles} {reduce}")
+    assert torch.equal(ys[0], ys[1])
+
+
 FULL = ["mixtral_prefill", "mixtral_decode", "deepseek_m64", "deepseek_m8192", "qwen_skew",
         "qwen_skew_lit"]
 
