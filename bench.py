@@ -978,6 +978,8 @@ def main():
                     help="grouped-GEMM tile shape (default: the library's automatic choice)")
     ap.add_argument("--reduce", default="auto", choices=["auto", "separate", "epilogue_atomic"],
                     help="TopKWeightAndReduce choice (default: the library's AUTO rule)")
+    ap.add_argument("--pdl", default="on", choices=["on", "off"],
+                    help="programmatic dependent launch between the library's kernels")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     OurStep.reduce = args.reduce
@@ -985,6 +987,9 @@ def main():
     if args.impl == "ours" and args.tiles != "auto":
         import mixture_experts_ffn_softmax_gb300 as pkg
         pkg.set_gemm_tiles(args.tiles)
+    if args.impl == "ours" and args.pdl == "off":
+        import mixture_experts_ffn_softmax_gb300 as pkg
+        pkg.set_pdl(False)
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     elif args.workload in wl.BATCHED_SPECS:

@@ -418,6 +418,14 @@ def set_gather_mode(mode: str = "auto"):
            "moe_set_gather_mode")
 
 
+def set_pdl(enabled: bool = True):
+    """Programmatic dependent launch between the library's consecutive
+    kernels (on by default): each kernel is scheduled while the one before
+    it runs and waits on the device for it to complete.  Results are
+    identical either way."""
+    _check(lib().moe_set_pdl(1 if enabled else 0), "moe_set_pdl")
+
+
 def profiler_start():
     _check(lib().moe_profiler_start(), "moe_profiler_start")
 
@@ -432,7 +440,7 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
-           "moe_forward_host", "HostStaging", "set_gather_mode",
+           "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
            "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",

@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kAlignWarps * 32)
     align_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int num_chunks,
                       int32_t* __restrict__ chunk_counts, int32_t* error_word,
                       const int32_t* __restrict__ emap, int E_global) {
+  pdl_begin();
   extern __shared__ int32_t hist_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kAlignWarps + warp;
@@ -146,6 +147,7 @@ constexpr int kColScanThreads = 256;
 __global__ void __launch_bounds__(kColScanThreads)
     align_colscan_kernel(int num_chunks, int32_t* __restrict__ chunk_counts,
                          int32_t* __restrict__ counts) {
+  pdl_begin();
   __shared__ int32_t s_warp[kColScanThreads / 32];
   __shared__ int32_t s_carry;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -192,6 +194,7 @@ __global__ void __launch_bounds__(kScanThreads)
     align_offsets_kernel(int E, int block_m, int32_t sentinel, int64_t cap,
                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                          int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted) {
+  pdl_begin();
   __shared__ int32_t s_count[1024];
   __shared__ int32_t s_off[1025];
   __shared__ int32_t s_warp[32];
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__(kScanThreads)
                        int32_t* __restrict__ counts, int32_t* __restrict__ block_expert,
                        int32_t* __restrict__ inv, int32_t* error_word,
                        const int32_t* __restrict__ emap, int E_global) {
+  pdl_begin();
   __shared__ int32_t s_cnt[32 * kSmallExperts];
   __shared__ int32_t s_count[kSmallExperts];
   __shared__ int32_t s_off[kSmallExperts + 1];
@@ -275,6 +279,7 @@ __global__ void __launch_bounds__(kAlignWarps * 32)
                          const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted,
                          int32_t* __restrict__ inv, const int32_t* __restrict__ emap,
                          int E_global) {
+  pdl_begin();
   extern __shared__ int32_t run_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kAlignWarps + warp;
@@ -307,6 +312,7 @@ __global__ void __launch_bounds__(kScanThreads)
                         int32_t sentinel, int64_t cap, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted,
                         int32_t* error_word) {
+  pdl_begin();
   __shared__ int32_t s_count[1024];
   __shared__ int32_t s_off[1025];
   __shared__ int32_t s_warp[32];
@@ -383,10 +389,9 @@ moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
   if ((a.R <= kSmallItems && a.E <= kSmallExperts) ||
       (a.R <= kSmallItemsFewExperts && a.E <= kFewExperts)) {
     prof_before("align_small", s);
-    align_small_kernel<<<1, kScanThreads, 0, s>>>(a.ids, static_cast<int>(a.R), a.E, a.block_m,
-                                                  a.cap, a.sorted, a.offsets, a.counts,
-                                                  a.block_expert, a.inv, a.error_word,
-                                                  a.expert_map, a.E_global);
+    launch_kernel(align_small_kernel, 1, kScanThreads, 0, s, a.ids, static_cast<int>(a.R), a.E,
+                  a.block_m, a.cap, a.sorted, a.offsets, a.counts, a.block_expert, a.inv,
+                  a.error_word, a.expert_map, a.E_global);
     prof_after("align_small", s);
     return check_launch("align_small");
   }
@@ -394,34 +399,31 @@ moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(kAlignWarps) * a.E * sizeof(int32_t);
   const unsigned grid = static_cast<unsigned>(ceil_div(num_chunks, kAlignWarps));
   prof_before("align_hist", s);
-  align_hist_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
-                                                         a.chunk_counts, a.error_word,
-                                                         a.expert_map, a.E_global);
+  launch_kernel(align_hist_kernel, grid, kAlignWarps * 32, smem, s, a.ids, a.R, a.E, num_chunks,
+                a.chunk_counts, a.error_word, a.expert_map, a.E_global);
   prof_after("align_hist", s);
   if (moe_status_t st = check_launch("align_hist")) return st;
   prof_before("align_colscan", s);
-  align_colscan_kernel<<<a.E, kColScanThreads, 0, s>>>(num_chunks, a.chunk_counts, a.counts);
+  launch_kernel(align_colscan_kernel, a.E, kColScanThreads, 0, s, num_chunks, a.chunk_counts,
+                a.counts);
   prof_after("align_colscan", s);
   if (moe_status_t st = check_launch("align_colscan")) return st;
   prof_before("align_offsets", s);
-  align_offsets_kernel<<<1, kScanThreads, 0, s>>>(a.E, a.block_m, static_cast<int32_t>(a.R),
-                                                  a.cap, a.counts, a.offsets, a.block_expert,
-                                                  a.sorted);
+  launch_kernel(align_offsets_kernel, 1, kScanThreads, 0, s, a.E, a.block_m,
+                static_cast<int32_t>(a.R), a.cap, a.counts, a.offsets, a.block_expert, a.sorted);
   prof_after("align_offsets", s);
   if (moe_status_t st = check_launch("align_offsets")) return st;
   prof_before("align_scatter", s);
-  align_scatter_kernel<<<grid, kAlignWarps * 32, smem, s>>>(a.ids, a.R, a.E, num_chunks,
-                                                            a.chunk_counts, a.offsets, a.sorted,
-                                                            a.inv, a.expert_map, a.E_global);
+  launch_kernel(align_scatter_kernel, grid, kAlignWarps * 32, smem, s, a.ids, a.R, a.E, num_chunks,
+                a.chunk_counts, a.offsets, a.sorted, a.inv, a.expert_map, a.E_global);
   prof_after("align_scatter", s);
   return check_launch("align_scatter");
 }
 
 moe_status_t launch_batched_plan(const BatchedPlanArgs& a, cudaStream_t s) {
   prof_before("batched_plan", s);
-  batched_plan_kernel<<<1, kScanThreads, 0, s>>>(a.counts_in, a.E, a.T, a.block_m, a.sentinel,
-                                                 a.cap, a.offsets, a.block_expert, a.sorted,
-                                                 a.error_word);
+  launch_kernel(batched_plan_kernel, 1, kScanThreads, 0, s, a.counts_in, a.E, a.T, a.block_m,
+                a.sentinel, a.cap, a.offsets, a.block_expert, a.sorted, a.error_word);
   prof_after("batched_plan", s);
   return check_launch("batched_plan");
 }

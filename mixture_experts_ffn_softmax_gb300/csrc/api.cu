@@ -46,9 +46,11 @@ cudaEvent_t take_event() {
 namespace {
 std::atomic<int> g_gemm_tile_mode{0};
 std::atomic<int> g_gather_mode{0};
+std::atomic<int> g_pdl{1};
 }  // namespace
 
 int gemm_tile_mode() { return g_gemm_tile_mode.load(std::memory_order_relaxed); }
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
 // Automatic choice: fused when the routed rows are few (<= 16 MiB of them).
 // The gather warp's 16-byte copies move ~16 B per cycle per SM, half of what
@@ -245,6 +247,12 @@ int64_t moe_launch_count(void) { return g_launches; }
 moe_status_t moe_set_gemm_tiles(int32_t mode) {
   if (mode < 0 || mode > 2) return set_error(MOE_ERR_INVALID_ARG, "gemm tile mode %d", mode);
   g_gemm_tile_mode.store(mode, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_set_pdl(int32_t enabled) {
+  if (enabled != 0 && enabled != 1) return set_error(MOE_ERR_INVALID_ARG, "pdl switch %d", enabled);
+  g_pdl.store(enabled, std::memory_order_relaxed);
   return MOE_OK;
 }
 

@@ -38,6 +38,39 @@ moe_status_t check_launch(const char* name);
 // GEMM tile shape selection: 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles.
 int gemm_tile_mode();
 
+// ---- programmatic dependent launch ----
+// Every kernel of the library is launched with programmatic stream
+// serialisation allowed (launch_kernel) and begins with pdl_begin(): it waits
+// until the grid before it in the stream has completed and that grid's
+// memory operations are visible (griddepcontrol.wait), then lets the next
+// grid be scheduled (griddepcontrol.launch_dependents).  The next kernel's
+// CTAs can thus be made resident, their launch latency spent, while this
+// kernel runs, and each still starts its work only after this one has
+// completed.  Every kernel waits before anything else, so completion order is
+// transitive along a chain of launches.  A kernel whose predecessor is not
+// such a launch (another library's kernel, a copy) waits for it as usual.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Whether launches carry the attribute (moe_set_pdl; on by default).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // A value computed once per device (function attributes, occupancy), safely
 // from several host threads: get(f) returns f()'s result for the current
 // device, calling f the first time for that device (again after a failure).

@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     gather_rows_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ index,
                        const int32_t* __restrict__ offsets, int E, int div, int32_t sentinel,
                        int H, int64_t cap, bf16* __restrict__ dst) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int64_t rows = min(static_cast<int64_t>(offsets[E]), cap);
   const int nvec = H / 8;  // 16-byte vectors per row
@@ -47,6 +48,7 @@ template <int V>
 __global__ void __launch_bounds__(256)
     reduce_sorted_kernel(const float* __restrict__ o, const int32_t* __restrict__ inv,
                          int64_t M, int k, int H, bf16* __restrict__ y) {
+  pdl_begin();
   const int hv = H / (4 * V);  // H % 8 == 0
   const int64_t total = M * hv;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -89,6 +91,7 @@ __global__ void __launch_bounds__(256)
 // y = bf16(acc), 8 elements per thread.
 __global__ void __launch_bounds__(256)
     cast_f32_bf16_kernel(const float* __restrict__ acc, int64_t n8, bf16* __restrict__ y) {
+  pdl_begin();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
@@ -128,8 +131,8 @@ moe_status_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   const int64_t want = ceil_div<int64_t>(a.cap, kGatherWarps);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
   prof_before("gather_rows", s);
-  gather_rows_kernel<<<grid, kGatherWarps * 32, 0, s>>>(a.src, a.index, a.offsets, a.E, a.div,
-                                                        a.sentinel, a.H, a.cap, a.dst);
+  launch_kernel(gather_rows_kernel, grid, kGatherWarps * 32, 0, s, a.src, a.index, a.offsets, a.E,
+                a.div, a.sentinel, a.H, a.cap, a.dst);
   prof_after("gather_rows", s);
   return check_launch("gather_rows");
 }
@@ -143,9 +146,9 @@ moe_status_t launch_reduce_sorted(const float* o_sorted, const int32_t* inv, int
       static_cast<unsigned>(std::min<int64_t>(ceil_div<int64_t>(total, 256), device_sms() * 8));
   prof_before("reduce_sorted", s);
   if (V == 2)
-    reduce_sorted_kernel<2><<<grid, 256, 0, s>>>(o_sorted, inv, M, k, H, y);
+    launch_kernel(reduce_sorted_kernel<2>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
   else
-    reduce_sorted_kernel<1><<<grid, 256, 0, s>>>(o_sorted, inv, M, k, H, y);
+    launch_kernel(reduce_sorted_kernel<1>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
   prof_after("reduce_sorted", s);
   return check_launch("reduce_sorted");
 }
@@ -156,7 +159,7 @@ moe_status_t launch_cast_f32_bf16(const float* acc, int64_t n, bf16* y, cudaStre
   const unsigned grid =
       static_cast<unsigned>(std::min<int64_t>(ceil_div<int64_t>(n8, 256), device_sms() * 8));
   prof_before("cast_f32_bf16", s);
-  cast_f32_bf16_kernel<<<grid, 256, 0, s>>>(acc, n8, y);
+  launch_kernel(cast_f32_bf16_kernel, grid, 256, 0, s, acc, n8, y);
   prof_after("cast_f32_bf16", s);
   return check_launch("cast_f32_bf16");
 }
@@ -178,6 +181,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     router_small_kernel(const bf16* __restrict__ x, const bf16* __restrict__ wg,
                         const bf16* __restrict__ bg, int64_t M, int H, int E,
                         float* __restrict__ s) {
+  pdl_begin();
   extern __shared__ float4 router_smem[];
   // W_g as fp32 [H][EMAX] (zero past E), 16 bytes of padding after every 8
   // rows so that the 32 lanes, 8 rows apart, hit different banks.
@@ -270,7 +274,8 @@ moe_status_t launch_router_small_t(const bf16* x, const bf16* wg, const bf16* bg
   const unsigned grid = static_cast<unsigned>(
       std::min<int64_t>(ceil_div<int64_t>(M, kRouterWarps), device_sms()));
   prof_before("router_small", st);
-  router_small_kernel<EMAX><<<grid, kRouterWarps * 32, smem, st>>>(x, wg, bg, M, H, E, s);
+  launch_kernel(router_small_kernel<EMAX>, grid, kRouterWarps * 32, smem, st, x, wg, bg, M, H, E,
+                s);
   prof_after("router_small", st);
   return check_launch("router_small");
 }
@@ -313,6 +318,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_tokens_fp8_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ inv,
                             int64_t M, int k, int H, uint8_t* __restrict__ q8,
                             float* __restrict__ scale, float* __restrict__ row_amax) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nvec = H / 8;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
@@ -372,6 +378,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_sorted_fp8_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ index,
                             const int32_t* __restrict__ offsets, int E, int32_t sentinel, int H,
                             int64_t cap, uint8_t* __restrict__ q8, float* __restrict__ scale_io) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int64_t rows = min(static_cast<int64_t>(offsets[E]), cap);
   const int nvec = H / 8;
@@ -419,6 +426,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_tokens_group_fp8_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ inv,
                                   int64_t M, int k, int H, uint8_t* __restrict__ q8,
                                   float* __restrict__ scale, int64_t ld) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
@@ -479,8 +487,8 @@ moe_status_t launch_quant_tokens_group_fp8(const QuantTokensArgs& a, int64_t ld,
   const int64_t want = ceil_div<int64_t>(a.M, kQuantWarps);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * per_sm));
   prof_before("quant_tokens_fp8", s);
-  quant_tokens_group_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(
-      a.x, a.inv, a.M, a.k, a.H, a.q8, a.scale, ld);
+  launch_kernel(quant_tokens_group_fp8_kernel, grid, kQuantWarps * 32, 0, s, a.x, a.inv, a.M, a.k,
+                a.H, a.q8, a.scale, ld);
   prof_after("quant_tokens_fp8", s);
   return check_launch("quant_tokens_fp8");
 }
@@ -490,8 +498,8 @@ moe_status_t launch_quant_tokens_fp8(const QuantTokensArgs& a, cudaStream_t s) {
   const int64_t want = ceil_div<int64_t>(a.M, kQuantWarps);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
   prof_before("quant_tokens_fp8", s);
-  quant_tokens_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(a.x, a.inv, a.M, a.k, a.H, a.q8,
-                                                            a.scale, a.row_amax);
+  launch_kernel(quant_tokens_fp8_kernel, grid, kQuantWarps * 32, 0, s, a.x, a.inv, a.M, a.k, a.H,
+                a.q8, a.scale, a.row_amax);
   prof_after("quant_tokens_fp8", s);
   return check_launch("quant_tokens_fp8");
 }
@@ -501,9 +509,8 @@ moe_status_t launch_quant_sorted_fp8(const QuantSortedArgs& a, cudaStream_t s) {
   const int64_t want = ceil_div<int64_t>(a.cap, kQuantWarps);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
   prof_before("quant_z_fp8", s);
-  quant_sorted_fp8_kernel<<<grid, kQuantWarps * 32, 0, s>>>(a.src, a.index, a.offsets, a.E,
-                                                            a.sentinel, a.H, a.cap, a.q8,
-                                                            a.scale_io);
+  launch_kernel(quant_sorted_fp8_kernel, grid, kQuantWarps * 32, 0, s, a.src, a.index, a.offsets,
+                a.E, a.sentinel, a.H, a.cap, a.q8, a.scale_io);
   prof_after("quant_z_fp8", s);
   return check_launch("quant_z_fp8");
 }

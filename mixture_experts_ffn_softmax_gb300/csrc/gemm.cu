@@ -232,6 +232,7 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int
 // One CTA waits on a barrier that nothing arrives at; the bounded wait must
 // end it with MOE_ERR_TIMEOUT.
 __global__ void wait_timeout_probe_kernel(int32_t* err, uint64_t limit_ns) {
+  pdl_begin();
   __shared__ uint64_t bar;
   __shared__ int32_t abort_flag;
   if (threadIdx.x == 0) {
@@ -1434,6 +1435,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  pdl_begin();
   gemm_body<EPI, 1, F8>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
 }
 
@@ -1442,6 +1444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  pdl_begin();
   gemm_body<EPI, 2, F8>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
 }
 
@@ -1453,6 +1456,7 @@ __global__ void __launch_bounds__(GA_THREADS, 1)
     grouped_gemm_ga_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  pdl_begin();
   gemm_body<EPI, 1, false, Wq::None, false, true>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
 }
 template <Epi EPI>
@@ -1460,6 +1464,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA_THREADS, 1)
     grouped_gemm_ga_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                 const __grid_constant__ CUtensorMap tmB,
                                 const __grid_constant__ CUtensorMap tmO, const KParams P) {
+  pdl_begin();
   gemm_body<EPI, 2, false, Wq::None, false, true>(&tmA, &tmB, &tmO, nullptr, nullptr, P);
 }
 
@@ -1471,6 +1476,7 @@ template <Epi EPI>
 __global__ void __launch_bounds__(BS_THREADS, 1)
     grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const KParams P) {
+  pdl_begin();
   gemm_body<EPI, 1, true, Wq::None, true>(&tmA, &tmB, &tmB, nullptr, nullptr, P);
 }
 
@@ -1482,6 +1488,7 @@ __global__ void __launch_bounds__(cta_threads<WQ>(), 1)
                            const __grid_constant__ CUtensorMap tmO,
                            const __grid_constant__ CUtensorMap tmS,
                            const __grid_constant__ CUtensorMap tmZ, const KParams P) {
+  pdl_begin();
   gemm_body<EPI, 1, false, WQ>(&tmA, &tmB, &tmO, &tmS, &tmZ, P);
 }
 
@@ -1494,6 +1501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<WQ>(), 1
                                 const __grid_constant__ CUtensorMap tmO,
                                 const __grid_constant__ CUtensorMap tmS,
                                 const __grid_constant__ CUtensorMap tmZ, const KParams P) {
+  pdl_begin();
   gemm_body<EPI, 2, false, WQ>(&tmA, &tmB, &tmO, &tmS, &tmZ, P);
 }
 
@@ -1692,7 +1700,8 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     // 1-2.5 % slower, so those keep the static round-robin
     if (a.K < 3072) P.sched = nullptr;
     prof_before(name, s);
-    grouped_gemm_pair_kernel<EPI, F8><<<2 * clusters, NTHREADS, G2::SMEM, s>>>(tmA, tmB, tmO, P);
+    launch_kernel(grouped_gemm_pair_kernel<EPI, F8>, 2 * clusters, NTHREADS, G2::SMEM, s, tmA, tmB,
+                  tmO, P);
     prof_after(name, s);
     return check_launch(name);
   }
@@ -1703,7 +1712,7 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   // 6.0-6.3 ms)
   P.sched = nullptr;
   prof_before(name, s);
-  grouped_gemm_kernel<EPI, F8><<<grid, NTHREADS, G1::SMEM, s>>>(tmA, tmB, tmO, P);
+  launch_kernel(grouped_gemm_kernel<EPI, F8>, grid, NTHREADS, G1::SMEM, s, tmA, tmB, tmO, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -1763,13 +1772,14 @@ moe_status_t launch_gemm1_ga(const GroupedGemmArgs& a, const char* name, cudaStr
     const int64_t max_pairs = (max_blocks / 2 + (a.E + 1) / 2 + 1) * NB;
     const unsigned clusters = static_cast<unsigned>(std::min<int64_t>(max_pairs, resident));
     prof_before(name, s);
-    grouped_gemm_ga_pair_kernel<EPI><<<2 * clusters, GA_THREADS, G2::SMEM, s>>>(tmA, tmB, tmO, P);
+    launch_kernel(grouped_gemm_ga_pair_kernel<EPI>, 2 * clusters, GA_THREADS, G2::SMEM, s, tmA, tmB,
+                  tmO, P);
     prof_after(name, s);
     return check_launch(name);
   }
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
   prof_before(name, s);
-  grouped_gemm_ga_kernel<EPI><<<grid, GA_THREADS, G1::SMEM, s>>>(tmA, tmB, tmO, P);
+  launch_kernel(grouped_gemm_ga_kernel<EPI>, grid, GA_THREADS, G1::SMEM, s, tmA, tmB, tmO, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -1797,7 +1807,7 @@ moe_status_t launch_gemm_bs(const GroupedGemmArgs& a, const char* name, cudaStre
   if (max_blocks <= 0) return MOE_OK;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
   prof_before(name, s);
-  grouped_gemm_bs_kernel<EPI><<<grid, BS_THREADS, G::SMEM, s>>>(tmA, tmB, P);
+  launch_kernel(grouped_gemm_bs_kernel<EPI>, grid, BS_THREADS, G::SMEM, s, tmA, tmB, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -1914,7 +1924,7 @@ moe_status_t launch_gemm_wq_cg(const GroupedGemmArgs& a, const char* name, cudaS
     grid = static_cast<unsigned>(std::min<int64_t>(max_blocks * NB, a.num_sms));
   }
   prof_before(name, s);
-  kernel<<<grid, cta_threads<WQ>(), G::SMEM, s>>>(tmA, tmB, tmO, tmS, tmZ, P);
+  launch_kernel(kernel, grid, cta_threads<WQ>(), G::SMEM, s, tmA, tmB, tmO, tmS, tmZ, P);
   prof_after(name, s);
   return check_launch(name);
 }
@@ -1929,7 +1939,8 @@ moe_status_t launch_gemm_wq(const GroupedGemmArgs& a, const char* name, cudaStre
 
 moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s) {
   prof_before("wait_timeout_probe", s);
-  wait_timeout_probe_kernel<<<1, 32, 0, s>>>(err, static_cast<uint64_t>(limit_us) * 1000ull);
+  launch_kernel(wait_timeout_probe_kernel, 1, 32, 0, s, err,
+                static_cast<uint64_t>(limit_us) * 1000ull);
   prof_after("wait_timeout_probe", s);
   return check_launch("wait_timeout_probe");
 }

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     route_kernel(const T* __restrict__ logits, int64_t M, int E, int top_k, int method,
                  int renormalize, int k_group, int group_count, int group_select_mode,
                  float scale, float* __restrict__ out_w, int32_t* __restrict__ out_ids) {
+  pdl_begin();
   extern __shared__ float route_smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -247,13 +248,14 @@ moe_status_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
     smem = static_cast<size_t>(kWarpsPerBlock) * (2 * a.E + 2 * a.group_count) * sizeof(float);
   prof_before("route", s);
   if (a.logits_bf16)
-    route_kernel<EPL, bf16><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, smem, s>>>(
-        static_cast<const bf16*>(a.logits), a.M, a.E, a.top_k, a.method, a.renormalize,
-        a.k_group, a.group_count, a.group_select_mode, a.scale, a.weights, a.ids);
+    launch_kernel(route_kernel<EPL, bf16>, static_cast<unsigned>(blocks), kWarpsPerBlock * 32, smem,
+                  s, static_cast<const bf16*>(a.logits), a.M, a.E, a.top_k, a.method, a.renormalize,
+                  a.k_group, a.group_count, a.group_select_mode, a.scale, a.weights, a.ids);
   else
-    route_kernel<EPL, float><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, smem, s>>>(
-        static_cast<const float*>(a.logits), a.M, a.E, a.top_k, a.method, a.renormalize,
-        a.k_group, a.group_count, a.group_select_mode, a.scale, a.weights, a.ids);
+    launch_kernel(route_kernel<EPL, float>, static_cast<unsigned>(blocks), kWarpsPerBlock * 32,
+                  smem, s, static_cast<const float*>(a.logits), a.M, a.E, a.top_k, a.method,
+                  a.renormalize, a.k_group, a.group_count, a.group_select_mode, a.scale, a.weights,
+                  a.ids);
   prof_after("route", s);
   return check_launch("route");
 }

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(256)
     dequant_weights_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scale,
                            const uint8_t* __restrict__ zero, int E, int K, int N, int G,
                            __nv_bfloat16* __restrict__ out) {
+  pdl_begin();
   using F = WqFmt<WQ>;
   const int n8 = N / 8;
   const int64_t units = static_cast<int64_t>(E) * K * n8;
@@ -74,9 +75,9 @@ moe_status_t launch_dequant_t(const WqDequantArgs& a, cudaStream_t s) {
   const unsigned grid =
       static_cast<unsigned>(std::min<int64_t>(ceil_div<int64_t>(units, 256), sm_count() * 16));
   prof_before("dequant_weights", s);
-  dequant_weights_kernel<WQ><<<grid, 256, 0, s>>>(
-      static_cast<const uint8_t*>(a.codes), static_cast<const uint8_t*>(a.scale),
-      static_cast<const uint8_t*>(a.zero), a.E, a.K, a.N, a.G, a.out);
+  launch_kernel(dequant_weights_kernel<WQ>, grid, 256, 0, s, static_cast<const uint8_t*>(a.codes),
+                static_cast<const uint8_t*>(a.scale), static_cast<const uint8_t*>(a.zero), a.E, a.K,
+                a.N, a.G, a.out);
   prof_after("dequant_weights", s);
   return check_launch("dequant_weights");
 }

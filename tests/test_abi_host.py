@@ -182,6 +182,14 @@ def test_gemm_tile_mode_validation():
         assert lib.moe_set_gemm_tiles(m) == OK
 
 
+def test_pdl_switch_validation():
+    lib = pkg.lib()
+    assert lib.moe_set_pdl(2) == INVALID
+    assert lib.moe_set_pdl(-1) == INVALID
+    for m in (0, 1):
+        assert lib.moe_set_pdl(m) == OK
+
+
 def test_gather_mode_validation():
     lib = pkg.lib()
     assert lib.moe_set_gather_mode(3) == INVALID
