@@ -520,11 +520,13 @@ GBMOE_API moe_status_t moe_profiler_stop(moe_kernel_time_t* out, int32_t capacit
 GBMOE_API moe_status_t moe_set_gemm_tiles(int32_t mode);
 /* Programmatic dependent launch (process-wide tuning / testing knob, on by
  * default): 1 = every kernel of the library is launched with programmatic
- * stream serialisation allowed, so the next kernel in the stream is
- * scheduled while this one runs and waits on the device (griddepcontrol.wait)
- * until it has completed -- the launch gaps between the library's
- * consecutive kernels are hidden; 0 = plain stream order.  Results are
- * identical either way.  Values other than 0 / 1 return MOE_ERR_INVALID_ARG. */
+ * stream serialisation allowed and begins by waiting on the device
+ * (griddepcontrol.wait) until the kernel before it has completed; kernels
+ * with small grids let their successor be scheduled at once, so the launch
+ * gaps between a small layer's kernels are hidden, while kernels with large
+ * grids let it be scheduled as their CTAs exit; 0 = plain stream order.
+ * Results are identical either way.  Values other than 0 / 1 return
+ * MOE_ERR_INVALID_ARG. */
 GBMOE_API moe_status_t moe_set_pdl(int32_t enabled);
 /* Where moe_forward / moe_forward_opts / moe_forward_host take GEMM1's rows
  * from (process-wide tuning / testing knob): 0 = automatic (fused when the

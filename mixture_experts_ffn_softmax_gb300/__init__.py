@@ -420,9 +420,9 @@ def set_gather_mode(mode: str = "auto"):
 
 def set_pdl(enabled: bool = True):
     """Programmatic dependent launch between the library's consecutive
-    kernels (on by default): each kernel is scheduled while the one before
-    it runs and waits on the device for it to complete.  Results are
-    identical either way."""
+    kernels (on by default): each kernel waits on the device for the one
+    before it, and kernels with small grids let the next one be scheduled
+    while they run.  Results are identical either way."""
     _check(lib().moe_set_pdl(1 if enabled else 0), "moe_set_pdl")
 
 

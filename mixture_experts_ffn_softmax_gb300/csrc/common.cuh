@@ -42,16 +42,22 @@ int gemm_tile_mode();
 // Every kernel of the library is launched with programmatic stream
 // serialisation allowed (launch_kernel) and begins with pdl_begin(): it waits
 // until the grid before it in the stream has completed and that grid's
-// memory operations are visible (griddepcontrol.wait), then lets the next
-// grid be scheduled (griddepcontrol.launch_dependents).  The next kernel's
-// CTAs can thus be made resident, their launch latency spent, while this
-// kernel runs, and each still starts its work only after this one has
-// completed.  Every kernel waits before anything else, so completion order is
-// transitive along a chain of launches.  A kernel whose predecessor is not
-// such a launch (another library's kernel, a copy) waits for it as usual.
+// memory operations are visible (griddepcontrol.wait).  A kernel with a small
+// grid then lets the next grid be scheduled at once
+// (griddepcontrol.launch_dependents): the next kernel's CTAs are made
+// resident, their launch latency spent, while it runs -- the gaps between
+// the short kernels of a small layer disappear.  A kernel with a large grid
+// does not: resident CTAs of the next kernel (a grouped GEMM's hold 53K
+// registers each) would take registers and warp slots from its own, so its
+// dependents are scheduled as its CTAs exit (the implicit trigger).  Every
+// kernel waits before anything else, so completion order is transitive along
+// a chain of launches; a kernel whose predecessor is not such a launch
+// (another library's kernel, a copy) waits for it as usual.
+constexpr unsigned kPdlEarlyTriggerCtas = 64;
 __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (gridDim.x * gridDim.y * gridDim.z <= kPdlEarlyTriggerCtas)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 // Whether launches carry the attribute (moe_set_pdl; on by default).
 bool pdl_enabled();

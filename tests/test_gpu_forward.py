@@ -240,7 +240,7 @@ def test_odd_and_even_row_blocks(reduce, tiles):
     """Experts with 0, 1, 2, 3 and 5 row blocks (a pair tile's second row
     block is absent for the odd ones: its rows are computed, never stored),
     ragged N in both GEMMs, biases, and a repeated call giving the same bits."""
-    counts = [0, 100, 128, 129, 300, 600, 256]
+    counts = [0, 100, 128, 129, 300, 600, 256, 1, 17, 33]
     E, H, I = len(counts), 392, 328
     rng = np.random.default_rng(21)
     ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)]).astype(np.int32)
