@@ -308,28 +308,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 8 per-channel weight scales starting at column n of expert e (or the
-// expert's one scale 8 times); ones when there is no scale.
-__device__ __forceinline__ void load_wscale8(const KParams& P, int e, int n, bool ok, float* f) {
-  if (P.w_scale == nullptr) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = 1.f;
-  } else if (!P.w_scale_per_channel) {
-    const float v = __ldg(P.w_scale + e);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = v;
-  } else if (ok) {
-    const float4* q = reinterpret_cast<const float4*>(P.w_scale +
-                                                      static_cast<int64_t>(e) * P.w_scale_ld + n);
-    const float4 a = __ldg(q), b = __ldg(q + 1);
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = 0.f;
-  }
-}
-
 // Loads 8 bf16 bias values as floats (zeros if bias == null or past n_lim).
 __device__ __forceinline__ void load_bias8(const bf16* bias, int64_t off, bool ok, float* f) {
   if (bias != nullptr && ok) {
@@ -1210,6 +1188,35 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
       if constexpr (EPI == Epi::SwiGLU) {
         if (mine) swiglu_prefetch<F8>(P, e, n_base, p, lane, sr);
       }
+      // The other epilogues: the row's item and weight, and the warp's 128
+      // columns' biases (and FP8 scales), four columns per lane, broadcast
+      // with shuffles when used -- loaded before the wait, not after it (a
+      // short tile cannot hide a chain of loads behind its MMAs otherwise).
+      int32_t pf_entry = -1;
+      float pf_wgt = 0.f, pf_sa = 1.f;
+      float pf_b[4] = {0.f, 0.f, 0.f, 0.f}, pf_s[4] = {1.f, 1.f, 1.f, 1.f};
+      if constexpr (EPI != Epi::SwiGLU) {
+        if (mine) {
+          pf_entry = (EPI == Epi::DenseF32) ? static_cast<int32_t>(p) : P.row_index[p];
+          const bool v = pf_entry >= 0 && pf_entry < P.sentinel;
+          pf_wgt = v ? (P.row_weight != nullptr ? P.row_weight[pf_entry] : 1.0f) : 0.0f;
+          const int N = P.N;
+          const int nl = nb * MMA_N + half * (MMA_N / 2) + 4 * lane;  // this lane's 4 columns
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const bool in = nl + i < N;
+            if (P.bias != nullptr && in)
+              pf_b[i] = __bfloat162float(P.bias[static_cast<int64_t>(e) * N + nl + i]);
+            if constexpr (F8) {
+              if (P.w_scale == nullptr) pf_s[i] = 1.f;
+              else if (!P.w_scale_per_channel) pf_s[i] = __ldg(P.w_scale + e);
+              else pf_s[i] = in ? __ldg(P.w_scale + static_cast<int64_t>(e) * P.w_scale_ld + nl + i)
+                                : 0.f;
+            }
+          }
+          if constexpr (F8) pf_sa = P.a_scale[p];
+        }
+      }
       const bool got = bounded_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, P.error_word);
       if (!__all_sync(0xffffffffu, got)) break;
       ptx::tc_fence_after();
@@ -1310,10 +1317,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         }
       } else {
         const int N = P.N;
-        const int32_t entry = (EPI == Epi::DenseF32) ? static_cast<int32_t>(p) : P.row_index[p];
+        const int32_t entry = pf_entry;
         const bool valid = entry >= 0 && entry < P.sentinel;
-        const float wgt = valid ? (P.row_weight != nullptr ? P.row_weight[entry] : 1.0f) : 0.0f;
-        const int64_t bias_row = static_cast<int64_t>(e) * N;
+        const float wgt = pf_wgt;
         uint8_t* stage_buf = staging + (warp - EPI0) * STAGING_BYTES;
         // a warp whose 32 rows are all padding has nothing to store
         const bool any_real = __ballot_sync(0xffffffffu, valid) != 0u;
@@ -1325,22 +1331,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           ptx::tmem_ld_32cols(taddr + c, a);
           ptx::tmem_ld_wait();
           float o[32];
+          // column c + j of the warp's 128 is held by lane (c - 128 half + j) / 4
+          const int lc0 = (c - half * (MMA_N / 2)) >> 2;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float b[8], sc[8];
-            load_bias8(P.bias, bias_row + n0 + v * 8, n0 + v * 8 < N, b);
-            if constexpr (F8) {
-              load_wscale8(P, e, n0 + v * 8, n0 + v * 8 < N, sc);
-              const float sa = P.a_scale[p];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) sc[i] *= sa;
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) sc[i] = 1.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[v * 8 + i] = (__uint_as_float(a[acc_pos(v * 8 + i)]) * sc[i] + b[i]) * wgt;
+          for (int j = 0; j < 32; ++j) {
+            const float b = __shfl_sync(0xffffffffu, pf_b[j & 3], lc0 + (j >> 2));
+            float sc = 1.f;
+            if constexpr (F8) sc = __shfl_sync(0xffffffffu, pf_s[j & 3], lc0 + (j >> 2)) * pf_sa;
+            o[j] = (__uint_as_float(a[acc_pos(j)]) * sc + b) * wgt;
           }
           if constexpr (EPI == Epi::SortedF32) {
             // Stage the warp's 32x32 fp32 block in the 128-byte-swizzled layout
