@@ -220,8 +220,13 @@ __global__ void __launch_bounds__(kScanThreads)
                        int32_t* __restrict__ sorted, int32_t* __restrict__ offsets,
                        int32_t* __restrict__ counts, int32_t* __restrict__ block_expert,
                        int32_t* __restrict__ inv, int32_t* error_word,
-                       const int32_t* __restrict__ emap, int E_global) {
+                       const int32_t* __restrict__ emap, int E_global, int32_t* zero_words,
+                       int zero_count) {
   pdl_begin();
+  if (zero_words != nullptr) {  // before any error can be recorded
+    for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero_words[i] = 0;
+    __syncthreads();
+  }
   __shared__ int32_t s_cnt[32 * kSmallExperts];
   __shared__ int32_t s_count[kSmallExperts];
   __shared__ int32_t s_off[kSmallExperts + 1];
@@ -232,10 +237,26 @@ __global__ void __launch_bounds__(kScanThreads)
   int32_t* cnt = s_cnt + warp * E;
   for (int e = lane; e < E; e += 32) cnt[e] = 0;
   __syncwarp();
+  // The warp's items, one per lane and pass, all loaded before any is used
+  // (one memory latency instead of one per pass), kept for both passes.
+  constexpr int kMaxPasses = kSmallItemsFewExperts / kScanThreads;
+  static_assert(kSmallItems / kScanThreads <= kMaxPasses, "passes of the one-block plan");
+  int ev[kMaxPasses];
+#pragma unroll
+  for (int i = 0; i < kMaxPasses; ++i) {
+    const int r = r0 + 32 * i + lane;
+    ev[i] = (32 * i < per && r < R) ? ids[r] : -1;
+  }
   bool bad = false;
-  for (int it = 0; it < per; it += 32) {
-    const int r = r0 + it + lane;
-    const int e = r < R ? local_expert(ids[r], E, emap, E_global, bad) : -1;
+#pragma unroll
+  for (int i = 0; i < kMaxPasses; ++i) {
+    const int r = r0 + 32 * i + lane;
+    if (32 * i < per && r < R) ev[i] = local_expert(ev[i], E, emap, E_global, bad);
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxPasses; ++i) {
+    if (32 * i >= per) break;  // warp-uniform
+    const int e = ev[i];
     const bool ok = e >= 0;
     const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
     if (ok && lane == __ffs(grp) - 1) cnt[e] += __popc(grp);
@@ -258,10 +279,11 @@ __global__ void __launch_bounds__(kScanThreads)
   for (int e = lane; e < E; e += 32) cnt[e] += s_off[e];
   __syncwarp();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int it = 0; it < per; it += 32) {
-    const int r = r0 + it + lane;
-    bool bad2 = false;
-    const int e = r < R ? local_expert(ids[r], E, emap, E_global, bad2) : -1;
+#pragma unroll
+  for (int i = 0; i < kMaxPasses; ++i) {
+    if (32 * i >= per) break;  // warp-uniform
+    const int r = r0 + 32 * i + lane;
+    const int e = ev[i];
     const bool ok = e >= 0;
     const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
     const int32_t pos = ok ? cnt[e] + __popc(grp & lt_mask) : -1;
@@ -313,6 +335,8 @@ __global__ void __launch_bounds__(kScanThreads)
                         int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted,
                         int32_t* error_word) {
   pdl_begin();
+  if (threadIdx.x == 0) *error_word = 0;  // before any error can be recorded
+  __syncthreads();
   __shared__ int32_t s_count[1024];
   __shared__ int32_t s_off[1025];
   __shared__ int32_t s_warp[32];
@@ -391,10 +415,13 @@ moe_status_t launch_align(const AlignArgs& a, cudaStream_t s) {
     prof_before("align_small", s);
     launch_kernel(align_small_kernel, 1, kScanThreads, 0, s, a.ids, static_cast<int>(a.R), a.E,
                   a.block_m, a.cap, a.sorted, a.offsets, a.counts, a.block_expert, a.inv,
-                  a.error_word, a.expert_map, a.E_global);
+                  a.error_word, a.expert_map, a.E_global, a.zero_words, a.zero_count);
     prof_after("align_small", s);
     return check_launch("align_small");
   }
+  if (a.zero_words != nullptr &&
+      cudaMemsetAsync(a.zero_words, 0, sizeof(int32_t) * a.zero_count, s) != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
   const int num_chunks = static_cast<int>(ceil_div<int64_t>(a.R, kChunk));
   const size_t smem = static_cast<size_t>(kAlignWarps) * a.E * sizeof(int32_t);
   const unsigned grid = static_cast<unsigned>(ceil_div(num_chunks, kAlignWarps));

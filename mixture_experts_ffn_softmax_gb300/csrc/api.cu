@@ -507,8 +507,7 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
   // the error word and, after it, the GEMMs' tile-schedule counters
   int32_t* sched1 = err + 16;  // GEMM1 {next tile, CTAs done}
   int32_t* sched2 = err + 24;  // GEMM2
-  if (reset_error && cudaMemsetAsync(err, 0, 32 * sizeof(int32_t), s) != cudaSuccess)
-    return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
+  // (the error word and the counters are cleared by the first chunk's plan)
 
   const bf16* x = static_cast<const bf16*>(hidden);
   bf16* y = static_cast<bf16*>(out);
@@ -524,6 +523,10 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
                  at<int32_t>(workspace, L.scratch), cap, err, inv};
     al.expert_map = opts->expert_map;
     al.E_global = opts->num_global_experts;
+    if (reset_error && c0 == 0) {
+      al.zero_words = err;
+      al.zero_count = 32;
+    }
     if (moe_status_t st = launch_align(al, s)) return st;
 
     bf16* a_perm = at<bf16>(workspace, L.a_perm);
@@ -1117,9 +1120,7 @@ moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens
   if (moe_status_t st = check_device(&sms)) return st;
   cudaStream_t s = stream;
   const BatLayout L = bat_layout(E, T, H, I);
-  int32_t* err = at<int32_t>(workspace, L.err);
-  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
-    return set_error(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
+  int32_t* err = at<int32_t>(workspace, L.err);  // cleared by the plan kernel
   const int32_t sentinel = E * T;
   int32_t* sorted = at<int32_t>(workspace, L.sorted);
   int32_t* offsets = at<int32_t>(workspace, L.offsets);

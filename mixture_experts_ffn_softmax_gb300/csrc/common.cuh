@@ -137,6 +137,11 @@ struct AlignArgs {
   // the item is skipped, not an error)
   const int32_t* expert_map = nullptr;
   int32_t E_global = 0;
+  // optional: words cleared before anything of the plan runs (the forward's
+  // error word and tile-schedule counters) -- by the one-block plan itself,
+  // else by a memset ahead of the four-kernel plan
+  int32_t* zero_words = nullptr;
+  int32_t zero_count = 0;
 };
 size_t align_scratch_bytes(int64_t R, int32_t E);
 moe_status_t launch_align(const AlignArgs& a, cudaStream_t s);
@@ -153,7 +158,7 @@ struct BatchedPlanArgs {
   int32_t* block_expert;
   int64_t cap;
   int32_t sentinel;
-  int32_t* error_word;
+  int32_t* error_word;  // cleared by the plan before use
 };
 moe_status_t launch_batched_plan(const BatchedPlanArgs& a, cudaStream_t s);
 
