@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kScanThreads)
                         int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted,
                         int32_t* error_word) {
   pdl_begin();
-  if (threadIdx.x == 0) *error_word = 0;  // before any error can be recorded
+  if (threadIdx.x == 0 && error_word != nullptr) *error_word = 0;  // before any error is recorded
   __syncthreads();
   __shared__ int32_t s_count[1024];
   __shared__ int32_t s_off[1025];
