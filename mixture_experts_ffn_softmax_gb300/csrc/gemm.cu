@@ -207,6 +207,10 @@ struct KParams {
   // block-scaled FP8: activation scales [K/128][a_ld] (group-major), weight
   // scales [E][K/128][w_scale_ld] per 128 x 128 block
   int64_t bs_a_ld;
+  // nonzero: tmB views the weights with the tile's 128-byte column chunks as
+  // a dimension of their own (stride 128 bytes), so that one TMA copy fills
+  // every chunk of a stage; zero: one copy per chunk
+  int32_t b_one_box;
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
@@ -796,15 +800,24 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
           if constexpr (CG == 1) {
             ptx::mbar_arrive_expect_tx(&ctl.full[stage], GA ? G::STAGE - G::B_OFF : G::STAGE);
             if constexpr (!GA) ptx::tma_load_2d(sa, tmA, &ctl.full[stage], kb * G::BKE, row0);
-#pragma unroll
-            for (int c = 0; c < G::CHUNKS; ++c) {
-              if constexpr (EPI == Epi::SwiGLU)  // gate cols [nb*128,+128), then the up half
-                ptx::tma_load_4d(sb + c * G::CHUNK_BYTES, tmB, &ctl.full[stage],
-                                 nb * (MMA_N / 2) + (c % (G::CHUNKS / 2)) * G::CW,
-                                 c / (G::CHUNKS / 2), kb * G::BKE, e);
+            if (P.b_one_box) {
+              // (column in chunk, k, chunk, [half,] expert)
+              if constexpr (EPI == Epi::SwiGLU)
+                ptx::tma_load_5d(sb, tmB, &ctl.full[stage], 0, kb * G::BKE,
+                                 nb * (G::CHUNKS / 2), 0, e);
               else
-                ptx::tma_load_3d(sb + c * G::CHUNK_BYTES, tmB, &ctl.full[stage],
-                                 nb * MMA_N + c * G::CW, kb * G::BKE, e);
+                ptx::tma_load_4d(sb, tmB, &ctl.full[stage], 0, kb * G::BKE, nb * G::CHUNKS, e);
+            } else {
+#pragma unroll
+              for (int c = 0; c < G::CHUNKS; ++c) {
+                if constexpr (EPI == Epi::SwiGLU)  // gate cols [nb*128,+128), then the up half
+                  ptx::tma_load_4d(sb + c * G::CHUNK_BYTES, tmB, &ctl.full[stage],
+                                   nb * (MMA_N / 2) + (c % (G::CHUNKS / 2)) * G::CW,
+                                   c / (G::CHUNKS / 2), kb * G::BKE, e);
+                else
+                  ptx::tma_load_3d(sb + c * G::CHUNK_BYTES, tmB, &ctl.full[stage],
+                                   nb * MMA_N + c * G::CW, kb * G::BKE, e);
+              }
             }
           } else {
             // both CTAs' copies complete on the even CTA's barrier, which
@@ -814,16 +827,25 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
               ptx::mbar_arrive_expect_tx(&ctl.full[stage],
                                          GA ? 2 * (G::STAGE - G::B_OFF) + kRelayBytes : 2 * G::STAGE);
             if constexpr (!GA) ptx::tma_load_2d_pair(sa, tmA, full0, kb * G::BKE, row0);
-#pragma unroll
-            for (int c = 0; c < G::B_CHUNKS_CTA; ++c) {
-              const int gc = static_cast<int>(rank) * G::B_CHUNKS_CTA + c;  // chunk of the tile
+            if (P.b_one_box) {
               if constexpr (EPI == Epi::SwiGLU)  // even CTA: gate columns, odd CTA: up columns
-                ptx::tma_load_4d_pair(sb + c * G::CHUNK_BYTES, tmB, full0,
-                                      nb * (MMA_N / 2) + (gc % (G::CHUNKS / 2)) * G::CW,
-                                      gc / (G::CHUNKS / 2), kb * G::BKE, e);
+                ptx::tma_load_5d_pair(sb, tmB, full0, 0, kb * G::BKE, nb * (G::CHUNKS / 2),
+                                      static_cast<int>(rank), e);
               else
-                ptx::tma_load_3d_pair(sb + c * G::CHUNK_BYTES, tmB, full0,
-                                      nb * MMA_N + gc * G::CW, kb * G::BKE, e);
+                ptx::tma_load_4d_pair(sb, tmB, full0, 0, kb * G::BKE,
+                                      nb * G::CHUNKS + static_cast<int>(rank) * G::B_CHUNKS_CTA, e);
+            } else {
+#pragma unroll
+              for (int c = 0; c < G::B_CHUNKS_CTA; ++c) {
+                const int gc = static_cast<int>(rank) * G::B_CHUNKS_CTA + c;  // chunk of the tile
+                if constexpr (EPI == Epi::SwiGLU)  // even CTA: gate columns, odd CTA: up columns
+                  ptx::tma_load_4d_pair(sb + c * G::CHUNK_BYTES, tmB, full0,
+                                        nb * (MMA_N / 2) + (gc % (G::CHUNKS / 2)) * G::CW,
+                                        gc / (G::CHUNKS / 2), kb * G::BKE, e);
+                else
+                  ptx::tma_load_3d_pair(sb + c * G::CHUNK_BYTES, tmB, full0,
+                                        nb * MMA_N + gc * G::CW, kb * G::BKE, e);
+              }
             }
           }
           if (++stage == G::NSTAGES) {
@@ -1589,8 +1611,18 @@ KParams base_params(const GroupedGemmArgs& a, int NB) {
 
 // Tensor maps of A (sorted rows, K-major) and B (expert weights, MN-major)
 // and the number of column blocks, shared by the grouped GEMM launchers.
+// `pairs`: the tiles are split over CTA pairs (each CTA loads half of B's
+// chunks).  Where the columns split into whole 128-byte chunks, B is viewed
+// with the chunk as a dimension of its own, so that one copy per stage loads
+// all of a CTA's chunks (*one_box = 1); otherwise, or where `allow_one_box`
+// is false, one copy per chunk.  Measured on GB300, the single copy took the
+// bf16 layers 1-3 % faster (Mixtral-shape prefill 1.85 -> 1.83 ms,
+// DeepSeek-V3 M = 8192 6.24 -> 6.08 ms) and the block-scaled FP8 GEMMs ~1 %
+// slower, so those keep one copy per chunk.
 template <Epi EPI, bool F8>
-moe_status_t make_ab_maps(const GroupedGemmArgs& a, CUtensorMap* tmA, CUtensorMap* tmB, int* NB) {
+moe_status_t make_ab_maps(const GroupedGemmArgs& a, bool pairs, CUtensorMap* tmA,
+                          CUtensorMap* tmB, int* NB, int32_t* one_box,
+                          bool allow_one_box = true) {
   using G1 = Geo<1, F8>;
   const CUtensorMapDataType dt =
       F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -1601,27 +1633,45 @@ moe_status_t make_ab_maps(const GroupedGemmArgs& a, CUtensorMap* tmA, CUtensorMa
     const uint32_t box[2] = {G1::BKE, BM};
     if (moe_status_t st = make_map(tmA, a.a, 2, dims, strides, box, dt)) return st;
   }
+  const uint64_t N = static_cast<uint64_t>(a.N), K = static_cast<uint64_t>(a.K),
+                 E = static_cast<uint64_t>(a.E);
+  const uint64_t chunks = allow_one_box ? N / G1::CW : 0;  // whole 128-byte column chunks
   if constexpr (EPI == Epi::SwiGLU) {
-    // w13 [E, K, 2, N] viewed 4-D: (n, half, k, e)
-    const uint64_t dims[4] = {static_cast<uint64_t>(a.N), 2, static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.E)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(a.N) * eb,
-                                 static_cast<uint64_t>(a.N) * 2 * eb,
-                                 static_cast<uint64_t>(a.N) * 2 * eb * a.K};
-    const uint32_t box[4] = {G1::CW, 1, G1::BKE, 1};
-    if (moe_status_t st = make_map(tmB, a.w, 4, dims, strides, box, dt)) return st;
     *NB = ceil_div(a.N, MMA_N / 2);
+    // w13 [E, K, 2, N]: a box is a CTA's chunks of the gate half, then (one
+    // CTA) the same chunks of the up half
+    const uint32_t per_half = G1::CHUNKS / 2;
+    if (N % G1::CW == 0 && chunks >= per_half) {
+      const uint64_t dims[5] = {G1::CW, K, chunks, 2, E};
+      const uint64_t strides[4] = {2 * N * eb, G1::CW * eb, N * eb, 2 * N * eb * K};
+      const uint32_t box[5] = {G1::CW, G1::BKE, per_half, pairs ? 1u : 2u, 1};
+      *one_box = 1;
+      return make_map(tmB, a.w, 5, dims, strides, box, dt);
+    }
+    // (n, half, k, e)
+    const uint64_t dims[4] = {N, 2, K, E};
+    const uint64_t strides[3] = {N * eb, N * 2 * eb, N * 2 * eb * K};
+    const uint32_t box[4] = {G1::CW, 1, G1::BKE, 1};
+    *one_box = 0;
+    return make_map(tmB, a.w, 4, dims, strides, box, dt);
   } else {
-    // w2 [E, K, N] viewed 3-D: (n, k, e)
-    const uint64_t dims[3] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.E)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(a.N) * eb,
-                                 static_cast<uint64_t>(a.N) * eb * a.K};
-    const uint32_t box[3] = {G1::CW, G1::BKE, 1};
-    if (moe_status_t st = make_map(tmB, a.w, 3, dims, strides, box, dt)) return st;
     *NB = ceil_div(a.N, MMA_N);
+    // w2 [E, K, N]
+    const uint32_t per_cta = pairs ? G1::CHUNKS / 2 : G1::CHUNKS;
+    if (N % G1::CW == 0 && chunks >= per_cta) {
+      const uint64_t dims[4] = {G1::CW, K, chunks, E};
+      const uint64_t strides[3] = {N * eb, G1::CW * eb, N * eb * K};
+      const uint32_t box[4] = {G1::CW, G1::BKE, per_cta, 1};
+      *one_box = 1;
+      return make_map(tmB, a.w, 4, dims, strides, box, dt);
+    }
+    // (n, k, e)
+    const uint64_t dims[3] = {N, K, E};
+    const uint64_t strides[2] = {N * eb, N * eb * K};
+    const uint32_t box[3] = {G1::CW, G1::BKE, 1};
+    *one_box = 0;
+    return make_map(tmB, a.w, 3, dims, strides, box, dt);
   }
-  return MOE_OK;
 }
 
 template <Epi EPI, bool F8 = false>
@@ -1641,9 +1691,11 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
       }) != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute(%s): %s", name,
                      cudaGetErrorString(cudaGetLastError()));
+  const bool pairs = EPI != Epi::DenseF32 && use_pairs(a);
   CUtensorMap tmA, tmB;
   int NB;
-  if (moe_status_t st = make_ab_maps<EPI, F8>(a, &tmA, &tmB, &NB)) return st;
+  int32_t one_box;
+  if (moe_status_t st = make_ab_maps<EPI, F8>(a, pairs, &tmA, &tmB, &NB, &one_box)) return st;
   CUtensorMap tmO;
   if constexpr (EPI == Epi::SortedF32) {
     // fp32 [cap, N] output, 32 x 32 boxes, 128-byte swizzle (matches staging)
@@ -1666,10 +1718,11 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
     tmO = tmA;  // unused
   }
   KParams P = base_params<EPI>(a, NB);
+  P.b_one_box = one_box;
   // grouped operands are padded to whole 128-row blocks; the dense one is not
   const int64_t max_blocks = (EPI == Epi::DenseF32) ? ceil_div<int64_t>(a.cap, BM) : a.cap / BM;
   if (max_blocks <= 0) return MOE_OK;
-  if (EPI != Epi::DenseF32 && use_pairs(a)) {
+  if (pairs) {
     // Persistent pairs: no more clusters than can be resident at once (the
     // tiles are split statically among them).
     static PerDevice clusters_per_device;
@@ -1736,9 +1789,11 @@ moe_status_t launch_gemm1_ga(const GroupedGemmArgs& a, const char* name, cudaStr
                      cudaGetErrorString(cudaGetLastError()));
   if ((a.K & 7) != 0 || (reinterpret_cast<uintptr_t>(a.a_rows) & 15u) != 0)
     return set_error(MOE_ERR_INVALID_ARG, "%s: token rows must be 16-byte aligned rows", name);
+  const bool pairs = use_pairs(a);
   CUtensorMap tmA, tmB, tmO;
   int NB;
-  if (moe_status_t st = make_ab_maps<EPI, false>(a, &tmA, &tmB, &NB)) return st;
+  int32_t one_box;
+  if (moe_status_t st = make_ab_maps<EPI, false>(a, pairs, &tmA, &tmB, &NB, &one_box)) return st;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.cap)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
@@ -1748,9 +1803,10 @@ moe_status_t launch_gemm1_ga(const GroupedGemmArgs& a, const char* name, cudaStr
       return st;
   }
   KParams P = base_params<EPI>(a, NB);
+  P.b_one_box = one_box;
   const int64_t max_blocks = a.cap / BM;
   if (max_blocks <= 0) return MOE_OK;
-  if (use_pairs(a)) {
+  if (pairs) {
     // persistent pairs: no more clusters than can be resident at once
     static PerDevice clusters_per_device;
     int resident = a.num_sms / 2;
@@ -1797,8 +1853,10 @@ moe_status_t launch_gemm_bs(const GroupedGemmArgs& a, const char* name, cudaStre
     return set_error(MOE_ERR_INVALID_ARG, "%s: z group scales and N %% 128 == 0 required", name);
   CUtensorMap tmA, tmB;
   int NB;
-  if (moe_status_t st = make_ab_maps<EPI, true>(a, &tmA, &tmB, &NB)) return st;
+  int32_t one_box;
+  if (moe_status_t st = make_ab_maps<EPI, true>(a, false, &tmA, &tmB, &NB, &one_box, false)) return st;
   KParams P = base_params<EPI>(a, NB);
+  P.b_one_box = one_box;
   P.w_scale_ld = ((EPI == Epi::SwiGLU) ? 2 * a.N : a.N) / 128;  // weight blocks per K block
   P.bs_a_ld = a.cap;
   const int64_t max_blocks = a.cap / BM;
