@@ -528,6 +528,15 @@ GBMOE_API moe_status_t moe_set_gemm_tiles(int32_t mode);
  * Results are identical either way.  Values other than 0 / 1 return
  * MOE_ERR_INVALID_ARG. */
 GBMOE_API moe_status_t moe_set_pdl(int32_t enabled);
+/* Weight-only decode GEMMs (process-wide tuning / testing knob, on by
+ * default): 1 = moe_forward_wq takes, for calls of at most 32 tokens (H a
+ * multiple of 64, E <= 1024, int formats with a power-of-two group of at
+ * least 32 rows), GEMMs that keep each expert's few rows as the MMA's N and
+ * expand the quantised weights in registers, GEMM2's K split into parts
+ * that the weight-and-reduce adds; 0 = always the grouped tensor-core GEMMs.
+ * Results agree up to fp32 summation order.  Values other than 0 / 1 return
+ * MOE_ERR_INVALID_ARG. */
+GBMOE_API moe_status_t moe_set_wq_decode(int32_t enabled);
 /* Where moe_forward / moe_forward_opts / moe_forward_host take GEMM1's rows
  * from (process-wide tuning / testing knob): 0 = automatic (fused when the
  * routed rows of a token chunk hold at most 16 MiB), 1 = a separate gather

@@ -426,6 +426,14 @@ def set_pdl(enabled: bool = True):
     _check(lib().moe_set_pdl(1 if enabled else 0), "moe_set_pdl")
 
 
+def set_wq_decode(enabled: bool = True):
+    """Weight-only layers of at most 32 tokens through the decode GEMMs
+    (weights expanded in registers, the expert's few rows as the MMA's N; on
+    by default) or always through the grouped tensor-core GEMMs.  Results
+    agree up to fp32 summation order."""
+    _check(lib().moe_set_wq_decode(1 if enabled else 0), "moe_set_wq_decode")
+
+
 def profiler_start():
     _check(lib().moe_profiler_start(), "moe_profiler_start")
 
@@ -440,7 +448,7 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
-           "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl",
+           "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl", "set_wq_decode",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
            "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",

@@ -47,6 +47,7 @@ namespace {
 std::atomic<int> g_gemm_tile_mode{0};
 std::atomic<int> g_gather_mode{0};
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_wq_decode{1};
 }  // namespace
 
 int gemm_tile_mode() { return g_gemm_tile_mode.load(std::memory_order_relaxed); }
@@ -253,6 +254,13 @@ moe_status_t moe_set_gemm_tiles(int32_t mode) {
 moe_status_t moe_set_pdl(int32_t enabled) {
   if (enabled != 0 && enabled != 1) return set_error(MOE_ERR_INVALID_ARG, "pdl switch %d", enabled);
   g_pdl.store(enabled, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_set_wq_decode(int32_t enabled) {
+  if (enabled != 0 && enabled != 1)
+    return set_error(MOE_ERR_INVALID_ARG, "weight-only decode switch %d", enabled);
+  g_wq_decode.store(enabled, std::memory_order_relaxed);
   return MOE_OK;
 }
 
@@ -1057,7 +1065,16 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
     g1.wq_group = w->group_size;
     g1.wq_scale = w->w13_scale;
     g1.wq_zero = w->w13_zero;
-    if (moe_status_t st = launch_gemm1_swiglu_wq(g1, s)) return st;
+    // a few rows per expert: the decode GEMMs (rows as the MMA's N, weights
+    // expanded in registers); otherwise the grouped tensor-core GEMMs
+    const bool decode = g_wq_decode.load(std::memory_order_relaxed) != 0 &&
+                        wq_decode_applies(Mc, H, I, E, w->format, w->group_size);
+    const int32_t* counts = at<int32_t>(workspace, L.counts);
+    if (decode) {
+      if (moe_status_t st = launch_wq_decode_gemm1(g1, counts, Mc, s)) return st;
+    } else {
+      if (moe_status_t st = launch_gemm1_swiglu_wq(g1, s)) return st;
+    }
     float* o = at<float>(workspace, L.o);
     GroupedGemmArgs g2{};
     g2.a = z;
@@ -1080,6 +1097,14 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
     g2.wq_group = w->group_size;
     g2.wq_scale = w->w2_scale;
     g2.wq_zero = w->w2_zero;
+    if (decode) {
+      // K split into parts, each a weighted fp32 row per routed item
+      const int32_t parts = wq_decode_splits(Mc, top_k, H, I, E, cap, sms);
+      if (moe_status_t st = launch_wq_decode_gemm2(g2, counts, Mc, parts, Rc, s)) return st;
+      if (moe_status_t st = launch_reduce_parts(o, inv, Mc, top_k, H, parts, y + c0 * H, s))
+        return st;
+      continue;
+    }
     if (moe_status_t st = launch_gemm2_sorted_wq(g2, s)) return st;
     if (moe_status_t st = launch_reduce_sorted(o, inv, Mc, top_k, H, y + c0 * H, s)) return st;
   }

@@ -304,5 +304,24 @@ moe_status_t launch_gemm2_sorted_fp8_block(const GroupedGemmArgs& a, cudaStream_
 moe_status_t launch_gemm1_swiglu_wq(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_gemm2_sorted_wq(const GroupedGemmArgs& a, cudaStream_t s);
 moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s);
+// A tensor map (cuTensorMapEncodeTiled through the driver entry point);
+// dims / strides innermost first, strides in bytes for dims 1..rank-1.
+moe_status_t encode_tensor_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                               const uint64_t* strides, const uint32_t* box,
+                               CUtensorMapDataType dtype, CUtensorMapSwizzle swz);
+// Weight-only quantised GEMMs for few rows per expert (M <= 32 tokens):
+// whether the call's shape takes them, the K parts of GEMM2, and the
+// launches.  GEMM1 writes z rows like launch_gemm1_swiglu_wq; GEMM2 writes
+// `splits` weighted fp32 partial rows per routed item, out[(s * R + r) * H],
+// which launch_reduce_parts adds per token.
+bool wq_decode_applies(int64_t M, int32_t H, int32_t I, int32_t E, int32_t format, int32_t group);
+int wq_decode_splits(int64_t M, int32_t top_k, int32_t H, int32_t I, int32_t E, int64_t cap,
+                     int32_t num_sms);
+moe_status_t launch_wq_decode_gemm1(const GroupedGemmArgs& a, const int32_t* counts, int64_t M,
+                                    cudaStream_t s);
+moe_status_t launch_wq_decode_gemm2(const GroupedGemmArgs& a, const int32_t* counts, int64_t M,
+                                    int32_t splits, int64_t R, cudaStream_t s);
+moe_status_t launch_reduce_parts(const float* parts, const int32_t* inv, int64_t M, int32_t k,
+                                 int32_t H, int32_t splits, bf16* y, cudaStream_t s);
 
 }  // namespace gbmoe

@@ -1993,6 +1993,12 @@ moe_status_t launch_gemm_wq(const GroupedGemmArgs& a, const char* name, cudaStre
 
 }  // namespace
 
+moe_status_t encode_tensor_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                               const uint64_t* strides, const uint32_t* box,
+                               CUtensorMapDataType dtype, CUtensorMapSwizzle swz) {
+  return make_map(m, base, rank, dims, strides, box, dtype, swz);
+}
+
 moe_status_t launch_wait_timeout_probe(int32_t* err, uint32_t limit_us, cudaStream_t s) {
   prof_before("wait_timeout_probe", s);
   launch_kernel(wait_timeout_probe_kernel, 1, 32, 0, s, err,

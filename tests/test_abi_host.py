@@ -190,6 +190,14 @@ def test_pdl_switch_validation():
         assert lib.moe_set_pdl(m) == OK
 
 
+def test_wq_decode_switch_validation():
+    lib = pkg.lib()
+    assert lib.moe_set_wq_decode(2) == INVALID
+    assert lib.moe_set_wq_decode(-1) == INVALID
+    for m in (0, 1):
+        assert lib.moe_set_wq_decode(m) == OK
+
+
 def test_gather_mode_validation():
     lib = pkg.lib()
     assert lib.moe_set_gather_mode(3) == INVALID
