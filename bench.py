@@ -783,7 +783,9 @@ def measure_wq(step, spec, K, W, world, pk):
     """Weight-only quantised experts on the same layer, prefill and the
     M = 16 decode: int4 (group 128, zero points), MX FP4 and MX FP6 (E2M3).  Decode is
     bound by the weight bytes: touched experts' codes + scales + zero points,
-    plus x, out and logits."""
+    plus x, out and logits.  Decode runs the decode GEMMs (weights expanded in
+    registers); decode_ms_grouped_gemm is the same call through the grouped
+    tensor-core GEMMs."""
     import mixture_experts_ffn_softmax_gb300 as pkg
     d = step.d
     dev = d["hidden"].device
@@ -810,6 +812,12 @@ def measure_wq(step, spec, K, W, world, pk):
         ms_p = max_over_ranks(time_steps(prefill, K, W, world) / K, world)
         Kd = max(K, 20)
         ms_d = max_over_ranks(time_steps(decode, Kd, max(W, 3), world) / Kd, world)
+        # the same decode call through the grouped tensor-core GEMMs, for context
+        pkg.set_wq_decode(False)
+        try:
+            ms_dg = max_over_ranks(time_steps(decode, Kd, max(W, 3), world) / Kd, world)
+        finally:
+            pkg.set_wq_decode(True)
         pkg.profiler_start()
         for _ in range(Kd):
             decode()
@@ -822,6 +830,7 @@ def measure_wq(step, spec, K, W, world, pk):
             "prefill_tokens_per_s": round(spec.M * world / (ms_p / 1e3), 1),
             "prefill_tflops": round(spec.flops() / (ms_p / 1e3) / 1e12, 1),
             "decode_ms_per_step": round(ms_d, 4),
+            "decode_ms_grouped_gemm": round(ms_dg, 4),
             "decode_tokens_per_s": round(dspec.M * world / (ms_d / 1e3), 1),
             "decode_weight_bytes": wbytes,
             "decode_hbm_roofline_frac": round(dbytes / (pk["hbm_gbs"] * 1e9) / (ms_d / 1e3), 4),

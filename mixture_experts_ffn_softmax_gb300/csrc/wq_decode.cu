@@ -19,9 +19,9 @@
 //     directly into the A-operand registers of mma.sync m16n8k16 (the weight
 //     columns as the MMA's M, the expert's rows as its N, 8 per tile; the
 //     operands never go back to shared memory);
-//   - int formats: (q - zp) is exact in bf16 and the group scale multiplies
-//     the fp32 partial sums once per group; MX formats: the block scale (a
-//     power of two) is applied in the expansion, exactly.
+//   - each weight leaves the expansion as the dequantised bf16 value, the
+//     exact (q - zp) * scale (int formats) or code value * 2^(s - 127) (MX)
+//     rounded once, as the standalone dequantisation gives it.
 // GEMM1 (SwiGLU): a warp unit is 32 gate columns and the same 32 up columns of
 // one expert over all of K; lane (g, c) with g < 4 holds gate columns, lane
 // (g + 4, c) the matching up columns, and one shuffle pairs them for
@@ -140,8 +140,9 @@ __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __e
 struct ColParams {
   uint32_t p2[8];  // Int4: bf16 pair (128 + zp, 128 + zp); MX: bf16 pair of the
                    // exact multiplier 2^bias * scale
+  uint32_t s2[8];  // Int4: bf16 pair (scale, scale)
   float zf[8];     // Int8: 2^23 + 128 + zp
-  float sf[8];     // int formats: the group scale
+  float sf[8];     // Int8: the group scale
 };
 
 // Parameter row `pr` of a stage: 64 columns, the lane's 8 at column 8g.
@@ -164,7 +165,13 @@ __device__ __forceinline__ void load_params(const uint8_t* ssm, const uint8_t* z
     const uint4 sc = lds128(ssm + (pr * kDecCols + 8 * g) * 2);
     const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) p.sf[j] = __uint_as_float(((sw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) << 16);
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t sb = (sw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+      if constexpr (WQ == Wq::Int4)
+        p.s2[j] = sb | (sb << 16);
+      else
+        p.sf[j] = __uint_as_float(sb << 16);
+    }
     const uint2 zw = has_zero ? lds64(zsm + pr * kDecCols + 8 * g) : make_uint2(0u, 0u);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -186,12 +193,16 @@ __device__ __forceinline__ void load_params(const uint8_t* ssm, const uint8_t* z
 template <Wq WQ>
 __device__ __forceinline__ uint32_t expand_pair(uint32_t t, const ColParams& p, int j) {
   if constexpr (WQ == Wq::Int4) {
-    // (128 + q) - (128 + zp) = q - zp exactly
-    return bf2u(__hsub2(u2bf((t & 0x000F000Fu) | 0x43004300u), u2bf(p.p2[j])));
+    // (128 + q) - (128 + zp) = q - zp exactly; one rounding in the product
+    return bf2u(__hmul2(__hsub2(u2bf((t & 0x000F000Fu) | 0x43004300u), u2bf(p.p2[j])),
+                        u2bf(p.s2[j])));
   } else if constexpr (WQ == Wq::Int8) {
-    const float lo = __uint_as_float(0x4B000000u | ((t ^ 0x80u) & 0xFFu)) - p.zf[j];
-    const float hi = __uint_as_float(0x4B000000u | (((t >> 16) ^ 0x80u) & 0xFFu)) - p.zf[j];
-    return bf2u(__floats2bfloat162_rn(lo, hi));  // q - zp, exact
+    // q - zp exactly, times the scale exactly in fp32 (16 significant bits
+    // at most), rounded once to bf16
+    const float lo = (__uint_as_float(0x4B000000u | ((t ^ 0x80u) & 0xFFu)) - p.zf[j]) * p.sf[j];
+    const float hi =
+        (__uint_as_float(0x4B000000u | (((t >> 16) ^ 0x80u) & 0xFFu)) - p.zf[j]) * p.sf[j];
+    return bf2u(__floats2bfloat162_rn(lo, hi));
   } else {
     // exponent and mantissa bits as the low exponent and high mantissa bits
     // of a bf16, the sign to bit 15, then the exact power-of-two multiplier
@@ -376,13 +387,13 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   int inflight = 0;  // stages issued and not yet consumed
   while (inflight < D && issue(inflight)) ++inflight;
 
-  float acc[4][NT][4], h[4][NT][4];
+  float acc[4][NT][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[i][t][q] = h[i][t][q] = 0.0f;
+      for (int q = 0; q < 4; ++q) acc[i][t][q] = 0.0f;
   ColParams prm;
   int slot = 0;
   uint32_t phase = 0;
@@ -443,21 +454,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 for (int i = 0; i < 4; ++i) mma_bf16(acc[i][t], a[i], b[t][0], b[t][1]);
               }
             }
-            if constexpr (INT) {
-              if (((kk + 16) & gmask) == 0 || kk + 16 >= kend) {
-                // the group's scale, once per group, on the fp32 sums
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                  for (int t = 0; t < NT; ++t) {
-                    h[i][t][0] = fmaf(prm.sf[2 * i], acc[i][t][0], h[i][t][0]);
-                    h[i][t][1] = fmaf(prm.sf[2 * i], acc[i][t][1], h[i][t][1]);
-                    h[i][t][2] = fmaf(prm.sf[2 * i + 1], acc[i][t][2], h[i][t][2]);
-                    h[i][t][3] = fmaf(prm.sf[2 * i + 1], acc[i][t][3], h[i][t][3]);
-                    acc[i][t][0] = acc[i][t][1] = acc[i][t][2] = acc[i][t][3] = 0.0f;
-                  }
-              }
-            }
           }
         }
         __syncwarp();
@@ -468,7 +464,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
       }
       // ---- epilogue of one row group of the unit ----
-      float (&V)[4][NT][4] = INT ? h : acc;
+      float (&V)[4][NT][4] = acc;
       if constexpr (SWI) {
         const int zc = U.cb * 32 + 8 * (g & 3);  // z column of the lane's first value
         float bg[8], bu[8];
@@ -558,54 +554,52 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) acc[i][t][q] = h[i][t][q] = 0.0f;
+          for (int q = 0; q < 4; ++q) acc[i][t][q] = 0.0f;
     }
   }
 }
 
 // y[t] = sum over the token's routed items r (those the align placed) and
 // the K parts s of parts[(s * R + r) * H]; the parts are weighted already.
-template <int V>
+// One thread per 4 columns of a token; the (item, part) rows are taken eight
+// at a time with their loads issued together (the call is a handful of
+// tokens, so the latency of dependent loads would bound it).
 __global__ void __launch_bounds__(256)
     reduce_parts_kernel(const float* __restrict__ parts, const int32_t* __restrict__ inv,
                         int64_t M, int k, int H, int S, bf16* __restrict__ y) {
   pdl_begin();
-  const int hv = H / (4 * V);
+  const int hv = H / 4;
   const int64_t R = M * k;
   const int64_t total = M * hv;
+  const int n = k * S;  // (item, part) rows of a token, item-major
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t t = i / hv;
     const int cc = static_cast<int>(i - t * hv);
-    float4 acc[V];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < n; q0 += 8) {
+      float4 v[8];
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int64_t r = t * k + j;
-      if (__ldg(inv + r) < 0) continue;
-      for (int s = 0; s < S; ++s) {
-        const float4* src = reinterpret_cast<const float4*>(parts + (s * R + r) * H) + V * cc;
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          const float4 x = __ldg(src + v);
-          acc[v].x += x.x;
-          acc[v].y += x.y;
-          acc[v].z += x.z;
-          acc[v].w += x.w;
+      for (int q = 0; q < 8; ++q) {
+        v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int qq = q0 + q;
+        if (qq < n) {
+          const int64_t r = t * k + qq / S;
+          if (__ldg(inv + r) >= 0)
+            v[q] = __ldg(reinterpret_cast<const float4*>(parts + ((qq % S) * R + r) * H) + cc);
         }
       }
-    }
-    uint32_t w[2 * V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      w[2 * v] = bf2u(__floats2bfloat162_rn(acc[v].x, acc[v].y));
-      w[2 * v + 1] = bf2u(__floats2bfloat162_rn(acc[v].z, acc[v].w));
+      for (int q = 0; q < 8; ++q) {
+        acc.x += v[q].x;
+        acc.y += v[q].y;
+        acc.z += v[q].z;
+        acc.w += v[q].w;
+      }
     }
-    bf16* dst = y + t * H + static_cast<int64_t>(cc) * 4 * V;
-    if constexpr (V == 2)
-      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-    else
-      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    const uint32_t w0 = bf2u(__floats2bfloat162_rn(acc.x, acc.y));
+    const uint32_t w1 = bf2u(__floats2bfloat162_rn(acc.z, acc.w));
+    *reinterpret_cast<uint2*>(y + t * H + static_cast<int64_t>(cc) * 4) = make_uint2(w0, w1);
   }
 }
 
@@ -770,14 +764,11 @@ moe_status_t launch_wq_decode_gemm2(const GroupedGemmArgs& a, const int32_t* cou
 moe_status_t launch_reduce_parts(const float* parts, const int32_t* inv, int64_t M, int32_t k,
                                  int32_t H, int32_t splits, bf16* y, cudaStream_t s) {
   if (M <= 0) return MOE_OK;
-  const int V = H % 8 == 0 ? 2 : 1;
-  const int64_t total = M * (H / (4 * V));
-  const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ceil_div<int64_t>(total, 256), 1024)));
+  const int64_t total = M * (H / 4);
+  const unsigned grid = static_cast<unsigned>(
+      std::max<int64_t>(1, std::min<int64_t>(ceil_div<int64_t>(total, 256), 4096)));
   prof_before("reduce_parts", s);
-  if (V == 2)
-    launch_kernel(reduce_parts_kernel<2>, grid, 256, 0, s, parts, inv, M, k, H, splits, y);
-  else
-    launch_kernel(reduce_parts_kernel<1>, grid, 256, 0, s, parts, inv, M, k, H, splits, y);
+  launch_kernel(reduce_parts_kernel, grid, 256, 0, s, parts, inv, M, k, H, splits, y);
   prof_after("reduce_parts", s);
   return check_launch("reduce_parts");
 }
