@@ -477,8 +477,10 @@ GBMOE_API moe_status_t moe_read_error(const int32_t* error_word, int32_t reset, 
  * expert_offsets [E+1], block_expert_ids, sorted_token_ids [cap], align
  * scratch, inverse permutation int32 [M*top_k] (sorted position of each
  * routed item, -1 if dropped), permuted token rows bf16 [cap, H],
- * z = SiLU(gate)*up bf16 [cap, I], fp32 item rows [cap, H] (sorted,
- * SEPARATE) / token accumulator [M, H] (EPILOGUE_ATOMIC) -- all for the
+ * z = SiLU(gate)*up bf16 [cap, I], the item rows of SEPARATE (sorted; fp32
+ * [cap, H], or fp16 [cap, H] followed by their exponents [ceil(H/32)][cap]
+ * bytes, as moe_set_item_rows picks) / the token accumulator fp32 [M, H] of
+ * EPILOGUE_ATOMIC, one region -- all for the
  * first token chunk; offsets[10] = cap (rows of the padded layout).
  * No GPU access.
  */
@@ -528,6 +530,19 @@ GBMOE_API moe_status_t moe_set_gemm_tiles(int32_t mode);
  * Results are identical either way.  Values other than 0 / 1 return
  * MOE_ERR_INVALID_ARG. */
 GBMOE_API moe_status_t moe_set_pdl(int32_t enabled);
+/* Item-row format of the separate weight-and-reduce (process-wide tuning /
+ * testing knob) for moe_forward, moe_forward_opts, moe_forward_host and
+ * moe_forward_fp8 with per-expert or per-channel weight scales (the
+ * block-scaled FP8 and weight-only forwards keep fp32 rows).  The rows are
+ * either fp32, or fp16 values times 2^-e with one exponent e >= 0 per row
+ * and 32-column chunk, the least that keeps the chunk finite (half the
+ * bytes, 11 significant bits, no overflow).  0 = automatic (fp16 when
+ * top_k >= 4, where a token's k rows dominate the reduce's traffic; the
+ * default), 1 = fp32, 2 = fp16.  "fused_moe.py 分析" rounds these rows to
+ * the compute dtype (bf16) before the k-sum; both formats here are more
+ * precise.  Results agree to fp16 rounding of each weighted item row.
+ * Values outside 0..2 return MOE_ERR_INVALID_ARG. */
+GBMOE_API moe_status_t moe_set_item_rows(int32_t mode);
 /* Weight-only decode GEMMs (process-wide tuning / testing knob, on by
  * default): 1 = moe_forward_wq takes, for calls of at most 32 tokens (H a
  * multiple of 64, E <= 1024, int formats with a power-of-two group of at

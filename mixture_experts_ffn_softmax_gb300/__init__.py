@@ -426,6 +426,17 @@ def set_pdl(enabled: bool = True):
     _check(lib().moe_set_pdl(1 if enabled else 0), "moe_set_pdl")
 
 
+def set_item_rows(fmt: str = "auto"):
+    """Item rows of the separate weight-and-reduce: "auto" (default: fp16
+    when top_k >= 4), "fp32", or "fp16" (fp16 values with a power-of-two
+    exponent per row and 32-column chunk).  Results agree to fp16 rounding
+    of each weighted item row."""
+    modes = {"auto": 0, "fp32": 1, "fp16": 2}
+    if fmt not in modes:
+        raise ValueError(f"item row format {fmt!r}")
+    _check(lib().moe_set_item_rows(modes[fmt]), "moe_set_item_rows")
+
+
 def set_wq_decode(enabled: bool = True):
     """Weight-only layers of at most 32 tokens through the decode GEMMs
     (weights expanded in registers, the expert's few rows as the MMA's N; on
@@ -448,7 +459,7 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
-           "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl", "set_wq_decode",
+           "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl", "set_wq_decode", "set_item_rows",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
            "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",

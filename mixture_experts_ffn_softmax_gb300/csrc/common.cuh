@@ -267,6 +267,9 @@ struct GroupedGemmArgs {
   // GEMM1 with the gather fused (bf16): the token rows [M, K] that A's rows
   // are copied from (row r = token row_index[r] / div), or null (A = a)
   const bf16* a_rows = nullptr;
+  // GEMM2 SortedF16: the exponent e of each row's 32-column chunk (rows
+  // stored as fp16 times 2^-e), [ceil(N/32)][cap] bytes
+  uint8_t* o_exp = nullptr;
   // bf16 grouped GEMMs: two int32 {next tile, CTAs done}, zero at launch
   // (reset by the kernel itself when it ends), for the dynamic tile
   // schedule; null: static schedule
@@ -293,6 +296,17 @@ moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s);
 // GEMM2, contiguous layout, ATOMIC reduce: out = acc fp32 [M, N]; each
 // weighted row is added into row row_index[p] / div with vector fp32 atomics.
 moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s);
+// GEMM2, SEPARATE reduce, item rows as fp16 times 2^-e with e per row and
+// 32-column chunk in a.o_exp (out = fp16 [cap, N]); bf16 and FP8 operands.
+moe_status_t launch_gemm2_sorted_f16(const GroupedGemmArgs& a, cudaStream_t s);
+moe_status_t launch_gemm2_sorted_f16_fp8(const GroupedGemmArgs& a, cudaStream_t s);
+// The weight-and-reduce over such rows (exponents [chunk][row], ld rows).
+moe_status_t launch_reduce_sorted_f16(const void* o16, const uint8_t* o_exp, int64_t ld,
+                                     const int32_t* inv, int64_t M, int32_t k, int32_t H, bf16* y,
+                                     cudaStream_t s);
+// Item-row format of the separate reduce for a call with top_k items per
+// token (moe_set_item_rows): true = fp16 with exponents, false = fp32.
+bool item_rows_fp16(int32_t top_k);
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 // FP8 with block-wise scales: a.w_scale [E, K/128, N'/128] per 128 x 128
 // weight block, a.a_scale [K/128][cap] per (sorted row, 128-wide K group),

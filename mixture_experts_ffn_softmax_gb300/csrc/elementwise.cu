@@ -7,6 +7,8 @@
 // list (the token of item r is r // top_k), and moe_sum adds each token's
 // top-k expert outputs.  "Fused MoE Modular Kernel" (vLLM): the permute /
 // unpermute steps of apply() and TopKWeightAndReduce.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "fp8q.cuh"
 
@@ -88,6 +90,59 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// As reduce_sorted_kernel for item rows stored as fp16 times 2^-e (e per row
+// and 32-column chunk in o_exp [chunk][row], ld rows): y[t, :] =
+// bf16(sum_j o16[pos_j, :] * 2^e), 8 x V columns per thread (within one
+// chunk: one exponent byte per item).
+template <int V>
+__global__ void __launch_bounds__(256)
+    reduce_sorted_f16_kernel(const __half* __restrict__ o, const uint8_t* __restrict__ o_exp,
+                             int64_t ld, const int32_t* __restrict__ inv, int64_t M, int k, int H,
+                             bf16* __restrict__ y) {
+  pdl_begin();
+  const int hv = H / (8 * V);
+  const int64_t total = M * hv;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / hv;
+    const int c = static_cast<int>(i - t * hv);
+    const int col = 8 * V * c;
+    float acc[8 * V];
+#pragma unroll
+    for (int v = 0; v < 8 * V; ++v) acc[v] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int32_t pos = __ldg(inv + t * k + j);
+      if (pos < 0) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(o + static_cast<int64_t>(pos) * H + col);
+      uint4 x[V];
+#pragma unroll
+      for (int v = 0; v < V; ++v) x[v] = __ldg(src + v);
+      const uint32_t e = __ldg(o_exp + static_cast<int64_t>(col >> 5) * ld + pos);
+      const float sc = __uint_as_float((127u + e) << 23);  // 2^e
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const uint32_t w[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+          acc[8 * v + 2 * q] = fmaf(f.x, sc, acc[8 * v + 2 * q]);
+          acc[8 * v + 2 * q + 1] = fmaf(f.y, sc, acc[8 * v + 2 * q + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * v + 2 * q], acc[8 * v + 2 * q + 1]);
+        w[q] = *reinterpret_cast<uint32_t*>(&b);
+      }
+      reinterpret_cast<uint4*>(y + t * H + col)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // y = bf16(acc), 8 elements per thread.
 __global__ void __launch_bounds__(256)
     cast_f32_bf16_kernel(const float* __restrict__ acc, int64_t n8, bf16* __restrict__ y) {
@@ -149,6 +204,24 @@ moe_status_t launch_reduce_sorted(const float* o_sorted, const int32_t* inv, int
     launch_kernel(reduce_sorted_kernel<2>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
   else
     launch_kernel(reduce_sorted_kernel<1>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
+  prof_after("reduce_sorted", s);
+  return check_launch("reduce_sorted");
+}
+
+moe_status_t launch_reduce_sorted_f16(const void* o16, const uint8_t* o_exp, int64_t ld,
+                                     const int32_t* inv, int64_t M, int32_t k, int32_t H, bf16* y,
+                                     cudaStream_t s) {
+  if (M <= 0) return MOE_OK;
+  const int V = (k <= 4 && H % 16 == 0) ? 2 : 1;
+  const int64_t total = M * (H / (8 * V));
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>(ceil_div<int64_t>(total, 256), device_sms() * 8));
+  const __half* o = static_cast<const __half*>(o16);
+  prof_before("reduce_sorted", s);
+  if (V == 2)
+    launch_kernel(reduce_sorted_f16_kernel<2>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
+  else
+    launch_kernel(reduce_sorted_f16_kernel<1>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
   prof_after("reduce_sorted", s);
   return check_launch("reduce_sorted");
 }

@@ -36,6 +36,10 @@
 //   SortedF32  : GEMM2, contiguous layout, separate reduce.  o = (acc + b2) *
 //                w(item) as fp32 rows in sorted order, staged through shared
 //                memory and written with TMA tensor stores (coalesced, async).
+//   SortedF16  : as SortedF32, the rows stored as fp16 values times 2^-e with
+//                e >= 0 per row and 32-column chunk, the least that keeps the
+//                chunk finite (exponents in o_exp [chunk][row]): half the
+//                bytes, 11 significant bits, no overflow.
 //   AtomicF32  : GEMM2, contiguous layout, reduce in the epilogue.  The same
 //                weighted row is added into the token's fp32 accumulator row
 //                with 16-byte vector atomics (the k-sum happens in L2).
@@ -45,6 +49,8 @@
 //                token order, fp32 output [M, E].
 // Every mbarrier wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT,
 // all roles stop, in-flight copies are given time to land, TMEM is freed.
+#include <cuda_fp16.h>
+
 #include <algorithm>
 #include <type_traits>
 
@@ -154,7 +160,7 @@ __host__ __device__ constexpr int cta_threads() {
   return 64 + 32 * conv_warps<WQ>() + (WQ == Wq::None ? 0 : 32) + EPI_WARPS * 32;
 }
 
-enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3, DenseF32 = 4 };
+enum class Epi { SwiGLU = 0, SortedF32 = 1, AtomicF32 = 2, RowsBF16 = 3, DenseF32 = 4, SortedF16 = 5 };
 
 template <int NS>
 struct Ctl {
@@ -207,6 +213,9 @@ struct KParams {
   // block-scaled FP8: activation scales [K/128][a_ld] (group-major), weight
   // scales [E][K/128][w_scale_ld] per 128 x 128 block
   int64_t bs_a_ld;
+  // SortedF16: the exponent e of each row's 32-column chunk, [ceil(N/32)][cap]
+  uint8_t* o_exp;
+  int64_t o_exp_ld;
   // nonzero: tmB views the weights with the tile's 128-byte column chunks as
   // a dimension of their own (stride 128 bytes), so that one TMA copy fills
   // every chunk of a stage; zero: one copy per chunk
@@ -484,7 +493,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
   if (warp == 0 && lane == 0) {
     if constexpr (!GA) ptx::prefetch_tmap(tmA);
     ptx::prefetch_tmap(tmB);
-    if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SwiGLU) ptx::prefetch_tmap(tmO);
+    if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SortedF16 || EPI == Epi::SwiGLU)
+      ptx::prefetch_tmap(tmO);
     if constexpr (WQM) {
       ptx::prefetch_tmap(tmS);
       if (P.wq_has_zero) ptx::prefetch_tmap(tmZ);
@@ -1378,6 +1388,39 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
               ptx::tma_store_2d(tmO, stage_buf, n0, row0 + q * 32);
               ptx::bulk_commit();
             }
+          } else if constexpr (EPI == Epi::SortedF16) {
+            // The row's 32 values as fp16 times 2^-e, e >= 0 the least with
+            // max |o| * 2^-e < 2^15 (finite in fp16); e in o_exp, chunk-major
+            // so that the warp's 32 rows write 32 consecutive bytes.  Staged
+            // as a 32 x 32 fp16 block in the 64-byte-swizzled layout of the
+            // tensor map (row = lane, 16-byte chunk j at j ^ ((row >> 1) & 3)),
+            // then one TMA store.
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(o[j]));
+            const int ex = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+            const int e = max(0, ex - 14);
+            const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+            uint32_t hw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const __half2 h2 = __floats2half2_rn(o[2 * j] * sc, o[2 * j + 1] * sc);
+              hw[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            if (lane == 0) ptx::bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(stage_buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(tmO, stage_buf, n0, row0 + q * 32);
+              ptx::bulk_commit();
+            }
+            P.o_exp[static_cast<int64_t>(n0 >> 5) * P.o_exp_ld + row0 + q * 32 + lane] =
+                static_cast<uint8_t>(e);
           } else if constexpr (EPI == Epi::AtomicF32) {
             if (valid) {
               float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(P.out) +
@@ -1422,7 +1465,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     }
   }
 
-  if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SwiGLU) {
+  if constexpr (EPI == Epi::SortedF32 || EPI == Epi::SortedF16 || EPI == Epi::SwiGLU) {
     if (warp >= EPI0 && lane == 0) ptx::bulk_wait0();  // TMA stores done before smem is released
   }
   __syncwarp();  // lane-0-only roles rejoin their warp before the aligned barriers
@@ -1606,6 +1649,8 @@ KParams base_params(const GroupedGemmArgs& a, int NB) {
   P.row_amax = a.row_amax;
   P.z_group_scale = a.z_group_scale;
   P.w_scale_ld = (EPI == Epi::SwiGLU) ? 2 * a.N : a.N;
+  P.o_exp = a.o_exp;
+  P.o_exp_ld = a.cap;
   return P;
 }
 
@@ -1697,7 +1742,16 @@ moe_status_t launch_gemm(const GroupedGemmArgs& a, const char* name, cudaStream_
   int32_t one_box;
   if (moe_status_t st = make_ab_maps<EPI, F8>(a, pairs, &tmA, &tmB, &NB, &one_box)) return st;
   CUtensorMap tmO;
-  if constexpr (EPI == Epi::SortedF32) {
+  if constexpr (EPI == Epi::SortedF16) {
+    // fp16 [cap, N] rows, 32 x 32 boxes, 64-byte swizzle (matches staging)
+    if (a.o_exp == nullptr) return set_error(MOE_ERR_INVALID_ARG, "%s: no exponent array", name);
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.cap)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
+    const uint32_t box[2] = {32, 32};
+    if (moe_status_t st = make_map(&tmO, a.out, 2, dims, strides, box,
+                                   CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_64B))
+      return st;
+  } else if constexpr (EPI == Epi::SortedF32) {
     // fp32 [cap, N] output, 32 x 32 boxes, 128-byte swizzle (matches staging)
     const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.cap)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 4};
@@ -2013,6 +2067,12 @@ moe_status_t launch_gemm1_swiglu(const GroupedGemmArgs& a, cudaStream_t s) {
 }
 moe_status_t launch_gemm2_sorted_f32(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::SortedF32>(a, "gemm2_sorted", s);
+}
+moe_status_t launch_gemm2_sorted_f16(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::SortedF16>(a, "gemm2_sorted", s);
+}
+moe_status_t launch_gemm2_sorted_f16_fp8(const GroupedGemmArgs& a, cudaStream_t s) {
+  return launch_gemm<Epi::SortedF16, true>(a, "gemm2_sorted_fp8", s);
 }
 moe_status_t launch_gemm2_atomic_f32(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_gemm<Epi::AtomicF32>(a, "gemm2_atomic", s);

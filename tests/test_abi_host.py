@@ -190,6 +190,16 @@ def test_pdl_switch_validation():
         assert lib.moe_set_pdl(m) == OK
 
 
+def test_item_rows_switch_validation():
+    lib = pkg.lib()
+    assert lib.moe_set_item_rows(3) == INVALID
+    assert lib.moe_set_item_rows(-1) == INVALID
+    for m in (2, 1, 0):
+        assert lib.moe_set_item_rows(m) == OK
+    with pytest.raises(ValueError):
+        pkg.set_item_rows("bf16")
+
+
 def test_wq_decode_switch_validation():
     lib = pkg.lib()
     assert lib.moe_set_wq_decode(2) == INVALID
