@@ -56,10 +56,11 @@ def test_item_row_formats_small_workloads(name, fmt, tiles, rows_restore):
 
 
 @pytest.mark.parametrize("shape", [(5, 136, 72, 3, 3), (70, 8, 24, 3, 1), (300, 256, 320, 16, 4),
-                                   (40, 64, 128, 8, 4)])
+                                   (40, 64, 128, 8, 4), (20000, 64, 64, 8, 4)])
 def test_item_rows_fp16_edge_shapes(shape, rows_restore):
     """H not a multiple of 32 (a ragged last chunk), H = 8 (one chunk of eight
-    columns), top_k = E."""
+    columns), top_k = E, and 20000 tokens (two token chunks of the forward, each
+    with its own rows and exponents)."""
     M, H, I, E, k = shape
     spec = wl.SMALL_SPECS["mixtral_small"].scaled("rows", M=M, H=H, I=I, E=E, top_k=k)
     d = wl.make_moe_inputs(spec, device="cuda")
