@@ -1205,7 +1205,10 @@ moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens
   g1.sentinel = sentinel;
   g1.error_word = err;
   g1.num_sms = sms;
-  g1.rows_hint = static_cast<int64_t>(E) * T / 2;
+  // the tile shape from the layout's capacity, T rows per expert: CTA pairs
+  // when an expert can hold four 128-row blocks (E = 32, T = 512 with ~60 %
+  // of the rows valid: 0.443 -> 0.426 ms against single-CTA tiles)
+  g1.rows_hint = static_cast<int64_t>(E) * T;
   if (moe_status_t st = launch_gemm1_swiglu(g1, s)) return st;
 
   GroupedGemmArgs g2{};
@@ -1223,7 +1226,7 @@ moe_status_t moe_forward_batched(const void* x, const int32_t* expert_num_tokens
   g2.sentinel = sentinel;
   g2.error_word = err;
   g2.num_sms = sms;
-  g2.rows_hint = static_cast<int64_t>(E) * T / 2;
+  g2.rows_hint = static_cast<int64_t>(E) * T;
   return launch_gemm2_rows_bf16(g2, s);
 }
 
