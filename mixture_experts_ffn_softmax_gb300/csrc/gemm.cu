@@ -1394,7 +1394,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
             // so that the warp's 32 rows write 32 consecutive bytes.  Staged
             // as a 32 x 32 fp16 block in the 64-byte-swizzled layout of the
             // tensor map (row = lane, 16-byte chunk j at j ^ ((row >> 1) & 3)),
-            // then one TMA store.
+            // then one TMA store; the warp's staging area holds two such
+            // blocks, used in turn, so a chunk is staged while the previous
+            // chunk's store still reads the other.
             float m = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(o[j]));
@@ -1407,16 +1409,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
               const __half2 h2 = __floats2half2_rn(o[2 * j] * sc, o[2 * j + 1] * sc);
               hw[j] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            if (lane == 0) ptx::bulk_wait_read0();
+            uint8_t* blk = stage_buf + ((c >> 5) & 1) * 2048;
+            if (lane == 0) ptx::bulk_wait_read1();  // the store that used blk is done reading
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(stage_buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+              *reinterpret_cast<uint4*>(blk + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
                   make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              ptx::tma_store_2d(tmO, stage_buf, n0, row0 + q * 32);
+              ptx::tma_store_2d(tmO, blk, n0, row0 + q * 32);
               ptx::bulk_commit();
             }
             P.o_exp[static_cast<int64_t>(n0 >> 5) * P.o_exp_ld + row0 + q * 32 + lane] =
