@@ -274,7 +274,10 @@ GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_we
  *  io->d_hidden      device bf16 [M, H];  io->d_logits device fp32 [M, E]
  *  io->topk_weights  device fp32 [M, top_k];  io->topk_ids device int32 [M, top_k]
  *  io->d_out         device bf16 [M, H]
- *                    (device staging, owned by the caller; 16-byte aligned)
+ *                    (device staging, owned by the caller; 16-byte aligned;
+ *                    its contents afterwards are unspecified: the last
+ *                    chunk's rows go straight to a mapped io->h_out, see
+ *                    moe_set_host_out_direct)
  *  route             routing parameters, with moe_route's meaning and limits
  *  w13, w2, w13_bias, w2_bias, workspace, workspace_bytes, reduce_mode:
  *                    as moe_forward
@@ -287,7 +290,9 @@ GBMOE_API moe_status_t moe_forward_opts(const void* hidden, const float* topk_we
  * (copied bytes x 11 > weight bytes) run as two token chunks (results
  * identical to one pass), so the second chunk's rows are copied in while
  * the first is computed and the first chunk's output is copied out while
- * the second is computed.  Returns after
+ * the second is computed.  The last chunk's output is written by its reduce
+ * directly into io->h_out when that is mapped page-locked memory (no copy
+ * after the reduce).  Returns after
  * enqueueing; io->h_out holds the result once `stream` has passed the call
  * (cudaStreamSynchronize or an event).  The call can be captured in a CUDA
  * graph.  Errors: as moe_route and moe_forward (checked before anything is
@@ -552,6 +557,15 @@ GBMOE_API moe_status_t moe_set_item_rows(int32_t mode);
  * Results agree up to fp32 summation order.  Values other than 0 / 1 return
  * MOE_ERR_INVALID_ARG. */
 GBMOE_API moe_status_t moe_set_wq_decode(int32_t enabled);
+/* Direct output of moe_forward_host (process-wide tuning / testing knob, on
+ * by default): 1 = when io->h_out is page-locked host memory mapped into the
+ * device's address space (cudaHostAlloc / cudaHostRegister; 16-byte
+ * aligned), the last token chunk's reduce writes its rows straight into it
+ * over the host link, and io->d_out is left unwritten for those rows;
+ * 0 = every chunk's output goes through io->d_out and a device-to-host
+ * copy.  Results are identical.  Values other than 0 / 1 return
+ * MOE_ERR_INVALID_ARG. */
+GBMOE_API moe_status_t moe_set_host_out_direct(int32_t enabled);
 /* Where moe_forward / moe_forward_opts / moe_forward_host take GEMM1's rows
  * from (process-wide tuning / testing knob): 0 = automatic (fused when the
  * routed rows of a token chunk hold at most 16 MiB), 1 = a separate gather

@@ -445,6 +445,14 @@ def set_wq_decode(enabled: bool = True):
     _check(lib().moe_set_wq_decode(1 if enabled else 0), "moe_set_wq_decode")
 
 
+def set_host_out_direct(enabled: bool = True):
+    """moe_forward_host with a pinned `out`: the last token chunk's reduce
+    writes its rows straight into it over the host link (on by default), or
+    every chunk goes through the device staging buffer and a copy.  Results
+    are identical."""
+    _check(lib().moe_set_host_out_direct(1 if enabled else 0), "moe_set_host_out_direct")
+
+
 def profiler_start():
     _check(lib().moe_profiler_start(), "moe_profiler_start")
 
@@ -459,7 +467,8 @@ def profiler_stop():
 
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
-           "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl", "set_wq_decode", "set_item_rows",
+           "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl", "set_wq_decode",
+           "set_item_rows", "set_host_out_direct",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
            "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",

@@ -49,7 +49,10 @@ std::atomic<int> g_gather_mode{0};
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_wq_decode{1};
 std::atomic<int> g_item_rows{0};
+std::atomic<int> g_direct_host_out{1};
 }  // namespace
+
+bool direct_host_out() { return g_direct_host_out.load(std::memory_order_relaxed) != 0; }
 
 // Automatic choice: fp16 rows when each token has at least four items.  The
 // k item rows a token's reduce reads then outweigh the rest of its traffic
@@ -265,6 +268,13 @@ moe_status_t moe_set_gemm_tiles(int32_t mode) {
 moe_status_t moe_set_pdl(int32_t enabled) {
   if (enabled != 0 && enabled != 1) return set_error(MOE_ERR_INVALID_ARG, "pdl switch %d", enabled);
   g_pdl.store(enabled, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_set_host_out_direct(int32_t enabled) {
+  if (enabled != 0 && enabled != 1)
+    return set_error(MOE_ERR_INVALID_ARG, "host output switch %d", enabled);
+  g_direct_host_out.store(enabled, std::memory_order_relaxed);
   return MOE_OK;
 }
 
@@ -742,6 +752,19 @@ moe_status_t moe_forward_host(const moe_host_io_t* io, int64_t M, int32_t H, int
   bf16* hy = static_cast<bf16*>(io->h_out);
   bf16* dx = static_cast<bf16*>(io->d_hidden);
   bf16* dy = static_cast<bf16*>(io->d_out);
+  // The last chunk's output follows its reduce with nothing left to overlap:
+  // into a pinned (device-mapped, 16-byte aligned) output buffer the reduce
+  // writes it directly over the host link instead of through d_out and a
+  // device-to-host copy.  Earlier chunks keep the copy, which runs under the
+  // next chunk's compute; pageable memory always takes it.
+  bf16* y_direct = nullptr;
+  if (direct_host_out()) {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, io->h_out) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer != nullptr && reinterpret_cast<uintptr_t>(pa.devicePointer) % 16 == 0)
+      y_direct = static_cast<bf16*>(pa.devicePointer);
+    cudaGetLastError();
+  }
   for (int c = 0; c < chunks; ++c) {
     const int64_t m0 = m0s[c], mc = m0s[c + 1] - m0s[c];
     if (cudaMemcpyAsync(io->d_logits + m0 * E, io->h_logits + m0 * E,
@@ -757,6 +780,7 @@ moe_status_t moe_forward_host(const moe_host_io_t* io, int64_t M, int32_t H, int
   }
   for (int c = 0; c < chunks; ++c) {
     const int64_t m0 = m0s[c], mc = m0s[c + 1] - m0s[c];
+    const bool direct = y_direct != nullptr && c == chunks - 1;
     moe_status_t st = MOE_OK;
     if (cudaStreamWaitEvent(s, lane->logits[c], 0) != cudaSuccess) st = cuda_fail("logits wait");
     if (st == MOE_OK)
@@ -768,9 +792,10 @@ moe_status_t moe_forward_host(const moe_host_io_t* io, int64_t M, int32_t H, int
     // right before the rows are first read
     if (st == MOE_OK)
       st = forward_launch(dx + m0 * H, io->topk_weights + m0 * k, io->topk_ids + m0 * k, mc, H,
-                          I, E, k, w13, w2, w13_bias, w2_bias, workspace, &o, dy + m0 * H, sms,
-                          lane->rows[c], s, /*reset_error=*/c == 0);
-    if (st == MOE_OK &&
+                          I, E, k, w13, w2, w13_bias, w2_bias, workspace, &o,
+                          (direct ? y_direct : dy) + m0 * H, sms, lane->rows[c], s,
+                          /*reset_error=*/c == 0);
+    if (st == MOE_OK && !direct &&
         (cudaEventRecord(lane->out[c], s) != cudaSuccess ||
          cudaStreamWaitEvent(lane->d2h, lane->out[c], 0) != cudaSuccess ||
          cudaMemcpyAsync(hy + m0 * H, dy + m0 * H, static_cast<size_t>(mc) * H * sizeof(bf16),

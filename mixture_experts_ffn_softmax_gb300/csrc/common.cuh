@@ -307,6 +307,9 @@ moe_status_t launch_reduce_sorted_f16(const void* o16, const uint8_t* o_exp, int
 // Item-row format of the separate reduce for a call with top_k items per
 // token (moe_set_item_rows): true = fp16 with exponents, false = fp32.
 bool item_rows_fp16(int32_t top_k);
+// Whether moe_forward_host writes a pinned output buffer directly
+// (moe_set_host_out_direct; on by default).
+bool direct_host_out();
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 // FP8 with block-wise scales: a.w_scale [E, K/128, N'/128] per 128 x 128
 // weight block, a.a_scale [K/128][cap] per (sorted row, 128-wide K group),

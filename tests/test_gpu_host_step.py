@@ -98,3 +98,38 @@ def test_host_step_validation_enqueues_nothing():
     kw = _route_kw(spec)
     y = pkg.moe_forward_host(hx[:0], hl[:0], d["w13"], d["w2"], **kw)   # M = 0: nothing to do
     assert y.shape == (0, spec.H)
+
+
+@pytest.fixture
+def direct_restore():
+    yield
+    pkg.set_host_out_direct(True)
+
+
+@pytest.mark.parametrize("name", ["mixtral_small", "qwen_small"])
+def test_host_step_output_buffers(name, direct_restore):
+    """The output's way back to the host: written by the reduce straight into
+    a pinned `out` (the default), through the device staging buffer and a
+    copy (switch off, pageable `out`, or a pinned `out` that is not 16-byte
+    aligned) -- the same bits every way."""
+    spec = wl.SMALL_SPECS[name]
+    d = wl.make_moe_inputs(spec, device="cuda")
+    hx, hl = d["hidden"].cpu().pin_memory(), d["router_logits"].cpu().pin_memory()
+    want = _device_layer(spec, d).cpu()
+    n = spec.M * spec.H
+    outs = {
+        "pinned": torch.empty(spec.M, spec.H, dtype=torch.bfloat16).pin_memory(),
+        "pageable": torch.empty(spec.M, spec.H, dtype=torch.bfloat16),
+        "pinned_unaligned":
+            torch.empty(n + 1, dtype=torch.bfloat16).pin_memory()[1:].view(spec.M, spec.H),
+    }
+    for direct in (True, False):
+        pkg.set_host_out_direct(direct)
+        for key, out in outs.items():
+            out.fill_(float("nan"))
+            y = pkg.moe_forward_host(hx, hl, d["w13"], d["w2"], w13_bias=d["w13_bias"],
+                                     w2_bias=d["w2_bias"], out=out,
+                                     stream=torch.cuda.current_stream(), **_route_kw(spec))
+            torch.cuda.synchronize()
+            assert y.data_ptr() == out.data_ptr()
+            assert torch.equal(out, want), (key, direct)
