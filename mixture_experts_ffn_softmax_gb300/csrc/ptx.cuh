@@ -400,6 +400,20 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// The same for a CTA pair (cta_group::2), issued by one thread of the even
+// CTA: each CTA's TMEM holds its 128 of A's rows and receives those rows of
+// D; B's columns are split across the two CTAs' shared memory (same offset).
+__device__ __forceinline__ void mma_bf16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (bf16 inputs, fp32 accum):
 // A's rows are TMEM lanes, each 32-bit column a pair of consecutive K
 // elements (the lower k in the low half).

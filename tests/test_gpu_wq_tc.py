@@ -2,10 +2,11 @@
 takes for calls of at most 32 tokens when the codes repacked along K are
 given: the repacked layout bit for bit against a numpy restatement of its
 definition; the layer against the oracle ("fused_moe.py 分析", "WNA16 路径":
-the layer on the dequantised weights) for group sizes 64..256, with and
+the layer on the dequantised weights) for group sizes 128 and 256, with and
 without zero points, 16- and 32-row passes; against the mma.sync decode GEMMs
-on the same call; with duplicate expert ids (row groups); and at the
-Mixtral-8x7B decode shape on every token."""
+on the same call; with duplicate expert ids (row groups); groups of 64 rows
+left to the mma.sync path; and at the Mixtral-8x7B decode shape on every
+token."""
 import numpy as np
 import pytest
 import torch
@@ -19,12 +20,12 @@ from test_gpu_wq import LazyDequant, _oracle_dequant, _route
 
 pytestmark = pytest.mark.gpu
 
-# (M, H, I, E, top_k): one 128-column unit per expert and part; K ending at a
-# part boundary inside a group; few of many experts touched; 32-row passes;
-# one token; a long GEMM2 K split into parts
-SHAPES = [(16, 256, 256, 8, 2), (5, 128, 192, 6, 3), (32, 128, 128, 16, 4), (1, 128, 64, 4, 2),
-          (9, 256, 1024, 3, 2), (24, 384, 320, 5, 2)]
-GROUPS = [(64, True), (128, True), (128, False), (256, True)]
+# (M, H, I, E, top_k): one 256-column unit per expert and part; GEMM2 parts
+# ending inside a group; few of many experts touched; 32-row passes; one
+# token; a long GEMM2 K split into parts
+SHAPES = [(16, 256, 256, 8, 2), (5, 256, 384, 6, 3), (32, 256, 128, 16, 4), (1, 256, 128, 4, 2),
+          (9, 256, 1024, 3, 2), (24, 512, 640, 5, 2)]
+GROUPS = [(128, True), (128, False), (256, True)]
 
 
 def _spec(M, H, I, E, k, bias=True):
@@ -125,10 +126,10 @@ def test_tc_equals_register_decode():
 def test_tc_duplicate_ids_take_row_groups():
     """Experts holding more rows than a 16-row pass (duplicate ids within a
     token) are taken in row groups."""
-    M, H, I, E, k = 8, 128, 256, 4, 4
+    M, H, I, E, k = 8, 256, 256, 4, 4
     spec = _spec(M, H, I, E, k)
     d = wl.make_moe_inputs(spec, device="cuda", weights=False)
-    q = wl.make_wq_weights(spec, "int4", 64, device="cuda")
+    q = wl.make_wq_weights(spec, "int4", 128, device="cuda")
     b13, b2 = _biases(spec)
     gen = torch.Generator().manual_seed(11)
     ids = torch.randint(0, 2, (M, k), generator=gen, dtype=torch.int32)
@@ -144,6 +145,25 @@ def test_tc_duplicate_ids_take_row_groups():
     ref = oracle.forward_wq(f64(d["hidden"]), w.numpy().astype(np.float64), ids.numpy(), w13, w2,
                             f64(b13), f64(b2))
     check_out(f64(y), ref, "tc duplicate ids")
+
+
+def test_group_64_takes_the_register_decode():
+    """Groups of 64 rows are shorter than a stage of the tcgen05 kernels: the
+    call takes the mma.sync decode GEMMs even with the repacked codes given,
+    and matches the oracle."""
+    spec = _spec(16, 256, 256, 8, 2)
+    d = wl.make_moe_inputs(spec, device="cuda", weights=False)
+    q = wl.make_wq_weights(spec, "int4", 64, device="cuda")
+    w32, ids = _route(spec, d)
+    pkg.profiler_start()
+    y = _run(d, torch.from_numpy(w32).cuda(), torch.from_numpy(ids).cuda(), q, _packed(q))
+    ran = pkg.profiler_stop()
+    torch.cuda.synchronize()
+    assert "gemm1_swiglu_int4_decode" in ran and "gemm1_swiglu_int4_tc" not in ran, sorted(ran)
+    w13 = _oracle_dequant("int4", q["w13_q"], q["w13_scale"], q["w13_zero"])
+    w2 = _oracle_dequant("int4", q["w2_q"], q["w2_scale"], q["w2_zero"])
+    ref = oracle.forward_wq(f64(d["hidden"]), w32.astype(np.float64), ids, w13, w2)
+    check_out(f64(y), ref, "group 64 register decode")
 
 
 def test_tc_full_size_mixtral_every_token():
