@@ -420,22 +420,7 @@ typedef struct {
   const void* w2_scale;
   const void* w13_zero; /* NULL, or both zero-point tensors given */
   const void* w2_zero;
-  /* int4 only, optional: the codes repacked along K by moe_wq_pack_k (NULL,
-   * or both given).  With them, calls of at most 32 tokens (H a multiple of
-   * 128, I of 64, G a power of two >= 64) take decode GEMMs on tcgen05. */
-  const void* w13_kpack;
-  const void* w2_kpack;
 } moe_wq_weights_t;
-
-/* moe_wq_pack_k: int4 codes repacked along K, once, for the tcgen05 decode
- * GEMMs of moe_forward_wq.  codes: uint8 [E, K, N/2] as above; out: uint8
- * [E, N, K/2] (written; caller-owned, 16-byte aligned): 32-bit word w of
- * column n holds the codes of K rows 8w..8w+7, row 8w + 2t in nibble t and
- * row 8w + 2t + 1 in nibble t + 4 (t = 0..3), so that one mask leaves a
- * pair of consecutive K rows as the two halves of a 32-bit operand.
- * Limits: int4 only, K a multiple of 8, N even.  Asynchronous on `stream`. */
-GBMOE_API moe_status_t moe_wq_pack_k(int32_t format, const void* codes, int32_t E, int32_t K,
-                                     int32_t N, void* out, moe_stream_t stream);
 
 /* moe_dequant_weights: the dequantisation alone (the pages' path before the
  * bf16 layer): out = bf16 [E, K, N] (written).  Limits: N % 16 == 0,

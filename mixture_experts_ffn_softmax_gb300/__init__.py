@@ -259,16 +259,12 @@ def moe_forward_wq(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: t
                    w13_bias: Optional[torch.Tensor] = None,
                    w2_bias: Optional[torch.Tensor] = None,
                    workspace: Optional[torch.Tensor] = None,
-                   out: Optional[torch.Tensor] = None, stream=None,
-                   w13_kpack: Optional[torch.Tensor] = None,
-                   w2_kpack: Optional[torch.Tensor] = None):
+                   out: Optional[torch.Tensor] = None, stream=None):
     """Layer with weight-only quantised experts.  int4 / MX FP4 codes uint8
     [E, K, N/2] (column 2j in the low nibble), int8 codes int8 [E, K, N],
     MX FP6 codes uint8 [E, K, N] (6-bit code in the low bits); scales bf16
     [E, K/G, N] (int) or uint8 UE8M0 [E, K/32, N] (MX); zero points uint8 /
-    int8 [E, K/G, N] or None.  w13: K = H, N = 2I; w2: K = I, N = H.
-    w13_kpack / w2_kpack (int4, optional): the codes repacked along K by
-    wq_pack_k, for the tcgen05 decode GEMMs."""
+    int8 [E, K/G, N] or None.  w13: K = H, N = 2I; w2: K = I, N = H."""
     M, H = hidden.shape
     E, _, N13 = _wq_shape(fmt, w13_q)
     I = N13 // 2
@@ -278,25 +274,10 @@ def moe_forward_wq(hidden: torch.Tensor, topk_weights: torch.Tensor, topk_ids: t
     if out is None:
         out = torch.empty_like(hidden)
     wts = _lib.WqWeights(WQ_FORMATS[fmt], group_size, _ptr(w13_q), _ptr(w2_q), _ptr(w13_scale),
-                         _ptr(w2_scale), _ptr(w13_zero), _ptr(w2_zero), _ptr(w13_kpack),
-                         _ptr(w2_kpack))
+                         _ptr(w2_scale), _ptr(w13_zero), _ptr(w2_zero))
     _check(lib().moe_forward_wq(_ptr(hidden), _ptr(topk_weights), _ptr(topk_ids), M, H, I, E, k,
                                 ctypes.byref(wts), _ptr(w13_bias), _ptr(w2_bias), _ptr(workspace),
                                 workspace.numel(), _ptr(out), _stream(stream)), "moe_forward_wq")
-    return out
-
-
-def wq_pack_k(fmt: str, codes: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
-    """int4 codes uint8 [E, K, N/2] repacked along K -> uint8 [E, N, K/2]
-    (word w of column n: K rows 8w..8w+7, row 8w + 2t in nibble t and
-    8w + 2t + 1 in nibble t + 4), once, for moe_forward_wq's tcgen05 decode
-    GEMMs."""
-    E, K, half = codes.shape
-    N = 2 * half
-    if out is None:
-        out = torch.empty(E, N, K // 2, dtype=torch.uint8, device=codes.device)
-    _check(lib().moe_wq_pack_k(WQ_FORMATS[fmt], _ptr(codes), E, K, N, _ptr(out), _stream(stream)),
-           "moe_wq_pack_k")
     return out
 
 
@@ -489,7 +470,7 @@ __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forw
            "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl", "set_wq_decode",
            "set_item_rows", "set_host_out_direct",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
-           "moe_dequant_weights", "moe_forward_wq", "wq_pack_k", "WQ_FORMATS",
+           "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",
            "workspace_size", "batched_workspace_size", "alloc_workspace", "align_capacity",
            "workspace_error_word", "read_error", "launch_count", "workspace_layout",

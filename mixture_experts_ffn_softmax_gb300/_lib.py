@@ -26,8 +26,7 @@ class WqWeights(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int32), ("group_size", ctypes.c_int32),
                 ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("w13_scale", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
-                ("w13_zero", ctypes.c_void_p), ("w2_zero", ctypes.c_void_p),
-                ("w13_kpack", ctypes.c_void_p), ("w2_kpack", ctypes.c_void_p)]
+                ("w13_zero", ctypes.c_void_p), ("w2_zero", ctypes.c_void_p)]
 
 
 class HostIo(ctypes.Structure):
@@ -97,7 +96,6 @@ SIGNATURES = {
     "moe_set_wq_decode": (c_i32, [c_i32]),
     "moe_set_item_rows": (c_i32, [c_i32]),
     "moe_set_host_out_direct": (c_i32, [c_i32]),
-    "moe_wq_pack_k": (c_i32, [c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp]),
     "moe_profiler_start": (c_i32, []),
     "moe_profiler_stop": (c_i32, [ctypes.POINTER(KernelTime), c_i32, P_i32]),
 }

@@ -1044,23 +1044,6 @@ moe_status_t moe_dequant_weights(int32_t format, const void* codes, const void* 
   return launch_dequant_weights(a, stream);
 }
 
-moe_status_t moe_wq_pack_k(int32_t format, const void* codes, int32_t E, int32_t K, int32_t N,
-                           void* out, moe_stream_t stream) {
-  g_detail[0] = 0;
-  if (format != MOE_WQ_INT4)
-    return set_error(MOE_ERR_INVALID_ARG, "K-packed codes: int4 only (format %d)", format);
-  if (E < 1 || K < 8 || K % 8 != 0 || N < 2 || N % 2 != 0)
-    return set_error(MOE_ERR_INVALID_ARG, "E=%d K=%d N=%d (K a multiple of 8, N even)", E, K, N);
-  if (static_cast<int64_t>(E) * K * N >= (int64_t(1) << 40))
-    return set_error(MOE_ERR_INVALID_ARG, "E*K*N too large");
-  if (!codes || !out) return set_error(MOE_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(codes) || !aligned16(out))
-    return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
-  int sms = 0;
-  if (moe_status_t st = check_device(&sms)) return st;
-  return launch_pack_k_int4(codes, E, K, N, out, stream);
-}
-
 moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
                             const int32_t* topk_ids, int64_t M, int32_t H, int32_t I, int32_t E,
                             int32_t top_k, const moe_wq_weights_t* w, const void* w13_bias,
@@ -1081,10 +1064,6 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
                      w->group_size, H, I);
   if ((w->w13_zero == nullptr) != (w->w2_zero == nullptr))
     return set_error(MOE_ERR_INVALID_ARG, "zero points for both w13 and w2, or for neither");
-  if ((w->w13_kpack == nullptr) != (w->w2_kpack == nullptr))
-    return set_error(MOE_ERR_INVALID_ARG, "K-packed codes for both w13 and w2, or for neither");
-  if (w->w13_kpack != nullptr && w->format != MOE_WQ_INT4)
-    return set_error(MOE_ERR_INVALID_ARG, "K-packed codes: int4 only");
   if (M == 0) return MOE_OK;
   if (!hidden || !topk_weights || !topk_ids || !w->w13 || !w->w2 || !w->w13_scale ||
       !w->w2_scale || !workspace || !out)
@@ -1092,8 +1071,7 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
   if (!aligned16(hidden) || !aligned16(out) || !aligned16(w->w13) || !aligned16(w->w2) ||
       !aligned16(w->w13_scale) || !aligned16(w->w2_scale) ||
       (w->w13_zero && !aligned16(w->w13_zero)) || (w->w2_zero && !aligned16(w->w2_zero)) ||
-      (w13_bias && !aligned16(w13_bias)) || (w2_bias && !aligned16(w2_bias)) ||
-      (w->w13_kpack && !aligned16(w->w13_kpack)) || (w->w2_kpack && !aligned16(w->w2_kpack)))
+      (w13_bias && !aligned16(w13_bias)) || (w2_bias && !aligned16(w2_bias)))
     return set_error(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return set_error(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -1149,14 +1127,8 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
     // expanded in registers); otherwise the grouped tensor-core GEMMs
     const bool decode = g_wq_decode.load(std::memory_order_relaxed) != 0 &&
                         wq_decode_applies(Mc, H, I, E, w->format, w->group_size);
-    // int4 codes repacked along K: the decode GEMMs on tcgen05 (the expanded
-    // codes as the MMA's A operand in TMEM, scale and zero point per group)
-    const bool tc = g_wq_decode.load(std::memory_order_relaxed) != 0 && w->w13_kpack != nullptr &&
-                    wq_tc_applies(Mc, H, I, E, w->format, w->group_size);
     const int32_t* counts = at<int32_t>(workspace, L.counts);
-    if (tc) {
-      if (moe_status_t st = launch_wq_tc_gemm1(g1, w->w13_kpack, counts, Mc, s)) return st;
-    } else if (decode) {
+    if (decode) {
       if (moe_status_t st = launch_wq_decode_gemm1(g1, counts, Mc, s)) return st;
     } else {
       if (moe_status_t st = launch_gemm1_swiglu_wq(g1, s)) return st;
@@ -1183,14 +1155,6 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
     g2.wq_group = w->group_size;
     g2.wq_scale = w->w2_scale;
     g2.wq_zero = w->w2_zero;
-    if (tc) {
-      const int32_t parts = wq_tc_splits(Mc, top_k, H, I, E, cap, sms);
-      if (moe_status_t st = launch_wq_tc_gemm2(g2, w->w2_kpack, counts, Mc, parts, Rc, s))
-        return st;
-      if (moe_status_t st = launch_reduce_parts(o, inv, Mc, top_k, H, parts, y + c0 * H, s))
-        return st;
-      continue;
-    }
     if (decode) {
       // K split into parts, each a weighted fp32 row per routed item
       const int32_t parts = wq_decode_splits(Mc, top_k, H, I, E, cap, sms);

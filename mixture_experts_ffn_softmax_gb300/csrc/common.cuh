@@ -307,18 +307,6 @@ moe_status_t launch_reduce_sorted_f16(const void* o16, const uint8_t* o_exp, int
 // Item-row format of the separate reduce for a call with top_k items per
 // token (moe_set_item_rows): true = fp16 with exponents, false = fp32.
 bool item_rows_fp16(int32_t top_k);
-// Weight-only int4 decode GEMMs on tcgen05 (A = the expanded codes in TMEM),
-// reading codes repacked along K by moe_wq_pack_k.
-bool wq_tc_applies(int64_t M, int32_t H, int32_t I, int32_t E, int32_t format, int32_t group);
-int wq_tc_splits(int64_t M, int32_t top_k, int32_t H, int32_t I, int32_t E, int64_t cap,
-                 int32_t num_sms);
-moe_status_t launch_wq_tc_gemm1(const GroupedGemmArgs& a, const void* kpack,
-                                const int32_t* counts, int64_t M, cudaStream_t s);
-moe_status_t launch_wq_tc_gemm2(const GroupedGemmArgs& a, const void* kpack,
-                                const int32_t* counts, int64_t M, int32_t splits, int64_t R,
-                                cudaStream_t s);
-moe_status_t launch_pack_k_int4(const void* codes, int32_t E, int32_t K, int32_t N, void* out,
-                                cudaStream_t s);
 // Whether moe_forward_host writes a pinned output buffer directly
 // (moe_set_host_out_direct; on by default).
 bool direct_host_out();
