@@ -757,11 +757,16 @@ moe_status_t moe_forward_host(const moe_host_io_t* io, int64_t M, int32_t H, int
   // writes it directly over the host link instead of through d_out and a
   // device-to-host copy.  Earlier chunks keep the copy, which runs under the
   // next chunk's compute; pageable memory always takes it.
+  // (page-locked under this device: memory pinned while another device was
+  // current may not be mapped for this one)
   bf16* y_direct = nullptr;
   if (direct_host_out()) {
     cudaPointerAttributes pa{};
-    if (cudaPointerGetAttributes(&pa, io->h_out) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
-        pa.devicePointer != nullptr && reinterpret_cast<uintptr_t>(pa.devicePointer) % 16 == 0)
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaPointerGetAttributes(&pa, io->h_out) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.device == dev && pa.devicePointer != nullptr &&
+        reinterpret_cast<uintptr_t>(pa.devicePointer) % 16 == 0)
       y_direct = static_cast<bf16*>(pa.devicePointer);
     cudaGetLastError();
   }
