@@ -204,7 +204,10 @@ def kernel_work(name, H, I, E, k, M, R, touched, bias=False):
     (2HI bytes each) + z read (2I) + the fp32 (4H) or bf16 (2H) row written.
     Gather 2H read + 2H written per row; reduce 4kH read + 2H written per
     token; route 4E read + 8k written per token; align 4 B read twice and
-    8 B written per row.  Returns None for a kernel not listed."""
+    8 B written per row.  The small-call kernels: GEMM1 as above + the fp32
+    token accumulator zeroed (4H per token); GEMM2 its w2, z read, and per
+    token the accumulator read (4H) and y written (2H).  Returns None for a
+    kernel not listed."""
     b13 = touched * 2 * I * 2 if bias else 0
     b2 = touched * H * 2 if bias else 0
     if name == "gemm1_swiglu":
@@ -215,6 +218,10 @@ def kernel_work(name, H, I, E, k, M, R, touched, bias=False):
         return 2.0 * R * H * I, touched * 2 * H * I + b2 + R * 2 * I + M * H * 4
     if name == "gemm2_rows_bf16":
         return 2.0 * R * H * I, touched * 2 * H * I + b2 + R * (2 * I + 2 * H)
+    if name == "small_gemm1":
+        return 4.0 * R * H * I, touched * 4 * H * I + b13 + R * (2 * H + 2 * I) + M * 4 * H
+    if name == "small_gemm2":
+        return 2.0 * R * H * I, touched * 2 * H * I + b2 + R * 2 * I + M * 6 * H
     if name == "gather_rows":
         return 0.0, R * 4 * H
     if name == "reduce_sorted":
@@ -557,13 +564,15 @@ def run_ours(args, world, rank, local):
     work = {n: w for n, w in work.items() if w is not None}
     roof_step, dom = _summary(kern, work, ms_step, flops, nbytes, pk)
     # The roofline object is GEMM1's (the step's dominant kernel on the
-    # prefill shapes): algorithmic work per launch / its average event time.
-    g1 = kern["gemm1_swiglu"]["avg_us"]
-    f1, b1 = work["gemm1_swiglu"]
-    roof = {"kernel": "gemm1_swiglu", **roofline_of(f1, b1, g1 * 1e-6, pk),
+    # prefill shapes; small calls run the small-call GEMM1): algorithmic work
+    # per launch / its average event time.
+    k1 = "gemm1_swiglu" if "gemm1_swiglu" in kern else "small_gemm1"
+    g1 = kern[k1]["avg_us"]
+    f1, b1 = work[k1]
+    roof = {"kernel": k1, **roofline_of(f1, b1, g1 * 1e-6, pk),
             "algorithmic_flops": f1, "algorithmic_bytes": int(b1),
-            "share_of_step": round(kern["gemm1_swiglu"]["launches"] * g1 / (ms_step * 1e3), 4)}
-    traffic, note = measured_traffic("gemm1_swiglu", spec.name)
+            "share_of_step": round(kern[k1]["launches"] * g1 / (ms_step * 1e3), 4)}
+    traffic, note = measured_traffic(k1, spec.name)
     roof["traffic"] = traffic
     roof["traffic_note"] = note
     roof["peak_source"] = pk["source"] + (

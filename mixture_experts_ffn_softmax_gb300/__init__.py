@@ -453,6 +453,14 @@ def set_host_out_direct(enabled: bool = True):
     _check(lib().moe_set_host_out_direct(1 if enabled else 0), "moe_set_host_out_direct")
 
 
+def set_small_path(enabled: bool = True):
+    """Small calls (at most 256 routed items, small expert weights, the
+    automatic reduce) in two kernels with the plan, gather and reduce folded
+    into the GEMMs (on by default), or always the general path.  Results
+    agree up to fp32 summation order."""
+    _check(lib().moe_set_small_path(1 if enabled else 0), "moe_set_small_path")
+
+
 def profiler_start():
     _check(lib().moe_profiler_start(), "moe_profiler_start")
 
@@ -468,7 +476,7 @@ def profiler_stop():
 
 __all__ = ["moe_route", "moe_router_logits", "moe_layer", "moe_align", "moe_forward",
            "moe_forward_host", "HostStaging", "set_gather_mode", "set_pdl", "set_wq_decode",
-           "set_item_rows", "set_host_out_direct",
+           "set_item_rows", "set_host_out_direct", "set_small_path",
            "moe_forward_batched", "moe_forward_fp8", "workspace_size_fp8", "moe_quant_rows_fp8",
            "moe_dequant_weights", "moe_forward_wq", "WQ_FORMATS",
            "fused_moe",

@@ -96,6 +96,7 @@ SIGNATURES = {
     "moe_set_wq_decode": (c_i32, [c_i32]),
     "moe_set_item_rows": (c_i32, [c_i32]),
     "moe_set_host_out_direct": (c_i32, [c_i32]),
+    "moe_set_small_path": (c_i32, [c_i32]),
     "moe_profiler_start": (c_i32, []),
     "moe_profiler_stop": (c_i32, [ctypes.POINTER(KernelTime), c_i32, P_i32]),
 }

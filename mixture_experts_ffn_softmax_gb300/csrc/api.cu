@@ -50,9 +50,11 @@ std::atomic<int> g_pdl{1};
 std::atomic<int> g_wq_decode{1};
 std::atomic<int> g_item_rows{0};
 std::atomic<int> g_direct_host_out{1};
+std::atomic<int> g_small_path{1};
 }  // namespace
 
 bool direct_host_out() { return g_direct_host_out.load(std::memory_order_relaxed) != 0; }
+bool small_path_enabled() { return g_small_path.load(std::memory_order_relaxed) != 0; }
 
 // Automatic choice: fp16 rows when each token has at least four items.  The
 // k item rows a token's reduce reads then outweigh the rest of its traffic
@@ -268,6 +270,13 @@ moe_status_t moe_set_gemm_tiles(int32_t mode) {
 moe_status_t moe_set_pdl(int32_t enabled) {
   if (enabled != 0 && enabled != 1) return set_error(MOE_ERR_INVALID_ARG, "pdl switch %d", enabled);
   g_pdl.store(enabled, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_set_small_path(int32_t enabled) {
+  if (enabled != 0 && enabled != 1)
+    return set_error(MOE_ERR_INVALID_ARG, "small-path switch %d", enabled);
+  g_small_path.store(enabled, std::memory_order_relaxed);
   return MOE_OK;
 }
 
@@ -546,6 +555,34 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
 
   const bf16* x = static_cast<const bf16*>(hidden);
   bf16* y = static_cast<bf16*>(out);
+  // a small call: the whole layer in two kernels (the plan, gather and
+  // reduce folded into the GEMMs; an atomic k-sum, as the automatic choice
+  // allows)
+  if (small_path_enabled() && reduce_mode == MOE_REDUCE_AUTO && !weight_on_input &&
+      opts->expert_map == nullptr && reset_error && small_forward_applies(M, H, I, E, top_k)) {
+    if (wait_rows != nullptr && cudaStreamWaitEvent(s, wait_rows, 0) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaStreamWaitEvent: %s",
+                       cudaGetErrorString(cudaGetLastError()));
+    SmallArgs sa{};
+    sa.x = x;
+    sa.w13 = static_cast<const bf16*>(w13);
+    sa.w2 = static_cast<const bf16*>(w2);
+    sa.b13 = static_cast<const bf16*>(w13_bias);
+    sa.b2 = static_cast<const bf16*>(w2_bias);
+    sa.ids = topk_ids;
+    sa.weights = topk_weights;
+    sa.z = at<bf16>(workspace, L.z);
+    sa.acc = at<float>(workspace, L.o);
+    sa.counter = at<int32_t>(workspace, L.a_perm);  // the gathered rows are not used
+    sa.error_word = err;
+    sa.y = y;
+    sa.M = M;
+    sa.H = H;
+    sa.I = I;
+    sa.E = E;
+    sa.k = top_k;
+    return launch_small_forward(sa, s);
+  }
   for (int64_t c0 = 0; c0 < M; c0 += Mc_max) {
     const int64_t Mc = (M - c0) < Mc_max ? (M - c0) : Mc_max;
     const int64_t Rc = Mc * top_k;

@@ -310,6 +310,29 @@ bool item_rows_fp16(int32_t top_k);
 // Whether moe_forward_host writes a pinned output buffer directly
 // (moe_set_host_out_direct; on by default).
 bool direct_host_out();
+
+// The whole layer of a small call in two kernels (small.cu): GEMM1 with the
+// plan and the gather folded in, GEMM2 with the weight-and-reduce.
+struct SmallArgs {
+  const bf16* x;
+  const bf16* w13;
+  const bf16* w2;
+  const bf16* b13;
+  const bf16* b2;
+  const int32_t* ids;
+  const float* weights;
+  bf16* z;          // workspace [M * k, I]
+  float* acc;       // workspace [M, H]
+  int32_t* counter; // workspace [H / 64]: GEMM2 CTAs done per 64 output columns
+  int32_t* error_word;
+  bf16* y;
+  int64_t M;
+  int32_t H, I, E, k;
+};
+bool small_forward_applies(int64_t M, int32_t H, int32_t I, int32_t E, int32_t top_k);
+moe_status_t launch_small_forward(const SmallArgs& a, cudaStream_t s);
+// moe_set_small_path: whether small calls take it (on by default).
+bool small_path_enabled();
 moe_status_t launch_gemm2_rows_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 // FP8 with block-wise scales: a.w_scale [E, K/128, N'/128] per 128 x 128
 // weight block, a.a_scale [K/128][cap] per (sorted row, 128-wide K group),

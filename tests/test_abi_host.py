@@ -200,6 +200,14 @@ def test_item_rows_switch_validation():
         pkg.set_item_rows("bf16")
 
 
+def test_small_path_switch_validation():
+    lib = pkg.lib()
+    assert lib.moe_set_small_path(2) == INVALID
+    assert lib.moe_set_small_path(-1) == INVALID
+    for m in (0, 1):
+        assert lib.moe_set_small_path(m) == OK
+
+
 def test_host_out_direct_switch_validation():
     lib = pkg.lib()
     assert lib.moe_set_host_out_direct(2) == INVALID

@@ -37,6 +37,7 @@ def test_profiler_counts_launches(gather):
     w13 = torch.zeros(E, H, 2 * I, device="cuda").bfloat16()
     w2 = torch.zeros(E, I, H, device="cuda").bfloat16()
     pkg.set_gather_mode(gather)
+    pkg.set_small_path(False)   # the general path's launches
     try:
         n0 = pkg.launch_count()
         pkg.profiler_start()
@@ -45,6 +46,7 @@ def test_profiler_counts_launches(gather):
         prof = pkg.profiler_stop()
     finally:
         pkg.set_gather_mode("auto")
+        pkg.set_small_path(True)
     assert pkg.launch_count() - n0 == sum(v[0] for v in prof.values())
     names = ["align_small", "gemm1_swiglu", "gemm2_sorted", "reduce_sorted"]
     if gather == "separate":
