@@ -53,9 +53,20 @@ def _ptr(t: Optional[torch.Tensor]):
     return t.data_ptr()
 
 
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_current_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    """The cudaStream_t handle of `stream`, else of the current stream.  The
+    current one is read as a raw handle once CUDA is initialised (building a
+    torch Stream object costs microseconds per call, as much as a launch)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_current_stream is not None and _current_device is not None and \
+            torch.cuda.is_initialized():
+        return _raw_current_stream(_current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def workspace_size(M: int, H: int, I: int, E: int, top_k: int, reduce: str = "auto") -> int:

@@ -74,3 +74,26 @@ def test_concurrent_threads_match_serial():
     for i in range(len(jobs)):
         assert torch.equal(got[i][0], want_dev[i])
         assert torch.equal(got[i][1], want_host[i])
+
+
+def test_default_stream_is_the_current_stream():
+    """With no stream given the binding launches on torch's current stream:
+    the default one, one entered with torch.cuda.stream, and in another
+    host thread that thread's own."""
+    from mixture_experts_ffn_softmax_gb300 import _stream
+    assert _stream() == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert _stream() == s.cuda_stream
+    assert _stream() == torch.cuda.current_stream().cuda_stream
+    seen = {}
+
+    def other():
+        t = torch.cuda.Stream()
+        with torch.cuda.stream(t):
+            seen["got"], seen["want"] = _stream(), t.cuda_stream
+
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert seen["got"] == seen["want"]
