@@ -13,7 +13,7 @@
 //   small_gemm1_kernel: one CTA per (expert, 64 z columns).  It finds its
 //     expert's items in topk_ids itself, in item order, gathers their token
 //     rows and the 64 gate and 64 up weight columns one 64-row K stage at a
-//     time (16-byte asynchronous copies, three stages in flight), multiplies
+//     time (16-byte asynchronous copies, up to four stages in flight), multiplies
 //     with mma.sync (32 items per pass as M) and writes z [item, I] in bf16.
 //     The CTAs also zero the fp32 token accumulator; CTA 0 zeroes the error
 //     word and the completion counters, then records ids outside [0, E)
@@ -32,7 +32,11 @@ namespace {
 
 constexpr int kSThreads = 128;           // four warps
 constexpr int kSKC = 64;                 // K rows per stage
-constexpr int kSStages = 4;              // stages in the shared-memory ring
+// stages in the shared-memory ring: the whole 64-column weight slice of a
+// GEMM1 CTA with H = 256 (4 stages) and of a GEMM2 CTA with I = 512 (8) is
+// in flight at once; both rings take 110 KB
+constexpr int kSStages1 = 5;
+constexpr int kSStages2 = 8;
 constexpr int kSRows = 32;               // items per pass (two 16-row MMA tiles)
 constexpr int kSMaxItems = 256;          // routed items of a call
 constexpr int kSXStride = kSKC + 8;      // bf16 per activation row in shared memory (padded)
@@ -113,7 +117,7 @@ __device__ int expert_items(const int32_t* __restrict__ ids, int R, int e, int32
 // -> col0 + n; NCOL = 128 -> 16-column groups alternating gate (col0 + ...)
 // and up (col_up + ...), so that warp w holds gate and up of the same 16
 // columns (group 2w gate, 2w + 1 up).
-template <int NCOL>
+template <int NCOL, int STAGES>
 __device__ __forceinline__ void small_pass(const bf16* __restrict__ x_rows, int64_t lda,
                                            bool token_rows, int k_top, const int32_t* s_items,
                                            int row0, int n_items, int K,
@@ -165,17 +169,17 @@ __device__ __forceinline__ void small_pass(const bf16* __restrict__ x_rows, int6
     }
   };
   // one commit group per stage (empty past the last), so that stage ks has
-  // landed once at most kSStages - 2 groups are pending
+  // landed once at most STAGES - 2 groups are pending
 #pragma unroll
-  for (int st = 0; st < kSStages - 1; ++st) {
+  for (int st = 0; st < STAGES - 1; ++st) {
     if (st < KS) load_stage(st, st);
     ptx::cp_async_commit();
   }
   for (int ks = 0; ks < KS; ++ks) {
-    const int buf = ks % kSStages;
-    ptx::cp_async_wait<kSStages - 2>();
+    const int buf = ks % STAGES;
+    ptx::cp_async_wait<STAGES - 2>();
     __syncthreads();  // stage ks visible to all; stage ks - 1's buffer free
-    if (ks + kSStages - 1 < KS) load_stage(ks + kSStages - 1, (ks + kSStages - 1) % kSStages);
+    if (ks + STAGES - 1 < KS) load_stage(ks + STAGES - 1, (ks + STAGES - 1) % STAGES);
     ptx::cp_async_commit();
     const uint8_t* xs = smem + buf * (XB + WB);
     const uint8_t* wsm = xs + XB;
@@ -206,9 +210,9 @@ __device__ __forceinline__ void small_pass(const bf16* __restrict__ x_rows, int6
   __syncthreads();  // the next pass refills the ring
 }
 
-template <int NCOL>
+template <int NCOL, int STAGES>
 constexpr int small_smem() {
-  return kSStages * (kSRows * kSXStride * 2 + kSKC * (NCOL + 8) * 2);
+  return STAGES * (kSRows * kSXStride * 2 + kSKC * (NCOL + 8) * 2);
 }
 
 __global__ void __launch_bounds__(kSThreads)
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kSThreads)
     }
   for (int row0 = 0; row0 < n; row0 += kSRows) {
     float acc[2][4][4];
-    small_pass<128>(P.x, P.H, true, P.k, s_items, row0, n, P.H, w_e, 2 * static_cast<int64_t>(P.I),
+    small_pass<128, kSStages1>(P.x, P.H, true, P.k, s_items, row0, n, P.H, w_e, 2 * static_cast<int64_t>(P.I),
                     zc0, P.I + zc0, smem, acc);
     // tiles 0, 1: gate; 2, 3: up of the same columns
 #pragma unroll
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kSThreads)
                        : 0.f;
     for (int row0 = 0; row0 < n; row0 += kSRows) {
       float acc[2][2][4];
-      small_pass<64>(P.z, P.I, false, P.k, s_items, row0, n, P.I, w_e, P.H, oc0, 0, smem, acc);
+      small_pass<64, kSStages2>(P.z, P.I, false, P.k, s_items, row0, n, P.I, w_e, P.H, oc0, 0, smem, acc);
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
 #pragma unroll
@@ -387,7 +391,8 @@ moe_status_t launch_small_forward(const SmallArgs& a, cudaStream_t s) {
   P.E = a.E;
   P.k = a.k;
   P.R = static_cast<int32_t>(a.M * a.k);
-  constexpr int S1 = small_smem<128>(), S2 = small_smem<64>();
+  constexpr int S1 = small_smem<128, kSStages1>(), S2 = small_smem<64, kSStages2>();
+  static_assert(S1 <= 227 * 1024 - 2048 && S2 <= 227 * 1024 - 2048, "shared memory per CTA");
   static PerDevice attrs;
   if (attrs.get([&](int*) {
         cudaError_t e1 = cudaFuncSetAttribute(small_gemm1_kernel,
