@@ -21,9 +21,12 @@ pytestmark = pytest.mark.gpu
 
 # (M, H, I, E, top_k, bias): the tiny layer; one token, one item; the Mixtral
 # decode proportions scaled down; 200 items over 16 experts; 256 items over
-# 64 experts (k = 8); a handful of items over 3 experts
+# 64 experts (k = 8); a handful of items over 3 experts; 240 items over 2
+# experts (four 32-item passes, GEMM1's ring wrapping 16 K stages); K = 4096
+# (64 stages) at the largest M * H; I = 2048 (GEMM2's ring over 32 stages)
 SHAPES = [(64, 256, 512, 8, 2, True), (1, 64, 64, 4, 1, False), (16, 512, 640, 8, 2, True),
-          (100, 128, 192, 16, 2, True), (32, 256, 128, 64, 8, False), (5, 64, 128, 3, 3, True)]
+          (100, 128, 192, 16, 2, True), (32, 256, 128, 64, 8, False), (5, 64, 128, 3, 3, True),
+          (120, 1024, 256, 2, 2, True), (64, 4096, 64, 4, 2, False), (8, 64, 2048, 4, 2, True)]
 
 
 @pytest.fixture
@@ -175,3 +178,19 @@ def test_small_path_host_step():
     assert "small_gemm1" in ran
     w, ids = _route(spec, d)
     check_out(f64(y), _oracle(d, w, ids), "host step small")
+
+
+@pytest.mark.parametrize("M,H,small", [(128, 64, True), (129, 64, False), (64, 4096, True),
+                                       (65, 4096, False)])
+def test_small_path_bounds(M, H, small):
+    """At most 256 routed items and M * H <= 2^18 take the small path; one
+    more token takes the general one; both match the oracle."""
+    spec = _spec(M, H, 64, 4, 2, False)
+    d = wl.make_moe_inputs(spec, device="cuda")
+    w, ids = _route(spec, d)
+    pkg.profiler_start()
+    y = _forward(d, w, ids)
+    ran = pkg.profiler_stop()
+    torch.cuda.synchronize()
+    assert ("small_gemm1" in ran) == small, sorted(ran)
+    check_out(f64(y), _oracle(d, w, ids), f"bounds M={M} H={H}")
