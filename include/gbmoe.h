@@ -571,11 +571,14 @@ GBMOE_API moe_status_t moe_set_host_out_direct(int32_t enabled);
  * no expert map or router weight on the input, at most 256 routed items,
  * M * H <= 2^18, H and I multiples of 64 and expert weights of at most
  * 64 MiB, run the layer in two kernels: GEMM1 finds each expert's items in
- * topk_ids itself and gathers their rows (no align plan, no permuted rows;
- * the workspace's plan regions are left unwritten), and GEMM2 adds the
- * weighted rows into an fp32 token accumulator with atomics, the last of its
- * CTAs writing out.  0 = always the general path.  Results agree up to fp32
- * summation order.  Values other than 0 / 1 return MOE_ERR_INVALID_ARG. */
+ * topk_ids itself and gathers their rows (no align plan and no permuted
+ * rows: the workspace's plan regions are left unwritten, and the start of
+ * its permuted-rows region holds one completion counter per 64 output
+ * columns), and GEMM2 adds the weighted rows into an fp32 token accumulator
+ * with atomics, the last CTA of each 64-column block writing that block out.
+ * 0 = always the general path.  Results agree up to fp32 summation order
+ * (for top_k <= 2 that order cannot change the sum).  Values other than
+ * 0 / 1 return MOE_ERR_INVALID_ARG. */
 GBMOE_API moe_status_t moe_set_small_path(int32_t enabled);
 /* Where moe_forward / moe_forward_opts / moe_forward_host take GEMM1's rows
  * from (process-wide tuning / testing knob): 0 = automatic (fused when the

@@ -40,7 +40,7 @@ constexpr int kSStages2 = 8;
 constexpr int kSRows = 32;               // items per pass (two 16-row MMA tiles)
 constexpr int kSMaxItems = 256;          // routed items of a call
 constexpr int kSXStride = kSKC + 8;      // bf16 per activation row in shared memory (padded)
-constexpr int64_t kSMaxAccum = 1 << 18;  // token accumulator elements the last CTA converts
+constexpr int64_t kSMaxAccum = 1 << 18;  // token accumulator elements (M * H) of a call
 
 struct SmallParams {
   const bf16* x;           // hidden [M, H]
