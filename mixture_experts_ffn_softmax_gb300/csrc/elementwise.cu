@@ -44,9 +44,11 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
 // y[t, :] = bf16(sum_j o_sorted[inv[t*k + j], :]) with V x 4 fp32 columns
 // per thread; items with inv < 0 (dropped: bad expert id) contribute
 // nothing.  V = 2 for small k (two 16-byte loads per item keep more bytes in
-// flight: Mixtral shape, k = 2, 35.3 -> 29.0 us), V = 1 for larger k (already
-// k loads in flight; k = 8 DeepSeek-V3 shape 289 us against 297 with V = 2).
-template <int V>
+// flight: Mixtral shape, k = 2, 35.3 -> 29.0 us), V = 1 for larger k.
+// KMAX > 0 (k <= KMAX): a token's k positions are loaded first and then all
+// its k rows at once, so that k * V loads per thread are in flight; the sum
+// is taken in the same order either way.
+template <int V, int KMAX>
 __global__ void __launch_bounds__(256)
     reduce_sorted_kernel(const float* __restrict__ o, const int32_t* __restrict__ inv,
                          int64_t M, int k, int H, bf16* __restrict__ y) {
@@ -60,19 +62,41 @@ __global__ void __launch_bounds__(256)
     float4 acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int32_t pos = __ldg(inv + t * k + j);
-      if (pos < 0) continue;
-      const float4* src = reinterpret_cast<const float4*>(o + static_cast<int64_t>(pos) * H) + V * c;
-      float4 x[V];
-#pragma unroll
-      for (int v = 0; v < V; ++v) x[v] = __ldg(src + v);
+    auto add = [&](const float4 (&x)[V]) {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         acc[v].x += x[v].x;
         acc[v].y += x[v].y;
         acc[v].z += x[v].z;
         acc[v].w += x[v].w;
+      }
+    };
+    if constexpr (KMAX > 0) {
+      int32_t pos[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) pos[j] = j < k ? __ldg(inv + t * k + j) : -1;
+      float4 x[KMAX][V];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        const float4* src =
+            reinterpret_cast<const float4*>(o + static_cast<int64_t>(pos[j] < 0 ? 0 : pos[j]) * H) +
+            V * c;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+          x[j][v] = pos[j] >= 0 ? __ldg(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (pos[j] >= 0) add(x[j]);
+    } else {
+      for (int j = 0; j < k; ++j) {
+        const int32_t pos = __ldg(inv + t * k + j);
+        if (pos < 0) continue;
+        const float4* src = reinterpret_cast<const float4*>(o + static_cast<int64_t>(pos) * H) + V * c;
+        float4 x[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) x[v] = __ldg(src + v);
+        add(x);
       }
     }
     uint32_t w[2 * V];
@@ -94,7 +118,7 @@ __global__ void __launch_bounds__(256)
 // and 32-column chunk in o_exp [chunk][row], ld rows): y[t, :] =
 // bf16(sum_j o16[pos_j, :] * 2^e), 8 x V columns per thread (within one
 // chunk: one exponent byte per item).
-template <int V>
+template <int V, int KMAX>
 __global__ void __launch_bounds__(256)
     reduce_sorted_f16_kernel(const __half* __restrict__ o, const uint8_t* __restrict__ o_exp,
                              int64_t ld, const int32_t* __restrict__ inv, int64_t M, int k, int H,
@@ -110,14 +134,7 @@ __global__ void __launch_bounds__(256)
     float acc[8 * V];
 #pragma unroll
     for (int v = 0; v < 8 * V; ++v) acc[v] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int32_t pos = __ldg(inv + t * k + j);
-      if (pos < 0) continue;
-      const uint4* src = reinterpret_cast<const uint4*>(o + static_cast<int64_t>(pos) * H + col);
-      uint4 x[V];
-#pragma unroll
-      for (int v = 0; v < V; ++v) x[v] = __ldg(src + v);
-      const uint32_t e = __ldg(o_exp + static_cast<int64_t>(col >> 5) * ld + pos);
+    auto add = [&](const uint4 (&x)[V], uint32_t e) {
       const float sc = __uint_as_float((127u + e) << 23);  // 2^e
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -128,6 +145,36 @@ __global__ void __launch_bounds__(256)
           acc[8 * v + 2 * q] = fmaf(f.x, sc, acc[8 * v + 2 * q]);
           acc[8 * v + 2 * q + 1] = fmaf(f.y, sc, acc[8 * v + 2 * q + 1]);
         }
+      }
+    };
+    const uint8_t* ex_col = o_exp + static_cast<int64_t>(col >> 5) * ld;
+    if constexpr (KMAX > 0) {
+      // all k positions, then all k rows and exponents in flight at once
+      int32_t pos[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) pos[j] = j < k ? __ldg(inv + t * k + j) : -1;
+      uint4 x[KMAX][V];
+      uint32_t e[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        const int64_t p = pos[j] < 0 ? 0 : pos[j];
+        const uint4* src = reinterpret_cast<const uint4*>(o + p * H + col);
+#pragma unroll
+        for (int v = 0; v < V; ++v) x[j][v] = pos[j] >= 0 ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        e[j] = pos[j] >= 0 ? __ldg(ex_col + p) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (pos[j] >= 0) add(x[j], e[j]);
+    } else {
+      for (int j = 0; j < k; ++j) {
+        const int32_t pos = __ldg(inv + t * k + j);
+        if (pos < 0) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(o + static_cast<int64_t>(pos) * H + col);
+        uint4 x[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) x[v] = __ldg(src + v);
+        add(x, __ldg(ex_col + pos));
       }
     }
 #pragma unroll
@@ -200,10 +247,14 @@ moe_status_t launch_reduce_sorted(const float* o_sorted, const int32_t* inv, int
   const unsigned grid =
       static_cast<unsigned>(std::min<int64_t>(ceil_div<int64_t>(total, 256), device_sms() * 8));
   prof_before("reduce_sorted", s);
-  if (V == 2)
-    launch_kernel(reduce_sorted_kernel<2>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
+  if (V == 2 && k <= 2)
+    launch_kernel(reduce_sorted_kernel<2, 2>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
+  else if (V == 2)
+    launch_kernel(reduce_sorted_kernel<2, 4>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
+  else if (k <= 8)
+    launch_kernel(reduce_sorted_kernel<1, 8>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
   else
-    launch_kernel(reduce_sorted_kernel<1>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
+    launch_kernel(reduce_sorted_kernel<1, 0>, grid, 256, 0, s, o_sorted, inv, M, k, H, y);
   prof_after("reduce_sorted", s);
   return check_launch("reduce_sorted");
 }
@@ -218,10 +269,14 @@ moe_status_t launch_reduce_sorted_f16(const void* o16, const uint8_t* o_exp, int
       static_cast<unsigned>(std::min<int64_t>(ceil_div<int64_t>(total, 256), device_sms() * 8));
   const __half* o = static_cast<const __half*>(o16);
   prof_before("reduce_sorted", s);
-  if (V == 2)
-    launch_kernel(reduce_sorted_f16_kernel<2>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
+  if (V == 2 && k <= 2)
+    launch_kernel(reduce_sorted_f16_kernel<2, 2>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
+  else if (V == 2)
+    launch_kernel(reduce_sorted_f16_kernel<2, 4>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
+  else if (k <= 8)
+    launch_kernel(reduce_sorted_f16_kernel<1, 8>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
   else
-    launch_kernel(reduce_sorted_f16_kernel<1>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
+    launch_kernel(reduce_sorted_f16_kernel<1, 0>, grid, 256, 0, s, o, o_exp, ld, inv, M, k, H, y);
   prof_after("reduce_sorted", s);
   return check_launch("reduce_sorted");
 }
