@@ -604,6 +604,8 @@ static moe_status_t forward_launch(const void* hidden, const float* topk_weights
     bf16* a_perm = at<bf16>(workspace, L.a_perm);
     GatherArgs ga{x + c0 * H, sorted, offsets, E, top_k, static_cast<int32_t>(Rc), H, cap,
                   a_perm};
+    ga.inv = inv;  // each token row read once
+    ga.tokens = Mc;
     if (wait_rows != nullptr && c0 == 0 && cudaStreamWaitEvent(s, wait_rows, 0) != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaStreamWaitEvent: %s",
                        cudaGetErrorString(cudaGetLastError()));
@@ -1144,6 +1146,8 @@ moe_status_t moe_forward_wq(const void* hidden, const float* topk_weights,
     bf16* a_perm = at<bf16>(workspace, L.a_perm);
     GatherArgs ga{x + c0 * H, sorted, offsets, E, top_k, static_cast<int32_t>(Rc), H, cap,
                   a_perm};
+    ga.inv = inv;  // each token row read once
+    ga.tokens = Mc;
     if (moe_status_t st = launch_gather(ga, s)) return st;
     bf16* z = at<bf16>(workspace, L.z);
     GroupedGemmArgs g1{};

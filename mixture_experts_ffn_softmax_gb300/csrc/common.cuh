@@ -174,6 +174,11 @@ struct GatherArgs {
   int32_t H;
   int64_t cap;
   bf16* dst;
+  // token-major form (inv != null): token t's row goes to the sorted rows
+  // inv[t * div + j] (j < div; -1: dropped) for t < tokens, each token row
+  // read once; index, offsets and sentinel are then unused
+  const int32_t* inv = nullptr;
+  int64_t tokens = 0;
 };
 moe_status_t launch_gather(const GatherArgs& a, cudaStream_t s);
 

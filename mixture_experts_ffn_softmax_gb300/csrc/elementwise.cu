@@ -41,6 +41,49 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
   }
 }
 
+// The same gather token by token: A_perm[inv[t*k + j], :] = src[t, :] for
+// every item j of token t with a sorted row (inv < 0: dropped).  In sorted
+// order each token row is read once per item, at random, and falls out of
+// L2 under the stream of stores (Qwen shape: 0.80 GB of DRAM traffic for
+// 0.54 GB of rows written); here it is read once.  A warp takes a token and
+// one segment of up to 32 * kTokVec 16-byte vectors of its row.
+constexpr int kTokVec = 8;
+__global__ void __launch_bounds__(kGatherWarps * 32)
+    gather_tokens_kernel(const bf16* __restrict__ src, const int32_t* __restrict__ inv,
+                         int64_t M, int k, int H, int64_t cap, bf16* __restrict__ dst) {
+  pdl_begin();
+  const int lane = threadIdx.x & 31;
+  const int nvec = H / 8;  // 16-byte vectors per row
+  const int segs = (nvec + 32 * kTokVec - 1) / (32 * kTokVec);
+  const int64_t units = M * segs;
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kGatherWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kGatherWarps;
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const int64_t t = u / segs;
+    const int v0 = static_cast<int>(u - t * segs) * 32 * kTokVec;
+    // the token's sorted rows: item j's in lane j % 32 of p[j / 32] (k <= 64)
+    const int32_t p0 = lane < k ? __ldg(inv + t * k + lane) : -1;
+    const int32_t p1 = lane + 32 < k ? __ldg(inv + t * k + lane + 32) : -1;
+    const uint4* sv = reinterpret_cast<const uint4*>(src + t * H);
+    uint4 x[kTokVec];
+#pragma unroll
+    for (int i = 0; i < kTokVec; ++i) {
+      const int v = v0 + 32 * i + lane;
+      if (v < nvec) x[i] = __ldg(sv + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int32_t pos = __shfl_sync(0xffffffffu, j < 32 ? p0 : p1, j & 31);
+      if (pos < 0 || pos >= cap) continue;  // warp-uniform
+      uint4* d = reinterpret_cast<uint4*>(dst + static_cast<int64_t>(pos) * H);
+#pragma unroll
+      for (int i = 0; i < kTokVec; ++i) {
+        const int v = v0 + 32 * i + lane;
+        if (v < nvec) d[v] = x[i];
+      }
+    }
+  }
+}
+
 // y[t, :] = bf16(sum_j o_sorted[inv[t*k + j], :]) with V x 4 fp32 columns
 // per thread; items with inv < 0 (dropped: bad expert id) contribute
 // nothing.  V = 2 for small k (two 16-byte loads per item keep more bytes in
@@ -230,6 +273,17 @@ int device_sms() {
 
 moe_status_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   if (a.cap <= 0) return MOE_OK;
+  if (a.inv != nullptr) {
+    if (a.tokens <= 0) return MOE_OK;
+    const int64_t segs = ceil_div<int64_t>(a.H / 8, 32 * kTokVec);
+    const int64_t want = ceil_div<int64_t>(a.tokens * segs, kGatherWarps);
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
+    prof_before("gather_rows", s);
+    launch_kernel(gather_tokens_kernel, grid, kGatherWarps * 32, 0, s, a.src, a.inv, a.tokens,
+                  a.div, a.H, a.cap, a.dst);
+    prof_after("gather_rows", s);
+    return check_launch("gather_rows");
+  }
   const int64_t want = ceil_div<int64_t>(a.cap, kGatherWarps);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, device_sms() * 8));
   prof_before("gather_rows", s);
