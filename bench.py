@@ -202,7 +202,8 @@ def kernel_work(name, H, I, E, k, M, R, touched, bias=False):
     rows.  GEMM1: 4HI FLOPs per row; its touched experts' w13 (4HI bytes each)
     + the rows read (2H) + z written (2I).  GEMM2: 2HI FLOPs per row; w2
     (2HI bytes each) + z read (2I) + the fp32 (4H) or bf16 (2H) row written.
-    Gather 2H read + 2H written per row; reduce 4kH read + 2H written per
+    Gather 2H read per token (each token row once) + 2H written per row (the
+    batched layout passes M = R); reduce 4kH read + 2H written per
     token; route 4E read + 8k written per token; align 4 B read twice and
     8 B written per row.  The small-call kernels: GEMM1 as above + the fp32
     token accumulator zeroed (4H per token); GEMM2 its w2, z read, and per
@@ -223,7 +224,7 @@ def kernel_work(name, H, I, E, k, M, R, touched, bias=False):
     if name == "small_gemm2":
         return 2.0 * R * H * I, touched * 2 * H * I + b2 + R * 2 * I + M * 6 * H
     if name == "gather_rows":
-        return 0.0, R * 4 * H
+        return 0.0, (M + R) * 2 * H
     if name == "reduce_sorted":
         return 0.0, M * (4 * k * H + 2 * H)
     if name == "cast_f32_bf16":
