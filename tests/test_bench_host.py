@@ -92,6 +92,24 @@ def test_kernel_work_matches_the_layer_totals():
     assert bench.kernel_work("no_such_kernel", 1, 1, 1, 1, 1, 1, 1) is None
 
 
+def test_kernel_work_small_calls_and_gather():
+    """The small-call GEMMs do the layer's 6 R H I FLOPs between them; their
+    bytes are the touched experts' weights, the rows and z, plus the fp32
+    token accumulator (zeroed by GEMM1, read back by GEMM2 with y written).
+    The gather reads each token row once and writes each routed row once;
+    the batched layout (M = R) reads and writes each row once."""
+    s = wl.SPECS["tiny"]
+    f1, b1 = bench.kernel_work("small_gemm1", s.H, s.I, s.E, s.top_k, s.M, s.R, 8)
+    f2, b2 = bench.kernel_work("small_gemm2", s.H, s.I, s.E, s.top_k, s.M, s.R, 8)
+    assert f1 + f2 == s.flops()
+    assert b1 == 8 * 4 * s.H * s.I + s.R * (2 * s.H + 2 * s.I) + s.M * 4 * s.H
+    assert b2 == 8 * 2 * s.H * s.I + s.R * 2 * s.I + s.M * 6 * s.H
+    q = wl.SPECS["qwen_skew"]
+    assert bench.kernel_work("gather_rows", q.H, q.I, q.E, q.top_k, q.M, q.R, 128)[1] == \
+        q.M * 2 * q.H + q.R * 2 * q.H
+    assert bench.kernel_work("gather_rows", q.H, q.I, q.E, 1, q.R, q.R, 128)[1] == q.R * 4 * q.H
+
+
 def test_roofline_picks_the_binding_term():
     pk = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "hbm_gbs": 8000.0}
     # 2 TFLOP and 1 GB in 2 ms: tensor term 1 ms, HBM term 0.125 ms
