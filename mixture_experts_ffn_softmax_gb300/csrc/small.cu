@@ -19,9 +19,10 @@
 //     word and the completion counters, then records ids outside [0, E)
 //     (those items contribute nothing).
 //   small_gemm2_kernel: one CTA per (expert, 64 output columns), the same
-//     way over z and W2; each item's weighted row is added into the token
-//     accumulator with fp32 atomics, and of the E CTAs of a 64-column block
-//     the last to finish writes that block of y in bf16.
+//     way over z and W2 (up to seven stages in flight); each item's weighted
+//     row is added into the token accumulator with fp32 atomics, and of the
+//     E CTAs of a 64-column block the last to finish writes that block of y
+//     in bf16.
 #include <algorithm>
 
 #include "common.cuh"
