@@ -534,6 +534,14 @@ def time_steps(step, K, W, world, ev_stream=None):
     return e0.elapsed_time(e1)
 
 
+def workload_config(spec):
+    """The workload fields of the line's config, the same on both arms."""
+    return {"workload": f"{spec.name}: Mixtral-8x7B-shape MoE layer" if "mixtral" in spec.name
+            else spec.name, "M": spec.M, "H": spec.H, "I": spec.I, "E": spec.E,
+            "top_k": spec.top_k, "routing": spec.routing_method,
+            "renormalize": spec.renormalize}
+
+
 def run_ours(args, world, rank, local):
     import mixture_experts_ffn_softmax_gb300 as pkg
     pk = peaks()
@@ -610,10 +618,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{spec.name}: Mixtral-8x7B-shape MoE layer" if "mixtral" in spec.name
-                   else spec.name, "M": spec.M, "H": spec.H, "I": spec.I, "E": spec.E,
-                   "top_k": spec.top_k, "routing": spec.routing_method,
-                   "renormalize": spec.renormalize, "parallelism": f"replicas x{world}",
+        "config": {**workload_config(spec), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (weights of every touched expert are read "
                          "each step)" if big else "inputs fit in L2 (warm)"},
         "tflops": round(tflops, 2),
@@ -968,8 +973,7 @@ def run_reference(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": spec.name, "M": spec.M, "H": spec.H, "I": spec.I,
-                       "E": spec.E, "top_k": spec.top_k, "parallelism": "cpu oracle"},
+            "config": {**workload_config(spec), "parallelism": "cpu oracle, one process"},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
                              "kind": "oracle",
                              "sample": f"{n} of {spec.M} tokens per step ({n_exp} experts "
