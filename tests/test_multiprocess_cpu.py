@@ -62,3 +62,8 @@ def test_reference_arm_under_torchrun_two_ranks():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the same workload fields as our arm's line prints
+    import bench
+    from mixture_experts_ffn_softmax_gb300 import workloads as wl
+    want = bench.workload_config(wl.SPECS["tiny"])
+    assert {k: line["config"][k] for k in want} == want
